@@ -1,0 +1,236 @@
+"""fp64 CPU oracle for the Simple GLA hot path.
+
+TEST INFRASTRUCTURE ONLY. The tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package; the library under ``gated_linear_attention_gb300``
+never does, and this package imports nothing from it. The two share no code.
+
+Three independent statements of the same computation:
+
+* :func:`recurrent` -- the token-by-token recurrence in C (``recurrent.c``), fp64, on
+  host threads. "MiniCPM-SALA — Complete Blueprint", section "B2 lightning-attn (Simple
+  GLA)", block "Simple GLA Recurrence": decay the state by exp(g), add k^T v, then
+  read o = scale * q S.
+* :func:`chunkwise` -- the chunked form with chunk size C, in numpy fp64, taking the steps
+  of "Formulas and Code for Adapting Inference to GDN/KDA Linear Modules", section 1.2
+  (chunk decay from the cumulative sum of g, the masked decay matrix, the inter-chunk
+  term (q * exp(g)) @ S, the intra-chunk term (q k^T * gamma).tril() @ v, and the state
+  refresh S * exp(g_last) + (k * exp(g_last - g))^T @ v), specialised to the Simple GLA
+  case: no delta rule, beta = 1, so the "new v" is v itself.
+* :func:`bruteforce` -- the quadratic parallel form, written from the unrolled closed form
+  of the same Blueprint page (section "Why Linear Attention Loses Information", Problem
+  1: S_n = alpha^n S_0 + sum_i alpha^(n-i) k_i^T v_i) with a per-token decay:
+  o_t = scale * [ sum_{j<=t} exp(G_t - G_j) (q_t . k_j) v_j + exp(G_t) q_t h0 ],
+  G_t = sum_{i<=t} g_i within the sequence. For tiny inputs only.
+
+All three take the exact values the GPU receives (bf16 q/k/v, fp32 g, fp32 h0) and compute
+in float64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_SRC = os.path.join(_HERE, "recurrent.c")
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile ``recurrent.c`` into ``oracle/_build/liboracle.so`` (plain gcc, -O2)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def load_library(path: str):
+    """ctypes handle with the argument types of ``oracle_recurrent`` declared."""
+    lib = ctypes.CDLL(path)
+    p = ctypes.c_void_p
+    i64 = ctypes.c_int64
+    lib.oracle_recurrent.argtypes = [p, p, p, p, ctypes.c_double, p, p, i64, i64, i64,
+                                     i64, p, i64, p, p, ctypes.c_int]
+    lib.oracle_recurrent.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    with _lib_lock:
+        if _lib is None:
+            build()
+            _lib = load_library(_LIB_PATH)
+    return _lib
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+# ----------------------------------------------------------------------------------------
+# argument helpers (no arithmetic of the method here)
+
+
+def _bf16_bits(x: torch.Tensor) -> np.ndarray:
+    assert x.dtype == torch.bfloat16 and x.device.type == "cpu"
+    return np.ascontiguousarray(x.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _as_f64(x) -> np.ndarray:
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu()
+        if x.dtype == torch.bfloat16:
+            x = x.float()
+        x = x.numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _packed(q, k, v, g, cu_seqlens):
+    """Flatten [B, T, H, d] to the packed [B*T, H, d] form and build cu_seqlens."""
+    if q.dim() == 4:
+        B, T = q.shape[0], q.shape[1]
+        q, k, v = (x.reshape(B * T, *x.shape[2:]) for x in (q, k, v))
+        g = g.reshape(B * T, g.shape[-1])
+        if cu_seqlens is None:
+            cu_seqlens = torch.arange(0, B + 1, dtype=torch.int64) * T
+    elif cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, q.shape[0]], dtype=torch.int64)
+    cu = np.ascontiguousarray(torch.as_tensor(cu_seqlens).cpu().numpy().astype(np.int64))
+    return q, k, v, g, cu
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ----------------------------------------------------------------------------------------
+# the recurrence (C, fp64)
+
+
+def recurrent(q, k, v, g, scale, h0=None, cu_seqlens=None, heads=None, want_o=True,
+              nthreads: int | None = None, _lib=None):
+    """Token-by-token fp64 recurrence.
+
+    q, k: bf16 [B, T, H, dk] or packed [T, H, dk]; v: bf16 [..., dv]; g: fp32 [B, T, H] or
+    [T, H]; h0: fp32/fp64 [nseq, H, dk, dv] or None; cu_seqlens: int64 [nseq+1] for packed
+    input. ``heads`` selects a subset of heads (outputs then hold only those heads, in that
+    order). Returns (o [T_total, nh, dv] float64 or None, hT [nseq, nh, dk, dv] float64).
+    ``_lib`` substitutes another build of ``recurrent.c`` (the mutation tests use it).
+    """
+    lib = _lib or _load()
+    q, k, v, g, cu = _packed(q, k, v, g, cu_seqlens)
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    nseq = len(cu) - 1
+    qb, kb, vb = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v)
+    gf = np.ascontiguousarray(g.float().numpy() if isinstance(g, torch.Tensor) else
+                              np.asarray(g, dtype=np.float32))
+    h0d = None if h0 is None else _as_f64(h0).reshape(nseq, H, dk, dv)
+    hs = None if heads is None else np.ascontiguousarray(np.asarray(heads, dtype=np.int64))
+    nh = H if hs is None else len(hs)
+    o = np.empty((T, nh, dv), dtype=np.float64) if want_o else None
+    hT = np.empty((nseq, nh, dk, dv), dtype=np.float64)
+    rc = lib.oracle_recurrent(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(gf), float(scale), _ptr(h0d),
+                              _ptr(cu), nseq, H, dk, dv, _ptr(hs), nh, _ptr(o), _ptr(hT),
+                              int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_recurrent rejected its arguments (code {rc})")
+    return o, hT
+
+
+# ----------------------------------------------------------------------------------------
+# the chunked form (numpy, fp64)
+
+
+def _chunkwise_one(q, k, v, g, scale, S, C):
+    """One sequence, one head: q, k [L, dk], v [L, dv], g [L], S [dk, dv] (all fp64)."""
+    L = q.shape[0]
+    o = np.empty((L, v.shape[1]), dtype=np.float64)
+    for c0 in range(0, L, C):
+        qi, ki, vi, gi = q[c0:c0 + C], k[c0:c0 + C], v[c0:c0 + C], g[c0:c0 + C]
+        b = np.cumsum(gi)                               # chunk decay: cumulative sum of g
+        gamma = np.exp(np.tril(b[:, None] - b[None, :]))  # masked difference, then exp
+        o_inter = (qi * np.exp(b)[:, None]) @ S
+        o_intra = np.tril(qi @ ki.T * gamma) @ vi
+        o[c0:c0 + C] = scale * (o_inter + o_intra)
+        S = S * np.exp(b[-1]) + (ki * np.exp(b[-1] - b)[:, None]).T @ vi   # state refresh
+    return o, S
+
+
+def chunkwise(q, k, v, g, scale, h0=None, cu_seqlens=None, chunk: int = 64):
+    """Chunked fp64 form. Same arguments and return shapes as :func:`recurrent` (all heads)."""
+    q, k, v, g, cu = _packed(q, k, v, g, cu_seqlens)
+    qd, kd, vd, gd = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(g)
+    T, H, dk = qd.shape
+    dv = vd.shape[-1]
+    nseq = len(cu) - 1
+    h0d = None if h0 is None else _as_f64(h0).reshape(nseq, H, dk, dv)
+    o = np.zeros((T, H, dv), dtype=np.float64)
+    hT = np.zeros((nseq, H, dk, dv), dtype=np.float64)
+    for n in range(nseq):
+        s, e = int(cu[n]), int(cu[n + 1])
+        for h in range(H):
+            S0 = np.zeros((dk, dv)) if h0d is None else h0d[n, h].copy()
+            o[s:e, h], hT[n, h] = _chunkwise_one(qd[s:e, h], kd[s:e, h], vd[s:e, h],
+                                                 gd[s:e, h], scale, S0, chunk)
+    return o, hT
+
+
+# ----------------------------------------------------------------------------------------
+# the quadratic parallel form (numpy, fp64, tiny inputs)
+
+
+def bruteforce(q, k, v, g, scale, h0=None, cu_seqlens=None):
+    """Quadratic fp64 form. Same arguments and return shapes as :func:`chunkwise`."""
+    q, k, v, g, cu = _packed(q, k, v, g, cu_seqlens)
+    qd, kd, vd, gd = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(g)
+    T, H, dk = qd.shape
+    dv = vd.shape[-1]
+    nseq = len(cu) - 1
+    h0d = None if h0 is None else _as_f64(h0).reshape(nseq, H, dk, dv)
+    o = np.zeros((T, H, dv), dtype=np.float64)
+    hT = np.zeros((nseq, H, dk, dv), dtype=np.float64)
+    for n in range(nseq):
+        s, e = int(cu[n]), int(cu[n + 1])
+        L = e - s
+        for h in range(H):
+            G = np.cumsum(gd[s:e, h])
+            # weight of token j in the state seen by token t: exp(G_t - G_j) for j <= t
+            W = np.zeros((L, L))
+            for t in range(L):
+                W[t, :t + 1] = np.exp(G[t] - G[:t + 1])
+            qk = qd[s:e, h] @ kd[s:e, h].T
+            o_n = (W * qk) @ vd[s:e, h]
+            S0 = np.zeros((dk, dv)) if h0d is None else h0d[n, h]
+            if L:
+                o_n += np.exp(G)[:, None] * (qd[s:e, h] @ S0)
+            o[s:e, h] = scale * o_n
+            # final state: exp(G_L - G_j) k_j^T v_j summed, plus exp(G_L) h0
+            GL = G[-1] if L else 0.0
+            w_end = np.exp(GL - G) if L else np.zeros(0)
+            hT[n, h] = np.exp(GL) * S0 + (kd[s:e, h] * w_end[:, None]).T @ vd[s:e, h]
+    return o, hT
+
+
+def rel_fro(x, ref) -> float:
+    """Relative Frobenius error ||x - ref||_F / ||ref||_F (fp64)."""
+    x = _as_f64(x)
+    ref = _as_f64(ref)
+    den = np.linalg.norm(ref.ravel())
+    num = np.linalg.norm((x - ref).ravel())
+    if den == 0.0:
+        return float(num)
+    return float(num / den)

@@ -1,0 +1,274 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Each pin is independent of the oracle's own code path: closed forms, the quadratic
+(parenthesised-the-other-way) form, printed values, special cases that reduce to plain
+linear algebra, and invariants of the recurrence. Shapes use d_k != d_v wherever possible so
+that a transposed state or operand cannot pass.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bf16(x):
+    return torch.as_tensor(x, dtype=torch.float32).to(torch.bfloat16)
+
+
+def _rand_case(T, H, dk, dv, seed, g_lo=-0.5, g_hi=0.0, nseq_lens=None, h0=True):
+    """Small random packed case in the oracle's input format."""
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn((T, H, dk), generator=gen).to(torch.bfloat16)
+    k = torch.randn((T, H, dk), generator=gen).to(torch.bfloat16)
+    v = torch.randn((T, H, dv), generator=gen).to(torch.bfloat16)
+    g = g_lo + (g_hi - g_lo) * torch.rand((T, H), generator=gen)
+    lens = nseq_lens or [T]
+    assert sum(lens) == T
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int64)
+    hz = torch.randn((len(lens), H, dk, dv), generator=gen) * 0.5 if h0 else None
+    return q, k, v, g.float(), hz, cu
+
+
+def _read_table(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line.split())
+    return rows
+
+
+# ---------------------------------------------------------------------------------------
+# (QK)V = Q(KV): with g = 0 the recurrence equals masked causal attention without softmax
+# ("MiniCPM-SALA — Complete Blueprint", "Why Not Just Use Linear Attention Everywhere?").
+
+
+@pytest.mark.parametrize("T,H,dk,dv", [(1, 1, 3, 5), (37, 2, 5, 3), (200, 1, 128, 128)])
+def test_associativity_g_zero(T, H, dk, dv):
+    q, k, v, _, _, cu = _rand_case(T, H, dk, dv, seed=T + dk)
+    g = torch.zeros((T, H))
+    scale = 0.37
+    o, hT = oracle.recurrent(q, k, v, g, scale, cu_seqlens=cu)
+    qd, kd, vd = (x.double().numpy() for x in (q, k, v))
+    for h in range(H):
+        # (Q K^T masked to j <= t) V, evaluated with numpy: the other parenthesisation
+        A = np.tril(qd[:, h] @ kd[:, h].T)
+        ref = scale * (A @ vd[:, h])
+        assert oracle.rel_fro(o[:, h], ref) < 1e-12
+        # K^T V is the state after all tokens
+        assert oracle.rel_fro(hT[0, h], kd[:, h].T @ vd[:, h]) < 1e-12
+
+
+# ---------------------------------------------------------------------------------------
+# Unrolled closed form for a constant per-head alpha ("MiniCPM-SALA — Complete Blueprint",
+# "Why Linear Attention Loses Information", Problem 1):
+#   S_n = alpha^n S_0 + sum_{i=1..n} alpha^(n-i) k_i^T v_i
+
+
+@pytest.mark.parametrize("n,dk,dv", [(1, 4, 6), (50, 4, 6), (300, 7, 2)])
+def test_closed_form_constant_alpha(n, dk, dv):
+    H = 3
+    alphas = [0.40, 0.80, 0.999]
+    q, k, v, _, h0, cu = _rand_case(n, H, dk, dv, seed=n)
+    g = torch.tensor([math.log(a) for a in alphas], dtype=torch.float32).expand(n, H).contiguous()
+    _, hT = oracle.recurrent(q, k, v, g, 1.0, h0=h0, cu_seqlens=cu)
+    kd, vd = k.double().numpy(), v.double().numpy()
+    for h in range(H):
+        a = math.exp(float(g[0, h]))       # the alpha the oracle sees (fp32 log-decay)
+        ref = a ** n * h0[0, h].double().numpy()
+        for i in range(1, n + 1):
+            ref = ref + a ** (n - i) * np.outer(kd[i - 1, h], vd[i - 1, h])
+        assert oracle.rel_fro(hT[0, h], ref) < 1e-12
+
+
+# ---------------------------------------------------------------------------------------
+# Printed decay values.
+
+
+def _decay_after(alpha, n):
+    """alpha^n as the oracle's state decay sees it: k = v = 0, h0 = 1, n tokens of g = ln alpha."""
+    one = torch.zeros((n, 1, 1), dtype=torch.bfloat16)
+    g = torch.full((n, 1), math.log(alpha), dtype=torch.float32)
+    h0 = torch.ones((1, 1, 1, 1), dtype=torch.float64)
+    _, hT = oracle.recurrent(one, one, one, g, 1.0, h0=h0)
+    return float(hT[0, 0, 0, 0])
+
+
+def test_decay_over_distance_table():
+    rows = _read_table("decay_over_distance.txt")
+    assert len(rows) == 18
+    for alpha_s, n_s, printed_s, check in rows:
+        alpha, n, printed = float(alpha_s), int(n_s), float(printed_s)
+        got = _decay_after(alpha, n)
+        if check == "zero":
+            assert 0.0 <= got < 1e-6, (alpha, n, got)
+        elif check == "rel1pct":
+            assert abs(got - printed) <= 0.01 * printed, (alpha, n, got)
+        else:
+            mant = printed_s.lower().split("e")[0]
+            exp10 = int(printed_s.lower().split("e")[1]) if "e" in printed_s.lower() else 0
+            decimals = len(mant.split(".")[1]) if "." in mant else 0
+            half_ulp = 0.5 * 10.0 ** (exp10 - decimals)
+            assert abs(got - printed) <= half_ulp, (alpha, n, got, printed)
+
+
+def test_per_head_decay_printed():
+    for g_s, alpha_s in _read_table("per_head_decay.txt"):
+        one = torch.zeros((1, 1, 1), dtype=torch.bfloat16)
+        g = torch.full((1, 1), float(g_s), dtype=torch.float32)
+        _, hT = oracle.recurrent(one, one, one, g, 1.0, h0=torch.ones((1, 1, 1, 1)))
+        decimals = len(alpha_s.split(".")[1])
+        assert abs(float(hT.ravel()[0]) - float(alpha_s)) <= 0.5 * 10.0 ** -decimals
+
+
+def test_scale_constant():
+    rows = dict((r[0], r[1]) for r in _read_table("constants.txt"))
+    from gated_linear_attention_gb300 import inputs
+    assert int(rows["head_dim"]) == inputs.D
+    assert abs(inputs.SCALE - float(rows["attn_scale"])) <= 0.5e-5
+
+
+# ---------------------------------------------------------------------------------------
+# Special case: k = v = 0 leaves only the initial state, decayed:
+#   o_t = scale * exp(G_t) q_t h0,  hT = exp(G_T) h0.
+
+
+def test_h0_only_path():
+    T, H, dk, dv = 70, 2, 6, 4
+    q, _, _, g, h0, cu = _rand_case(T, H, dk, dv, seed=5, g_lo=-0.3)
+    z = torch.zeros((T, H, dk), dtype=torch.bfloat16)
+    zv = torch.zeros((T, H, dv), dtype=torch.bfloat16)
+    o, hT = oracle.recurrent(q, z, zv, g, 0.25, h0=h0, cu_seqlens=cu)
+    G = np.cumsum(g.double().numpy(), axis=0)          # [T, H]
+    qd = q.double().numpy()
+    for h in range(H):
+        H0 = h0[0, h].double().numpy()
+        ref_o = 0.25 * np.exp(G[:, h])[:, None] * (qd[:, h] @ H0)
+        assert oracle.rel_fro(o[:, h], ref_o) < 1e-13
+        assert oracle.rel_fro(hT[0, h], math.exp(G[-1, h]) * H0) < 1e-13
+
+
+# ---------------------------------------------------------------------------------------
+# The quadratic form with per-token decay and a nonzero h0 (brute force, tiny sizes).
+
+
+@pytest.mark.parametrize("lens,H,dk,dv", [([1], 1, 2, 3), ([5, 0, 12], 2, 3, 5),
+                                           ([33, 64, 1], 3, 8, 4), ([130], 1, 16, 16)])
+def test_recurrent_vs_bruteforce(lens, H, dk, dv):
+    T = sum(lens)
+    q, k, v, g, h0, cu = _rand_case(T, H, dk, dv, seed=T + H, g_lo=-1.0, nseq_lens=lens)
+    o, hT = oracle.recurrent(q, k, v, g, 0.3, h0=h0, cu_seqlens=cu)
+    ob, hb = oracle.bruteforce(q, k, v, g, 0.3, h0=h0, cu_seqlens=cu)
+    assert oracle.rel_fro(o, ob) < 1e-12
+    assert oracle.rel_fro(hT, hb) < 1e-12
+
+
+# ---------------------------------------------------------------------------------------
+# Chunked form (its own code path, following the GDN/KDA page's chunk recipe) against the
+# recurrence: the two forms compute the same thing.
+
+
+@pytest.mark.parametrize("lens,chunk", [([1], 64), ([63], 64), ([64], 64), ([65], 64),
+                                        ([127, 200, 0, 3], 64), ([300], 16)])
+def test_chunkwise_vs_recurrent(lens, chunk):
+    T, H, dk, dv = sum(lens), 2, 12, 20
+    q, k, v, g, h0, cu = _rand_case(T, H, dk, dv, seed=7 + T, g_lo=-0.9, nseq_lens=lens)
+    o, hT = oracle.recurrent(q, k, v, g, 0.125, h0=h0, cu_seqlens=cu)
+    oc, hc = oracle.chunkwise(q, k, v, g, 0.125, h0=h0, cu_seqlens=cu, chunk=chunk)
+    assert oracle.rel_fro(oc, o) < 1e-10
+    assert oracle.rel_fro(hc, hT) < 1e-10
+
+
+def test_chunkwise_vs_recurrent_full_dim():
+    T, H = 200, 2
+    q, k, v, g, h0, cu = _rand_case(T, H, 128, 128, seed=11, g_lo=-0.2)
+    o, hT = oracle.recurrent(q, k, v, g, 128 ** -0.5, h0=h0, cu_seqlens=cu)
+    oc, hc = oracle.chunkwise(q, k, v, g, 128 ** -0.5, h0=h0, cu_seqlens=cu)
+    assert oracle.rel_fro(oc, o) < 1e-10
+    assert oracle.rel_fro(hc, hT) < 1e-10
+
+
+# ---------------------------------------------------------------------------------------
+# Invariants: the state is the whole memory of the past (fixed size regardless of T), so a
+# sequence split in two calls chained through hT -> h0 equals one call; packed varlen equals
+# separate calls; a zero-length sequence returns h0.
+
+
+def test_split_resume():
+    T, H, dk, dv = 150, 2, 8, 6
+    q, k, v, g, h0, cu = _rand_case(T, H, dk, dv, seed=3, g_lo=-0.4)
+    o, hT = oracle.recurrent(q, k, v, g, 0.5, h0=h0, cu_seqlens=cu)
+    for cut in (0, 1, 64, 97, 150):
+        o1, h1 = oracle.recurrent(q[:cut], k[:cut], v[:cut], g[:cut], 0.5, h0=h0,
+                                  cu_seqlens=torch.tensor([0, cut]))
+        o2, h2 = oracle.recurrent(q[cut:], k[cut:], v[cut:], g[cut:], 0.5, h0=h1,
+                                  cu_seqlens=torch.tensor([0, T - cut]))
+        np.testing.assert_allclose(np.concatenate([o1, o2]), o, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(h2, hT, rtol=1e-12, atol=1e-14)
+
+
+def test_varlen_equals_separate_calls():
+    lens = [17, 0, 64, 5]
+    T, H, dk, dv = sum(lens), 3, 4, 4
+    q, k, v, g, h0, cu = _rand_case(T, H, dk, dv, seed=9, nseq_lens=lens)
+    o, hT = oracle.recurrent(q, k, v, g, 0.7, h0=h0, cu_seqlens=cu)
+    for n, (s, e) in enumerate(zip(cu[:-1].tolist(), cu[1:].tolist())):
+        on, hn = oracle.recurrent(q[s:e], k[s:e], v[s:e], g[s:e], 0.7, h0=h0[n:n + 1],
+                                  cu_seqlens=torch.tensor([0, e - s]))
+        np.testing.assert_array_equal(on, o[s:e])
+        np.testing.assert_array_equal(hn[0], hT[n])
+    # the empty sequence keeps its initial state exactly
+    np.testing.assert_array_equal(hT[1], h0[1].double().numpy())
+
+
+def test_head_subset_matches_all_heads():
+    T, H = 40, 5
+    q, k, v, g, h0, cu = _rand_case(T, H, 8, 8, seed=2)
+    o, hT = oracle.recurrent(q, k, v, g, 0.2, h0=h0, cu_seqlens=cu)
+    heads = [4, 0, 2]
+    os_, hs = oracle.recurrent(q, k, v, g, 0.2, h0=h0, cu_seqlens=cu, heads=heads)
+    np.testing.assert_array_equal(os_, o[:, heads])
+    np.testing.assert_array_equal(hs, hT[:, heads])
+
+
+def test_decode_steps_equal_prefill():
+    """N one-token steps carried through the state equal one pass over the N tokens."""
+    T, H, dk, dv = 25, 2, 6, 5
+    q, k, v, g, h0, cu = _rand_case(T, H, dk, dv, seed=13)
+    o, hT = oracle.recurrent(q, k, v, g, 0.9, h0=h0, cu_seqlens=cu)
+    S = h0
+    for t in range(T):
+        ot, S = oracle.recurrent(q[t:t + 1], k[t:t + 1], v[t:t + 1], g[t:t + 1], 0.9, h0=S,
+                                 cu_seqlens=torch.tensor([0, 1]))
+        np.testing.assert_allclose(ot[0], o[t], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(S, hT, rtol=1e-13, atol=1e-15)
+
+
+def test_bf16_inputs_read_exactly():
+    """The oracle reads bf16 bit patterns exactly (no re-rounding): with one token, h0 = 0 and
+    g = 0, o = scale (q . k) v and hT = k^T v in fp64 from the bf16 values."""
+    vals = torch.tensor([[1.0 + 2 ** -7, -3.0, 2 ** -20]], dtype=torch.float32)
+    q = vals.to(torch.bfloat16).reshape(1, 1, 3)
+    k = torch.tensor([[0.5, 0.25, -1.0 - 2 ** -7]]).to(torch.bfloat16).reshape(1, 1, 3)
+    v = torch.tensor([[7.0, -2 ** -9]]).to(torch.bfloat16).reshape(1, 1, 2)
+    g = torch.zeros((1, 1))
+    o, hT = oracle.recurrent(q, k, v, g, 1.0)
+    qd, kd, vd = q.double().numpy()[0, 0], k.double().numpy()[0, 0], v.double().numpy()[0, 0]
+    assert o[0, 0, 0] == float(np.dot(qd, kd)) * vd[0]
+    np.testing.assert_array_equal(hT[0, 0], np.outer(kd, vd))
+
+
+def test_oracle_rejects_bad_arguments():
+    q = torch.zeros((4, 1, 2), dtype=torch.bfloat16)
+    g = torch.zeros((4, 1))
+    with pytest.raises(ValueError):
+        oracle.recurrent(q, q, q, g, 1.0, cu_seqlens=torch.tensor([0, 3, 2]))
+    with pytest.raises(ValueError):
+        oracle.recurrent(q, q, q, g, 1.0, heads=[1])

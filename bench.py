@@ -1,0 +1,483 @@
+#!/usr/bin/env python
+"""Benchmark of the Simple GLA hot path on GB300.
+
+Step = one chunked prefill (``sala_gla_chunk_fwd``) of the MiniCPM-SALA lightning-layer
+workload: B=1, T=8192, H=32, d=128, bf16 q/k/v with RMS-normalised q/k, fixed per-head
+log-decay g_h = -2^(-8(h+1)/32), h0 = 0, returning o and the final state. Inputs are synthetic
+and seeded, resident in HBM before the timed region; two input sets alternate between steps
+and each set (201 MB of q/k/v plus 67 MB of o) is larger than the 126 MB L2.
+
+Prints ONE JSON line (rank 0). Beside the headline prefill number it reports: the roofline
+of the dominant kernel (per-kernel CUDA-event time measured inside the timed region by the
+library's timing instrumentation), the end-to-end rate through the C ABI with host buffers
+(host->device copies of q/k/v/g and device->host copies of o/hT inside the timed region), the
+fp64 CPU oracle timed on the host cores on a bounded sample, the SM clocks sampled during the
+run, and the batched recurrent decode workload (256 sequences x 32 heads, 1000 consecutive
+steps on a 512 MB fp32 state updated in place) in GB/s against the HBM roofline.
+
+``--impl reference`` times the fp64 oracle instead (the reference arm of this benchmark).
+Multi-GPU (torchrun): every rank runs its own copy of the workload (weak scaling; prefill units
+are independent, no data-path collective); the timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prefill tokens/s (H=32,d=128) and decode HBM GB/s, as % of GB300 roofline"
+D = 128
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="sala_layer")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=p["hbm_gbs"], bf16_tflops=p["bf16_tflops"],
+                    bf16_tflops_sustained=p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                source="fallback")
+
+
+# ---------------------------------------------------------------------------------------
+# distributed plumbing (timing only: barriers and a max over ranks)
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64,
+                         device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64,
+                         device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------------------
+# clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+        self.t0 = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+            self.t0 = time.time()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), max=float(parts[2]),
+                                     power=float(parts[3]) if parts[3] not in ("[N/A]", "") else 0.0,
+                                     active=parts[4], hw=parts[5], hwt=parts[6], swt=parts[7],
+                                     pcap=parts[8]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        return rows
+
+
+def summarise_clocks(rows):
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+    # samples under load: the upper half by power draw
+    pw = sorted(r["power"] for r in rows)
+    cut = pw[len(pw) // 2] if pw else 0.0
+    loaded = [r for r in rows if r["power"] >= cut] or rows
+    reasons = set()
+    for r in loaded:
+        if r["hw"] == "Active":
+            reasons.add("hw_slowdown")
+        if r["hwt"] == "Active":
+            reasons.add("hw_thermal_slowdown")
+        if r["swt"] == "Active":
+            reasons.add("sw_thermal_slowdown")
+        if r["pcap"] == "Active":
+            reasons.add("sw_power_cap")
+    return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+            "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
+            "samples": len(loaded), "power_w_max": max(r["power"] for r in rows)}
+
+
+# ---------------------------------------------------------------------------------------
+# byte / flop accounting (algorithmic: each input read once, each output written once)
+
+
+def prefill_bytes(T, H, nseq, has_h0, has_hT):
+    per_token = H * (3 * D * 2 + 4 + D * 2)      # q, k, v bf16 + g fp32 + o bf16
+    state = nseq * H * D * D * 4
+    return T * per_token + (state if has_h0 else 0) + (state if has_hT else 0)
+
+
+def prefill_flops(T, H):
+    # causal intra-chunk QK^T and PV (2 d (C+1) per token), Q S and K^T V (2 d^2 each)
+    return T * H * (2 * D * (64 + 1) + 4 * D * D)
+
+
+def decode_bytes(N, H):
+    return N * H * (2 * D * D * 4 + 3 * D * 2 + 4 + D * 2)
+
+
+# ---------------------------------------------------------------------------------------
+# the oracle on the host cores (reference arm and CPU baseline)
+
+
+def oracle_sample_rate(x, tokens, reps=1):
+    """tokens/s of the fp64 oracle on the first `tokens` tokens (all heads) of workload x."""
+    import oracle
+    q, k, v, g = (x[n][:, :tokens] for n in ("q", "k", "v", "g"))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.recurrent(q, k, v, g, x["scale"], h0=None)
+    dt = time.perf_counter() - t0
+    return tokens * reps / dt, dt
+
+
+def cpu_baseline(x, target_s):
+    import oracle
+    T = x["q"].shape[1]
+    probe = min(T, 64)
+    _, dt = oracle_sample_rate(x, probe)
+    tokens = int(min(T, max(probe, probe * target_s / max(dt, 1e-6))))
+    tokens = max(64, (tokens // 64) * 64) if T >= 64 else T
+    rate, dt = oracle_sample_rate(x, tokens)
+    return {"value": rate, "unit": "tokens/s", "cores": oracle.default_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 recurrence, first {tokens} of {T} tokens x all {x['q'].shape[2]} "
+                      f"heads of the same workload ({dt:.1f} s)"}
+
+
+def run_reference(args, dist):
+    from gated_linear_attention_gb300 import inputs
+    import oracle
+    oracle.build()
+    if dist.rank != 0:
+        return
+    w = inputs.WORKLOADS[args.workload]
+    x = inputs.make_prefill(w)
+    tokens = min(w.T, 1024)
+    for _ in range(args.warmup):
+        oracle_sample_rate(x, tokens)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample_rate(x, tokens)
+    dt = time.perf_counter() - t0
+    value = tokens * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": 1, "T": w.T, "H": w.H, "d": D, "chunk": 64,
+                   "description": w.description},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.default_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: fp64 recurrence over the first {tokens} of "
+                                   f"{w.T} tokens x all {w.H} heads"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------
+# our arm
+
+
+def run_ours(args, dist):
+    import torch
+    torch.cuda.set_device(dist.local)
+    dist.init("nccl")
+    from gated_linear_attention_gb300 import build as libbuild
+    if dist.rank == 0:
+        libbuild.build()
+    dist.barrier()
+    from gated_linear_attention_gb300 import inputs, sala_gla
+    sala_gla.load()
+    peaks = load_peaks()
+    dev = torch.device("cuda", dist.local)
+    w = inputs.WORKLOADS[args.workload]
+    assert w.kind == "prefill"
+
+    # two input sets (the second with another seed), resident in HBM
+    host = inputs.make_prefill(w, seed=w.seed + 1000 * dist.rank)
+    alt = inputs.make_prefill(w, seed=w.seed + 1000 * dist.rank + 500)
+    sets = []
+    for x in (host, alt):
+        sets.append({n: (x[n].to(dev) if x[n] is not None else None)
+                     for n in ("q", "k", "v", "g", "h0", "cu_seqlens")})
+    T_total = host["q"].shape[0] * host["q"].shape[1] if host["q"].dim() == 4 else host["q"].shape[0]
+    nseq = len(w.seqlens)
+    outs = [(torch.empty_like(s["q"]), torch.empty((nseq, w.H, D, D), device=dev))
+            for s in sets]
+    scale = host["scale"]
+
+    def step(i):
+        s, (o, hT) = sets[i % 2], outs[i % 2]
+        sala_gla.chunk_fwd(s["q"], s["k"], s["v"], s["g"], scale, h0=s["h0"],
+                           cu_seqlens=s["cu_seqlens"], o=o, hT=hT)
+
+    clocks = ClockSampler(dist.local)
+    clocks.start()
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    assert sala_gla.get_device_status() == 0
+
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    sala_gla.timing_enable(True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    sala_gla.timing_enable(False)
+    ms = ev0.elapsed_time(ev1)
+    kern = sala_gla.timing_read()
+    ms_max = dist.max(ms)
+    tokens_all = dist.sum(T_total * args.steps)
+    value = tokens_all / (ms_max / 1e3)
+    launches = sum(n for _, n in kern.values())
+
+    # dominant kernel and its roofline (algorithmic bytes per launch / mean launch time)
+    top = max(kern.items(), key=lambda kv: kv[1][0])
+    top_name, (top_ms, top_n) = top
+    bytes_per_kernel = {
+        "output_pass": T_total * w.H * (3 * D * 2 + 4 + D * 2),
+        "state_pass": T_total * w.H * (2 * D * 2 + 4),
+    }
+    if top_name in bytes_per_kernel and top_n:
+        ach = bytes_per_kernel[top_name] / (top_ms / top_n / 1e3) / 1e9
+        roof = {"kernel": top_name, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                "peak_source": peaks["source"], "mean_launch_us": 1e3 * top_ms / top_n}
+    else:
+        roof = {"kernel": top_name, "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": None, "traffic": None}
+    step_bytes = prefill_bytes(T_total, w.H, nseq, host["h0"] is not None, True)
+    step_roof_rate = T_total / (step_bytes / (peaks["hbm_gbs"] * 1e9))
+    kernels = {k: {"ms_total": v[0], "launches": v[1],
+                   "us_per_launch": (1e3 * v[0] / v[1]) if v[1] else None}
+               for k, v in kern.items() if v[1]}
+
+    # end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hg = (host[n].pin_memory() for n in ("q", "k", "v", "g"))
+        ho = torch.empty(host["q"].shape, dtype=torch.bfloat16).pin_memory()
+        hh = torch.empty((nseq, w.H, D, D), dtype=torch.float32).pin_memory()
+        dq, dk, dv, dg = (torch.empty_like(t, device=dev) for t in (hq, hk, hv, hg))
+        do, dh = torch.empty_like(dq), torch.empty((nseq, w.H, D, D), device=dev)
+
+        def e2e_step():
+            for d_, h_ in ((dq, hq), (dk, hk), (dv, hv), (dg, hg)):
+                d_.copy_(h_, non_blocking=True)
+            sala_gla.chunk_fwd(dq, dk, dv, dg, scale, o=do, hT=dh)
+            ho.copy_(do, non_blocking=True)
+            hh.copy_(dh, non_blocking=True)
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        dist.barrier()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = dist.max(ev0.elapsed_time(ev1))
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg))
+        d2h = ho.numel() * 2 + hh.numel() * 4
+        e2e = {"value": tokens_all / (e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms / args.steps}
+        del dq, dk, dv, dg, do, dh
+
+    # batched recurrent decode: 1000 consecutive steps, state updated in place
+    decode = None
+    if not args.no_decode:
+        decode = run_decode(args, dist, dev, peaks, sala_gla, inputs)
+        launches_decode = decode.pop("_launches")
+    else:
+        launches_decode = 0
+
+    rows = clocks.stop()
+
+    cpu = None
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(host, args.cpu_seconds)
+
+    if dist.rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "B": 1, "T": w.T, "H": w.H, "d": D, "chunk": 64,
+                       "parallelism": f"replica x{dist.world} (independent prefills)",
+                       "l2": "inputs larger than L2 (201 MB q/k/v per set), two sets alternated",
+                       "description": w.description},
+            "roofline": roof,
+            "step_roofline": {"bytes_per_step": step_bytes,
+                              "roofline_tokens_per_s": step_roof_rate,
+                              "frac": (value / dist.world) / step_roof_rate},
+            "kernels": kernels,
+            "gpu_launches": launches,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": summarise_clocks(rows),
+            "decode": decode,
+            "gpu_launches_decode": launches_decode,
+        }
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+def run_decode(args, dist, dev, peaks, sala_gla, inputs):
+    import torch
+    w = inputs.WORKLOADS["decode"]
+    x = inputs.make_decode_steps(w)
+    S0 = inputs.make_decode_state(w)
+    q, k, v, g = (x[n].to(dev) for n in ("q", "k", "v", "g"))
+    S = S0.to(dev)
+    o = torch.empty_like(q[0])
+    scale = x["scale"]
+    # warm-up on a scratch copy of the state, then restore it
+    Sw = S.clone()
+    for s in range(max(3, args.warmup)):
+        sala_gla.recurrent_step(q[s], k[s], v[s], g[s], scale, Sw, o=o)
+    torch.cuda.synchronize()
+    del Sw
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    sala_gla.timing_enable(True)
+    ev0.record(stream)
+    for s in range(w.steps):
+        sala_gla.recurrent_step(q[s], k[s], v[s], g[s], scale, S, o=o)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sala_gla.timing_enable(False)
+    kern = sala_gla.timing_read()["recurrent_step"]
+    ms = dist.max(ev0.elapsed_time(ev1))
+    per_step = decode_bytes(w.nseq, w.H)
+    gbs = per_step * w.steps / (ms / 1e3) / 1e9 * dist.world
+    k_ach = per_step / (kern[0] / kern[1] / 1e3) / 1e9
+    return {
+        "metric": "decode HBM GB/s", "value": gbs, "unit": "GB/s",
+        "ms_per_step": ms / w.steps, "tokens_per_s": w.nseq * w.steps / (ms / 1e3) * dist.world,
+        "config": {"workload": w.name, "N": w.nseq, "H": w.H, "d": D, "steps": w.steps,
+                   "state_bytes": w.nseq * w.H * D * D * 4, "bytes_per_step": per_step},
+        "roofline": {"kernel": "recurrent_step", "bound": "hbm", "achieved": k_ach,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": k_ach / peaks["hbm_gbs"],
+                     "traffic": None, "peak_source": peaks["source"],
+                     "mean_launch_us": 1e3 * kern[0] / kern[1]},
+        "_launches": kern[1],
+    }
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    if args.impl == "reference":
+        if dist.rank != 0:
+            return
+        run_reference(args, dist)
+        return
+    run_ours(args, dist)
+
+
+if __name__ == "__main__":
+    main()

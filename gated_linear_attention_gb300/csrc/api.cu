@@ -1,0 +1,295 @@
+// C ABI of the sala_gla library: argument validation, per-device set-up, scratch and launch
+// order. Declarations and the contract of every entry point are in include/sala_gla.h.
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "launch.h"
+
+namespace sala {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Device-side status word (first error recorded by a kernel since the last query).
+__device__ int g_device_status;
+
+struct DeviceState {
+    std::once_flag once;
+    cudaError_t init_error = cudaSuccess;
+    bool supported = false;
+    int sm_count = 0;
+    int *status = nullptr;         // device address of g_device_status
+    cudaMemPool_t pool = nullptr;  // the library's own stream-ordered pool for scratch
+};
+DeviceState g_dev[kMaxDevices];
+
+DeviceState *device_state(int *err) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *err = SALA_ERR_CUDA;
+        return nullptr;
+    }
+    DeviceState &d = g_dev[dev];
+    std::call_once(d.once, [&d, dev]() {
+        cudaDeviceProp prop;
+        d.init_error = cudaGetDeviceProperties(&prop, dev);
+        if (d.init_error != cudaSuccess) return;
+        d.supported = prop.major == 10 && prop.minor == 3;
+        d.sm_count = prop.multiProcessorCount;
+        if (!d.supported) return;
+        d.init_error = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_device_status);
+        if (d.init_error != cudaSuccess) return;
+        // Scratch comes from a private pool that keeps its memory between calls (release
+        // threshold = unlimited), so steady-state calls do not map or unmap device memory.
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        d.init_error = cudaMemPoolCreate(&d.pool, &props);
+        if (d.init_error != cudaSuccess) return;
+        uint64_t keep = ~uint64_t(0);
+        d.init_error = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (d.init_error != cudaSuccess) return;
+        d.init_error = setup_simt_kernels();
+    });
+    if (d.init_error != cudaSuccess) {
+        *err = SALA_ERR_CUDA;
+        return nullptr;
+    }
+    if (!d.supported) {
+        *err = SALA_ERR_UNSUPPORTED;
+        return nullptr;
+    }
+    return &d;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Half-open byte ranges [a, a + na) and [b, b + nb) intersect (null or empty never does).
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Segment length (tokens, a multiple of 64) for a prefill of T tokens in nseq sequences and
+// H heads: aim at about `waves` units per SM so the state and output passes fill the GPU,
+// while keeping segments long (the per-segment scratch traffic is 256 KB per unit).
+int64_t choose_seg_len(int64_t T, int64_t H, int sm_count) {
+    const int64_t target_units = 4LL * sm_count;
+    int64_t chunks = ceil_div(T * H, kChunk * target_units);
+    if (chunks < 1) chunks = 1;
+    if (chunks > 256) chunks = 256;
+    return chunks * kChunk;
+}
+
+// ---- timing instrumentation -------------------------------------------------------------
+const char *const kKernelNames[kKernelCount] = {"seg_table", "state_pass", "segment_scan",
+                                                "output_pass", "recurrent_step"};
+struct TimingRecord {
+    int id;
+    cudaEvent_t start, stop;
+};
+std::atomic<bool> g_timing{false};
+std::mutex g_timing_mu;
+std::vector<TimingRecord> g_records;
+
+void clear_records_locked() {
+    for (auto &r : g_records) {
+        cudaEventDestroy(r.start);
+        cudaEventDestroy(r.stop);
+    }
+    g_records.clear();
+}
+
+}  // namespace
+
+LaunchTimer::LaunchTimer(KernelId id, cudaStream_t stream) : id_(id), stream_(stream) {
+    if (!g_timing.load(std::memory_order_relaxed)) return;
+    if (cudaEventCreate(&start_) != cudaSuccess) {
+        start_ = nullptr;
+        return;
+    }
+    if (cudaEventRecord(start_, stream_) != cudaSuccess) {
+        cudaEventDestroy(start_);
+        start_ = nullptr;
+    }
+}
+
+LaunchTimer::~LaunchTimer() {
+    if (!start_) return;
+    cudaEvent_t stop = nullptr;
+    if (cudaEventCreate(&stop) != cudaSuccess || cudaEventRecord(stop, stream_) != cudaSuccess) {
+        cudaEventDestroy(start_);
+        if (stop) cudaEventDestroy(stop);
+        return;
+    }
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    g_records.push_back({id_, start_, stop});
+}
+
+}  // namespace sala
+
+using namespace sala;
+
+extern "C" {
+
+const char *sala_gla_version(void) { return "0.1.0"; }
+
+int sala_gla_kernel_count(void) { return kKernelCount; }
+
+const char *sala_gla_kernel_name(int kernel) {
+    return (kernel >= 0 && kernel < kKernelCount) ? kKernelNames[kernel] : "unknown";
+}
+
+int sala_gla_timing_enable(int enable) {
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    if (enable) clear_records_locked();
+    g_timing.store(enable != 0);
+    return SALA_OK;
+}
+
+int sala_gla_timing_read(int kernel, double *total_ms, int64_t *launches) {
+    if (kernel < 0 || kernel >= kKernelCount || !total_ms || !launches) return SALA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    double sum = 0.0;
+    int64_t count = 0;
+    for (const auto &r : g_records) {
+        if (r.id != kernel) continue;
+        float ms = 0.f;
+        if (cudaEventSynchronize(r.stop) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess)
+            return SALA_ERR_CUDA;
+        sum += ms;
+        ++count;
+    }
+    *total_ms = sum;
+    *launches = count;
+    return SALA_OK;
+}
+
+const char *sala_gla_status_string(int status) {
+    switch (status) {
+    case SALA_OK: return "success";
+    case SALA_ERR_INVALID_ARG: return "invalid argument";
+    case SALA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case SALA_ERR_UNSUPPORTED: return "unsupported device (needs compute capability 10.3)";
+    case SALA_ERR_CUDA: return "CUDA runtime error";
+    case SALA_ERR_TIMEOUT: return "device-side wait timed out";
+    case SALA_ERR_BAD_SEQLENS: return "cu_seqlens is not monotone from 0 to T";
+    default: return "unknown status";
+    }
+}
+
+int sala_gla_get_device_status(void *stream) {
+    int err = SALA_OK;
+    DeviceState *d = device_state(&err);
+    if (!d) return err;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SALA_ERR_CUDA;
+    int value = 0, zero = 0;
+    if (cudaMemcpy(&value, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SALA_ERR_CUDA;
+    if (cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+        return SALA_ERR_CUDA;
+    return value;
+}
+
+int sala_gla_recurrent_step(const void *q, const void *k, const void *v, const float *g,
+                            float scale, float *S_inout, void *o, int64_t N, int32_t H,
+                            void *stream) {
+    if (N < 0 || H < 1) return SALA_ERR_INVALID_ARG;
+    if (N == 0) return SALA_OK;
+    if (N > (int64_t(1) << 31) / H) return SALA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !g || !S_inout || !o) return SALA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(S_inout) ||
+        !aligned16(o))
+        return SALA_ERR_MISALIGNED;
+    const size_t units = static_cast<size_t>(N) * H;
+    const size_t vec = units * kD * 2, gb = units * 4, sb = units * kD * kD * 4;
+    const void *ins[4] = {q, k, v, g};
+    const size_t in_sz[4] = {vec, vec, vec, gb};
+    for (int i = 0; i < 4; ++i)
+        if (overlaps(S_inout, sb, ins[i], in_sz[i]) || overlaps(o, vec, ins[i], in_sz[i]))
+            return SALA_ERR_INVALID_ARG;
+    if (overlaps(S_inout, sb, o, vec)) return SALA_ERR_INVALID_ARG;
+    int err = SALA_OK;
+    if (!device_state(&err)) return err;
+    if (launch_recurrent_step(q, k, v, g, scale, S_inout, o, static_cast<int64_t>(units),
+                              static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SALA_ERR_CUDA;
+    return SALA_OK;
+}
+
+int sala_gla_chunk_fwd(const void *q, const void *k, const void *v, const float *g, float scale,
+                       const float *h0, const int64_t *cu_seqlens, void *o, float *hT,
+                       int64_t B, int64_t T, int32_t H, int64_t num_seqs, void *stream) {
+    if (B < 1 || T < 0 || H < 1) return SALA_ERR_INVALID_ARG;
+    if (cu_seqlens && (B != 1 || num_seqs < 1)) return SALA_ERR_INVALID_ARG;
+    const int64_t nseq = cu_seqlens ? num_seqs : B;
+    const int64_t T_total = B * T;
+    if (T_total > (int64_t(1) << 40) || nseq > (int64_t(1) << 31)) return SALA_ERR_INVALID_ARG;
+    if (T_total > 0 && (!q || !k || !v || !g || !o)) return SALA_ERR_INVALID_ARG;
+    const void *al[7] = {q, k, v, g, o, h0, hT};
+    for (const void *p : al)
+        if (p && !aligned16(p)) return SALA_ERR_MISALIGNED;
+    if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 7u)) return SALA_ERR_MISALIGNED;
+    const size_t vec = static_cast<size_t>(T_total) * H * kD * 2, gb = static_cast<size_t>(T_total) * H * 4;
+    const size_t sb = static_cast<size_t>(nseq) * H * kD * kD * 4;
+    const void *ins[6] = {q, k, v, g, h0, cu_seqlens};
+    const size_t in_sz[6] = {vec, vec, vec, gb, h0 ? sb : 0, cu_seqlens ? size_t(nseq + 1) * 8 : 0};
+    for (int i = 0; i < 6; ++i)
+        if (overlaps(o, vec, ins[i], in_sz[i]) || overlaps(hT, sb, ins[i], in_sz[i]))
+            return SALA_ERR_INVALID_ARG;
+    if (overlaps(o, vec, hT, sb)) return SALA_ERR_INVALID_ARG;
+    if (!hT && T_total == 0) return SALA_OK;
+
+    int err = SALA_OK;
+    DeviceState *d = device_state(&err);
+    if (!d) return err;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    const int64_t seg_len = choose_seg_len(T_total, H, d->sm_count);
+    const int64_t max_segs = T_total / seg_len + nseq;  // sum of ceil(len/L) <= T/L + nseq
+    const int64_t max_units = max_segs * H;
+    if (max_units > (int64_t(1) << 31) - 1) return SALA_ERR_INVALID_ARG;
+
+    // scratch: segment table, per-(segment, head) decay and state
+    const size_t off_bytes = ((static_cast<size_t>(nseq) + 2) * 8 + 255) & ~size_t(255);
+    const size_t dec_bytes = (static_cast<size_t>(max_units) * 4 + 255) & ~size_t(255);
+    const size_t st_bytes = static_cast<size_t>(max_units) * kD * kD * 4;
+    char *ws = nullptr;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void **>(&ws), off_bytes + dec_bytes + st_bytes,
+                                d->pool, st) != cudaSuccess)
+        return SALA_ERR_CUDA;
+
+    SegTable tab;
+    tab.cu = cu_seqlens;
+    tab.T_row = T;
+    tab.nseq = nseq;
+    tab.seg_len = seg_len;
+    tab.seg_off = reinterpret_cast<int64_t *>(ws);
+    ChunkArgs a;
+    a.q = static_cast<const uint16_t *>(q);
+    a.k = static_cast<const uint16_t *>(k);
+    a.v = static_cast<const uint16_t *>(v);
+    a.g = g;
+    a.scale = scale;
+    a.o = static_cast<uint16_t *>(o);
+    a.H = H;
+    a.ws_decay = reinterpret_cast<float *>(ws + off_bytes);
+    a.ws_state = reinterpret_cast<float *>(ws + off_bytes + dec_bytes);
+
+    int rc = SALA_OK;
+    if (launch_seg_table(tab, T_total, d->status, st) != cudaSuccess ||
+        launch_state_pass(a, tab, max_units, st) != cudaSuccess ||
+        launch_segment_scan(tab, H, a.ws_state, a.ws_decay, h0, hT, st) != cudaSuccess ||
+        launch_output_pass(a, tab, max_units, st) != cudaSuccess)
+        rc = SALA_ERR_CUDA;
+    if (cudaFreeAsync(ws, st) != cudaSuccess) rc = SALA_ERR_CUDA;
+    return rc;
+}
+
+}  // extern "C"

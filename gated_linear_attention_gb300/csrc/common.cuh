@@ -1,0 +1,35 @@
+// Shared device helpers of the sala_gla library (not part of the public ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sala_gla.h"
+
+namespace sala {
+
+constexpr int kD = 128;     // head dimension (d_k = d_v)
+constexpr int kChunk = 64;  // chunk length of the chunked prefill
+
+// Record the first device-side error in the status word (later errors keep the first).
+__device__ __forceinline__ void record_status(int *status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Two bf16 in one 32-bit word -> two floats (low half is the lower address).
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Round two floats to nearest-even bf16 and pack them (x at the lower address).
+__device__ __forceinline__ uint32_t float2_to_bf16x2(float x, float y) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(x, y);
+    return *reinterpret_cast<uint32_t *>(&p);
+}
+
+}  // namespace sala

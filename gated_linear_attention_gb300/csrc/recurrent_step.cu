@@ -1,0 +1,94 @@
+// One-token recurrent decode of Simple GLA, state updated in place.
+//
+// "MiniCPM-SALA — Complete Blueprint", section "B2 lightning-attn (Simple GLA)", block
+// "Simple GLA Recurrence": per head, alpha = exp(g); S = alpha S; S += k^T (outer) v;
+// o = q S x scale; the updated state is saved back to where it was loaded from. The page
+// notes that the state read and write is the whole cost of this step ("Per-Token Decode
+// Bandwidth": GLA recurrence = state R/W), so the kernel is a single streaming pass over
+// the fp32 state: every byte of S is loaded once and stored once.
+//
+// Work split: one CTA of 256 threads (8 warps) per (sequence, head) unit. Warp w owns state
+// rows [16w, 16w + 16); lane l owns columns [4l, 4l + 4), so each warp instruction moves
+// one whole 512-byte row with 128-bit accesses. All 16 row loads of a thread are issued
+// before any arithmetic (64 KB in flight per CTA), with the streaming cache hint since the
+// state is touched exactly once per step. The q S reduction over rows is split: each thread
+// accumulates its 16 rows, then the 8 warp partials are summed through shared memory.
+#include "launch.h"
+
+namespace sala {
+
+constexpr int kDecodeThreads = 256;
+constexpr int kRowsPerWarp = kD / (kDecodeThreads / 32);  // 16
+
+__global__ void __launch_bounds__(kDecodeThreads)
+recurrent_step_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
+                      const uint16_t *__restrict__ v, const float *__restrict__ g, float scale,
+                      float *__restrict__ S, uint16_t *__restrict__ o) {
+    const int unit = blockIdx.x;  // n * H + h
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float *Su = S + static_cast<size_t>(unit) * kD * kD;
+    const int row0 = warp * kRowsPerWarp;
+
+    // 1. stream the state rows in (issued first: nothing depends on them yet)
+    float4 s[kRowsPerWarp];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r)
+        s[r] = __ldcs(reinterpret_cast<const float4 *>(Su + (row0 + r) * kD) + lane);
+
+    // 2. the token's q, k (for my rows) and v (for my columns)
+    __shared__ float q_s[kD], k_s[kD];
+    __shared__ float part[kDecodeThreads / 32][kD];
+    const size_t vec = static_cast<size_t>(unit) * kD;
+    if (threadIdx.x < kD) {
+        q_s[threadIdx.x] = bf16_bits_to_float(q[vec + threadIdx.x]);
+        k_s[threadIdx.x] = bf16_bits_to_float(k[vec + threadIdx.x]);
+    }
+    const uint2 vw = *reinterpret_cast<const uint2 *>(v + vec + 4 * lane);
+    const float2 v01 = bf16x2_to_float2(vw.x), v23 = bf16x2_to_float2(vw.y);
+    const float alpha = expf(g[unit]);
+    __syncthreads();
+
+    // 3. decay + rank-1 update, store back, and accumulate q S for my 4 columns
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        const float ki = k_s[row0 + r], qi = q_s[row0 + r];
+        float4 x = s[r];
+        x.x = fmaf(alpha, x.x, ki * v01.x);
+        x.y = fmaf(alpha, x.y, ki * v01.y);
+        x.z = fmaf(alpha, x.z, ki * v23.x);
+        x.w = fmaf(alpha, x.w, ki * v23.y);
+        __stcs(reinterpret_cast<float4 *>(Su + (row0 + r) * kD) + lane, x);
+        acc.x = fmaf(qi, x.x, acc.x);
+        acc.y = fmaf(qi, x.y, acc.y);
+        acc.z = fmaf(qi, x.z, acc.z);
+        acc.w = fmaf(qi, x.w, acc.w);
+    }
+    *reinterpret_cast<float4 *>(&part[warp][4 * lane]) = acc;
+    __syncthreads();
+
+    // 4. o_j = scale * sum over the 8 warp partials
+    if (threadIdx.x < kD / 2) {
+        const int j = 2 * threadIdx.x;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < kDecodeThreads / 32; ++w) {
+            a0 += part[w][j];
+            a1 += part[w][j + 1];
+        }
+        reinterpret_cast<uint32_t *>(o + vec)[threadIdx.x] = float2_to_bf16x2(scale * a0, scale * a1);
+    }
+}
+
+cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, const float *g,
+                                  float scale, float *S, void *o, int64_t units,
+                                  cudaStream_t stream) {
+    if (units == 0) return cudaSuccess;
+    LaunchTimer timer(kKRecurrentStep, stream);
+    recurrent_step_kernel<<<static_cast<unsigned>(units), kDecodeThreads, 0, stream>>>(
+        static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k),
+        static_cast<const uint16_t *>(v), g, scale, S, static_cast<uint16_t *>(o));
+    return cudaGetLastError();
+}
+
+}  // namespace sala

@@ -1,0 +1,196 @@
+"""ctypes binding of ``libsala_gla.so`` (argument marshalling only).
+
+Every function here checks shapes and dtypes, allocates outputs with torch when the caller
+did not pass them, and calls the C entry point of the same name on the current CUDA stream.
+All arithmetic runs in the library's kernels. If the library has not been built, importing
+this module raises: there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+_lib = None
+
+SALA_OK = 0
+STATUS_NAMES = {
+    0: "SALA_OK", 1: "SALA_ERR_INVALID_ARG", 2: "SALA_ERR_MISALIGNED",
+    3: "SALA_ERR_UNSUPPORTED", 4: "SALA_ERR_CUDA", 5: "SALA_ERR_TIMEOUT",
+    6: "SALA_ERR_BAD_SEQLENS",
+}
+
+# exported symbols and their ctypes signatures (must match include/sala_gla.h)
+_p, _i64, _i32, _f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+SIGNATURES = {
+    "sala_gla_chunk_fwd": ([_p, _p, _p, _p, _f32, _p, _p, _p, _p, _i64, _i64, _i32, _i64, _p],
+                           ctypes.c_int),
+    "sala_gla_recurrent_step": ([_p, _p, _p, _p, _f32, _p, _p, _i64, _i32, _p], ctypes.c_int),
+    "sala_gla_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "sala_gla_get_device_status": ([_p], ctypes.c_int),
+    "sala_gla_version": ([], ctypes.c_char_p),
+    "sala_gla_timing_enable": ([ctypes.c_int], ctypes.c_int),
+    "sala_gla_timing_read": ([ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                              ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
+    "sala_gla_kernel_count": ([], ctypes.c_int),
+    "sala_gla_kernel_name": ([ctypes.c_int], ctypes.c_char_p),
+}
+
+
+class SalaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({status_string(status)})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load the compiled library (raises OSError if it is missing)."""
+    global _lib
+    if _lib is None or path is not None:
+        p = path or _build.LIB
+        if not os.path.exists(p):
+            raise OSError(f"{p} not found: build it with gated_linear_attention_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        for name, (argtypes, restype) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = argtypes
+            fn.restype = restype
+        if path is not None:
+            return lib
+        _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().sala_gla_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return load().sala_gla_version().decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(rc: int, what: str):
+    if rc != SALA_OK:
+        raise SalaError(rc, what)
+
+
+def _need(t, name, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def chunk_fwd(q, k, v, g, scale, h0=None, cu_seqlens=None, output_final_state=True, o=None,
+              hT=None, stream=None):
+    """Chunked prefill, ``sala_gla_chunk_fwd``.
+
+    q, k, v: bf16 [B, T, H, 128] (or [1, T, H, 128] / [T, H, 128] packed with cu_seqlens);
+    g: fp32 [B, T, H] (or [T, H]); h0: fp32 [Nseq, H, 128, 128] or None; cu_seqlens: int64
+    CUDA tensor [Nseq + 1] or None. Returns (o, hT); hT is None unless output_final_state.
+    """
+    packed = q.dim() == 3
+    if packed:
+        if cu_seqlens is None:
+            raise ValueError("packed [T, H, 128] input needs cu_seqlens")
+        T, H, D = q.shape
+        B = 1
+    else:
+        B, T, H, D = q.shape
+    if D != 128:
+        raise ValueError("head dimension must be 128")
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16, q.shape)
+    _need(v, "v", torch.bfloat16, q.shape)
+    _need(g, "g", torch.float32, q.shape[:-1])
+    nseq = B
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int64)
+        if B != 1:
+            raise ValueError("cu_seqlens needs B == 1")
+        nseq = cu_seqlens.numel() - 1
+        if nseq < 1:
+            raise ValueError("cu_seqlens needs at least two entries")
+    if h0 is not None:
+        _need(h0, "h0", torch.float32, (nseq, H, 128, 128))
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _need(o, "o", torch.bfloat16, q.shape)
+    if output_final_state and hT is None:
+        hT = torch.empty((nseq, H, 128, 128), dtype=torch.float32, device=q.device)
+    elif hT is not None:
+        _need(hT, "hT", torch.float32, (nseq, H, 128, 128))
+    rc = load().sala_gla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), float(scale), _ptr(h0),
+                                   _ptr(cu_seqlens), _ptr(o), _ptr(hT), B, T, H,
+                                   nseq if cu_seqlens is not None else 0, _stream(stream))
+    _check(rc, "sala_gla_chunk_fwd")
+    return o, hT
+
+
+def recurrent_step(q, k, v, g, scale, S, o=None, stream=None):
+    """One decode step, ``sala_gla_recurrent_step``; S [N, H, 128, 128] fp32 is updated in
+    place. q, k, v: bf16 [N, H, 128]; g: fp32 [N, H]. Returns o (bf16 [N, H, 128])."""
+    N, H, D = q.shape
+    if D != 128:
+        raise ValueError("head dimension must be 128")
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16, q.shape)
+    _need(v, "v", torch.bfloat16, q.shape)
+    _need(g, "g", torch.float32, (N, H))
+    _need(S, "S", torch.float32, (N, H, 128, 128))
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _need(o, "o", torch.bfloat16, q.shape)
+    rc = load().sala_gla_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), float(scale),
+                                        _ptr(S), _ptr(o), N, H, _stream(stream))
+    _check(rc, "sala_gla_recurrent_step")
+    return o
+
+
+def get_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device-side status word."""
+    return int(load().sala_gla_get_device_status(_stream(stream)))
+
+
+def timing_enable(enable: bool = True) -> None:
+    """Start (clearing old records) or stop the per-kernel event timing."""
+    _check(load().sala_gla_timing_enable(1 if enable else 0), "sala_gla_timing_enable")
+
+
+def timing_read() -> dict:
+    """{kernel name: (total device ms, launches)} since the last timing_enable(True)."""
+    lib = load()
+    out = {}
+    for i in range(lib.sala_gla_kernel_count()):
+        ms, n = ctypes.c_double(), ctypes.c_int64()
+        _check(lib.sala_gla_timing_read(i, ctypes.byref(ms), ctypes.byref(n)),
+               "sala_gla_timing_read")
+        out[lib.sala_gla_kernel_name(i).decode()] = (ms.value, n.value)
+    return out

@@ -1,0 +1,144 @@
+/*
+ * sala_gla.h -- C ABI of the Simple GLA (Lightning attention) hot path on GB300 (sm_103a).
+ *
+ * The operation. Per sequence n and head h, with a [d_k x d_v] = [128 x 128] fp32 state S
+ * (row index = key dimension, column index = value dimension):
+ *
+ *     S_t = exp(g_t) * S_{t-1} + k_t^T v_t          (decay, then rank-1 update)
+ *     o_t = scale * q_t S_t                          (query reads the updated state)
+ *
+ * Source: "MiniCPM-SALA — Complete Blueprint", section "B2 lightning-attn (Simple GLA)",
+ * block "Simple GLA Recurrence" (decay by alpha = exp(g), add k^T (outer) v, read
+ * o = q S x 0.08839 = 1/sqrt(128)); the state is the recurrent memory held per request and
+ * layer ("Memory Architecture", MambaPool temporal states, written back after each step).
+ * The call shape (q, k, v, g, scale, initial state, whether to return the final state,
+ * packed sequences through cu_seqlens) follows the chunked/recurrent operator interface
+ * shown in "Formulas and Code for Adapting Inference to GDN/KDA Linear Modules", section 2.1.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library keeps none of
+ *     them after the call returns. Buffers must stay valid until the work queued on
+ *     `stream` has executed.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Work is
+ *     queued asynchronously; no call synchronises the host except
+ *     sala_gla_get_device_status().
+ *   - Layouts are row-major with the last index contiguous. bf16 is IEEE bfloat16 stored in
+ *     16-bit words. Every pointer must be 16-byte aligned.
+ *   - Head dimension is fixed at 128 for q, k and v.
+ *   - A call returns a sala_status. Argument errors are detected on the host before anything
+ *     is queued. Errors that only the device can see (malformed cu_seqlens contents) are
+ *     recorded in a per-device status word, the affected work is skipped, and
+ *     sala_gla_get_device_status() reports them.
+ *   - Entry points are thread-safe. Per-device one-time set-up (kernel attributes) happens
+ *     on the first call on that device.
+ */
+#ifndef SALA_GLA_H
+#define SALA_GLA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SALA_OK = 0,
+    SALA_ERR_INVALID_ARG = 1, /* null pointer where one is required, bad size, aliasing */
+    SALA_ERR_MISALIGNED = 2,  /* a pointer is not 16-byte aligned */
+    SALA_ERR_UNSUPPORTED = 3, /* device is not sm_103 / compute capability 10.3 */
+    SALA_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, allocation) */
+    SALA_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up */
+    SALA_ERR_BAD_SEQLENS = 6  /* device-detected: cu_seqlens not monotone or last != T */
+} sala_status;
+
+/*
+ * Chunked prefill (chunk size 64).
+ *
+ * Computes o and, optionally, the final state of every sequence, exactly as the recurrence
+ * above run token by token from h0. Internally the sequence is cut into 64-token chunks
+ * (intra-chunk causal (Q K^T * decay mask) V plus inter-chunk q S and the state carry;
+ * "Formulas and Code for Adapting Inference to GDN/KDA Linear Modules", section 1.2, taken
+ * without the delta rule) and the state is carried across chunks by a chunk-parallel state
+ * pass followed by an output pass.
+ *
+ *   q, k, v    bf16 [B, T, H, 128]. With cu_seqlens: B must be 1 and the T tokens hold the
+ *              num_seqs sequences packed back to back.
+ *   g          fp32 [B, T, H] per-token, per-head log-decay (<= 0 for a decaying state).
+ *   scale      output scale, typically 128^-0.5.
+ *   h0         fp32 [Nseq, H, 128, 128] initial states, or NULL for zeros. Nseq = B without
+ *              cu_seqlens, num_seqs with it.
+ *   cu_seqlens int64 [num_seqs + 1] DEVICE array of sequence offsets (0 = cu[0] <= cu[1]
+ *              <= ... <= cu[num_seqs] = T), or NULL. A sequence may be empty: its final
+ *              state is h0 (or zeros).
+ *   o          bf16 [B, T, H, 128] output (written; round to nearest even).
+ *   hT         fp32 [Nseq, H, 128, 128] final states, or NULL (not computed). hT may not
+ *              alias h0.
+ *   B, T, H    sizes; B >= 1, T >= 0, H >= 1. num_seqs >= 1 when cu_seqlens is given,
+ *              ignored otherwise.
+ *
+ * Scratch: the state pass needs per-segment states (64 KB per segment and head). They are
+ * taken from a stream-ordered memory pool that the library creates once per device
+ * (cudaMallocFromPoolAsync on `stream`) and returned to it when the call's work is done
+ * (cudaFreeAsync), so the host never waits. The pool keeps its memory for later calls.
+ * Errors: SALA_ERR_INVALID_ARG, SALA_ERR_MISALIGNED, SALA_ERR_UNSUPPORTED, SALA_ERR_CUDA.
+ */
+int sala_gla_chunk_fwd(const void *q, const void *k, const void *v, const float *g, float scale,
+                       const float *h0, const int64_t *cu_seqlens, void *o, float *hT,
+                       int64_t B, int64_t T, int32_t H, int64_t num_seqs, void *stream);
+
+/*
+ * One-token recurrent decode, state updated in place.
+ *
+ * For each of the N sequences and H heads: S = exp(g) S + k^T v; o = scale q S (the
+ * Blueprint page's decode step: load the state, decay, outer-product update, query, save
+ * the updated state back).
+ *
+ *   q, k, v    bf16 [N, H, 128]
+ *   g          fp32 [N, H]
+ *   S_inout    fp32 [N, H, 128, 128], read and overwritten with the updated states. Must not
+ *              overlap q, k, v, g or o.
+ *   o          bf16 [N, H, 128] output.
+ *   N, H       N >= 0 (0 is a no-op), H >= 1.
+ * Errors: SALA_ERR_INVALID_ARG, SALA_ERR_MISALIGNED, SALA_ERR_UNSUPPORTED, SALA_ERR_CUDA.
+ */
+int sala_gla_recurrent_step(const void *q, const void *k, const void *v, const float *g,
+                            float scale, float *S_inout, void *o, int64_t N, int32_t H,
+                            void *stream);
+
+/* Static English description of a sala_status value (never NULL). */
+const char *sala_gla_status_string(int status);
+
+/*
+ * Synchronises `stream`, then returns and clears the device-side status word of the current
+ * device (SALA_OK if no kernel recorded an error since the last call). Returns SALA_ERR_CUDA
+ * if the synchronisation itself fails.
+ */
+int sala_gla_get_device_status(void *stream);
+
+/* Library version, "major.minor.patch". */
+const char *sala_gla_version(void);
+
+/*
+ * Kernel timing instrumentation (off by default; process-wide).
+ *
+ * While enabled, every kernel the library launches is bracketed by a pair of CUDA events
+ * recorded on the launching stream, so per-kernel device time is measured in place, inside
+ * the caller's own timed region. The kernels are identified by an index in
+ * [0, sala_gla_kernel_count()); sala_gla_kernel_name() names them.
+ *
+ * sala_gla_timing_enable(1) clears earlier records and starts recording; (0) stops.
+ * sala_gla_timing_read() waits for the recorded events, then stores the summed device time
+ * in milliseconds and the number of launches of kernel `kernel` since the last enable.
+ * Returns SALA_ERR_INVALID_ARG for an unknown index or null outputs, SALA_ERR_CUDA if an
+ * event query fails.
+ */
+int sala_gla_timing_enable(int enable);
+int sala_gla_timing_read(int kernel, double *total_ms, int64_t *launches);
+int sala_gla_kernel_count(void);
+const char *sala_gla_kernel_name(int kernel);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SALA_GLA_H */

@@ -1,0 +1,135 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads, exports every
+symbol that include/sala_gla.h declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from gated_linear_attention_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+no_gpu = pytest.mark.skipif(torch.cuda.is_available(),
+                            reason="fake pointers must never reach a real device")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = B.build()
+    from gated_linear_attention_gb300 import sala_gla
+    return sala_gla.load()
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(sala_gla_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("sala_gla_chunk_fwd", "sala_gla_recurrent_step", "sala_gla_status_string",
+              "sala_gla_get_device_status", "sala_gla_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_every_declared_symbol():
+    from gated_linear_attention_gb300 import sala_gla
+    assert sorted(sala_gla.SIGNATURES) == declared_functions()
+
+
+def test_library_is_sm103a_only_and_links_cudart_statically(lib):
+    with open(B.LIB, "rb") as f:
+        blob = f.read()
+    # a statically linked runtime: no dynamic dependency on libcudart
+    import subprocess
+    out = subprocess.run(["ldd", B.LIB], capture_output=True, text=True).stdout
+    assert "libcudart" not in out
+    assert b"sm_103a" in blob or b"sm_103" in blob
+
+
+def test_status_strings(lib):
+    from gated_linear_attention_gb300 import sala_gla
+    assert sala_gla.status_string(0) == "success"
+    for s in range(1, 7):
+        assert sala_gla.status_string(s) not in ("", "unknown status")
+    assert sala_gla.status_string(99) == "unknown status"
+    assert sala_gla.version().count(".") == 2
+
+
+P = ctypes.c_void_p
+
+
+def _chunk(lib, q=0x10000, k=0x20000, v=0x30000, g=0x40000, h0=None, cu=None, o=0x50000,
+           hT=0x60000, Bn=1, T=64, H=2, nseq=0):
+    return lib.sala_gla_chunk_fwd(P(q), P(k), P(v), P(g), 0.1, P(h0) if h0 else None,
+                                  P(cu) if cu else None, P(o), P(hT) if hT else None,
+                                  Bn, T, H, nseq, None)
+
+
+def _step(lib, q=0x10000, k=0x20000, v=0x30000, g=0x40000, S=0x100000, o=0x50000, N=2, H=2):
+    return lib.sala_gla_recurrent_step(P(q), P(k), P(v), P(g), 0.1, P(S), P(o), N, H, None)
+
+
+@no_gpu
+def test_chunk_fwd_argument_errors(lib):
+    INVALID, MISALIGNED = 1, 2
+    # sizes far apart so that only the intended overlap exists: T*H*128*2 = 32 KB per tensor
+    assert _chunk(lib, Bn=0) == INVALID
+    assert _chunk(lib, T=-1) == INVALID
+    assert _chunk(lib, H=0) == INVALID
+    assert _chunk(lib, q=0) == INVALID
+    assert _chunk(lib, o=0) == INVALID
+    assert _chunk(lib, cu=0x70000, nseq=0) == INVALID         # cu_seqlens needs num_seqs >= 1
+    assert _chunk(lib, cu=0x70000, nseq=2, Bn=2) == INVALID   # and B == 1
+    assert _chunk(lib, q=0x10008) == MISALIGNED
+    assert _chunk(lib, hT=0x60004) == MISALIGNED
+    assert _chunk(lib, h0=0x80002) == MISALIGNED
+    assert _chunk(lib, cu=0x70004, nseq=1) == MISALIGNED
+    assert _chunk(lib, o=0x10000 + 16) == INVALID              # o overlaps q
+    assert _chunk(lib, hT=0x30000) == INVALID                  # hT overlaps v
+    assert _chunk(lib, h0=0x60000) == INVALID                  # hT aliases h0
+    # T = 0 and no hT: nothing to do
+    assert _chunk(lib, T=0, hT=None) == 0
+
+
+@no_gpu
+def test_recurrent_step_argument_errors(lib):
+    INVALID, MISALIGNED = 1, 2
+    assert _step(lib, N=-1) == INVALID
+    assert _step(lib, H=0) == INVALID
+    assert _step(lib, N=0) == 0                                # empty batch is a no-op
+    assert _step(lib, S=0) == INVALID
+    assert _step(lib, g=0x40001) == MISALIGNED
+    assert _step(lib, S=0x100000, o=0x100000 + 1024) == INVALID   # o inside S
+    assert _step(lib, S=0x10000) == INVALID                        # S overlaps q
+
+
+@no_gpu
+def test_valid_arguments_without_a_gpu_report_cuda_error(lib):
+    # validation passes, then the runtime finds no device: nothing is launched
+    assert _chunk(lib) == 4
+    assert _step(lib) == 4
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    from gated_linear_attention_gb300 import sala_gla
+    q = torch.zeros((1, 4, 1, 128), dtype=torch.bfloat16)
+    g = torch.zeros((1, 4, 1))
+    with pytest.raises(ValueError):
+        sala_gla.chunk_fwd(q, q, q, g, 0.1)
+    with pytest.raises(ValueError):
+        sala_gla.recurrent_step(q[0], q[0], q[0], g[0], 0.1,
+                                torch.zeros((4, 1, 128, 128)))

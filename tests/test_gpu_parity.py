@@ -1,0 +1,319 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Tolerances: relative Frobenius error <= 1e-2 for outputs o (bf16) and <= 5e-3 for final
+states hT (fp32), over whole tensors, on identical seeded inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_linear_attention_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 1e-2
+S_TOL = 5e-3
+
+
+@pytest.fixture(scope="module")
+def sg():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from gated_linear_attention_gb300 import build, sala_gla
+    build.build()
+    return sala_gla
+
+
+def _cuda(x):
+    return None if x is None else x.cuda()
+
+
+def run_prefill(sg, x, output_final_state=True):
+    cu = _cuda(x["cu_seqlens"])
+    o, hT = sg.chunk_fwd(_cuda(x["q"]), _cuda(x["k"]), _cuda(x["v"]), _cuda(x["g"]),
+                         x["scale"], h0=_cuda(x["h0"]), cu_seqlens=cu,
+                         output_final_state=output_final_state)
+    torch.cuda.synchronize()
+    assert sg.get_device_status() == 0
+    return o.cpu(), None if hT is None else hT.cpu()
+
+
+def ref_prefill(x, heads=None, want_o=True):
+    return oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["scale"], h0=x["h0"],
+                            cu_seqlens=x["cu_seqlens"], heads=heads, want_o=want_o)
+
+
+def _flat(o):
+    """[B, T, H, d] or [T, H, d] -> [B*T, H, d]"""
+    return o.reshape(-1, o.shape[-2], o.shape[-1])
+
+
+def check(o, hT, o_ref, h_ref, heads=None):
+    of = _flat(o).float()
+    if heads is not None:
+        of = of[:, heads]
+    eo = oracle.rel_fro(of, o_ref)
+    assert eo <= O_TOL, f"output rel err {eo:.3e}"
+    if h_ref is not None:
+        hs = hT if heads is None else hT[:, heads]
+        eh = oracle.rel_fro(hs, h_ref)
+        assert eh <= S_TOL, f"state rel err {eh:.3e}"
+        return eo, eh
+    return eo, None
+
+
+def small(seqlens, H=4, gate="logsigmoid", h0=True, seed=0, qk="l2"):
+    w = inputs.Workload("case", "prefill", H=H, seqlens=tuple(seqlens), qk_norm=qk, gate=gate,
+                        h0=h0, seed=seed, varlen=len(seqlens) > 1)
+    return inputs.make_prefill(w)
+
+
+# ---------------------------------------------------------------------------------------
+# prefill: small and ragged shapes
+
+
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 127, 128, 200, 1000])
+def test_prefill_ragged_lengths(sg, T):
+    x = small([T], H=3, seed=T)
+    o, hT = run_prefill(sg, x)
+    check(o, hT, *ref_prefill(x))
+
+
+def test_prefill_tiny_workload(sg):
+    x = inputs.make_prefill("tiny")
+    o, hT = run_prefill(sg, x)
+    check(o, hT, *ref_prefill(x))
+
+
+@pytest.mark.parametrize("lens", [[0, 5, 1, 64, 0, 130], [1, 1, 1], [700, 0], [64] * 9,
+                                  [3000, 17, 2500]])
+def test_prefill_varlen_with_empty_and_short(sg, lens):
+    x = small(lens, H=2, seed=len(lens))
+    o, hT = run_prefill(sg, x)
+    o_ref, h_ref = ref_prefill(x)
+    check(o, hT, o_ref, h_ref)
+    # empty sequences return h0 exactly
+    for n, L in enumerate(lens):
+        if L == 0:
+            assert torch.equal(hT[n], x["h0"][n])
+
+
+def test_prefill_batched_rows(sg):
+    # B = 3 rows of T = 100 without cu_seqlens
+    x = small([100], H=2, seed=3)
+    w = inputs.Workload("b3", "prefill", H=2, seqlens=(300,), qk_norm="l2", gate="logsigmoid",
+                        h0=False, seed=5)
+    y = inputs.make_prefill(w)
+    q, k, v, g = (y[n].reshape(3, 100, *y[n].shape[2:]) for n in ("q", "k", "v", "g"))
+    h0 = torch.randn((3, 2, 128, 128)) * 0.02
+    xb = dict(q=q, k=k, v=v, g=g, h0=h0, cu_seqlens=None, scale=x["scale"])
+    o, hT = run_prefill(sg, xb)
+    check(o, hT, *ref_prefill(xb))
+
+
+@pytest.mark.parametrize("H", [1, 3, 32])
+def test_prefill_head_counts(sg, H):
+    x = small([333], H=H, seed=H, qk="rms", gate="const")
+    o, hT = run_prefill(sg, x)
+    check(o, hT, *ref_prefill(x))
+
+
+def test_prefill_g_zero(sg):
+    x = small([500], H=2, seed=9)
+    x["g"] = torch.zeros_like(x["g"])
+    o, hT = run_prefill(sg, x)
+    check(o, hT, *ref_prefill(x))
+
+
+def test_prefill_g_very_negative(sg):
+    x = small([300], H=2, seed=10)
+    x["g"] = torch.full_like(x["g"], -30.0)
+    o, hT = run_prefill(sg, x)
+    check(o, hT, *ref_prefill(x))
+
+
+def test_prefill_h0_only(sg):
+    x = small([200], H=2, seed=11)
+    x["k"] = torch.zeros_like(x["k"])
+    x["v"] = torch.zeros_like(x["v"])
+    o, hT = run_prefill(sg, x)
+    check(o, hT, *ref_prefill(x))
+
+
+def test_prefill_without_final_state(sg):
+    x = small([150], H=2, seed=12)
+    o, hT = run_prefill(sg, x, output_final_state=False)
+    assert hT is None
+    o_ref, _ = ref_prefill(x)
+    check(o, None, o_ref, None)
+
+
+def test_prefill_zero_tokens_returns_h0(sg):
+    x = small([0, 0], H=2, seed=13)
+    o, hT = run_prefill(sg, x)
+    assert torch.equal(hT, x["h0"])
+
+
+# ---------------------------------------------------------------------------------------
+# invariants of the CUDA path
+
+
+def test_split_call_equals_single_call(sg):
+    x = small([777], H=2, seed=21)
+    o, hT = run_prefill(sg, x)
+    cut = 300
+    a = {n: x[n][:, :cut] for n in ("q", "k", "v", "g")}
+    b = {n: x[n][:, cut:].contiguous() for n in ("q", "k", "v", "g")}
+    o1, h1 = run_prefill(sg, dict(a, h0=x["h0"], cu_seqlens=None, scale=x["scale"]))
+    o2, h2 = run_prefill(sg, dict(b, h0=h1, cu_seqlens=None, scale=x["scale"]))
+    o12 = torch.cat([o1, o2], dim=1)
+    assert oracle.rel_fro(o12.float(), o.float()) < 5e-3
+    assert oracle.rel_fro(h2, hT) < 2e-3
+
+
+def test_packed_equals_separate_calls(sg):
+    lens = [100, 257, 64]
+    x = small(lens, H=2, seed=22)
+    o, hT = run_prefill(sg, x)
+    cu = x["cu_seqlens"].tolist()
+    for n in range(len(lens)):
+        s, e = cu[n], cu[n + 1]
+        one = {k: x[k][s:e].unsqueeze(0).contiguous() for k in ("q", "k", "v", "g")}
+        on, hn = run_prefill(sg, dict(one, h0=x["h0"][n:n + 1].contiguous(), cu_seqlens=None,
+                                      scale=x["scale"]))
+        assert oracle.rel_fro(on[0].float(), o[s:e].float()) < 5e-3
+        assert oracle.rel_fro(hn[0], hT[n]) < 2e-3
+
+
+def test_one_token_prefill_equals_decode_step(sg):
+    x = small([1] * 6, H=4, seed=23)
+    o, hT = run_prefill(sg, x)
+    S = x["h0"].cuda().clone()
+    od = sg.recurrent_step(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["g"].cuda(),
+                           x["scale"], S)
+    torch.cuda.synchronize()
+    assert oracle.rel_fro(od.cpu().float(), o.float()) < 5e-3
+    assert oracle.rel_fro(S.cpu(), hT) < 1e-5
+
+
+def test_decode_steps_equal_prefill(sg):
+    steps, N, H = 40, 3, 2
+    x = inputs.make_decode_steps("decode", 0, steps, nseq=N, H=H)
+    S0 = inputs.make_decode_state("decode", nseq=N, H=H)
+    S = S0.cuda().clone()
+    outs = []
+    for s in range(steps):
+        outs.append(sg.recurrent_step(x["q"][s].cuda(), x["k"][s].cuda(), x["v"][s].cuda(),
+                                      x["g"][s].cuda(), x["scale"], S))
+    od = torch.stack(outs).cpu()                       # [steps, N, H, 128]
+    # the same tokens as N packed sequences of `steps` tokens
+    q = x["q"].transpose(0, 1).reshape(N * steps, H, 128).contiguous()
+    k = x["k"].transpose(0, 1).reshape(N * steps, H, 128).contiguous()
+    v = x["v"].transpose(0, 1).reshape(N * steps, H, 128).contiguous()
+    g = x["g"].transpose(0, 1).reshape(N * steps, H).contiguous()
+    cu = torch.arange(N + 1, dtype=torch.int64) * steps
+    o, hT = run_prefill(sg, dict(q=q, k=k, v=v, g=g, h0=S0, cu_seqlens=cu, scale=x["scale"]))
+    assert oracle.rel_fro(od.transpose(0, 1).reshape(N * steps, H, 128).float(), o.float()) < 5e-3
+    assert oracle.rel_fro(S.cpu(), hT) < 2e-3
+
+
+# ---------------------------------------------------------------------------------------
+# decode
+
+
+@pytest.mark.parametrize("N,H,steps", [(1, 1, 1), (5, 3, 7), (64, 32, 3)])
+def test_decode_small(sg, N, H, steps):
+    x = inputs.make_decode_steps("decode", 0, steps, nseq=N, H=H)
+    S0 = inputs.make_decode_state("decode", nseq=N, H=H)
+    S = S0.cuda().clone()
+    outs = []
+    for s in range(steps):
+        outs.append(sg.recurrent_step(x["q"][s].cuda(), x["k"][s].cuda(), x["v"][s].cuda(),
+                                      x["g"][s].cuda(), x["scale"], S).cpu())
+    torch.cuda.synchronize()
+    q = x["q"].transpose(0, 1).reshape(N * steps, H, 128).contiguous()
+    k = x["k"].transpose(0, 1).reshape(N * steps, H, 128).contiguous()
+    v = x["v"].transpose(0, 1).reshape(N * steps, H, 128).contiguous()
+    g = x["g"].transpose(0, 1).reshape(N * steps, H).contiguous()
+    cu = torch.arange(N + 1, dtype=torch.int64) * steps
+    o_ref, h_ref = oracle.recurrent(q, k, v, g, x["scale"], h0=S0, cu_seqlens=cu)
+    od = torch.stack(outs).transpose(0, 1).reshape(N * steps, H, 128)
+    assert oracle.rel_fro(od.float(), o_ref) <= O_TOL
+    assert oracle.rel_fro(S.cpu(), h_ref) <= S_TOL
+
+
+def test_decode_empty_batch_is_noop(sg):
+    z = torch.zeros((0, 2, 128), dtype=torch.bfloat16, device="cuda")
+    S = torch.zeros((0, 2, 128, 128), device="cuda")
+    o = sg.recurrent_step(z, z, z, torch.zeros((0, 2), device="cuda"), 0.1, S)
+    assert o.shape == (0, 2, 128)
+
+
+# ---------------------------------------------------------------------------------------
+# device-side validation of cu_seqlens
+
+
+@pytest.mark.parametrize("cu", [[0, 50, 30, 100], [0, 40, 90], [5, 40, 100]])
+def test_bad_cu_seqlens_reported_and_skipped(sg, cu):
+    x = small([100], H=2, seed=31)
+    q, k, v = (x[n][0].cuda() for n in ("q", "k", "v"))
+    g = x["g"][0].cuda()
+    cu_t = torch.tensor(cu, dtype=torch.int64, device="cuda")
+    o = torch.full_like(q, 7.0)
+    hT = torch.full((len(cu) - 1, 2, 128, 128), 3.0, device="cuda")
+    sg.chunk_fwd(q, k, v, g, x["scale"], cu_seqlens=cu_t, o=o, hT=hT)
+    assert sg.get_device_status() == 6          # SALA_ERR_BAD_SEQLENS
+    assert sg.get_device_status() == 0          # cleared by the first query
+    assert torch.all(o == 7.0) and torch.all(hT == 3.0)   # nothing written
+
+
+# ---------------------------------------------------------------------------------------
+# full-size workloads, in the configuration the benchmark times
+
+
+def test_full_sala_layer(sg):
+    x = inputs.make_prefill("sala_layer")
+    o, hT = run_prefill(sg, x)
+    check(o, hT, *ref_prefill(x))
+
+
+def test_full_varlen(sg):
+    x = inputs.make_prefill("varlen")
+    o, hT = run_prefill(sg, x)
+    heads = [0, 5, 17, 31]
+    o_ref, _ = ref_prefill(x, heads=heads)
+    _, h_ref = ref_prefill(x, want_o=False)
+    check(o, hT, o_ref, None, heads=heads)
+    assert oracle.rel_fro(hT, h_ref) <= S_TOL
+
+
+def test_full_long(sg):
+    x = inputs.make_prefill("long")
+    o, hT = run_prefill(sg, x)
+    heads = [0, 13, 31]
+    o_ref, _ = ref_prefill(x, heads=heads)
+    _, h_ref = ref_prefill(x, want_o=False)
+    check(o, hT, o_ref, None, heads=heads)
+    assert oracle.rel_fro(hT, h_ref) <= S_TOL
+
+
+def test_full_decode_sampled_sequences(sg):
+    w = inputs.WORKLOADS["decode"]
+    x = inputs.make_decode_steps(w)
+    S0 = inputs.make_decode_state(w)
+    S = S0.cuda()
+    qd, kd, vd, gd = x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["g"].cuda()
+    o_all = torch.empty_like(qd)
+    for s in range(w.steps):
+        sg.recurrent_step(qd[s], kd[s], vd[s], gd[s], x["scale"], S, o=o_all[s])
+    torch.cuda.synchronize()
+    seqs = [0, 77, 200, 255]
+    N, H = len(seqs), w.H
+    sel = lambda t: t[:, seqs].transpose(0, 1).reshape(N * w.steps, *t.shape[2:]).contiguous()
+    cu = torch.arange(N + 1, dtype=torch.int64) * w.steps
+    o_ref, h_ref = oracle.recurrent(sel(x["q"]), sel(x["k"]), sel(x["v"]), sel(x["g"]),
+                                    x["scale"], h0=S0[seqs], cu_seqlens=cu)
+    od = o_all[:, seqs].cpu().transpose(0, 1).reshape(N * w.steps, H, 128)
+    assert oracle.rel_fro(od.float(), o_ref) <= O_TOL
+    assert oracle.rel_fro(S[seqs].cpu(), h_ref) <= S_TOL

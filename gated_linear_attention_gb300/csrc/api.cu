@@ -107,6 +107,10 @@ void clear_records_locked() {
 
 }  // namespace
 
+cudaError_t device_status_address(int **out) {
+    return cudaGetSymbolAddress(reinterpret_cast<void **>(out), g_device_status);
+}
+
 LaunchTimer::LaunchTimer(KernelId id, cudaStream_t stream) : id_(id), stream_(stream) {
     if (!g_timing.load(std::memory_order_relaxed)) return;
     if (cudaEventCreate(&start_) != cudaSuccess) {
@@ -180,6 +184,8 @@ const char *sala_gla_status_string(int status) {
     case SALA_ERR_CUDA: return "CUDA runtime error";
     case SALA_ERR_TIMEOUT: return "device-side wait timed out";
     case SALA_ERR_BAD_SEQLENS: return "cu_seqlens is not monotone from 0 to T";
+    case SALA_ERR_TOO_LARGE:
+        return "problem needs more scratch than the no-allocation entry point's fixed buffer";
     default: return "unknown status";
     }
 }

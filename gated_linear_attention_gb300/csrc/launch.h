@@ -29,6 +29,9 @@ class LaunchTimer {
     cudaEvent_t start_ = nullptr;
 };
 
+// Device address of the library's status word on the current device.
+cudaError_t device_status_address(int **out);
+
 cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, const float *g,
                                   float scale, float *S, void *o, int64_t units,
                                   cudaStream_t stream);

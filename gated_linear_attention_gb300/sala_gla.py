@@ -20,7 +20,7 @@ SALA_OK = 0
 STATUS_NAMES = {
     0: "SALA_OK", 1: "SALA_ERR_INVALID_ARG", 2: "SALA_ERR_MISALIGNED",
     3: "SALA_ERR_UNSUPPORTED", 4: "SALA_ERR_CUDA", 5: "SALA_ERR_TIMEOUT",
-    6: "SALA_ERR_BAD_SEQLENS",
+    6: "SALA_ERR_BAD_SEQLENS", 7: "SALA_ERR_TOO_LARGE",
 }
 
 # exported symbols and their ctypes signatures (must match include/sala_gla.h)
@@ -29,6 +29,8 @@ SIGNATURES = {
     "sala_gla_chunk_fwd": ([_p, _p, _p, _p, _f32, _p, _p, _p, _p, _i64, _i64, _i32, _i64, _p],
                            ctypes.c_int),
     "sala_gla_recurrent_step": ([_p, _p, _p, _p, _f32, _p, _p, _i64, _i32, _p], ctypes.c_int),
+    "sala_gla_chunk_fwd_noalloc": ([_p, _p, _p, _p, _f32, _p, _p, _p, _p, _i64, _i64, _i32,
+                                    _i64, _p], ctypes.c_int),
     "sala_gla_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "sala_gla_get_device_status": ([_p], ctypes.c_int),
     "sala_gla_version": ([], ctypes.c_char_p),
@@ -107,8 +109,9 @@ def _need(t, name, dtype, shape=None):
 
 
 def chunk_fwd(q, k, v, g, scale, h0=None, cu_seqlens=None, output_final_state=True, o=None,
-              hT=None, stream=None):
-    """Chunked prefill, ``sala_gla_chunk_fwd``.
+              hT=None, stream=None, noalloc=False):
+    """Chunked prefill, ``sala_gla_chunk_fwd`` (``sala_gla_chunk_fwd_noalloc`` when
+    ``noalloc``: scratch from the library's fixed 64 MiB device array instead of a pool).
 
     q, k, v: bf16 [B, T, H, 128] (or [1, T, H, 128] / [T, H, 128] packed with cu_seqlens);
     g: fp32 [B, T, H] (or [T, H]); h0: fp32 [Nseq, H, 128, 128] or None; cu_seqlens: int64
@@ -146,10 +149,11 @@ def chunk_fwd(q, k, v, g, scale, h0=None, cu_seqlens=None, output_final_state=Tr
         hT = torch.empty((nseq, H, 128, 128), dtype=torch.float32, device=q.device)
     elif hT is not None:
         _need(hT, "hT", torch.float32, (nseq, H, 128, 128))
-    rc = load().sala_gla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), float(scale), _ptr(h0),
-                                   _ptr(cu_seqlens), _ptr(o), _ptr(hT), B, T, H,
-                                   nseq if cu_seqlens is not None else 0, _stream(stream))
-    _check(rc, "sala_gla_chunk_fwd")
+    lib = load()
+    fn = lib.sala_gla_chunk_fwd_noalloc if noalloc else lib.sala_gla_chunk_fwd
+    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), float(scale), _ptr(h0), _ptr(cu_seqlens), _ptr(o),
+            _ptr(hT), B, T, H, nseq if cu_seqlens is not None else 0, _stream(stream))
+    _check(rc, "sala_gla_chunk_fwd_noalloc" if noalloc else "sala_gla_chunk_fwd")
     return o, hT
 
 

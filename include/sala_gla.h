@@ -48,7 +48,8 @@ typedef enum {
     SALA_ERR_UNSUPPORTED = 3, /* device is not sm_103 / compute capability 10.3 */
     SALA_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, allocation) */
     SALA_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up */
-    SALA_ERR_BAD_SEQLENS = 6  /* device-detected: cu_seqlens not monotone or last != T */
+    SALA_ERR_BAD_SEQLENS = 6, /* device-detected: cu_seqlens not monotone or last != T */
+    SALA_ERR_TOO_LARGE = 7    /* sala_gla_chunk_fwd_noalloc: problem exceeds its fixed scratch */
 } sala_status;
 
 /*
@@ -104,6 +105,34 @@ int sala_gla_chunk_fwd(const void *q, const void *k, const void *v, const float 
 int sala_gla_recurrent_step(const void *q, const void *k, const void *v, const float *g,
                             float scale, float *S_inout, void *o, int64_t N, int32_t H,
                             void *stream);
+
+/*
+ * Chunked prefill that allocates nothing: same arguments, layouts, results and errors as
+ * sala_gla_chunk_fwd, plus SALA_ERR_TOO_LARGE. The pages have no counterpart to this entry
+ * point; it exists for callers that cannot allocate device memory while they run the layer:
+ * serving engines that reserve nearly all of HBM for their own pools at start-up (so any
+ * further allocation fails), plug-in hosts whose execute path forbids allocation, and
+ * latency-critical loops that cannot afford an allocator call, which may synchronise.
+ *
+ * Its scratch (segment table, per-segment states and decays) lives in one fixed device
+ * array of SALA_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library. Every GPU that loads
+ * the library holds that array until the process exits. The call picks segments long
+ * enough for the scratch to fit; when even one segment per sequence does not fit (roughly
+ * num_seqs * H > 1000) it returns SALA_ERR_TOO_LARGE before queuing any work.
+ *
+ * The first call on a device looks up the array's device address (and sets kernel
+ * attributes) with that device current; make that first call before any stream capture.
+ * All calls share the one array and it keeps the last call's contents (every call fully
+ * rewrites what it reads, so no clearing is needed between calls). Calls whose work
+ * overlaps on the GPU (different streams, or different host threads) race on the array:
+ * serialise them on one stream. The call performs no cudaMalloc/cudaFree or other
+ * allocation.
+ */
+#define SALA_NOALLOC_SCRATCH_BYTES (64ull << 20)
+int sala_gla_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *g,
+                               float scale, const float *h0, const int64_t *cu_seqlens, void *o,
+                               float *hT, int64_t B, int64_t T, int32_t H, int64_t num_seqs,
+                               void *stream);
 
 /* Static English description of a sala_status value (never NULL). */
 const char *sala_gla_status_string(int status);

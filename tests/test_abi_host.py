@@ -63,7 +63,7 @@ def test_library_is_sm103a_only_and_links_cudart_statically(lib):
 def test_status_strings(lib):
     from gated_linear_attention_gb300 import sala_gla
     assert sala_gla.status_string(0) == "success"
-    for s in range(1, 7):
+    for s in range(1, 8):
         assert sala_gla.status_string(s) not in ("", "unknown status")
     assert sala_gla.status_string(99) == "unknown status"
     assert sala_gla.version().count(".") == 2

@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--decode-steps", type=int, default=None,
+                    help="decode steps to run (default: the workload's 1000; fewer for profiling)")
     return ap.parse_args()
 
 
@@ -408,7 +410,7 @@ def run_ours(args, dist):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic",
+            "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": 1, "T": w.T, "H": w.H, "d": D, "chunk": 64,
                        "parallelism": f"replica x{dist.world} (independent prefills)",
                        "l2": "inputs larger than L2 (201 MB q/k/v per set), two sets alternated",
@@ -432,6 +434,9 @@ def run_ours(args, dist):
 def run_decode(args, dist, dev, peaks, sala_gla, inputs):
     import torch
     w = inputs.WORKLOADS["decode"]
+    if args.decode_steps is not None:
+        import dataclasses
+        w = dataclasses.replace(w, steps=max(args.decode_steps, max(3, args.warmup)))
     x = inputs.make_decode_steps(w)
     S0 = inputs.make_decode_state(w)
     q, k, v, g = (x[n].to(dev) for n in ("q", "k", "v", "g"))

@@ -51,7 +51,7 @@ DeviceState *device_state(int *err) {
         uint64_t keep = ~uint64_t(0);
         d.init_error = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
         if (d.init_error != cudaSuccess) return;
-        d.init_error = setup_simt_kernels();
+        d.init_error = setup_tc_kernels();
     });
     if (d.init_error != cudaSuccess) {
         *err = SALA_ERR_CUDA;
@@ -290,9 +290,9 @@ int sala_gla_chunk_fwd(const void *q, const void *k, const void *v, const float 
 
     int rc = SALA_OK;
     if (launch_seg_table(tab, T_total, d->status, st) != cudaSuccess ||
-        launch_state_pass(a, tab, max_units, st) != cudaSuccess ||
+        launch_state_pass(a, tab, T_total, max_units, d->status, st) != cudaSuccess ||
         launch_segment_scan(tab, H, a.ws_state, a.ws_decay, h0, hT, st) != cudaSuccess ||
-        launch_output_pass(a, tab, max_units, st) != cudaSuccess)
+        launch_output_pass(a, tab, T_total, max_units, d->status, st) != cudaSuccess)
         rc = SALA_ERR_CUDA;
     if (cudaFreeAsync(ws, st) != cudaSuccess) rc = SALA_ERR_CUDA;
     return rc;

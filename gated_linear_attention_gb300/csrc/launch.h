@@ -1,6 +1,8 @@
 // Host-side launchers of the library's kernels (internal).
 #pragma once
 
+#include <mutex>
+
 #include "chunk_common.cuh"
 
 namespace sala {
@@ -40,10 +42,12 @@ cudaError_t launch_seg_table(const SegTable &t, int64_t T_total, int *status, cu
 cudaError_t launch_segment_scan(const SegTable &t, int H, float *ws_state, const float *ws_decay,
                                 const float *h0, float *hT, cudaStream_t st);
 
-cudaError_t setup_simt_kernels();
-cudaError_t launch_state_pass(const ChunkArgs &a, const SegTable &t, int64_t max_units,
-                              cudaStream_t st);
-cudaError_t launch_output_pass(const ChunkArgs &a, const SegTable &t, int64_t max_units,
-                               cudaStream_t st);
+// Tensor-core state and output passes (chunk_tc.cu). `status` receives SALA_ERR_TIMEOUT if a
+// bounded device-side wait gives up.
+cudaError_t setup_tc_kernels();
+cudaError_t launch_state_pass(const ChunkArgs &a, const SegTable &t, int64_t T_total,
+                              int64_t max_units, int *status, cudaStream_t st);
+cudaError_t launch_output_pass(const ChunkArgs &a, const SegTable &t, int64_t T_total,
+                               int64_t max_units, int *status, cudaStream_t st);
 
 }  // namespace sala

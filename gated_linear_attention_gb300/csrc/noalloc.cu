@@ -53,7 +53,7 @@ NoAllocDevice *noalloc_device(int *err) {
         if (d.error != cudaSuccess) return;
         d.error = device_status_address(&d.status);
         if (d.error != cudaSuccess) return;
-        d.error = setup_simt_kernels();
+        d.error = setup_tc_kernels();
     });
     if (d.error != cudaSuccess) {
         *err = SALA_ERR_CUDA;
@@ -153,9 +153,9 @@ extern "C" int sala_gla_chunk_fwd_noalloc(const void *q, const void *k, const vo
     a.ws_state = reinterpret_cast<float *>(ws + table + dec_bytes);
 
     if (launch_seg_table(tab, T_total, d->status, st) != cudaSuccess ||
-        launch_state_pass(a, tab, max_units, st) != cudaSuccess ||
+        launch_state_pass(a, tab, T_total, max_units, d->status, st) != cudaSuccess ||
         launch_segment_scan(tab, H, a.ws_state, a.ws_decay, h0, hT, st) != cudaSuccess ||
-        launch_output_pass(a, tab, max_units, st) != cudaSuccess)
+        launch_output_pass(a, tab, T_total, max_units, d->status, st) != cudaSuccess)
         return SALA_ERR_CUDA;
     return SALA_OK;
 }

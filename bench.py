@@ -340,9 +340,10 @@ def run_ours(args, dist):
     # dominant kernel and its roofline (algorithmic bytes per launch / mean launch time)
     top = max(kern.items(), key=lambda kv: kv[1][0])
     top_name, (top_ms, top_n) = top
+    # the fused prefill kernel moves the whole step's algorithmic bytes: q, k, v, g read
+    # once, o written once, h0 read and hT written once per (sequence, head)
     bytes_per_kernel = {
-        "output_pass": T_total * w.H * (3 * D * 2 + 4 + D * 2),
-        "state_pass": T_total * w.H * (2 * D * 2 + 4),
+        "prefill_fused": prefill_bytes(T_total, w.H, nseq, host["h0"] is not None, True),
     }
     if top_name in bytes_per_kernel and top_n:
         ach = bytes_per_kernel[top_name] / (top_ms / top_n / 1e3) / 1e9

@@ -1,6 +1,7 @@
 // C ABI of the sala_gla library: argument validation, per-device set-up, scratch and launch
 // order. Declarations and the contract of every entry point are in include/sala_gla.h.
 #include <atomic>
+#include <cstdlib>
 #include <mutex>
 #include <vector>
 
@@ -51,7 +52,7 @@ DeviceState *device_state(int *err) {
         uint64_t keep = ~uint64_t(0);
         d.init_error = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
         if (d.init_error != cudaSuccess) return;
-        d.init_error = setup_tc_kernels();
+        d.init_error = setup_fused_kernel();
     });
     if (d.init_error != cudaSuccess) {
         *err = SALA_ERR_CUDA;
@@ -73,22 +74,11 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
-int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
-// Segment length (tokens, a multiple of 64) for a prefill of T tokens in nseq sequences and
-// H heads: aim at about `waves` units per SM so the state and output passes fill the GPU,
-// while keeping segments long (the per-segment scratch traffic is 256 KB per unit).
-int64_t choose_seg_len(int64_t T, int64_t H, int sm_count) {
-    const int64_t target_units = 4LL * sm_count;
-    int64_t chunks = ceil_div(T * H, kChunk * target_units);
-    if (chunks < 1) chunks = 1;
-    if (chunks > 256) chunks = 256;
-    return chunks * kChunk;
-}
+std::atomic<uint32_t> g_epoch{0};
 
 // ---- timing instrumentation -------------------------------------------------------------
-const char *const kKernelNames[kKernelCount] = {"seg_table", "state_pass", "segment_scan",
-                                                "output_pass", "recurrent_step"};
+const char *const kKernelNames[kKernelCount] = {"seg_table", "prefill_fused", "empty_seq_state",
+                                                "recurrent_step"};
 struct TimingRecord {
     int id;
     cudaEvent_t start, stop;
@@ -106,6 +96,31 @@ void clear_records_locked() {
 }
 
 }  // namespace
+
+// Tokens per segment: long enough that the per-unit overhead (hand-off state, chunk
+// pipeline fill) stays small, short enough that a segment's k and v are still in L2 when the
+// output pass re-reads them and that there are several units per SM. SALA_GLA_SEGMENT_TOKENS
+// overrides the choice (rounded up to a multiple of 64).
+int64_t choose_segment_tokens(int64_t T_total, int64_t H, int sm_count) {
+    static const int64_t forced = []() -> int64_t {
+        const char *e = getenv("SALA_GLA_SEGMENT_TOKENS");
+        if (!e) return 0;
+        const long long v = atoll(e);
+        return v > 0 ? ((v + kChunk - 1) / kChunk) * kChunk : 0;
+    }();
+    if (forced) return forced;
+    (void)H;
+    (void)sm_count;
+    int64_t L = 512;
+    if (T_total < L) L = ((T_total + kChunk - 1) / kChunk) * kChunk;
+    return L < kChunk ? kChunk : L;
+}
+
+uint32_t next_prefill_epoch() {
+    uint32_t e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+    if (e == 0) e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+    return e;
+}
 
 cudaError_t device_status_address(int **out) {
     return cudaGetSymbolAddress(reinterpret_cast<void **>(out), g_device_status);
@@ -257,18 +272,20 @@ int sala_gla_chunk_fwd(const void *q, const void *k, const void *v, const float 
     if (!d) return err;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-    const int64_t seg_len = choose_seg_len(T_total, H, d->sm_count);
+    const int64_t seg_len = choose_segment_tokens(T_total, H, d->sm_count);
     const int64_t max_segs = T_total / seg_len + nseq;  // sum of ceil(len/L) <= T/L + nseq
     const int64_t max_units = max_segs * H;
     if (max_units > (int64_t(1) << 31) - 1) return SALA_ERR_INVALID_ARG;
 
-    // scratch: segment table, per-(segment, head) decay and state
+    // scratch: segment table, work ticket, hand-off flags, hand-off states
     const size_t off_bytes = ((static_cast<size_t>(nseq) + 2) * 8 + 255) & ~size_t(255);
-    const size_t dec_bytes = (static_cast<size_t>(max_units) * 4 + 255) & ~size_t(255);
+    const size_t tick_bytes = 256;
+    const size_t flag_bytes = (static_cast<size_t>(max_units) * 4 + 255) & ~size_t(255);
     const size_t st_bytes = static_cast<size_t>(max_units) * kD * kD * 4;
     char *ws = nullptr;
-    if (cudaMallocFromPoolAsync(reinterpret_cast<void **>(&ws), off_bytes + dec_bytes + st_bytes,
-                                d->pool, st) != cudaSuccess)
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void **>(&ws),
+                                off_bytes + tick_bytes + flag_bytes + st_bytes, d->pool,
+                                st) != cudaSuccess)
         return SALA_ERR_CUDA;
 
     SegTable tab;
@@ -285,14 +302,14 @@ int sala_gla_chunk_fwd(const void *q, const void *k, const void *v, const float 
     a.scale = scale;
     a.o = static_cast<uint16_t *>(o);
     a.H = H;
-    a.ws_decay = reinterpret_cast<float *>(ws + off_bytes);
-    a.ws_state = reinterpret_cast<float *>(ws + off_bytes + dec_bytes);
+    uint32_t *ticket = reinterpret_cast<uint32_t *>(ws + off_bytes);
+    uint32_t *flags = reinterpret_cast<uint32_t *>(ws + off_bytes + tick_bytes);
+    float *incl = reinterpret_cast<float *>(ws + off_bytes + tick_bytes + flag_bytes);
 
     int rc = SALA_OK;
-    if (launch_seg_table(tab, T_total, d->status, st) != cudaSuccess ||
-        launch_state_pass(a, tab, T_total, max_units, d->status, st) != cudaSuccess ||
-        launch_segment_scan(tab, H, a.ws_state, a.ws_decay, h0, hT, st) != cudaSuccess ||
-        launch_output_pass(a, tab, T_total, max_units, d->status, st) != cudaSuccess)
+    if (launch_seg_table(tab, T_total, ticket, flags, max_units, d->status, st) != cudaSuccess ||
+        launch_prefill_fused(a, tab, T_total, max_units, h0, hT, incl, flags, ticket,
+                             next_prefill_epoch(), d->sm_count, d->status, st) != cudaSuccess)
         rc = SALA_ERR_CUDA;
     if (cudaFreeAsync(ws, st) != cudaSuccess) rc = SALA_ERR_CUDA;
     return rc;

@@ -28,8 +28,6 @@ struct ChunkArgs {
     float scale;
     uint16_t *o;                // bf16 [T_total, H, 128]
     int H;
-    float *ws_state;            // [segments, H, 128, 128]: dS, then S_in
-    float *ws_decay;            // [segments, H]: total log-decay of each segment
 };
 
 __device__ __forceinline__ int64_t seq_begin(const SegTable &t, int64_t n) {

@@ -10,9 +10,8 @@ namespace sala {
 // Kernels of the library, for the timing instrumentation (names in api.cu).
 enum KernelId {
     kKSegTable = 0,
-    kKStatePass,
-    kKSegmentScan,
-    kKOutputPass,
+    kKPrefillFused,
+    kKEmptySeq,
     kKRecurrentStep,
     kKernelCount
 };
@@ -38,16 +37,25 @@ cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, c
                                   float scale, float *S, void *o, int64_t units,
                                   cudaStream_t stream);
 
-cudaError_t launch_seg_table(const SegTable &t, int64_t T_total, int *status, cudaStream_t st);
-cudaError_t launch_segment_scan(const SegTable &t, int H, float *ws_state, const float *ws_decay,
-                                const float *h0, float *hT, cudaStream_t st);
+// Segment table from cu_seqlens (or B equal rows); also zeroes the work ticket and the
+// hand-off flags of the fused prefill.
+cudaError_t launch_seg_table(const SegTable &t, int64_t T_total, uint32_t *ticket,
+                             uint32_t *flags, int64_t nflags, int *status, cudaStream_t st);
 
-// Tensor-core state and output passes (chunk_tc.cu). `status` receives SALA_ERR_TIMEOUT if a
-// bounded device-side wait gives up.
-cudaError_t setup_tc_kernels();
-cudaError_t launch_state_pass(const ChunkArgs &a, const SegTable &t, int64_t T_total,
-                              int64_t max_units, int *status, cudaStream_t st);
-cudaError_t launch_output_pass(const ChunkArgs &a, const SegTable &t, int64_t T_total,
-                               int64_t max_units, int *status, cudaStream_t st);
+// The fused tensor-core prefill (prefill_fused.cu): one persistent launch of `grid` CTAs,
+// then the final state of empty sequences. `incl` holds [max_units, 128, 128] fp32 hand-off
+// states, `flags` [max_units] words, `ticket` one word; `epoch` is nonzero and differs from
+// the previous call's. `status` receives SALA_ERR_TIMEOUT if a bounded wait gives up.
+cudaError_t setup_fused_kernel();
+cudaError_t launch_prefill_fused(const ChunkArgs &a, const SegTable &t, int64_t T_total,
+                                 int64_t max_units, const float *h0, float *hT, float *incl,
+                                 uint32_t *flags, uint32_t *ticket, uint32_t epoch, int grid,
+                                 int *status, cudaStream_t st);
+
+// Nonzero tag of one prefill call for the hand-off flags (differs from the previous call's).
+uint32_t next_prefill_epoch();
+
+// Tokens per segment of the fused prefill for T_total tokens and H heads on sm_count SMs.
+int64_t choose_segment_tokens(int64_t T_total, int64_t H, int sm_count);
 
 }  // namespace sala

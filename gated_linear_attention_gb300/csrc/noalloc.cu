@@ -13,7 +13,7 @@ namespace {
 
 constexpr size_t kScratchBytes = SALA_NOALLOC_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
-constexpr size_t kUnitBytes = size_t(kD) * kD * 4 + 4;  // one (segment, head): state + decay
+constexpr size_t kUnitBytes = size_t(kD) * kD * 4 + 4;  // one (segment, head): state + flag
 
 // The scratch itself: one per device that loads the library, held until the process exits.
 // In host code this name is only a stand-in; its device address comes from
@@ -53,7 +53,7 @@ NoAllocDevice *noalloc_device(int *err) {
         if (d.error != cudaSuccess) return;
         d.error = device_status_address(&d.status);
         if (d.error != cudaSuccess) return;
-        d.error = setup_tc_kernels();
+        d.error = setup_fused_kernel();
     });
     if (d.error != cudaSuccess) {
         *err = SALA_ERR_CUDA;
@@ -107,10 +107,10 @@ extern "C" int sala_gla_chunk_fwd_noalloc(const void *q, const void *k, const vo
     if (overlap(o, vec, hT, sb)) return SALA_ERR_INVALID_ARG;
     if (!hT && T_total == 0) return SALA_OK;
 
-    // Segment length: the usual choice (about 4 units per SM) unless the fixed scratch
-    // needs longer segments. With L tokens per segment there are at most T/L + nseq
-    // segments, so floor(T/L) may not exceed r = (segments that fit) - nseq.
-    const size_t table = round256(size_t(nseq + 2) * 8);
+    // Segment length: the usual choice unless the fixed scratch needs longer segments. With L
+    // tokens per segment there are at most T/L + nseq segments, so floor(T/L) may not exceed
+    // r = (segments that fit) - nseq.
+    const size_t table = round256(size_t(nseq + 2) * 8) + 256;   // segment table + ticket
     if (table + 256 + H * kUnitBytes > kScratchBytes) return SALA_ERR_TOO_LARGE;
     const int64_t units_fit = static_cast<int64_t>((kScratchBytes - table - 256) / kUnitBytes);
     const int64_t r = units_fit / H - nseq;
@@ -120,17 +120,14 @@ extern "C" int sala_gla_chunk_fwd_noalloc(const void *q, const void *k, const vo
     NoAllocDevice *d = noalloc_device(&err);
     if (!d) return err;
 
-    int64_t chunks = (T_total * H + kChunk * 4LL * d->sm_count - 1) / (kChunk * 4LL * d->sm_count);
-    if (chunks < 1) chunks = 1;
-    if (chunks > 256) chunks = 256;
+    int64_t seg_len = choose_segment_tokens(T_total, H, d->sm_count);
     const int64_t need_len = (T_total + 1 + r) / (r + 1);  // floor(T / need_len) <= r
-    const int64_t need_chunks = (need_len + kChunk - 1) / kChunk;
-    if (chunks < need_chunks) chunks = need_chunks;
-    const int64_t seg_len = chunks * kChunk;
+    const int64_t need = ((need_len + kChunk - 1) / kChunk) * kChunk;
+    if (seg_len < need) seg_len = need;
     const int64_t max_segs = T_total / seg_len + nseq;
     const int64_t max_units = max_segs * H;
-    const size_t dec_bytes = round256(size_t(max_units) * 4);
-    if (table + dec_bytes + size_t(max_units) * kD * kD * 4 > kScratchBytes)
+    const size_t flag_bytes = round256(size_t(max_units) * 4);
+    if (table + flag_bytes + size_t(max_units) * kD * kD * 4 > kScratchBytes)
         return SALA_ERR_TOO_LARGE;
 
     unsigned char *ws = d->scratch;
@@ -149,13 +146,13 @@ extern "C" int sala_gla_chunk_fwd_noalloc(const void *q, const void *k, const vo
     a.scale = scale;
     a.o = static_cast<uint16_t *>(o);
     a.H = H;
-    a.ws_decay = reinterpret_cast<float *>(ws + table);
-    a.ws_state = reinterpret_cast<float *>(ws + table + dec_bytes);
+    uint32_t *ticket = reinterpret_cast<uint32_t *>(ws + table - 256);
+    uint32_t *flags = reinterpret_cast<uint32_t *>(ws + table);
+    float *incl = reinterpret_cast<float *>(ws + table + flag_bytes);
 
-    if (launch_seg_table(tab, T_total, d->status, st) != cudaSuccess ||
-        launch_state_pass(a, tab, T_total, max_units, d->status, st) != cudaSuccess ||
-        launch_segment_scan(tab, H, a.ws_state, a.ws_decay, h0, hT, st) != cudaSuccess ||
-        launch_output_pass(a, tab, T_total, max_units, d->status, st) != cudaSuccess)
+    if (launch_seg_table(tab, T_total, ticket, flags, max_units, d->status, st) != cudaSuccess ||
+        launch_prefill_fused(a, tab, T_total, max_units, h0, hT, incl, flags, ticket,
+                             next_prefill_epoch(), d->sm_count, d->status, st) != cudaSuccess)
         return SALA_ERR_CUDA;
     return SALA_OK;
 }

@@ -36,13 +36,19 @@ __device__ __forceinline__ bool named_any(int id, int n, bool x) {
     return r != 0;
 }
 
-// Bounded wait that also gives up as soon as another role has aborted. The thread sleeps in
-// hardware between checks (up to 20 us at a time).
+// How the bounded waits poll: SALA_WAIT_POLL_NS > 0 tests the phase without suspending and
+// sleeps that long between tests; 0 uses try_wait, which may suspend the thread in hardware.
+#ifndef SALA_WAIT_POLL_NS
+#define SALA_WAIT_POLL_NS 64
+#endif
+
+// Bounded wait that also gives up as soon as another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
                                               volatile int *abort_flag, int *status) {
-    if (tc::mbar_try_wait(bar, parity)) return true;
+    if (tc::mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = tc::global_timer_ns();
-    while (!tc::mbar_try_wait_sleep(bar, parity, 20000u)) {
+    while (!(SALA_WAIT_POLL_NS ? tc::mbar_test_wait(bar, parity) : tc::mbar_try_wait(bar, parity))) {
+        if (SALA_WAIT_POLL_NS) __nanosleep(SALA_WAIT_POLL_NS);
         if (*abort_flag) return false;
         if (tc::global_timer_ns() - t0 > kWaitNs) {
             *abort_flag = 1;
@@ -77,14 +83,13 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t w, float s) {
 }
 
 struct TcMaps {
-    CUtensorMap q, k, v;
+    CUtensorMap q, k, v;   // loads: box 64 x 1 x 64, 128-byte swizzle
+    CUtensorMap o;         // stores: box 128 x 1 x 32, no swizzle
 };
 
-
-// host: 3-D tensor maps over q, k, v viewed as [T_total, H, 128] bf16, box 64 x 1 x 64,
-// 128-byte swizzle
-cudaError_t make_maps(TcMaps *m, const void *q, const void *k, const void *v, int64_t T_total,
-                      int H);
+// host: 3-D tensor maps over q, k, v and o viewed as [T_total, H, 128] bf16
+cudaError_t make_maps(TcMaps *m, const void *q, const void *k, const void *v, const void *o,
+                      int64_t T_total, int H);
 
 }  // namespace tck
 }  // namespace sala

@@ -10,8 +10,8 @@
 // already running on some CTA. For each unit a CTA runs:
 //
 //  A. state pass over the segment's chunks, last to first: dS = sum_t exp(B_end - B_t)
-//     k_t^T v_t accumulated by tcgen05 in tensor memory (k_t pre-scaled in shared memory by
-//     its decay to the segment end, so every weight is <= 1), and the total log-decay B;
+//     k_t^T v_t accumulated by tcgen05 in tensor memory (k_t scaled by its decay to the
+//     segment end, so every weight is <= 1), and the total log-decay B;
 //  hand-off: S_in = h0 (first segment) or the state the predecessor published; publish
 //     S_out = exp(B) S_in + dS for the successor (hT for the last segment). This is the
 //     Blueprint's unrolled form S_n = alpha^n S_0 + sum alpha^(n-i) k_i^T v_i applied a whole
@@ -19,27 +19,33 @@
 //  C. output pass over the chunks, first to last, from S_in. With b_t the cumulative
 //     log-decay of the chunk up to token t and S the state entering the chunk:
 //       o_t = scale exp(b_t) [ q_t S + sum_{s<=t} (q_t . k_s) exp(-b_s) v_s ]
-//       S  <- exp(b_C) S + sum_s exp(b_C - b_s) k_s^T v_s
+//       S  <- exp(b_C) [ S + sum_s exp(-b_s) k_s^T v_s ]
 //     which keeps both output terms in one accumulator (the weights become per-column
 //     factors exp(-b_s) on the scores and per-row factors exp(b_t) on the output). When a
 //     chunk's decay range is too wide for those factors (|b_t| > 60), the chunk takes the
-//     exact route instead: per-entry factors exp(b_t - b_s) on the scores and q_t scaled by
-//     exp(b_t) in place. Contractions (tcgen05.mma kind::f16, bf16 in, fp32 in TMEM):
-//       M1  P    = Q K^T       M=64  N=64  K=128   A=Q (K-major)      B=K (K-major)
-//       M2  O^T  = S^T Q^T     M=128 N=64  K=128   A=S bf16 (MN-major) B=Q (K-major)
-//       M3  O^T += V^T P'^T    M=128 N=64  K=64    A=V (MN-major)      B=P' (K-major)
-//       M4  dS   = K'^T V      M=128 N=128 K=64    A=K' (MN-major)     B=V (MN-major)
+//     exact route instead: per-entry factors exp(b_t - b_s) on the scores, q_t scaled by
+//     exp(b_t) in place, and S <- exp(b_C) S + sum_s exp(b_C - b_s) k_s^T v_s.
 //
-// K and V are read in A and again in C shortly after, while they are still in L2 (the A
-// loads ask L2 to keep them, the C loads let them go).
+// The state is kept transposed (S^T, value index j in the tensor-memory lane), so that its
+// bf16 copy can sit in tensor memory as the A operand of the q.S product. Contractions
+// (tcgen05.mma kind::f16, bf16 in, fp32 accumulators in tensor memory):
+//   M1  P    = Q K~^T      M=64  N=64  K=128   A=Q smem (K-major)     B=K~ smem (K-major)
+//   M2  O^T  = S^T Q^T     M=128 N=64  K=128   A=S^T bf16 in TMEM     B=Q smem (K-major)
+//   M3  O^T += V^T P'^T    M=128 N=64  K=64    A=V smem (MN-major)    B=P' smem (K-major)
+//   M4  dS^T = V^T K~      M=128 N=128 K=64    A=V smem (MN-major)    B=K~ smem (MN-major)
+// K~ is k scaled per token (the factors above); the scaling warps make it from a global load
+// straight into shared memory, so no warp reads shared memory with ordinary loads while the
+// tensor core streams its operands from it (such loads stall far behind the tensor core's).
+// Q and V tiles arrive by TMA.
 //
-// Roles: warp 0 loads (TMA tiles; the lanes load the chunk's 64 log-decays and publish their
-// prefix sums), warp 1 issues MMAs and owns the tensor memory, warpgroup 0 (warps 2-5)
-// scales K and the scores and owns state columns 0-63, warpgroup 1 (warps 6-9) owns state
-// columns 64-127 and writes o, warp 10 publishes hand-off flags. Scores, outputs, dS and the
-// bf16 state are double-buffered so that only the fp32 state update is serial per chunk.
-// Every wait is bounded (2 s of %globaltimer); a timeout records SALA_ERR_TIMEOUT, stops the
-// CTA's work, drains its copies and MMAs, frees its tensor memory and returns.
+// Roles: warp 0 loads (TMA), warp 1 issues MMAs and owns the tensor memory, warp 2 publishes
+// hand-off flags, warps 4-7 scale K, turn scores into P' and (exact route) scale Q, warps
+// 8-11 and 12-15 each own 64 of the state's key rows i (all 128 value columns j, one per
+// lane), carry the state, and write o for 32 of the chunk's tokens. Every per-token factor is
+// computed by the warp that needs it from g (an in-warp prefix sum), never passed through
+// shared memory. Every wait is bounded (2 s of %globaltimer); a timeout records
+// SALA_ERR_TIMEOUT, stops the CTA's work, drains its copies and MMAs, frees its tensor memory
+// and returns.
 #include "chunk_tc.cuh"
 
 namespace sala {
@@ -47,41 +53,33 @@ namespace {
 
 using namespace tck;
 
-constexpr int kStages = 3;
-constexpr int kThreads = 352;
+constexpr int kStages = 4;
+constexpr int kThreads = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kFastRange = 60.f;   // max |b_t| (natural log) for the factored route
 
 // dynamic shared memory (offsets from a 1024-aligned base)
-constexpr uint32_t kStage = 3 * kTile;              // Q | K | V
-constexpr uint32_t kKp = kStages * kStage;          // K' [2] (MN-major A of M4)
-constexpr uint32_t kPp = kKp + 2 * kTile;           // P' (K-major B of M3)
-constexpr uint32_t kSb = kPp + kRegion;             // S bf16 (MN-major A of M2), 32 KB
-constexpr uint32_t kMeta = kSb + 2 * kSRegion;      // per stage: chunk metadata (512 B)
-constexpr uint32_t kVals = kMeta + kStages * 512;   // per warpgroup: 64 floats
-constexpr uint32_t kBytes = kVals + 2 * 64 * 4;
+constexpr uint32_t kStage = 2 * kTile;              // Q | V
+constexpr uint32_t kKp = kStages * kStage;          // K~ [2] (factored or exact weights)
+constexpr uint32_t kKr = kKp + 2 * kTile;           // raw K [2] (exact-route M1)
+constexpr uint32_t kPp = kKr + 2 * kTile;           // P' (K-major B of M3)
+constexpr uint32_t kOst = kPp + kRegion;            // o staging [2 state groups][32 t][256 B]
+constexpr uint32_t kOstBytes = 32 * 256;
+constexpr uint32_t kBytes = kOst + 2 * kOstBytes;
 constexpr uint32_t kSmemAlloc = kBytes + 1024;
 
-struct alignas(16) ChunkMeta {
-    float b[64];   // inclusive prefix sums of g over the chunk (0 past the valid tokens)
-    float bC;      // b at the last valid token
-    int fast;      // 1: factored weights are safe (max |b_t| <= kFastRange)
-    int nv;        // valid tokens
-    int pad_[61];  // one 512-byte slot per stage
-};
-static_assert(sizeof(ChunkMeta) == 512, "one 512-byte metadata slot per stage");
-
-// TMEM columns: P [2] (M=64 layout), O [2], dS [2]
-constexpr uint32_t kTP = 0, kTO = 128, kTdS = 256, kTCols = 512;
+// TMEM columns: P (M=64 layout), S^T bf16 (A of M2), O^T [2], dS^T [2]
+constexpr uint32_t kTP = 0, kTSb = 64, kTO = 128, kTdS = 256, kTCols = 512;
 constexpr uint32_t kIdescP = tc::idesc_bf16_f32(64, 64, 0, 0);
-constexpr uint32_t kIdescO = tc::idesc_bf16_f32(128, 64, 1, 0);
+constexpr uint32_t kIdescO2 = tc::idesc_bf16_f32(128, 64, 0, 0);
+constexpr uint32_t kIdescO3 = tc::idesc_bf16_f32(128, 64, 1, 0);
 constexpr uint32_t kIdescS = tc::idesc_bf16_f32(128, 128, 1, 1);
 
 struct FusedArgs {
     ChunkArgs c;            // q, k, v, g, scale, o, H
     const float *h0;        // [nseq, H, 128, 128] or null
     float *hT;              // [nseq, H, 128, 128] or null
-    float *incl;            // [units, 128, 128]: state after each (segment, head)
+    float *incl;            // [units, 128, 128]: S_out of each (segment, head), row-major like hT
     uint32_t *flags;        // [units]: == epoch once incl of that unit is published
     uint32_t *ticket;       // work counter, zeroed by the table kernel
     uint32_t epoch;
@@ -93,11 +91,16 @@ struct UnitInfo {
 };
 
 // Event trace of CTA 0 for latency analysis (compiled only with -DSALA_TRACE): SM clock,
-// role, event id and chunk index, kept in shared memory and copied out at exit.
+// role, event id and chunk index, written to a global array.
 #ifdef SALA_TRACE
 constexpr int kTraceN = 512;
-__device__ unsigned long long g_trace[4][kTraceN];
-__device__ unsigned int g_trace_n[4];
+__device__ unsigned long long g_trace[5][kTraceN];
+__device__ unsigned int g_trace_n[5];
+__device__ long long g_wts[16][8];
+#define WTS(k)                                                                                \
+    do {                                                                                      \
+        if (blockIdx.x == 0 && lane == 0 && us == 0) g_wts[warp][k] = clock64();             \
+    } while (0)
 #define TRACE(role, ev, idx)                                                                  \
     do {                                                                                      \
         if (blockIdx.x == 0 && tr_i < kTraceN) {                                              \
@@ -113,6 +116,9 @@ __device__ unsigned int g_trace_n[4];
 #define TRACE(role, ev, idx) \
     do {                     \
     } while (0)
+#define WTS(k) \
+    do {       \
+    } while (0)
 #endif
 
 // shared-memory matrix descriptors: fixed part | (start address >> 4)
@@ -122,56 +128,51 @@ __device__ __forceinline__ uint64_t desc_k(uint32_t addr) {          // K-major,
 __device__ __forceinline__ uint64_t desc_mn8(uint32_t addr) {        // MN-major, 8 KB atoms
     return tc::smem_desc_sw128(0, kRegion, 1024) | ((addr >> 4) & 0x3FFFu);
 }
-__device__ __forceinline__ uint64_t desc_mn16(uint32_t addr) {       // MN-major, 16 KB atoms
-    return tc::smem_desc_sw128(0, kSRegion, 1024) | ((addr >> 4) & 0x3FFFu);
+
+// Log-decays of one chunk as seen by one warp: lane l holds the inclusive prefix sums
+// b[2l], b[2l+1] of g over the chunk's nv valid tokens (constant past nv).
+struct Gate {
+    float b0, b1;   // b[2 lane], b[2 lane + 1]
+    float bC;       // b at the last valid token
+    bool fast;      // max |b| <= kFastRange: factored weights are safe
+};
+
+// Raw g of the chunk for lane l (tokens 2l, 2l+1; 0 past nv): loaded early, scanned later.
+__device__ __forceinline__ float2 load_gate(const float *__restrict__ g, int64_t c0, int nv, int H,
+                                            int h) {
+    const int l = threadIdx.x & 31;
+    return make_float2(2 * l < nv ? __ldg(g + (c0 + 2 * l) * H + h) : 0.f,
+                       2 * l + 1 < nv ? __ldg(g + (c0 + 2 * l + 1) * H + h) : 0.f);
 }
 
-__device__ __forceinline__ void store_bf16_row64(uint8_t *region, int row, const float *S) {
+__device__ __forceinline__ Gate scan_gate(float2 a, int nv) {
+    const int l = threadIdx.x & 31;
+    const float pair = a.x + a.y;
+    float run = pair;
 #pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) {
-        uint4 w;
-        w.x = float2_to_bf16x2(S[8 * c8 + 0], S[8 * c8 + 1]);
-        w.y = float2_to_bf16x2(S[8 * c8 + 2], S[8 * c8 + 3]);
-        w.z = float2_to_bf16x2(S[8 * c8 + 4], S[8 * c8 + 5]);
-        w.w = float2_to_bf16x2(S[8 * c8 + 6], S[8 * c8 + 7]);
-        *reinterpret_cast<uint4 *>(region + sw(row, c8)) = w;
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, run, off);
+        if (l >= off) run += y;
     }
+    Gate G;
+    G.b0 = run - pair + a.x;
+    G.b1 = run;
+    float mx = fmaxf(fabsf(G.b0), fabsf(G.b1));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    G.bC = __shfl_sync(0xffffffffu, ((nv - 1) & 1) ? G.b1 : G.b0, (nv - 1) >> 1);
+    G.fast = mx <= kFastRange;
+    return G;
 }
 
-// Scale 16-byte pieces p0 + stride*m (m < N) of a [64 x 128] bf16 tile (two SW128 regions)
-// by a per-row factor 2^(base + sign * b[t] * log2(e)), writing to dst (same layout); rows
-// >= nv become zero. All loads are issued before any store (dst may equal src).
-template <int N>
-__device__ __forceinline__ void scale_rows(const uint8_t *src, uint8_t *dst, int p0, int stride,
-                                           int nv, const float *b, float base, float sign) {
-    uint4 x[N];
-    uint32_t off[N];
-    int tr[N];
-#pragma unroll
-    for (int m = 0; m < N; ++m) {
-        const int idx = p0 + stride * m;
-        const int rg = idx >> 9, ch = idx & 7;
-        tr[m] = (idx >> 3) & 63;
-        off[m] = rg * kRegion + sw(tr[m], ch);
-        x[m] = *reinterpret_cast<const uint4 *>(src + off[m]);
-    }
-#pragma unroll
-    for (int m = 0; m < N; ++m) {
-        if (tr[m] < nv) {
-            const float w = tc::ex2(fmaf(sign * kLog2e, b[tr[m]], base));
-            x[m].x = mul_bf16x2(x[m].x, w);
-            x[m].y = mul_bf16x2(x[m].y, w);
-            x[m].z = mul_bf16x2(x[m].z, w);
-            x[m].w = mul_bf16x2(x[m].w, w);
-        } else {
-            x[m] = make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
-#pragma unroll
-    for (int m = 0; m < N; ++m) *reinterpret_cast<uint4 *>(dst + off[m]) = x[m];
+// b[t] for a warp-uniform or per-lane t in [0, 64) (all lanes must call).
+__device__ __forceinline__ float gate_at(const Gate &G, int t) {
+    const float x = __shfl_sync(0xffffffffu, G.b0, t >> 1);
+    const float y = __shfl_sync(0xffffffffu, G.b1, t >> 1);
+    return (t & 1) ? y : x;
 }
 
-// Bounded wait (if `need`) whose failure only sets the abort flag (see the epilogue loop).
+// Bounded wait (if `need`) whose failure only sets the abort flag (see the epilogue loops).
 __device__ __forceinline__ void wait_nv(uint64_t *bar, uint32_t par, bool need,
                                         volatile int *abort_v, int *status) {
     if (need) (void)wait_or_abort(bar, par & 1, abort_v, status);
@@ -185,6 +186,22 @@ __device__ __forceinline__ bool wg_wait(uint64_t *bar, uint32_t par, bool need, 
     return !named_any(bar_id, 128, bad);
 }
 
+// 64 bf16 of one row, scaled by f, to a [64 x 128 B] SW128 region row (and, if raw_dst, also
+// unscaled to a second tile).
+__device__ __forceinline__ void store_row_scaled(uint8_t *dst, uint8_t *raw_dst, int row,
+                                                 const uint4 (&x)[8], float f) {
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8) {
+        uint4 y;
+        y.x = mul_bf16x2(x[c8].x, f);
+        y.y = mul_bf16x2(x[c8].y, f);
+        y.z = mul_bf16x2(x[c8].z, f);
+        y.w = mul_bf16x2(x[c8].w, f);
+        *reinterpret_cast<uint4 *>(dst + sw(row, c8)) = y;
+        if (raw_dst) *reinterpret_cast<uint4 *>(raw_dst + sw(row, c8)) = x[c8];
+    }
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -194,9 +211,12 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                                               ~uintptr_t(1023));
     __shared__ uint64_t full[kStages], empty[kStages], unit_full[2], unit_empty[2];
     __shared__ uint64_t kp_ready[2], kp_free[2], pub_ready, drain;
-    __shared__ uint64_t ds_full[2], ds_free[2], p_full[2], p_free[2], pp_ready, pp_free;
+    __shared__ uint64_t ds_full[2], ds_free[2], p_full, p_free, pp_ready, pp_free;
     __shared__ uint64_t o_full[2], o_free[2], sb_ready, sb_free;
+    __shared__ uint64_t d_ready, d_free;
     __shared__ UnitInfo units[2];
+    __shared__ int kfast[2];
+    __shared__ float unit_D;   // total log-decay of the current unit's segment
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 #ifdef SALA_TRACE
@@ -206,35 +226,32 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
     const ChunkArgs &a = f.c;
     const int H = a.H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    ChunkMeta *meta = reinterpret_cast<ChunkMeta *>(sm + kMeta);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            tc::mbar_init(&full[s], 33);   // expect_tx arrival + one per producer lane
-            tc::mbar_init(&empty[s], 3);   // warpgroup 0, warpgroup 1, MMA commit
+            tc::mbar_init(&full[s], 1);    // expect_tx arrival
+            tc::mbar_init(&empty[s], 1);   // MMA commit
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&unit_full[i], 1);
-            tc::mbar_init(&unit_empty[i], 4);
-            tc::mbar_init(&ds_full[i], 1);
-            tc::mbar_init(&ds_free[i], 2);
-            tc::mbar_init(&p_full[i], 1);
-            tc::mbar_init(&p_free[i], 1);
-
-            tc::mbar_init(&o_full[i], 1);
-            tc::mbar_init(&o_free[i], 1);
-
-        }
-        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&unit_empty[i], 5);   // MMA, publisher, scaler, two state groups
             tc::mbar_init(&kp_ready[i], 1);
             tc::mbar_init(&kp_free[i], 1);
+            tc::mbar_init(&ds_full[i], 1);
+            tc::mbar_init(&ds_free[i], 2);
+            tc::mbar_init(&o_full[i], 1);
+            tc::mbar_init(&o_free[i], 2);
         }
-        tc::mbar_init(&pub_ready, 2);
+        tc::mbar_init(&p_full, 1);
+        tc::mbar_init(&p_free, 1);
         tc::mbar_init(&pp_ready, 1);
         tc::mbar_init(&pp_free, 1);
         tc::mbar_init(&sb_ready, 2);
         tc::mbar_init(&sb_free, 1);
+        tc::mbar_init(&pub_ready, 2);
         tc::mbar_init(&drain, 1);
+        tc::mbar_init(&d_ready, 1);
+        tc::mbar_init(&d_free, 2);      // both state groups have read unit_D
         abort_flag = 0;
         tc::fence_barrier_init();
     }
@@ -257,54 +274,37 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             tc::tma_prefetch_desc(&maps.q);
             tc::tma_prefetch_desc(&maps.k);
             tc::tma_prefetch_desc(&maps.v);
+            tc::tma_prefetch_desc(&maps.o);
         }
         uint32_t job = 0, us = 0;
         bool ok = true;
+        // one job: V (state pass) or Q and V (output pass) of the chunk at token c0, with L2
+        // prefetches of the chunk's K rows and log-decays (read by other warps a little later)
         auto load_job = [&](int64_t c0, int nv, int h, bool with_q) -> bool {
             const uint32_t st = job % kStages;
             bool bad = false;
             if (job >= kStages)
                 bad = !wait_or_abort(&empty[st], ((job / kStages) - 1) & 1, abort_v, status);
             if (__any_sync(0xffffffffu, bad)) return false;
-            uint8_t *base = sm + st * kStage;
+            if (2 * lane < nv) tc::prefetch_l2_keep(a.g + (c0 + 2 * lane) * H + h);
+            if (2 * lane + 1 < nv) tc::prefetch_l2_keep(a.g + (c0 + 2 * lane + 1) * H + h);
             if (lane == 0) {
                 TRACE(0, with_q ? 2 : 1, job);
+                uint8_t *base = sm + st * kStage;
                 const int32_t x0 = static_cast<int32_t>(c0);
-                tc::mbar_arrive_expect_tx(&full[st], (with_q ? 3 : 2) * kTile);
+                tc::mbar_arrive_expect_tx(&full[st], (with_q ? 2 : 1) * kTile);
                 if (with_q) {
                     tc::tma_load_3d_hint(base, &maps.q, 0, h, x0, &full[st], drop);
                     tc::tma_load_3d_hint(base + kRegion, &maps.q, 64, h, x0, &full[st], drop);
                 }
                 const uint64_t pol = with_q ? drop : keep;
-                tc::tma_load_3d_hint(base + kTile, &maps.k, 0, h, x0, &full[st], pol);
-                tc::tma_load_3d_hint(base + kTile + kRegion, &maps.k, 64, h, x0, &full[st], pol);
-                tc::tma_load_3d_hint(base + 2 * kTile, &maps.v, 0, h, x0, &full[st], pol);
-                tc::tma_load_3d_hint(base + 2 * kTile + kRegion, &maps.v, 64, h, x0, &full[st], pol);
+                tc::tma_load_3d_hint(base + kTile, &maps.v, 0, h, x0, &full[st], pol);
+                tc::tma_load_3d_hint(base + kTile + kRegion, &maps.v, 64, h, x0, &full[st], pol);
+                // the scaling warps read this chunk's K rows with ordinary loads a little later
+                tc::tma_prefetch_l2_3d(&maps.k, 0, h, x0, pol);
+                tc::tma_prefetch_l2_3d(&maps.k, 64, h, x0, pol);
             }
-            // the chunk's log-decays: inclusive prefix sums, last value, factored-route check
-            const int i0 = 2 * lane, i1 = 2 * lane + 1;
-            const float g0 = i0 < nv ? a.g[(c0 + i0) * H + h] : 0.f;
-            const float g1 = i1 < nv ? a.g[(c0 + i1) * H + h] : 0.f;
-            const float pair = g0 + g1;
-            float run = pair;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, run, off);
-                if (lane >= off) run += y;
-            }
-            const float b0 = run - pair + g0, b1 = run;
-            float mx = fmaxf(fabsf(b0), fabsf(b1));
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float bC = __shfl_sync(0xffffffffu, ((nv - 1) & 1) ? b1 : b0, (nv - 1) >> 1);
-            ChunkMeta &md = meta[st];
-            *reinterpret_cast<float2 *>(&md.b[i0]) = make_float2(b0, b1);
-            if (lane == 0) {
-                md.bC = bC;
-                md.fast = mx <= kFastRange ? 1 : 0;
-                md.nv = nv;
-            }
-            tc::mbar_arrive(&full[st]);
+            __syncwarp();
             ++job;
             return true;
         };
@@ -361,7 +361,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 tc::mbar_arrive(&unit_empty[slot]);
                 if (!info.valid) break;
                 bool ok = true;
-                // ---- A: dS = sum over chunks of K'^T V, one accumulator
+                // ---- A: dS^T = sum over chunks of V^T K', one accumulator
                 const uint32_t dA = dsc & 1;
                 if (dsc >= 2) ok = W(&ds_free[dA], (dsc >> 1) - 1);
                 for (int r = 0; r < info.nch && ok; ++r) {
@@ -372,11 +372,12 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                     ++kpc;
                     TRACE(1, 1, r);
                     tc::tc_fence_after();
-                    const uint32_t v_s = sb + st * kStage + 2 * kTile;
+                    const uint32_t v_s = sb + st * kStage + kTile;
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        tc::umma_bf16(tmem + kTdS + 128 * dA, desc_mn8(sb + kKp + kb * kTile + ks * 2048),
-                                      desc_mn8(v_s + ks * 2048), kIdescS, (r > 0 || ks > 0) ? 1u : 0u);
+                        tc::umma_bf16(tmem + kTdS + 128 * dA, desc_mn8(v_s + ks * 2048),
+                                      desc_mn8(sb + kKp + kb * kTile + ks * 2048), kIdescS,
+                                      (r > 0 || ks > 0) ? 1u : 0u);
                     tc::umma_commit(&kp_free[kb]);
                     tc::umma_commit(&empty[st]);
                     ++job;
@@ -388,49 +389,48 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 const uint32_t sb_base = sbc;
                 for (int c = 0; c < info.nch && ok; ++c) {
                     const uint32_t st = job % kStages;
-                    const uint32_t q_s = sb + st * kStage, k_s = q_s + kTile, v_s = q_s + 2 * kTile;
-                    const uint32_t pb = cc & 1;
-                    if (!W(&full[st], job / kStages)) { ok = false; break; }
-                    const bool fast = meta[st].fast != 0;
-                    // M1: P = Q K''^T (factored route) or Q K^T (exact route)
+                    const uint32_t q_s = sb + st * kStage, v_s = q_s + kTile;
+                    const uint32_t ob = cc & 1;
                     const uint32_t kb = kpc & 1;
-                    if (!W(&kp_ready[kb], kpc >> 1)) { ok = false; break; }
+                    if (!W(&full[st], job / kStages) || !W(&kp_ready[kb], kpc >> 1)) { ok = false; break; }
                     ++kpc;
-                    if (cc >= 2 && !W(&p_free[pb], (cc >> 1) - 1)) { ok = false; break; }
+                    const bool fast = kfast[kb] != 0;
+                    // M1: P = Q K''^T (factored route) or Q K^T (exact route)
+                    if (cc >= 1 && !W(&p_free, cc - 1)) { ok = false; break; }
                     TRACE(1, 2, c);
                     tc::tc_fence_after();
-                    const uint32_t kp_s = sb + kKp + kb * kTile;
-                    const uint32_t kb_s = fast ? kp_s : k_s;
+                    const uint32_t k1 = sb + (fast ? kKp : kKr) + kb * kTile;
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
-                        tc::umma_bf16(tmem + kTP + 64 * pb, desc_k(q_s + off), desc_k(kb_s + off),
-                                      kIdescP, ks > 0);
+                        tc::umma_bf16(tmem + kTP, desc_k(q_s + off), desc_k(k1 + off), kIdescP, ks > 0);
                     }
-                    tc::umma_commit(&p_full[pb]);
-                    // M4: dS = K''^T V or K'^T V
-                    const uint32_t db = dsc & 1;
-                    if (dsc >= 2 && !W(&ds_free[db], (dsc >> 1) - 1)) { ok = false; break; }
-                    TRACE(1, 3, c);
+                    tc::umma_commit(&p_full);
+                    // M4: dS^T = V^T K~ (not needed after the last chunk)
+                    if (c + 1 < info.nch) {
+                        const uint32_t db = dsc & 1;
+                        if (dsc >= 2 && !W(&ds_free[db], (dsc >> 1) - 1)) { ok = false; break; }
+                        TRACE(1, 3, c);
+                        tc::tc_fence_after();
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        tc::umma_bf16(tmem + kTdS + 128 * db, desc_mn8(kp_s + ks * 2048),
-                                      desc_mn8(v_s + ks * 2048), kIdescS, ks > 0);
-                    tc::umma_commit(&ds_full[db]);
+                        for (int ks = 0; ks < 4; ++ks)
+                            tc::umma_bf16(tmem + kTdS + 128 * db, desc_mn8(v_s + ks * 2048),
+                                          desc_mn8(sb + kKp + kb * kTile + ks * 2048), kIdescS, ks > 0);
+                        tc::umma_commit(&ds_full[db]);
+                        ++dsc;
+                    }
                     tc::umma_commit(&kp_free[kb]);
-                    ++dsc;
                     // M2: O^T = S^T Q^T (Q scaled in place first on the exact route)
-                    const uint32_t sbu = sb_base + c;
-                    if (!W(&sb_ready, sbu)) { ok = false; break; }
-                    if (cc >= 2 && !W(&o_free[pb], (cc >> 1) - 1)) { ok = false; break; }
+                    if (!W(&sb_ready, sb_base + c)) { ok = false; break; }
+                    if (cc >= 2 && !W(&o_free[ob], (cc >> 1) - 1)) { ok = false; break; }
                     if (!fast && !W(&pp_ready, cc)) { ok = false; break; }
                     TRACE(1, 4, c);
                     tc::tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t b_off = (ks >> 2) * kRegion + (ks & 3) * 32;
-                        tc::umma_bf16(tmem + kTO + 64 * pb, desc_mn16(sb + kSb + ks * 2048),
-                                      desc_k(q_s + b_off), kIdescO, ks > 0);
+                        const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
+                        tc::umma_bf16_ta(tmem + kTO + 64 * ob, tmem + kTSb + 8 * ks, desc_k(q_s + off),
+                                         kIdescO2, ks > 0);
                     }
                     tc::umma_commit(&sb_free);
                     // M3: O^T += V^T P'^T
@@ -439,9 +439,9 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                     tc::tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        tc::umma_bf16(tmem + kTO + 64 * pb, desc_mn8(v_s + ks * 2048),
-                                      desc_k(sb + kPp + ks * 32), kIdescO, 1u);
-                    tc::umma_commit(&o_full[pb]);
+                        tc::umma_bf16(tmem + kTO + 64 * ob, desc_mn8(v_s + ks * 2048),
+                                      desc_k(sb + kPp + ks * 32), kIdescO3, 1u);
+                    tc::umma_commit(&o_full[ob]);
                     tc::umma_commit(&pp_free);
                     tc::umma_commit(&empty[st]);
                     ++job;
@@ -455,7 +455,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             tc::umma_commit(&drain);
             tc::mbar_wait(&drain, 0, kWaitNs);
         }
-    } else if (warp == 10) {
+    } else if (warp == 2) {
         // =============================== publisher ===============================
         if (lane == 0) {
             uint32_t us = 0, pc = 0;
@@ -473,36 +473,220 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 ++us;
             }
         }
-    } else {
-        // =============================== epilogue warpgroups ===============================
-        // Waits inside a chunk do not vote: a thread whose wait gives up has set the abort
-        // flag, and every later wait returns at once, so all threads still pass the same
-        // barriers; one OR-vote per chunk (and per hand-off) then ends the loop uniformly.
-        const int wg = (warp - 2) >> 2;
-        const int wtid = threadIdx.x - 64 - 128 * wg;
+    } else if (warp >= 4 && warp < 8) {
+        // =============================== scaling warps ===============================
+        // Thread wtid makes row s = wtid & 63, columns 64 * (wtid >> 6) .. + 64 of each K~ tile.
+        const int wtid = threadIdx.x - 128;
+        const int srow = wtid & 63, shalf = wtid >> 6;
         const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;   // state row i / value column j
-        const int bar_id = 1 + wg;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        const int jc0 = 64 * wg;
-        float *vals = reinterpret_cast<float *>(sm + kVals) + 64 * wg;
-        uint32_t job = 0, us = 0, kpc = 0, dsc = 0, cc = 0, sbc = 0;
-        float S[64];
+        constexpr int kBar = 1;
+        const uint64_t keep = tc::policy_evict_last(), drop = tc::policy_evict_first();
+        uint32_t us = 0, kpc = 0, cc = 0, job = 0;   // job: stage counter as the producer's
 
-        // K' for one chunk (warpgroup 0): factors exp(base - b_t) into K' buffer kpc & 1
-        auto make_kprime = [&](uint32_t st, float base) {
+        // K rows and raw g of a chunk still to scale, loaded ahead into registers (two jobs ahead
+        // in the state pass, one in the output pass, which has the scores to do in between)
+        uint4 kx[8], ky[8];
+        float2 graw = make_float2(0.f, 0.f), gry = make_float2(0.f, 0.f);
+        auto prefetch_into = [&](uint4 (&buf)[8], float2 &gb, int64_t c0, int nv, int h,
+                                 bool state_pass) {
+            gb = load_gate(a.g, c0, nv, H, h);
+            if (srow < nv) {
+                const uint8_t *src = reinterpret_cast<const uint8_t *>(
+                    a.k + ((c0 + srow) * H + h) * kD + 64 * shalf);
+                const uint64_t pol = state_pass ? keep : drop;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) buf[c8] = tc::ldg_nc_hint(src + 16 * c8, pol);
+            } else {
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) buf[c8] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        };
+        auto prefetch = [&](int64_t c0, int nv, int h, bool state_pass) {
+            prefetch_into(kx, graw, c0, nv, h, state_pass);
+        };
+        // K~ = K exp(base - b_s) into buffer kpc & 1 (and raw K if `raw`); rows >= nv zero.
+        auto make_k = [&](const uint4 (&x)[8], const Gate &G, float base, int nv, bool raw,
+                          int fast_flag) {
             const uint32_t kb = kpc & 1;
             wait_nv(&kp_free[kb], (kpc >> 1) - 1, kpc >= 2, abort_v, status);
-            if (wtid == 0) TRACE(2, 20, kpc);
-            const ChunkMeta &m = meta[st];
-            scale_rows<8>(sm + st * kStage + kTile, sm + kKp + kb * kTile, wtid, 128, m.nv, m.b,
-                          base * kLog2e, -1.f);
-            if (wtid == 0) TRACE(2, 21, kpc);
+            if (wtid == 0) TRACE(2, 9, kpc);
+            const float bs = gate_at(G, srow);
+            const float fac = srow < nv ? tc::ex2((base - bs) * kLog2e) : 0.f;
+            store_row_scaled(sm + kKp + kb * kTile + shalf * kRegion,
+                             raw ? sm + kKr + kb * kTile + shalf * kRegion : nullptr, srow, x, fac);
+            if (wtid == 0) TRACE(2, 10, kpc);
             tc::fence_proxy_async_smem();
-            named_sync(bar_id, 128);
-            if (wtid == 0) TRACE(2, 22, kpc);
-            if (wtid == 0) tc::mbar_arrive(&kp_ready[kb]);
+            named_sync(kBar, 128);
+            if (wtid == 0) {
+                kfast[kb] = fast_flag;
+                tc::mbar_arrive(&kp_ready[kb]);
+            }
             ++kpc;
+        };
+
+        for (;;) {
+            const uint32_t slot = us & 1;
+            if (!wg_wait(&unit_full[slot], us >> 1, true, kBar, abort_v, status)) break;
+            const UnitInfo info = units[slot];
+            named_sync(kBar, 128);
+            if (wtid == 0) tc::mbar_arrive(&unit_empty[slot]);
+            if (!info.valid) break;
+            const int h = info.h, nch = info.nch;
+            auto chunk_c0 = [&](int idx) { return info.t0 + int64_t(idx) * kChunk; };
+            auto chunk_nv = [&](int idx) {
+                return static_cast<int>(min(int64_t(kChunk), info.t1 - chunk_c0(idx)));
+            };
+
+            // ---------------- A: K' = K exp(B_end - B_s), chunks last to first ----------------
+            // job r is chunk nch - 1 - r; job nch is the output pass's chunk 0. Jobs alternate
+            // between the register buffers (kx, graw) and (ky, gry).
+            auto job_c0 = [&](int r) { return chunk_c0(r < nch ? nch - 1 - r : 0); };
+            auto job_nv = [&](int r) { return chunk_nv(r < nch ? nch - 1 - r : 0); };
+            prefetch_into(kx, graw, job_c0(0), job_nv(0), h, true);
+            prefetch_into(ky, gry, job_c0(1), job_nv(1), h, nch > 1);
+            float D = 0.f;   // total log-decay of the chunks already visited (the later ones)
+            auto a_job = [&](int r, uint4 (&buf)[8], float2 &gb) {
+                const int nv = job_nv(r);
+                if (wtid == 0) TRACE(2, 1, r);
+                const Gate G = scan_gate(gb, nv);
+                if (wtid == 0) TRACE(2, 7, r);
+                make_k(buf, G, G.bC + D, nv, false, 1);
+                if (wtid == 0) TRACE(2, 8, r);
+                D += G.bC;
+                if (r + 2 <= nch) prefetch_into(buf, gb, job_c0(r + 2), job_nv(r + 2), h, r + 2 < nch);
+            };
+            for (int r = 0; r < nch; r += 2) {
+                a_job(r, kx, graw);
+                if (r + 1 < nch) a_job(r + 1, ky, gry);
+            }
+            if (nch & 1) {   // the output pass's chunk 0 went to the second buffer
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) kx[c8] = ky[c8];
+                graw = gry;
+            }
+            wait_nv(&d_free, us - 1, us >= 1, abort_v, status);
+            if (wtid == 0) {
+                unit_D = D;
+                tc::mbar_arrive(&d_ready);
+            }
+
+            // ---------------- C ----------------
+            // K~ of chunk 0; then per chunk: K~ of the next chunk, P' of this one
+            Gate Gc = scan_gate(graw, chunk_nv(0));
+            make_k(kx, Gc, Gc.fast ? 0.f : Gc.bC, chunk_nv(0), !Gc.fast, Gc.fast);
+            if (nch > 1) prefetch(chunk_c0(1), chunk_nv(1), h, false);
+            for (int c = 0; c < nch; ++c) {
+                const int64_t c0 = chunk_c0(c);
+                const int nv = chunk_nv(c);
+                const Gate G = Gc;
+                if (c + 1 < nch) {
+                    const int nv1 = chunk_nv(c + 1);
+                    Gc = scan_gate(graw, nv1);
+                    make_k(kx, Gc, Gc.fast ? 0.f : Gc.bC, nv1, !Gc.fast, Gc.fast);
+                    if (c + 2 < nch) prefetch(chunk_c0(c + 2), chunk_nv(c + 2), h, false);
+                    if (wtid == 0) TRACE(2, 3, c);
+                }
+                // scores -> P' (bf16, K-major rows t): mask s <= t < nv; exact route weights
+                wait_nv(&p_full, cc, true, abort_v, status);
+                wait_nv(&pp_free, cc - 1, cc >= 1, abort_v, status);
+                if (wtid == 0) TRACE(2, 5, c);
+                tc::tc_fence_after();
+                // M=64 accumulator layout: row t = 16 * quarter + lane in lanes 0-15
+                const int tr = quarter * 16 + (lane & 15);
+                const float bt = gate_at(G, tr) * kLog2e;
+                uint8_t *pp = sm + kPp;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t p[32];
+                    tc::tmem_ld_32x32b_x32(tmem + lane_base + kTP + 32 * half, p);
+                    tc::tmem_ld_wait();
+                    if (half == 1) {
+                        tc::tc_fence_before();
+                        named_sync(kBar, 128);
+                        if (wtid == 0) tc::mbar_arrive(&p_free);
+                    }
+                    if (!G.fast) {
+                        // exact route: P'[t, s] = P[t, s] exp(b_t - b_s)
+#pragma unroll
+                        for (int s = 0; s < 32; ++s)
+                            p[s] = __float_as_uint(__uint_as_float(p[s]) *
+                                                   tc::ex2(bt - gate_at(G, 32 * half + s) * kLog2e));
+                    }
+                    if (lane < 16) {
+                        const bool live = tr < nv;
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int si = 8 * c4 + 2 * e, s = 32 * half + si;
+                                const float f0 = (live && s <= tr) ? __uint_as_float(p[si]) : 0.f;
+                                const float f1 = (live && s + 1 <= tr) ? __uint_as_float(p[si + 1]) : 0.f;
+                                w[e] = float2_to_bf16x2(f0, f1);
+                            }
+                            *reinterpret_cast<uint4 *>(pp + sw(tr, 4 * half + c4)) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
+                if (!G.fast) {
+                    // exact route: q_t <- exp(b_t) q_t in place (M1 has read Q already); the
+                    // rows come from global memory, not from the tile
+                    uint8_t *qt = sm + ((job + nch + c) % kStages) * kStage + shalf * kRegion;
+                    uint4 x[8];
+                    if (srow < nv) {
+                        const uint8_t *src = reinterpret_cast<const uint8_t *>(
+                            a.q + ((c0 + srow) * H + h) * kD + 64 * shalf);
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; ++c8) x[c8] = tc::ldg_nc_hint(src + 16 * c8, drop);
+                    } else {
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; ++c8) x[c8] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    store_row_scaled(qt, nullptr, srow, x, tc::ex2(gate_at(G, srow) * kLog2e));
+                }
+                tc::fence_proxy_async_smem();
+                named_sync(kBar, 128);
+                if (wtid == 0) {
+                    tc::mbar_arrive(&pp_ready);
+                    TRACE(2, 6, c);
+                }
+                ++cc;
+            }
+            // one uniform decision per unit (after an abort every wait returns at once, so all
+            // threads still pass the same barriers inside the unit)
+            if (named_any(kBar, 128, *abort_v != 0)) break;
+            job += 2 * nch;
+            ++us;
+        }
+    } else if (warp >= 8) {
+        // =============================== state warps ===============================
+        // Waits inside a unit do not vote: a thread whose wait gives up has set the abort
+        // flag, and every later wait returns at once, so all threads still pass the same
+        // barriers; one OR-vote per hand-off and per unit then ends the loop uniformly.
+        const int wg = (warp - 8) >> 2;
+        const int wtid = threadIdx.x - 256 - 128 * wg;
+        const int quarter = warp & 3;
+        const int j = quarter * 32 + lane;     // value column = TMEM lane
+        const int i0 = 64 * wg;                // my key rows i0 .. i0 + 63
+        const int bar_id = 2 + wg;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        uint32_t us = 0, dsc = 0, cc = 0, sbc = 0;
+        float S[64];   // S^T[j][i0 + i] = S[i0 + i][j]
+
+        // bf16 copy of S^T for M2: my 64 keys -> 32 packed columns of the A operand
+        auto write_sb = [&]() {
+            wait_nv(&sb_free, sbc - 1, sbc >= 1, abort_v, status);
+            uint32_t w[32];
+#pragma unroll
+            for (int m = 0; m < 32; ++m) w[m] = float2_to_bf16x2(S[2 * m], S[2 * m + 1]);
+            tc::tmem_st_32x32b_x32(tmem + lane_base + kTSb + 32 * wg, w);
+            tc::tmem_st_wait();
+            tc::tc_fence_before();
+            named_sync(bar_id, 128);
+            if (wtid == 0) tc::mbar_arrive(&sb_ready);
+            ++sbc;
         };
 
         for (;;) {
@@ -512,30 +696,19 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             named_sync(bar_id, 128);
             if (wtid == 0) tc::mbar_arrive(&unit_empty[slot]);
             if (!info.valid) break;
-            const int h = info.h;
-
-            // ---------------- A: K' = K exp(B_end - B_t) (warpgroup 0) ----------------
-            float D = 0.f;   // total log-decay of the chunks already visited (the later ones)
-            for (int r = 0; r < info.nch; ++r) {
-                const uint32_t st = job % kStages;
-                wait_nv(&full[st], job / kStages, true, abort_v, status);
-                const float bC = meta[st].bC;
-                if (wtid == 0) TRACE(2 + wg, 1, r);
-                if (wg == 0) {
-                    make_kprime(st, bC + D);
-                    if (wtid == 0) tc::mbar_arrive(&empty[st]);
-                } else {
-                    named_sync(bar_id, 128);   // every thread has read this stage's metadata
-                    if (wtid == 0) tc::mbar_arrive(&empty[st]);
-                }
-                D += bC;
-                ++job;
-            }
+            const int h = info.h, nch = info.nch;
+            if (wtid == 0) TRACE(3 + wg, 1, us);
+            WTS(0);
 
             // ---------------- hand-off: S_in, publish S_out, bf16 S_in for M2 ----------------
             {
                 const uint32_t db = dsc & 1;
                 bool bad = !wait_or_abort(&ds_full[db], (dsc >> 1) & 1, abort_v, status);
+                WTS(1);
+                if (wtid == 0) TRACE(3 + wg, 11, us);
+                bad = bad || !wait_or_abort(&d_ready, us & 1, abort_v, status);
+                WTS(2);
+                if (wtid == 0) TRACE(3 + wg, 12, us);
                 ++dsc;
                 if (!bad && !info.first && wtid == 0) {
                     const uint32_t *flag = f.flags + (info.sigma - 1) * H + h;
@@ -550,222 +723,147 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                         }
                     }
                 }
+                WTS(3);
                 if (named_any(bar_id, 128, bad || *abort_v)) break;
-                if (wtid == 0) TRACE(2 + wg, 2, 0);
+                WTS(4);
+                if (wtid == 0) TRACE(3 + wg, 2, 0);
                 tc::tc_fence_after();
                 if (info.first) {
                     if (f.h0) {
-                        const float *src = f.h0 + ((info.n * H + h) * kD + row) * kD + jc0;
+                        const float *src = f.h0 + ((info.n * H + h) * kD + i0) * kD + j;
 #pragma unroll
-                        for (int j = 0; j < 64; j += 4) {
-                            const float4 x = *reinterpret_cast<const float4 *>(src + j);
-                            S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
-                        }
+                        for (int i = 0; i < 64; ++i) S[i] = __ldg(src + i * kD);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 64; ++j) S[j] = 0.f;
+                        for (int i = 0; i < 64; ++i) S[i] = 0.f;
                     }
                 } else {
-                    const float *src = f.incl + (static_cast<size_t>(info.sigma - 1) * H + h) * kD * kD +
-                                       row * kD + jc0;
+                    // the predecessor's S_out, written by another SM: read through L2
+                    const float *src = f.incl + ((static_cast<size_t>(info.sigma - 1) * H + h) * kD + i0) * kD + j;
 #pragma unroll
-                    for (int j = 0; j < 64; j += 4) {
-                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(src + j));
-                        S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
-                    }
+                    for (int i = 0; i < 64; ++i) S[i] = __ldcg(src + i * kD);
                 }
-                const float eB = tc::ex2(D * kLog2e);
-                float *dst = info.last ? (f.hT ? f.hT + ((info.n * H + h) * kD + row) * kD + jc0 : nullptr)
-                                       : f.incl + (static_cast<size_t>(info.sigma) * H + h) * kD * kD +
-                                             row * kD + jc0;
+                if (wtid == 0) TRACE(3 + wg, 13, us);
+                const float eB = tc::ex2(unit_D * kLog2e);
+                named_sync(bar_id, 128);
+                if (wtid == 0) tc::mbar_arrive(&d_free);
+                // S_out = exp(B) S_in + dS: to hT (last segment) or to the successor; each warp
+                // store covers one 128-byte row segment (32 consecutive j)
+                float *dst = info.last ? (f.hT ? f.hT + (info.n * H + h) * kD * kD : nullptr)
+                                       : f.incl + (static_cast<size_t>(info.sigma) * H + h) * kD * kD;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t d[32];
-                    tc::tmem_ld_32x32b_x32(tmem + lane_base + kTdS + 128 * db + jc0 + 32 * half, d);
+                    tc::tmem_ld_32x32b_x32(tmem + lane_base + kTdS + 128 * db + i0 + 32 * half, d);
                     tc::tmem_ld_wait();
                     if (dst) {
+                        float *p = dst + (i0 + 32 * half) * kD + j;
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4 *>(dst + 32 * half + j) = make_float4(
-                                fmaf(eB, S[32 * half + j], __uint_as_float(d[j])),
-                                fmaf(eB, S[32 * half + j + 1], __uint_as_float(d[j + 1])),
-                                fmaf(eB, S[32 * half + j + 2], __uint_as_float(d[j + 2])),
-                                fmaf(eB, S[32 * half + j + 3], __uint_as_float(d[j + 3])));
+                        for (int i = 0; i < 32; ++i)
+                            p[i * kD] = fmaf(eB, S[32 * half + i], __uint_as_float(d[i]));
                     }
                 }
+                if (wtid == 0) TRACE(3 + wg, 14, us);
                 tc::tc_fence_before();
                 named_sync(bar_id, 128);
                 if (wtid == 0) {
                     tc::mbar_arrive(&ds_free[db]);
                     if (!info.last) tc::mbar_arrive(&pub_ready);   // publisher fences and flags
                 }
-                // bf16 S_in for the first chunk's M2
-                wait_nv(&sb_free, sbc - 1, sbc >= 1, abort_v, status);
-                store_bf16_row64(sm + kSb + wg * kSRegion, row, S);
-                tc::fence_proxy_async_smem();
-                named_sync(bar_id, 128);
-                if (wtid == 0) tc::mbar_arrive(&sb_ready);
-                ++sbc;
-                if (wtid == 0) TRACE(2 + wg, 3, 0);
+                write_sb();
+                if (wtid == 0) TRACE(3 + wg, 3, 0);
             }
 
             // ---------------- C ----------------
-            if (wg == 0) {
-                // K'' of chunk 0 (warpgroup 0 stays one chunk ahead)
-                const uint32_t st = job % kStages;
-                wait_nv(&full[st], job / kStages, true, abort_v, status);
-                make_kprime(st, meta[st].fast ? 0.f : meta[st].bC);
-            }
-            bool ok = true;
-            for (int c = 0; c < info.nch; ++c) {
-                const uint32_t st = job % kStages;
-                const uint32_t pb = cc & 1;
+            float2 graw = load_gate(a.g, info.t0, static_cast<int>(min(int64_t(kChunk), info.t1 - info.t0)), H, h);
+            for (int c = 0; c < nch; ++c) {
                 const int64_t c0 = info.t0 + int64_t(c) * kChunk;
-                wait_nv(&full[st], job / kStages, true, abort_v, status);
-                const ChunkMeta &md = meta[st];
-                const int nv = md.nv;
-                const bool fast = md.fast != 0;
-                const float eC = tc::ex2(md.bC * kLog2e);
-                if (wtid == 0) TRACE(2 + wg, 4, c);
+                const int nv = static_cast<int>(min(int64_t(kChunk), info.t1 - c0));
+                const Gate G = scan_gate(graw, nv);
+                if (c + 1 < nch)
+                    graw = load_gate(a.g, c0 + kChunk, static_cast<int>(min(int64_t(kChunk), info.t1 - c0 - kChunk)), H, h);
+                if (wtid == 0) TRACE(3 + wg, 4, c);
 
-                if (wg == 0) {
-                    // (a) K'' of the next chunk: exp(-b_s) (factored) or exp(b_C - b_s) (exact)
-                    if (c + 1 < info.nch) {
-                        const uint32_t sn = (job + 1) % kStages;
-                        wait_nv(&full[sn], (job + 1) / kStages, true, abort_v, status);
-                        make_kprime(sn, meta[sn].fast ? 0.f : meta[sn].bC);
-                    }
-                    // (b) scores -> P' (bf16, K-major rows t)
-                    wait_nv(&p_full[pb], cc >> 1, true, abort_v, status);
-                    wait_nv(&pp_free, cc - 1, cc >= 1, abort_v, status);
-                    if (wtid == 0) TRACE(2, 5, c);
-                    tc::tc_fence_after();
-                    // M=64 accumulator layout: row t = 16 * quarter + lane in lanes 0-15
-                    const int tr = quarter * 16 + (lane & 15);
-                    const float bt = md.b[tr] * kLog2e;
-                    uint8_t *pp = sm + kPp;
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t p[32];
-                        tc::tmem_ld_32x32b_x32(tmem + lane_base + kTP + 64 * pb + 32 * half, p);
-                        tc::tmem_ld_wait();
-                        if (wtid == 0) TRACE(2, 23 + half, c);
-                        if (half == 1) {
-                            tc::tc_fence_before();
-                            named_sync(bar_id, 128);
-                            if (wtid == 0) tc::mbar_arrive(&p_free[pb]);
-                            if (wtid == 0) TRACE(2, 25, c);
-                        }
-                        if (lane < 16) {
-                            uint32_t w[16];
-#pragma unroll
-                            for (int e = 0; e < 32; e += 2) {
-                                const int sc = 32 * half + e;
-                                float f0 = __uint_as_float(p[e]), f1 = __uint_as_float(p[e + 1]);
-                                if (!fast) {
-                                    f0 *= tc::ex2(bt - md.b[sc] * kLog2e);
-                                    f1 *= tc::ex2(bt - md.b[sc + 1] * kLog2e);
-                                }
-                                w[e >> 1] = float2_to_bf16x2(sc <= tr ? f0 : 0.f, sc + 1 <= tr ? f1 : 0.f);
-                            }
-#pragma unroll
-                            for (int c8 = 0; c8 < 4; ++c8)
-                                *reinterpret_cast<uint4 *>(pp + sw(tr, 4 * half + c8)) =
-                                    make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
-                        }
-                    }
-                    if (wtid == 0) TRACE(2, 26, c);
-                    if (!fast) {
-                        // exact route: q_t <- exp(b_t) q_t in place (M1 has read Q already)
-                        uint8_t *qt = sm + st * kStage;
-                        scale_rows<8>(qt, qt, wtid, 128, nv, md.b, 0.f, 1.f);
-                    }
-                    tc::fence_proxy_async_smem();
-                    named_sync(bar_id, 128);
-                    if (wtid == 0) {
-                        tc::mbar_arrive(&pp_ready);
-                        tc::mbar_arrive(&empty[st]);
-                        TRACE(2, 6, c);
-                    }
-                } else {
-                    // output row factors for (d), then release the stage
-                    if (wtid < 64) vals[wtid] = fast ? a.scale * tc::ex2(md.b[wtid] * kLog2e) : a.scale;
-                    named_sync(bar_id, 128);
-                    if (wtid == 0) tc::mbar_arrive(&empty[st]);
-                }
-
-                // (c) state carry for my 64 columns; bf16 copy for the next chunk's M2
-                {
+                // state carry for my 64 keys; bf16 copy for the next chunk's M2
+                if (c + 1 < nch) {
                     const uint32_t db = dsc & 1;
                     wait_nv(&ds_full[db], dsc >> 1, true, abort_v, status);
                     ++dsc;
-                    if (wtid == 0) TRACE(2 + wg, 7, c);
+                    if (wtid == 0) TRACE(3 + wg, 7, c);
                     tc::tc_fence_after();
+                    const float eC = tc::ex2(G.bC * kLog2e);
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         uint32_t d[32];
-                        tc::tmem_ld_32x32b_x32(tmem + lane_base + kTdS + 128 * db + jc0 + 32 * half, d);
+                        tc::tmem_ld_32x32b_x32(tmem + lane_base + kTdS + 128 * db + i0 + 32 * half, d);
                         tc::tmem_ld_wait();
-                        if (fast) {
+                        if (G.fast) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) S[32 * half + j] = eC * (S[32 * half + j] + __uint_as_float(d[j]));
+                            for (int i = 0; i < 32; ++i) S[32 * half + i] = eC * (S[32 * half + i] + __uint_as_float(d[i]));
                         } else {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) S[32 * half + j] = fmaf(eC, S[32 * half + j], __uint_as_float(d[j]));
+                            for (int i = 0; i < 32; ++i) S[32 * half + i] = fmaf(eC, S[32 * half + i], __uint_as_float(d[i]));
                         }
                     }
-                    if (wtid == 0 && wg == 0) TRACE(2, 27, c);
                     tc::tc_fence_before();
                     named_sync(bar_id, 128);
-                    if (wtid == 0 && wg == 0) TRACE(2, 28, c);
                     if (wtid == 0) tc::mbar_arrive(&ds_free[db]);
-                    if (c + 1 < info.nch) {
-                        wait_nv(&sb_free, sbc - 1, sbc >= 1, abort_v, status);
-                        if (wtid == 0 && wg == 0) TRACE(2, 29, c);
-                        store_bf16_row64(sm + kSb + wg * kSRegion, row, S);
-                        if (wtid == 0 && wg == 0) TRACE(2, 30, c);
-                        tc::fence_proxy_async_smem();
-                        named_sync(bar_id, 128);
-                        if (wtid == 0) tc::mbar_arrive(&sb_ready);
-                        ++sbc;
-                    }
-                    if (wtid == 0) TRACE(2 + wg, 8, c);
+                    write_sb();
+                    if (wtid == 0) TRACE(3 + wg, 8, c);
                 }
 
-                if (wg == 1) {
-                    // (d) o_t = factor_t * O[t] for value column j = row; stage, store
-                    wait_nv(&o_full[pb], cc >> 1, true, abort_v, status);
-                    if (wtid == 0) TRACE(3, 9, c);
+                // o_t = factor_t O^T[j][t] for my 32 tokens t = 32 wg + tt: staged as a
+                // [32 t x 128 j] bf16 tile and written by one TMA store (direct stores when the
+                // group has rows past the chunk's valid tokens, which belong to another sequence)
+                {
+                    const uint32_t ob = cc & 1;
+                    wait_nv(&o_full[ob], cc >> 1, true, abort_v, status);
+                    if (wtid == 0) TRACE(3 + wg, 9, c);
                     tc::tc_fence_after();
-                    uint16_t *orow = a.o + (c0 * H + h) * kD + row;   // column j = row of o[c0 + t, h, :]
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t o[32];
-                        tc::tmem_ld_32x32b_x32(tmem + lane_base + kTO + 64 * pb + 32 * half, o);
-                        tc::tmem_ld_wait();
-                        if (half == 1) {
-                            tc::tc_fence_before();
-                            named_sync(bar_id, 128);
-                            if (wtid == 0) tc::mbar_arrive(&o_free[pb]);
-                        }
+                    uint32_t o[32];
+                    tc::tmem_ld_32x32b_x32(tmem + lane_base + kTO + 64 * ob + 32 * wg, o);
+                    tc::tmem_ld_wait();
+                    tc::tc_fence_before();
+                    if (wtid == 0) tc::tma_store_wait_read<0>();   // staging buffer free again
+                    named_sync(bar_id, 128);
+                    if (wtid == 0) tc::mbar_arrive(&o_free[ob]);
+                    // lane l's factor for token 32 wg + l, then broadcast
+                    const float bl = gate_at(G, 32 * wg + lane);
+                    const float fl = G.fast ? a.scale * tc::ex2(bl * kLog2e) : a.scale;
+                    if (32 * wg + 32 <= nv) {
+                        uint8_t *stg = sm + kOst + wg * kOstBytes + 2 * j;
 #pragma unroll
                         for (int tt = 0; tt < 32; ++tt) {
-                            const int t = 32 * half + tt;
-                            if (t < nv)
-                                orow[static_cast<size_t>(t) * H * kD] =
-                                    __bfloat16_as_ushort(__float2bfloat16_rn(vals[t] * __uint_as_float(o[tt])));
+                            const float ft = __shfl_sync(0xffffffffu, fl, tt);
+                            *reinterpret_cast<uint16_t *>(stg + tt * 256) =
+                                __bfloat16_as_ushort(__float2bfloat16_rn(ft * __uint_as_float(o[tt])));
+                        }
+                        tc::fence_proxy_async_smem();
+                        named_sync(bar_id, 128);
+                        if (wtid == 0) {
+                            tc::tma_store_3d(&maps.o, 0, h, static_cast<int32_t>(c0 + 32 * wg),
+                                             sm + kOst + wg * kOstBytes);
+                            tc::tma_store_commit();
+                        }
+                    } else {
+                        uint16_t *orow = a.o + (c0 * H + h) * kD + j;
+#pragma unroll
+                        for (int tt = 0; tt < 32; ++tt) {
+                            const float ft = __shfl_sync(0xffffffffu, fl, tt);
+                            const int tk = 32 * wg + tt;
+                            if (tk < nv)
+                                orow[static_cast<size_t>(tk) * H * kD] =
+                                    __bfloat16_as_ushort(__float2bfloat16_rn(ft * __uint_as_float(o[tt])));
                         }
                     }
-                    if (wtid == 0) TRACE(3, 10, c);
+                    if (wtid == 0) TRACE(3 + wg, 10, c);
                 }
                 ++cc;
-                ++job;
-                // one uniform decision per chunk (also orders the staging buffer's reuse)
-                if (named_any(bar_id, 128, *abort_v != 0)) { ok = false; break; }
             }
-            if (!ok) break;
+            if (named_any(bar_id, 128, *abort_v != 0)) break;
             ++us;
         }
+        if (wtid == 0) tc::tma_store_wait_all<0>();
     }
 
     tc::tc_fence_before();
@@ -775,7 +873,6 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         tc::tmem_dealloc(tmem, kTCols);
     }
 }
-
 // ---------------------------------------------------------------------------------------
 // hT of empty sequences: the initial state (or zeros). One block per (sequence, head).
 __global__ void __launch_bounds__(256)
@@ -800,7 +897,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 cudaError_t g_encode_err = cudaSuccess;
 std::once_flag g_encode_once;
 
-cudaError_t encode_map(CUtensorMap *map, const void *base, int64_t T_total, int H) {
+cudaError_t encode_map(CUtensorMap *map, const void *base, int64_t T_total, int H, bool store) {
     std::call_once(g_encode_once, []() {
         cudaDriverEntryPointQueryResult q;
         g_encode_err = cudaGetDriverEntryPointByVersion(
@@ -813,21 +910,23 @@ cudaError_t encode_map(CUtensorMap *map, const void *base, int64_t T_total, int 
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H),
                           static_cast<cuuint64_t>(T_total)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(H) * kD * 2};
-    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t box_load[3] = {64, 1, 64}, box_store[3] = {128, 1, 32};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          strides, store ? box_store : box_load, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          store ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 }  // namespace
 
-cudaError_t make_maps(TcMaps *m, const void *q, const void *k, const void *v, int64_t T_total,
-                      int H) {
-    cudaError_t e = encode_map(&m->q, q, T_total, H);
-    if (e == cudaSuccess) e = encode_map(&m->k, k, T_total, H);
-    if (e == cudaSuccess) e = encode_map(&m->v, v, T_total, H);
+cudaError_t make_maps(TcMaps *m, const void *q, const void *k, const void *v, const void *o,
+                      int64_t T_total, int H) {
+    cudaError_t e = encode_map(&m->q, q, T_total, H, false);
+    if (e == cudaSuccess) e = encode_map(&m->k, k, T_total, H, false);
+    if (e == cudaSuccess) e = encode_map(&m->v, v, T_total, H, false);
+    if (e == cudaSuccess) e = encode_map(&m->o, o, T_total, H, true);
     return e;
 }
 
@@ -844,7 +943,7 @@ cudaError_t launch_prefill_fused(const ChunkArgs &a, const SegTable &t, int64_t 
                                  int *status, cudaStream_t st) {
     if (T_total > 0 && max_units > 0) {
         tck::TcMaps maps;
-        cudaError_t e = tck::make_maps(&maps, a.q, a.k, a.v, T_total, a.H);
+        cudaError_t e = tck::make_maps(&maps, a.q, a.k, a.v, a.o, T_total, a.H);
         if (e != cudaSuccess) return e;
         FusedArgs f;
         f.c = a;
@@ -872,13 +971,16 @@ cudaError_t launch_prefill_fused(const ChunkArgs &a, const SegTable &t, int64_t 
 }  // namespace sala
 
 #ifdef SALA_TRACE
+extern "C" int sala_gla_debug_wts(long long *out) {
+    return cudaMemcpyFromSymbol(out, sala::g_wts, sizeof(sala::g_wts)) == cudaSuccess ? 0 : -1;
+}
 extern "C" int sala_gla_debug_trace(unsigned long long *out, int max) {
-    unsigned int n[4];
+    unsigned int n[5];
     if (cudaMemcpyFromSymbol(n, sala::g_trace_n, sizeof(n)) != cudaSuccess) return -1;
-    static unsigned long long buf[4][sala::kTraceN];
+    static unsigned long long buf[5][sala::kTraceN];
     if (cudaMemcpyFromSymbol(buf, sala::g_trace, sizeof(buf)) != cudaSuccess) return -1;
     int k = 0;
-    for (int r = 0; r < 4; ++r)
+    for (int r = 0; r < 5; ++r)
         for (unsigned i = 0; i < n[r] && i < static_cast<unsigned>(sala::kTraceN) && k < max; ++i)
             out[k++] = buf[r][i];
     return k;

@@ -39,7 +39,7 @@ __device__ __forceinline__ bool named_any(int id, int n, bool x) {
 // How the bounded waits poll: SALA_WAIT_POLL_NS > 0 tests the phase without suspending and
 // sleeps that long between tests; 0 uses try_wait, which may suspend the thread in hardware.
 #ifndef SALA_WAIT_POLL_NS
-#define SALA_WAIT_POLL_NS 64
+#define SALA_WAIT_POLL_NS 0
 #endif
 
 // Bounded wait that also gives up as soon as another role has aborted.
@@ -80,6 +80,13 @@ __device__ __forceinline__ float2 warp_chunk_cumsum(const float *__restrict__ g,
 __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t w, float s) {
     const float2 f = bf16x2_to_float2(w);
     return float2_to_bf16x2(f.x * s, f.y * s);
+}
+
+// Two bf16 times a bf16 factor pair, rounded to nearest (one packed multiply).
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t w, __nv_bfloat162 f2) {
+    __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&w);
+    __nv_bfloat162 y = __hmul2(x, f2);
+    return *reinterpret_cast<uint32_t *>(&y);
 }
 
 struct TcMaps {

@@ -33,19 +33,23 @@
 //   M2  O^T  = S^T Q^T     M=128 N=64  K=128   A=S^T bf16 in TMEM     B=Q smem (K-major)
 //   M3  O^T += V^T P'^T    M=128 N=64  K=64    A=V smem (MN-major)    B=P' smem (K-major)
 //   M4  dS^T = V^T K~      M=128 N=128 K=64    A=V smem (MN-major)    B=K~ smem (MN-major)
-// K~ is k scaled per token (the factors above); the scaling warps make it from a global load
-// straight into shared memory, so no warp reads shared memory with ordinary loads while the
-// tensor core streams its operands from it (such loads stall far behind the tensor core's).
-// Q and V tiles arrive by TMA.
+// K~ is k scaled per token (the factors above). In the state pass the K tile arrives by TMA
+// and is scaled in place in shared memory (the tensor core only runs the short M4 there). In
+// the output pass, where the tensor core streams operands most of the time, the scaling
+// warps make K~ from a global load straight into shared memory instead: ordinary
+// shared-memory loads issued while the tensor core reads its operands stall far behind them.
+// Q and V tiles arrive by TMA, o leaves by TMA stores.
 //
-// Roles: warp 0 loads (TMA), warp 1 issues MMAs and owns the tensor memory, warp 2 publishes
-// hand-off flags, warps 4-7 scale K, turn scores into P' and (exact route) scale Q, warps
-// 8-11 and 12-15 each own 64 of the state's key rows i (all 128 value columns j, one per
-// lane), carry the state, and write o for 32 of the chunk's tokens. Every per-token factor is
-// computed by the warp that needs it from g (an in-warp prefix sum), never passed through
-// shared memory. Every wait is bounded (2 s of %globaltimer); a timeout records
-// SALA_ERR_TIMEOUT, stops the CTA's work, drains its copies and MMAs, frees its tensor memory
-// and returns.
+// Roles: warp 0 loads (TMA), warp 1 issues MMAs and owns the tensor memory, warps 4-7 scale K,
+// turn scores into P' and (exact route) scale Q, warps 8-11 and 12-15 each own 64 of the
+// state's key rows i (all 128 value columns j, one per lane), carry the state, publish the
+// hand-off flag and write o for 32 of the chunk's tokens. Every per-token factor is computed
+// by the warp that needs it from g (an in-warp prefix sum), never passed through shared
+// memory. mbarrier waits compare phase parity only, so every barrier has at most one phase
+// in flight per waiter: each waiter consumes every phase of the barriers it waits on, and a
+// producer cannot complete a second phase before its consumer has consumed the first.
+// Every wait is bounded (2 s of %globaltimer); a timeout records SALA_ERR_TIMEOUT, stops the
+// CTA's work, drains its copies and MMAs, frees its tensor memory and returns.
 #include "chunk_tc.cuh"
 
 namespace sala {
@@ -178,12 +182,12 @@ __device__ __forceinline__ void wait_nv(uint64_t *bar, uint32_t par, bool need,
     if (need) (void)wait_or_abort(bar, par & 1, abort_v, status);
 }
 
-// Bounded wait on an mbarrier phase by every thread of a warpgroup (if `need`), then an
-// OR-vote so that all 128 threads take the same branch. Returns false if any thread failed.
+// Bounded wait on an mbarrier phase by every thread of a group of n threads (if `need`),
+// then an OR-vote so that all of them take the same branch. Returns false if any failed.
 __device__ __forceinline__ bool wg_wait(uint64_t *bar, uint32_t par, bool need, int bar_id,
-                                        volatile int *abort_v, int *status) {
+                                        volatile int *abort_v, int *status, int n = 128) {
     const bool bad = need ? !wait_or_abort(bar, par & 1, abort_v, status) : false;
-    return !named_any(bar_id, 128, bad);
+    return !named_any(bar_id, n, bad);
 }
 
 // 64 bf16 of one row, scaled by f, to a [64 x 128 B] SW128 region row (and, if raw_dst, also
@@ -210,7 +214,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
     __shared__ uint64_t full[kStages], empty[kStages], unit_full[2], unit_empty[2];
-    __shared__ uint64_t kp_ready[2], kp_free[2], pub_ready, drain;
+    __shared__ uint64_t kp_ready[2], kp_free[2], ka_ready[kStages], drain;
     __shared__ uint64_t ds_full[2], ds_free[2], p_full, p_free, pp_ready, pp_free;
     __shared__ uint64_t o_full[2], o_free[2], sb_ready, sb_free;
     __shared__ uint64_t d_ready, d_free;
@@ -234,7 +238,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&unit_full[i], 1);
-            tc::mbar_init(&unit_empty[i], 5);   // MMA, publisher, scaler, two state groups
+            tc::mbar_init(&unit_empty[i], 4);   // MMA, scaler, two state groups
             tc::mbar_init(&kp_ready[i], 1);
             tc::mbar_init(&kp_free[i], 1);
             tc::mbar_init(&ds_full[i], 1);
@@ -248,8 +252,10 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         tc::mbar_init(&pp_free, 1);
         tc::mbar_init(&sb_ready, 2);
         tc::mbar_init(&sb_free, 1);
-        tc::mbar_init(&pub_ready, 2);
         tc::mbar_init(&drain, 1);
+        for (int s = 0; s < kStages; ++s)
+            tc::mbar_init(&ka_ready[s], 1);   // the state-pass K' tile of this stage is scaled
+                                              // (phases count this stage's state-pass jobs)
         tc::mbar_init(&d_ready, 1);
         tc::mbar_init(&d_free, 2);      // both state groups have read unit_D
         abort_flag = 0;
@@ -278,8 +284,9 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         }
         uint32_t job = 0, us = 0;
         bool ok = true;
-        // one job: V (state pass) or Q and V (output pass) of the chunk at token c0, with L2
-        // prefetches of the chunk's K rows and log-decays (read by other warps a little later)
+        // one job: K and V (state pass; K goes to the first tile of the stage) or Q and V
+        // (output pass) of the chunk at token c0, with L2 prefetches of the chunk's log-decays
+        // (read by other warps a little later)
         auto load_job = [&](int64_t c0, int nv, int h, bool with_q) -> bool {
             const uint32_t st = job % kStages;
             bool bad = false;
@@ -292,11 +299,10 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 TRACE(0, with_q ? 2 : 1, job);
                 uint8_t *base = sm + st * kStage;
                 const int32_t x0 = static_cast<int32_t>(c0);
-                tc::mbar_arrive_expect_tx(&full[st], (with_q ? 2 : 1) * kTile);
-                if (with_q) {
-                    tc::tma_load_3d_hint(base, &maps.q, 0, h, x0, &full[st], drop);
-                    tc::tma_load_3d_hint(base + kRegion, &maps.q, 64, h, x0, &full[st], drop);
-                }
+                tc::mbar_arrive_expect_tx(&full[st], 2 * kTile);
+                const CUtensorMap *first = with_q ? &maps.q : &maps.k;
+                tc::tma_load_3d_hint(base, first, 0, h, x0, &full[st], with_q ? drop : keep);
+                tc::tma_load_3d_hint(base + kRegion, first, 64, h, x0, &full[st], with_q ? drop : keep);
                 const uint64_t pol = with_q ? drop : keep;
                 tc::tma_load_3d_hint(base + kTile, &maps.v, 0, h, x0, &full[st], pol);
                 tc::tma_load_3d_hint(base + kTile + kRegion, &maps.v, 64, h, x0, &full[st], pol);
@@ -353,6 +359,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         if (lane == 0) {
             const uint32_t sb = tc::smem_u32(sm);
             uint32_t job = 0, us = 0, kpc = 0, dsc = 0, cc = 0, sbc = 0;
+            uint32_t ka_par = 0;   // bit st: phase parity of ka_ready[st] (state-pass jobs only)
             auto W = [&](uint64_t *bar, uint32_t par) { return wait_or_abort(bar, par & 1, abort_v, status); };
             for (;;) {
                 const uint32_t slot = us & 1;
@@ -366,19 +373,16 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 if (dsc >= 2) ok = W(&ds_free[dA], (dsc >> 1) - 1);
                 for (int r = 0; r < info.nch && ok; ++r) {
                     const uint32_t st = job % kStages;
-                    const uint32_t kb = kpc & 1;
-                    ok = W(&full[st], job / kStages) && W(&kp_ready[kb], kpc >> 1);
+                    ok = W(&full[st], job / kStages) && W(&ka_ready[st], (ka_par >> st) & 1);
                     if (!ok) break;
-                    ++kpc;
+                    ka_par ^= 1u << st;
                     TRACE(1, 1, r);
                     tc::tc_fence_after();
-                    const uint32_t v_s = sb + st * kStage + kTile;
+                    const uint32_t k_s = sb + st * kStage, v_s = k_s + kTile;   // K' scaled in place
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
                         tc::umma_bf16(tmem + kTdS + 128 * dA, desc_mn8(v_s + ks * 2048),
-                                      desc_mn8(sb + kKp + kb * kTile + ks * 2048), kIdescS,
-                                      (r > 0 || ks > 0) ? 1u : 0u);
-                    tc::umma_commit(&kp_free[kb]);
+                                      desc_mn8(k_s + ks * 2048), kIdescS, (r > 0 || ks > 0) ? 1u : 0u);
                     tc::umma_commit(&empty[st]);
                     ++job;
                 }
@@ -455,24 +459,6 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             tc::umma_commit(&drain);
             tc::mbar_wait(&drain, 0, kWaitNs);
         }
-    } else if (warp == 2) {
-        // =============================== publisher ===============================
-        if (lane == 0) {
-            uint32_t us = 0, pc = 0;
-            for (;;) {
-                const uint32_t slot = us & 1;
-                if (!wait_or_abort(&unit_full[slot], (us >> 1) & 1, abort_v, status)) break;
-                const UnitInfo info = units[slot];
-                tc::mbar_arrive(&unit_empty[slot]);
-                if (!info.valid) break;
-                if (!info.last) {
-                    if (!wait_or_abort(&pub_ready, (pc++) & 1, abort_v, status)) break;
-                    __threadfence();
-                    tc::st_release_gpu(f.flags + info.sigma * H + info.h, f.epoch);
-                }
-                ++us;
-            }
-        }
     } else if (warp >= 4 && warp < 8) {
         // =============================== scaling warps ===============================
         // Thread wtid makes row s = wtid & 63, columns 64 * (wtid >> 6) .. + 64 of each K~ tile.
@@ -484,26 +470,23 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         const uint64_t keep = tc::policy_evict_last(), drop = tc::policy_evict_first();
         uint32_t us = 0, kpc = 0, cc = 0, job = 0;   // job: stage counter as the producer's
 
-        // K rows and raw g of a chunk still to scale, loaded ahead into registers (two jobs ahead
-        // in the state pass, one in the output pass, which has the scores to do in between)
-        uint4 kx[8], ky[8];
+        // K rows and raw g of the output-pass chunk still to scale, loaded one chunk ahead into
+        // registers (the scores of the current chunk are done in between); raw g of the
+        // state-pass jobs, two jobs ahead
+        uint4 kx[8];
         float2 graw = make_float2(0.f, 0.f), gry = make_float2(0.f, 0.f);
-        auto prefetch_into = [&](uint4 (&buf)[8], float2 &gb, int64_t c0, int nv, int h,
-                                 bool state_pass) {
-            gb = load_gate(a.g, c0, nv, H, h);
+        auto prefetch = [&](int64_t c0, int nv, int h, bool state_pass) {
+            graw = load_gate(a.g, c0, nv, H, h);
             if (srow < nv) {
                 const uint8_t *src = reinterpret_cast<const uint8_t *>(
                     a.k + ((c0 + srow) * H + h) * kD + 64 * shalf);
                 const uint64_t pol = state_pass ? keep : drop;
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) buf[c8] = tc::ldg_nc_hint(src + 16 * c8, pol);
+                for (int c8 = 0; c8 < 8; ++c8) kx[c8] = tc::ldg_nc_hint(src + 16 * c8, pol);
             } else {
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) buf[c8] = make_uint4(0u, 0u, 0u, 0u);
+                for (int c8 = 0; c8 < 8; ++c8) kx[c8] = make_uint4(0u, 0u, 0u, 0u);
             }
-        };
-        auto prefetch = [&](int64_t c0, int nv, int h, bool state_pass) {
-            prefetch_into(kx, graw, c0, nv, h, state_pass);
         };
         // K~ = K exp(base - b_s) into buffer kpc & 1 (and raw K if `raw`); rows >= nv zero.
         auto make_k = [&](const uint4 (&x)[8], const Gate &G, float base, int nv, bool raw,
@@ -539,32 +522,44 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             };
 
             // ---------------- A: K' = K exp(B_end - B_s), chunks last to first ----------------
-            // job r is chunk nch - 1 - r; job nch is the output pass's chunk 0. Jobs alternate
-            // between the register buffers (kx, graw) and (ky, gry).
-            auto job_c0 = [&](int r) { return chunk_c0(r < nch ? nch - 1 - r : 0); };
-            auto job_nv = [&](int r) { return chunk_nv(r < nch ? nch - 1 - r : 0); };
-            prefetch_into(kx, graw, job_c0(0), job_nv(0), h, true);
-            prefetch_into(ky, gry, job_c0(1), job_nv(1), h, nch > 1);
+            // job r is chunk nch - 1 - r; its K tile arrived by TMA in the first tile of the
+            // stage and is scaled there in place (ordinary shared-memory loads are cheap here:
+            // the tensor core only runs the short state-pass products). The log-decays are
+            // loaded two jobs ahead.
+            auto job_c0 = [&](int r) { return chunk_c0(nch - 1 - r); };
+            auto job_nv = [&](int r) { return chunk_nv(nch - 1 - r); };
+            graw = load_gate(a.g, job_c0(0), job_nv(0), H, h);
+            if (nch > 1) gry = load_gate(a.g, job_c0(1), job_nv(1), H, h);
             float D = 0.f;   // total log-decay of the chunks already visited (the later ones)
-            auto a_job = [&](int r, uint4 (&buf)[8], float2 &gb) {
+            auto a_job = [&](int r, float2 &gb) {
                 const int nv = job_nv(r);
+                const uint32_t st = job % kStages;
                 if (wtid == 0) TRACE(2, 1, r);
                 const Gate G = scan_gate(gb, nv);
+                if (r + 2 < nch) gb = load_gate(a.g, job_c0(r + 2), job_nv(r + 2), H, h);
+                wait_nv(&full[st], job / kStages, true, abort_v, status);
                 if (wtid == 0) TRACE(2, 7, r);
-                make_k(buf, G, G.bC + D, nv, false, 1);
-                if (wtid == 0) TRACE(2, 8, r);
+                const float bs = gate_at(G, srow);
+                const float fac = srow < nv ? tc::ex2((G.bC + D - bs) * kLog2e) : 0.f;
+                uint8_t *kt = sm + st * kStage + shalf * kRegion;
+                uint4 x[8];
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) x[c8] = *reinterpret_cast<const uint4 *>(kt + sw(srow, c8));
+                store_row_scaled(kt, nullptr, srow, x, fac);
+                tc::fence_proxy_async_smem();
+                named_sync(kBar, 128);
+                if (wtid == 0) {
+                    tc::mbar_arrive(&ka_ready[st]);
+                    TRACE(2, 8, r);
+                }
                 D += G.bC;
-                if (r + 2 <= nch) prefetch_into(buf, gb, job_c0(r + 2), job_nv(r + 2), h, r + 2 < nch);
+                ++job;
             };
             for (int r = 0; r < nch; r += 2) {
-                a_job(r, kx, graw);
-                if (r + 1 < nch) a_job(r + 1, ky, gry);
+                a_job(r, graw);
+                if (r + 1 < nch) a_job(r + 1, gry);
             }
-            if (nch & 1) {   // the output pass's chunk 0 went to the second buffer
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) kx[c8] = ky[c8];
-                graw = gry;
-            }
+            prefetch(chunk_c0(0), chunk_nv(0), h, false);
             wait_nv(&d_free, us - 1, us >= 1, abort_v, status);
             if (wtid == 0) {
                 unit_D = D;
@@ -572,8 +567,15 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             }
 
             // ---------------- C ----------------
-            // K~ of chunk 0; then per chunk: K~ of the next chunk, P' of this one
+            // K~ of chunk 0; then per chunk: K~ of the next chunk, P' of this one. The scaling
+            // warps wait on every stage phase (mbarrier waits compare parity only, so a waiter
+            // must not skip phases), although here they read K with ordinary global loads.
+            const uint32_t job_c = job;
+            auto wait_stage = [&](int c) {
+                wait_nv(&full[(job_c + c) % kStages], (job_c + c) / kStages, true, abort_v, status);
+            };
             Gate Gc = scan_gate(graw, chunk_nv(0));
+            wait_stage(0);
             make_k(kx, Gc, Gc.fast ? 0.f : Gc.bC, chunk_nv(0), !Gc.fast, Gc.fast);
             if (nch > 1) prefetch(chunk_c0(1), chunk_nv(1), h, false);
             for (int c = 0; c < nch; ++c) {
@@ -583,6 +585,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 if (c + 1 < nch) {
                     const int nv1 = chunk_nv(c + 1);
                     Gc = scan_gate(graw, nv1);
+                    wait_stage(c + 1);
                     make_k(kx, Gc, Gc.fast ? 0.f : Gc.bC, nv1, !Gc.fast, Gc.fast);
                     if (c + 2 < nch) prefetch(chunk_c0(c + 2), chunk_nv(c + 2), h, false);
                     if (wtid == 0) TRACE(2, 3, c);
@@ -633,7 +636,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 if (!G.fast) {
                     // exact route: q_t <- exp(b_t) q_t in place (M1 has read Q already); the
                     // rows come from global memory, not from the tile
-                    uint8_t *qt = sm + ((job + nch + c) % kStages) * kStage + shalf * kRegion;
+                    uint8_t *qt = sm + ((job_c + c) % kStages) * kStage + shalf * kRegion;
                     uint4 x[8];
                     if (srow < nv) {
                         const uint8_t *src = reinterpret_cast<const uint8_t *>(
@@ -657,14 +660,16 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             // one uniform decision per unit (after an abort every wait returns at once, so all
             // threads still pass the same barriers inside the unit)
             if (named_any(kBar, 128, *abort_v != 0)) break;
-            job += 2 * nch;
+            job = job_c + nch;
             ++us;
         }
     } else if (warp >= 8) {
         // =============================== state warps ===============================
         // Waits inside a unit do not vote: a thread whose wait gives up has set the abort
         // flag, and every later wait returns at once, so all threads still pass the same
-        // barriers; one OR-vote per hand-off and per unit then ends the loop uniformly.
+        // barriers; one OR-vote per hand-off and per unit, taken over both groups together
+        // (they also share a barrier in the hand-off), then ends the loop uniformly.
+        constexpr int kBarBoth = 4;
         const int wg = (warp - 8) >> 2;
         const int wtid = threadIdx.x - 256 - 128 * wg;
         const int quarter = warp & 3;
@@ -691,7 +696,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
 
         for (;;) {
             const uint32_t slot = us & 1;
-            if (!wg_wait(&unit_full[slot], us >> 1, true, bar_id, abort_v, status)) break;
+            if (!wg_wait(&unit_full[slot], us >> 1, true, kBarBoth, abort_v, status, 256)) break;
             const UnitInfo info = units[slot];
             named_sync(bar_id, 128);
             if (wtid == 0) tc::mbar_arrive(&unit_empty[slot]);
@@ -724,7 +729,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                     }
                 }
                 WTS(3);
-                if (named_any(bar_id, 128, bad || *abort_v)) break;
+                if (named_any(kBarBoth, 256, bad || *abort_v)) break;
                 WTS(4);
                 if (wtid == 0) TRACE(3 + wg, 2, 0);
                 tc::tc_fence_after();
@@ -765,10 +770,13 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 }
                 if (wtid == 0) TRACE(3 + wg, 14, us);
                 tc::tc_fence_before();
-                named_sync(bar_id, 128);
-                if (wtid == 0) {
-                    tc::mbar_arrive(&ds_free[db]);
-                    if (!info.last) tc::mbar_arrive(&pub_ready);   // publisher fences and flags
+                named_sync(kBarBoth, 256);   // both state groups have stored S_out and read dS
+                if (wtid == 0) tc::mbar_arrive(&ds_free[db]);
+                if (wg == 0 && wtid == 0 && !info.last) {
+                    // publish for the successor: the barrier orders the groups' stores before
+                    // this thread's device-scope fence and release of the flag
+                    __threadfence();
+                    tc::st_release_gpu(f.flags + info.sigma * H + h, f.epoch);
                 }
                 write_sb();
                 if (wtid == 0) TRACE(3 + wg, 3, 0);
@@ -860,7 +868,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 }
                 ++cc;
             }
-            if (named_any(bar_id, 128, *abort_v != 0)) break;
+            if (named_any(kBarBoth, 256, *abort_v != 0)) break;
             ++us;
         }
         if (wtid == 0) tc::tma_store_wait_all<0>();

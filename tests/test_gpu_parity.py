@@ -99,6 +99,18 @@ def test_prefill_varlen_with_empty_and_short(sg, lens):
             assert torch.equal(hT[n], x["h0"][n])
 
 
+@pytest.mark.parametrize("seed", [11, 12, 13])
+def test_prefill_mixed_segment_shapes(sg, seed):
+    # Many packed sequences whose segments hold every chunk count from 1 to 8 plus ragged
+    # tails, with enough heads that units of different shapes run side by side on one CTA's
+    # pipeline in every order (state-pass and output-pass jobs interleave on the stages).
+    lens = (1, 63, 64, 65, 128, 191, 256, 300, 448, 512, 513, 700, 1023, 1100, 1537, 2048)
+    x = inputs.make_prefill("varlen", seqlens=lens, H=16, seed=seed)
+    o, hT = run_prefill(sg, x)
+    o_ref, h_ref = ref_prefill(x)
+    check(o, hT, o_ref, h_ref)
+
+
 def test_prefill_batched_rows(sg):
     # B = 3 rows of T = 100 without cu_seqlens
     x = small([100], H=2, seed=3)

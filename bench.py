@@ -192,6 +192,12 @@ def summarise_clocks(rows):
 # byte / flop accounting (algorithmic: each input read once, each output written once)
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of
+# each kernel as it stands, on the workload the bench times (profiles/prefill_fused_sala_layer.md,
+# profiles/recurrent_step_decode.md); retaken whenever a kernel changes.
+MEASURED_TRAFFIC = {"prefill_fused": 257_271_296, "recurrent_step": 1_023_500_000}
+
+
 def prefill_bytes(T, H, nseq, has_h0, has_hT):
     per_token = H * (3 * D * 2 + 4 + D * 2)      # q, k, v bf16 + g fp32 + o bf16
     state = nseq * H * D * D * 4
@@ -347,8 +353,9 @@ def run_ours(args, dist):
     }
     if top_name in bytes_per_kernel and top_n:
         ach = bytes_per_kernel[top_name] / (top_ms / top_n / 1e3) / 1e9
+        traffic = MEASURED_TRAFFIC.get(top_name) if w.name == "sala_layer" else None
         roof = {"kernel": top_name, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": traffic,
                 "peak_source": peaks["source"], "mean_launch_us": 1e3 * top_ms / top_n}
     else:
         roof = {"kernel": top_name, "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"],
@@ -473,8 +480,8 @@ def run_decode(args, dist, dev, peaks, sala_gla, inputs):
                    "state_bytes": w.nseq * w.H * D * D * 4, "bytes_per_step": per_step},
         "roofline": {"kernel": "recurrent_step", "bound": "hbm", "achieved": k_ach,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": k_ach / peaks["hbm_gbs"],
-                     "traffic": None, "peak_source": peaks["source"],
-                     "mean_launch_us": 1e3 * kern[0] / kern[1]},
+                     "traffic": MEASURED_TRAFFIC["recurrent_step"] if w.nseq == 256 else None,
+                     "peak_source": peaks["source"], "mean_launch_us": 1e3 * kern[0] / kern[1]},
         "_launches": kern[1],
     }
 

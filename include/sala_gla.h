@@ -77,10 +77,13 @@ typedef enum {
  *   B, T, H    sizes; B >= 1, T >= 0, H >= 1. num_seqs >= 1 when cu_seqlens is given,
  *              ignored otherwise.
  *
- * Scratch: the state pass needs per-segment states (64 KB per segment and head). They are
- * taken from a stream-ordered memory pool that the library creates once per device
- * (cudaMallocFromPoolAsync on `stream`) and returned to it when the call's work is done
- * (cudaFreeAsync), so the host never waits. The pool keeps its memory for later calls.
+ * Scratch: the sequences are cut into segments whose states are handed from one segment to
+ * the next (64 KB per segment and head, plus a segment table and one flag word per segment
+ * and head). This scratch is taken from a stream-ordered memory pool that the library
+ * creates once per device (cudaMallocFromPoolAsync on `stream`) and returned to it when the
+ * call's work is done (cudaFreeAsync), so the host never waits. The pool keeps its memory
+ * for later calls. A device-side wait that gives up (2 s) records SALA_ERR_TIMEOUT in the
+ * status word (sala_gla_get_device_status).
  * Errors: SALA_ERR_INVALID_ARG, SALA_ERR_MISALIGNED, SALA_ERR_UNSUPPORTED, SALA_ERR_CUDA.
  */
 int sala_gla_chunk_fwd(const void *q, const void *k, const void *v, const float *g, float scale,
@@ -114,7 +117,7 @@ int sala_gla_recurrent_step(const void *q, const void *k, const void *v, const f
  * further allocation fails), plug-in hosts whose execute path forbids allocation, and
  * latency-critical loops that cannot afford an allocator call, which may synchronise.
  *
- * Its scratch (segment table, per-segment states and decays) lives in one fixed device
+ * Its scratch (segment table, per-segment hand-off states and flags) lives in one fixed device
  * array of SALA_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library. Every GPU that loads
  * the library holds that array until the process exits. The call picks segments long
  * enough for the scratch to fit; when even one segment per sequence does not fit (roughly

@@ -66,8 +66,8 @@ constexpr float kFastRange = 60.f;   // max |b_t| (natural log) for the factored
 constexpr uint32_t kStage = 2 * kTile;              // Q | V
 constexpr uint32_t kKp = kStages * kStage;          // K~ [2] (factored or exact weights)
 constexpr uint32_t kKr = kKp + 2 * kTile;           // raw K [2] (exact-route M1)
-constexpr uint32_t kPp = kKr + 2 * kTile;           // P' (K-major B of M3)
-constexpr uint32_t kOst = kPp + kRegion;            // o staging [2 state groups][32 t][256 B]
+constexpr uint32_t kPp = kKr + 2 * kTile;           // P' [2] (K-major B of M3)
+constexpr uint32_t kOst = kPp + 2 * kRegion;        // o staging [2 state groups][32 t][256 B]
 constexpr uint32_t kOstBytes = 32 * 256;
 constexpr uint32_t kBytes = kOst + 2 * kOstBytes;
 constexpr uint32_t kSmemAlloc = kBytes + 1024;
@@ -100,11 +100,6 @@ struct UnitInfo {
 constexpr int kTraceN = 512;
 __device__ unsigned long long g_trace[5][kTraceN];
 __device__ unsigned int g_trace_n[5];
-__device__ long long g_wts[16][8];
-#define WTS(k)                                                                                \
-    do {                                                                                      \
-        if (blockIdx.x == 0 && lane == 0 && us == 0) g_wts[warp][k] = clock64();             \
-    } while (0)
 #define TRACE(role, ev, idx)                                                                  \
     do {                                                                                      \
         if (blockIdx.x == 0 && tr_i < kTraceN) {                                              \
@@ -119,9 +114,6 @@ __device__ long long g_wts[16][8];
 #else
 #define TRACE(role, ev, idx) \
     do {                     \
-    } while (0)
-#define WTS(k) \
-    do {       \
     } while (0)
 #endif
 
@@ -191,16 +183,27 @@ __device__ __forceinline__ bool wg_wait(uint64_t *bar, uint32_t par, bool need, 
 }
 
 // 64 bf16 of one row, scaled by f, to a [64 x 128 B] SW128 region row (and, if raw_dst, also
-// unscaled to a second tile).
+// unscaled to a second tile). kExact: product in fp32, rounded once; otherwise f is rounded to
+// bf16 and each pair takes one packed multiply (about 5x fewer instructions, one more
+// rounding of the factor: used for the output pass, whose tolerance has more room).
+template <bool kExact>
 __device__ __forceinline__ void store_row_scaled(uint8_t *dst, uint8_t *raw_dst, int row,
                                                  const uint4 (&x)[8], float f) {
+    const __nv_bfloat162 f2 = __float2bfloat162_rn(f);
 #pragma unroll
     for (int c8 = 0; c8 < 8; ++c8) {
         uint4 y;
-        y.x = mul_bf16x2(x[c8].x, f);
-        y.y = mul_bf16x2(x[c8].y, f);
-        y.z = mul_bf16x2(x[c8].z, f);
-        y.w = mul_bf16x2(x[c8].w, f);
+        if constexpr (kExact) {
+            y.x = mul_bf16x2(x[c8].x, f);
+            y.y = mul_bf16x2(x[c8].y, f);
+            y.z = mul_bf16x2(x[c8].z, f);
+            y.w = mul_bf16x2(x[c8].w, f);
+        } else {
+            y.x = mul_bf16x2(x[c8].x, f2);
+            y.y = mul_bf16x2(x[c8].y, f2);
+            y.z = mul_bf16x2(x[c8].z, f2);
+            y.w = mul_bf16x2(x[c8].w, f2);
+        }
         *reinterpret_cast<uint4 *>(dst + sw(row, c8)) = y;
         if (raw_dst) *reinterpret_cast<uint4 *>(raw_dst + sw(row, c8)) = x[c8];
     }
@@ -215,7 +218,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                                               ~uintptr_t(1023));
     __shared__ uint64_t full[kStages], empty[kStages], unit_full[2], unit_empty[2];
     __shared__ uint64_t kp_ready[2], kp_free[2], ka_ready[kStages], drain;
-    __shared__ uint64_t ds_full[2], ds_free[2], p_full, p_free, pp_ready, pp_free;
+    __shared__ uint64_t ds_full[2], ds_free[2], p_full, p_free, pp_ready[2], pp_free[2];
     __shared__ uint64_t o_full[2], o_free[2], sb_ready, sb_free;
     __shared__ uint64_t d_ready, d_free;
     __shared__ UnitInfo units[2];
@@ -248,8 +251,10 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         }
         tc::mbar_init(&p_full, 1);
         tc::mbar_init(&p_free, 1);
-        tc::mbar_init(&pp_ready, 1);
-        tc::mbar_init(&pp_free, 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&pp_ready[i], 1);
+            tc::mbar_init(&pp_free[i], 1);
+        }
         tc::mbar_init(&sb_ready, 2);
         tc::mbar_init(&sb_free, 1);
         tc::mbar_init(&drain, 1);
@@ -389,27 +394,36 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 if (!ok) break;
                 tc::umma_commit(&ds_full[dA]);
                 ++dsc;
-                // ---- C
+                // ---- C, software-pipelined: M1 of chunk c+1 goes out right after M2 of chunk c
+                // (before M3 of chunk c), so the scores of c+1 are made while chunk c finishes
                 const uint32_t sb_base = sbc;
-                for (int c = 0; c < info.nch && ok; ++c) {
-                    const uint32_t st = job % kStages;
-                    const uint32_t q_s = sb + st * kStage, v_s = q_s + kTile;
-                    const uint32_t ob = cc & 1;
-                    const uint32_t kb = kpc & 1;
-                    if (!W(&full[st], job / kStages) || !W(&kp_ready[kb], kpc >> 1)) { ok = false; break; }
-                    ++kpc;
-                    const bool fast = kfast[kb] != 0;
-                    // M1: P = Q K''^T (factored route) or Q K^T (exact route)
-                    if (cc >= 1 && !W(&p_free, cc - 1)) { ok = false; break; }
-                    TRACE(1, 2, c);
-                    tc::tc_fence_after();
+                auto issue_m1 = [&](uint32_t q_s, uint32_t kb, bool fast) {
                     const uint32_t k1 = sb + (fast ? kKp : kKr) + kb * kTile;
+                    tc::tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
                         tc::umma_bf16(tmem + kTP, desc_k(q_s + off), desc_k(k1 + off), kIdescP, ks > 0);
                     }
                     tc::umma_commit(&p_full);
+                };
+                // M1 of chunk 0: P = Q K''^T (factored route) or Q K^T (exact route)
+                uint32_t kb = kpc & 1;
+                {
+                    const uint32_t st = job % kStages;
+                    ok = W(&full[st], job / kStages) && W(&kp_ready[kb], kpc >> 1) &&
+                         (cc == 0 || W(&p_free, cc - 1));
+                    if (ok) {
+                        ++kpc;
+                        TRACE(1, 2, 0);
+                        issue_m1(sb + st * kStage, kb, kfast[kb] != 0);
+                    }
+                }
+                for (int c = 0; c < info.nch && ok; ++c) {
+                    const uint32_t st = job % kStages;
+                    const uint32_t q_s = sb + st * kStage, v_s = q_s + kTile;
+                    const uint32_t ob = cc & 1, pb = cc & 1;
+                    const bool fast = kfast[kb] != 0;
                     // M4: dS^T = V^T K~ (not needed after the last chunk)
                     if (c + 1 < info.nch) {
                         const uint32_t db = dsc & 1;
@@ -423,11 +437,10 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                         tc::umma_commit(&ds_full[db]);
                         ++dsc;
                     }
-                    tc::umma_commit(&kp_free[kb]);
                     // M2: O^T = S^T Q^T (Q scaled in place first on the exact route)
                     if (!W(&sb_ready, sb_base + c)) { ok = false; break; }
                     if (cc >= 2 && !W(&o_free[ob], (cc >> 1) - 1)) { ok = false; break; }
-                    if (!fast && !W(&pp_ready, cc)) { ok = false; break; }
+                    if (!fast && !W(&pp_ready[pb], cc >> 1)) { ok = false; break; }
                     TRACE(1, 4, c);
                     tc::tc_fence_after();
 #pragma unroll
@@ -437,16 +450,27 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                                          kIdescO2, ks > 0);
                     }
                     tc::umma_commit(&sb_free);
+                    tc::umma_commit(&kp_free[kb]);   // M1, M4 and M2 of chunk c have read its set
+                    // M1 of chunk c+1, once the scores of chunk c have been read
+                    if (c + 1 < info.nch) {
+                        const uint32_t st1 = (job + 1) % kStages;
+                        kb = kpc & 1;
+                        if (!W(&full[st1], (job + 1) / kStages) || !W(&kp_ready[kb], kpc >> 1) ||
+                            !W(&p_free, cc)) { ok = false; break; }
+                        ++kpc;
+                        TRACE(1, 2, c + 1);
+                        issue_m1(sb + st1 * kStage, kb, kfast[kb] != 0);
+                    }
                     // M3: O^T += V^T P'^T
-                    if (fast && !W(&pp_ready, cc)) { ok = false; break; }
+                    if (fast && !W(&pp_ready[pb], cc >> 1)) { ok = false; break; }
                     TRACE(1, 5, c);
                     tc::tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
                         tc::umma_bf16(tmem + kTO + 64 * ob, desc_mn8(v_s + ks * 2048),
-                                      desc_k(sb + kPp + ks * 32), kIdescO3, 1u);
+                                      desc_k(sb + kPp + pb * kRegion + ks * 32), kIdescO3, 1u);
                     tc::umma_commit(&o_full[ob]);
-                    tc::umma_commit(&pp_free);
+                    tc::umma_commit(&pp_free[pb]);
                     tc::umma_commit(&empty[st]);
                     ++job;
                     ++cc;
@@ -496,7 +520,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             if (wtid == 0) TRACE(2, 9, kpc);
             const float bs = gate_at(G, srow);
             const float fac = srow < nv ? tc::ex2((base - bs) * kLog2e) : 0.f;
-            store_row_scaled(sm + kKp + kb * kTile + shalf * kRegion,
+            store_row_scaled<false>(sm + kKp + kb * kTile + shalf * kRegion,
                              raw ? sm + kKr + kb * kTile + shalf * kRegion : nullptr, srow, x, fac);
             if (wtid == 0) TRACE(2, 10, kpc);
             tc::fence_proxy_async_smem();
@@ -545,7 +569,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 uint4 x[8];
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) x[c8] = *reinterpret_cast<const uint4 *>(kt + sw(srow, c8));
-                store_row_scaled(kt, nullptr, srow, x, fac);
+                store_row_scaled<true>(kt, nullptr, srow, x, fac);
                 tc::fence_proxy_async_smem();
                 named_sync(kBar, 128);
                 if (wtid == 0) {
@@ -591,14 +615,15 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                     if (wtid == 0) TRACE(2, 3, c);
                 }
                 // scores -> P' (bf16, K-major rows t): mask s <= t < nv; exact route weights
+                const uint32_t pb = cc & 1;
                 wait_nv(&p_full, cc, true, abort_v, status);
-                wait_nv(&pp_free, cc - 1, cc >= 1, abort_v, status);
+                wait_nv(&pp_free[pb], (cc >> 1) - 1, cc >= 2, abort_v, status);
                 if (wtid == 0) TRACE(2, 5, c);
                 tc::tc_fence_after();
                 // M=64 accumulator layout: row t = 16 * quarter + lane in lanes 0-15
                 const int tr = quarter * 16 + (lane & 15);
                 const float bt = gate_at(G, tr) * kLog2e;
-                uint8_t *pp = sm + kPp;
+                uint8_t *pp = sm + kPp + pb * kRegion;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t p[32];
@@ -647,12 +672,12 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
 #pragma unroll
                         for (int c8 = 0; c8 < 8; ++c8) x[c8] = make_uint4(0u, 0u, 0u, 0u);
                     }
-                    store_row_scaled(qt, nullptr, srow, x, tc::ex2(gate_at(G, srow) * kLog2e));
+                    store_row_scaled<false>(qt, nullptr, srow, x, tc::ex2(gate_at(G, srow) * kLog2e));
                 }
                 tc::fence_proxy_async_smem();
                 named_sync(kBar, 128);
                 if (wtid == 0) {
-                    tc::mbar_arrive(&pp_ready);
+                    tc::mbar_arrive(&pp_ready[pb]);
                     TRACE(2, 6, c);
                 }
                 ++cc;
@@ -703,16 +728,13 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             if (!info.valid) break;
             const int h = info.h, nch = info.nch;
             if (wtid == 0) TRACE(3 + wg, 1, us);
-            WTS(0);
 
-            // ---------------- hand-off: S_in, publish S_out, bf16 S_in for M2 ----------------
+            // ---------------- hand-off: S_in, bf16 S_in for M2, publish S_out ----------------
             {
                 const uint32_t db = dsc & 1;
                 bool bad = !wait_or_abort(&ds_full[db], (dsc >> 1) & 1, abort_v, status);
-                WTS(1);
                 if (wtid == 0) TRACE(3 + wg, 11, us);
                 bad = bad || !wait_or_abort(&d_ready, us & 1, abort_v, status);
-                WTS(2);
                 if (wtid == 0) TRACE(3 + wg, 12, us);
                 ++dsc;
                 if (!bad && !info.first && wtid == 0) {
@@ -728,9 +750,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                         }
                     }
                 }
-                WTS(3);
                 if (named_any(kBarBoth, 256, bad || *abort_v)) break;
-                WTS(4);
                 if (wtid == 0) TRACE(3 + wg, 2, 0);
                 tc::tc_fence_after();
                 if (info.first) {
@@ -752,6 +772,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 const float eB = tc::ex2(unit_D * kLog2e);
                 named_sync(bar_id, 128);
                 if (wtid == 0) tc::mbar_arrive(&d_free);
+                write_sb();   // bf16 S_in for the first chunk's M2 first: the output pass can start
                 // S_out = exp(B) S_in + dS: to hT (last segment) or to the successor; each warp
                 // store covers one 128-byte row segment (32 consecutive j)
                 float *dst = info.last ? (f.hT ? f.hT + (info.n * H + h) * kD * kD : nullptr)
@@ -778,7 +799,6 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                     __threadfence();
                     tc::st_release_gpu(f.flags + info.sigma * H + h, f.epoch);
                 }
-                write_sb();
                 if (wtid == 0) TRACE(3 + wg, 3, 0);
             }
 
@@ -979,9 +999,6 @@ cudaError_t launch_prefill_fused(const ChunkArgs &a, const SegTable &t, int64_t 
 }  // namespace sala
 
 #ifdef SALA_TRACE
-extern "C" int sala_gla_debug_wts(long long *out) {
-    return cudaMemcpyFromSymbol(out, sala::g_wts, sizeof(sala::g_wts)) == cudaSuccess ? 0 : -1;
-}
 extern "C" int sala_gla_debug_trace(unsigned long long *out, int max) {
     unsigned int n[5];
     if (cudaMemcpyFromSymbol(n, sala::g_trace_n, sizeof(n)) != cudaSuccess) return -1;

@@ -42,10 +42,11 @@ __device__ __forceinline__ bool named_any(int id, int n, bool x) {
 #define SALA_WAIT_POLL_NS 0
 #endif
 
-// Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
-                                              volatile int *abort_flag, int *status) {
-    if (tc::mbar_test_wait(bar, parity)) return true;
+// Bounded wait that also gives up as soon as another role has aborted. The fast path (phase
+// already complete) is inline; the polling loop is a call, which keeps the many wait sites of
+// the persistent kernels small (their code shares one instruction cache).
+__device__ __noinline__ bool wait_or_abort_slow(uint64_t *bar, uint32_t parity,
+                                                volatile int *abort_flag, int *status) {
     const uint64_t t0 = tc::global_timer_ns();
     while (!(SALA_WAIT_POLL_NS ? tc::mbar_test_wait(bar, parity) : tc::mbar_try_wait(bar, parity))) {
         if (SALA_WAIT_POLL_NS) __nanosleep(SALA_WAIT_POLL_NS);
@@ -57,6 +58,12 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
         }
     }
     return true;
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
+                                              volatile int *abort_flag, int *status) {
+    if (tc::mbar_test_wait(bar, parity)) return true;
+    return wait_or_abort_slow(bar, parity, abort_flag, status);
 }
 
 // Inclusive prefix sum of g over the chunk's n valid tokens (zeros past n); lane l returns
@@ -91,7 +98,7 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t w, __nv_bfloat162 f2) {
 
 struct TcMaps {
     CUtensorMap q, k, v;   // loads: box 64 x 1 x 64, 128-byte swizzle
-    CUtensorMap o;         // stores: box 128 x 1 x 32, no swizzle
+    CUtensorMap o;         // stores: box 32 x 1 x 64, no swizzle
 };
 
 // host: 3-D tensor maps over q, k, v and o viewed as [T_total, H, 128] bf16

@@ -16,40 +16,46 @@
 //     S_out = exp(B) S_in + dS for the successor (hT for the last segment). This is the
 //     Blueprint's unrolled form S_n = alpha^n S_0 + sum alpha^(n-i) k_i^T v_i applied a whole
 //     segment at a time;
-//  C. output pass over the chunks, first to last, from S_in. With b_t the cumulative
-//     log-decay of the chunk up to token t and S the state entering the chunk:
-//       o_t = scale exp(b_t) [ q_t S + sum_{s<=t} (q_t . k_s) exp(-b_s) v_s ]
-//       S  <- exp(b_C) [ S + sum_s exp(-b_s) k_s^T v_s ]
-//     which keeps both output terms in one accumulator (the weights become per-column
-//     factors exp(-b_s) on the scores and per-row factors exp(b_t) on the output). When a
-//     chunk's decay range is too wide for those factors (|b_t| > 60), the chunk takes the
-//     exact route instead: per-entry factors exp(b_t - b_s) on the scores, q_t scaled by
-//     exp(b_t) in place, and S <- exp(b_C) S + sum_s exp(b_C - b_s) k_s^T v_s.
+//  C. output pass over the chunks, first to last, from S_in. The state lives in tensor
+//     memory in fp32 and the tensor core adds each chunk to it directly. It is kept relative
+//     to a reference point r: with B_t the log-decay from r to token t, the stored state is
+//     Z = exp(-B) S, and
+//       o_t = scale exp(B_t) [ q_t Z + sum_{s<=t in the chunk} (q_t . k_s) exp(-B_s) v_s ]
+//       Z  <- Z + sum_{s in the chunk} exp(-B_s) k_s^T v_s
+//     so the weights become per-column factors exp(-B_s) on the keys and per-row factors
+//     exp(B_t) on the output, and no per-chunk decay touches the state. Before a chunk whose
+//     factors would leave [e^-60, e^60] the reference moves to the chunk start (Z is rescaled
+//     once in tensor memory). When the chunk's own decay range is wider than that, the chunk
+//     takes the exact route: per-entry weights exp(b_t - b_s) on the scores, q_t scaled by
+//     exp(b_t) in place, Z rescaled to the chunk end and k_s weighted by exp(b_C - b_s).
 //
 // The state is kept transposed (S^T, value index j in the tensor-memory lane), so that its
 // bf16 copy can sit in tensor memory as the A operand of the q.S product. Contractions
 // (tcgen05.mma kind::f16, bf16 in, fp32 accumulators in tensor memory):
 //   M1  P    = Q K~^T      M=64  N=64  K=128   A=Q smem (K-major)     B=K~ smem (K-major)
-//   M2  O^T  = S^T Q^T     M=128 N=64  K=128   A=S^T bf16 in TMEM     B=Q smem (K-major)
+//   M2  O^T  = Z^T Q^T     M=128 N=64  K=128   A=Z^T bf16 in TMEM     B=Q smem (K-major)
 //   M3  O^T += V^T P'^T    M=128 N=64  K=64    A=V smem (MN-major)    B=P' smem (K-major)
-//   M4  dS^T = V^T K~      M=128 N=128 K=64    A=V smem (MN-major)    B=K~ smem (MN-major)
-// K~ is k scaled per token (the factors above). In the state pass the K tile arrives by TMA
-// and is scaled in place in shared memory (the tensor core only runs the short M4 there). In
-// the output pass, where the tensor core streams operands most of the time, the scaling
-// warps make K~ from a global load straight into shared memory instead: ordinary
-// shared-memory loads issued while the tensor core reads its operands stall far behind them.
-// Q and V tiles arrive by TMA, o leaves by TMA stores.
+//   M4  Z^T += V^T K~      M=128 N=128 K=64    A=V smem (MN-major)    B=K~ smem (MN-major)
+// (the state pass runs M4 into its own accumulator dS^T). K~ is k scaled per token. In the
+// state pass the K tile arrives by TMA and is scaled in place in shared memory (the tensor
+// core only runs the short M4 there). In the output pass, where the tensor core streams
+// operands most of the time, the scaling warps make K~ from a global load straight into
+// shared memory instead: ordinary shared-memory loads issued while the tensor core reads its
+// operands stall far behind them. Q and V tiles arrive by TMA, o leaves by TMA stores.
 //
-// Roles: warp 0 loads (TMA), warp 1 issues MMAs and owns the tensor memory, warps 4-7 scale K,
-// turn scores into P' and (exact route) scale Q, warps 8-11 and 12-15 each own 64 of the
-// state's key rows i (all 128 value columns j, one per lane), carry the state, publish the
-// hand-off flag and write o for 32 of the chunk's tokens. Every per-token factor is computed
-// by the warp that needs it from g (an in-warp prefix sum), never passed through shared
-// memory. mbarrier waits compare phase parity only, so every barrier has at most one phase
-// in flight per waiter: each waiter consumes every phase of the barriers it waits on, and a
-// producer cannot complete a second phase before its consumer has consumed the first.
-// Every wait is bounded (2 s of %globaltimer); a timeout records SALA_ERR_TIMEOUT, stops the
-// CTA's work, drains its copies and MMAs, frees its tensor memory and returns.
+// Roles: warp 0 loads (TMA), warp 1 issues MMAs and owns the tensor memory, warp 2 publishes
+// the hand-off flags, warp 3 reads g ahead of everyone and publishes each chunk's prefix sums
+// and plan (reference point, rescaling, route) in a small ring of shared-memory records,
+// warps 4-7 scale K and turn scores into P' (and, exact route, scale Q), warps 8-11 do the
+// hand-off and make the bf16 copy of the state for every chunk (rescaling it when the
+// reference moves), warps 12-15 write o (each warp 32 value columns of the chunk's 64
+// tokens). The other roles take their per-token factors from the records, so no role waits
+// on a load of g or on a prefix sum of its own.
+// mbarrier waits compare phase parity only, so every barrier has at most one phase in flight
+// per waiter: each waiter consumes every phase of the barriers it waits on, and a producer
+// cannot complete a second phase before its consumer has consumed the first. Every wait is
+// bounded (2 s of %globaltimer); a timeout records SALA_ERR_TIMEOUT, stops the CTA's work,
+// drains its copies and MMAs, frees its tensor memory and returns.
 #include "chunk_tc.cuh"
 
 namespace sala {
@@ -60,24 +66,34 @@ using namespace tck;
 constexpr int kStages = 4;
 constexpr int kThreads = 512;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kFastRange = 60.f;   // max |b_t| (natural log) for the factored route
+constexpr float kFastRange = 60.f;   // max |log-factor| (natural log) of the factored route
 
 // dynamic shared memory (offsets from a 1024-aligned base)
 constexpr uint32_t kStage = 2 * kTile;              // Q | V
 constexpr uint32_t kKp = kStages * kStage;          // K~ [2] (factored or exact weights)
 constexpr uint32_t kKr = kKp + 2 * kTile;           // raw K [2] (exact-route M1)
-constexpr uint32_t kPp = kKr + 2 * kTile;           // P' [2] (K-major B of M3)
-constexpr uint32_t kOst = kPp + 2 * kRegion;        // o staging [2 state groups][32 t][256 B]
-constexpr uint32_t kOstBytes = 32 * 256;
-constexpr uint32_t kBytes = kOst + 2 * kOstBytes;
+constexpr uint32_t kPp = kKr + 2 * kTile;           // P' (K-major B of M3)
+constexpr uint32_t kOst = kPp + kRegion;            // o staging, per output warp [64 t][32 j]
+constexpr uint32_t kOstWarp = 64 * 64;
+constexpr uint32_t kGate = kOst + 4 * kOstWarp;     // gate records: state pass [kRecA], output pass [kRecC]
+constexpr int kRecA = 4, kRecC = 8;
+constexpr uint32_t kBytes = kGate + (kRecA + kRecC) * 288;
 constexpr uint32_t kSmemAlloc = kBytes + 1024;
 
-// TMEM columns: P (M=64 layout), S^T bf16 (A of M2), O^T [2], dS^T [2]
-constexpr uint32_t kTP = 0, kTSb = 64, kTO = 128, kTdS = 256, kTCols = 512;
+// TMEM columns: state-pass dS^T, Z^T (fp32), Z^T bf16 (A of M2), P (M=64 layout), O^T [2].
+// The bf16 copy is double-buffered; its second buffer borrows the first 64 columns of dS^T,
+// which the output pass does not use: the hand-off has read dS^T before the output pass
+// starts, and the next state pass is issued after the output pass's last M2 (tcgen05.mma
+// operations of one thread execute in issue order).
+constexpr uint32_t kTdS = 0, kTZ = 128, kTZb = 256, kTP = 320, kTO = 384, kTCols = 512;
+__device__ __forceinline__ uint32_t zb_col(uint32_t buf) { return buf ? kTdS : kTZb; }
 constexpr uint32_t kIdescP = tc::idesc_bf16_f32(64, 64, 0, 0);
 constexpr uint32_t kIdescO2 = tc::idesc_bf16_f32(128, 64, 0, 0);
 constexpr uint32_t kIdescO3 = tc::idesc_bf16_f32(128, 64, 1, 0);
 constexpr uint32_t kIdescS = tc::idesc_bf16_f32(128, 128, 1, 1);
+
+// named barriers (0 is __syncthreads)
+constexpr int kBarScale = 1, kBarConv = 2, kBarOut = 3;
 
 struct FusedArgs {
     ChunkArgs c;            // q, k, v, g, scale, o, H
@@ -98,8 +114,8 @@ struct UnitInfo {
 // role, event id and chunk index, written to a global array.
 #ifdef SALA_TRACE
 constexpr int kTraceN = 512;
-__device__ unsigned long long g_trace[5][kTraceN];
-__device__ unsigned int g_trace_n[5];
+__device__ unsigned long long g_trace[8][kTraceN];
+__device__ unsigned int g_trace_n[8];
 #define TRACE(role, ev, idx)                                                                  \
     do {                                                                                      \
         if (blockIdx.x == 0 && tr_i < kTraceN) {                                              \
@@ -111,10 +127,21 @@ __device__ unsigned int g_trace_n[5];
             g_trace_n[role] = tr_i;                                                           \
         }                                                                                     \
     } while (0)
+// Per-site wait-cycle totals of CTA 0's MMA thread (slots 0-15) and of scaling thread 0
+// (slots 16-31), kept in registers (wacc_) and written once at the end.
+__device__ unsigned long long g_wait_acc[32];
+#define TIMED(slot, expr)                                        \
+    ([&]() {                                                     \
+        const long long t0_ = clock64();                         \
+        const bool r_ = (expr);                                  \
+        wacc_[slot] += clock64() - t0_;                          \
+        return r_;                                               \
+    }())
 #else
 #define TRACE(role, ev, idx) \
     do {                     \
     } while (0)
+#define TIMED(slot, expr) (expr)
 #endif
 
 // shared-memory matrix descriptors: fixed part | (start address >> 4)
@@ -130,7 +157,7 @@ __device__ __forceinline__ uint64_t desc_mn8(uint32_t addr) {        // MN-major
 struct Gate {
     float b0, b1;   // b[2 lane], b[2 lane + 1]
     float bC;       // b at the last valid token
-    bool fast;      // max |b| <= kFastRange: factored weights are safe
+    float mx;       // max |b| over the chunk
 };
 
 // Raw g of the chunk for lane l (tokens 2l, 2l+1; 0 past nv): loaded early, scanned later.
@@ -157,16 +184,56 @@ __device__ __forceinline__ Gate scan_gate(float2 a, int nv) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     G.bC = __shfl_sync(0xffffffffu, ((nv - 1) & 1) ? G.b1 : G.b0, (nv - 1) >> 1);
-    G.fast = mx <= kFastRange;
+    G.mx = mx;
     return G;
 }
 
-// b[t] for a warp-uniform or per-lane t in [0, 64) (all lanes must call).
-__device__ __forceinline__ float gate_at(const Gate &G, int t) {
-    const float x = __shfl_sync(0xffffffffu, G.b0, t >> 1);
-    const float y = __shfl_sync(0xffffffffu, G.b1, t >> 1);
-    return (t & 1) ? y : x;
+// How one chunk of the output pass is weighted, from its gate and `run`, the log-decay from
+// the reference point to the chunk start (updated to the next chunk's).
+struct Plan {
+    float base;   // factored route: log-decay from the reference point to the chunk start
+    float pre;    // log-factor the stored state takes before this chunk (0 if it keeps its scale)
+    bool fast;    // factored route (else the exact route)
+    bool moved;   // the reference moves before this chunk (the stored state is rescaled)
+};
+
+__device__ __forceinline__ Plan plan_chunk(const Gate &G, float &run) {
+    Plan p;
+    if (fabsf(run) + G.mx <= kFastRange) {          // factors stay in range: keep the reference
+        p.fast = true;
+        p.moved = false;
+        p.pre = 0.f;
+        p.base = run;
+        run = run + G.bC;
+    } else if (G.mx <= kFastRange) {                // move the reference to the chunk start
+        p.fast = true;
+        p.moved = true;
+        p.pre = run;
+        p.base = 0.f;
+        run = G.bC;
+    } else {                                        // exact route, reference to the chunk end
+        p.fast = false;
+        p.moved = true;
+        p.pre = run;
+        p.base = 0.f;
+        run = 0.f;
+    }
+    return p;
 }
+
+// What the gate warp publishes for one chunk: the inclusive prefix sums b of its log-decays
+// and, for the state pass, the chunk's total bC and the total D of the later chunks of the
+// segment; for the output pass, the plan (reference offset, rescaling factors, route).
+struct alignas(16) GateRec {
+    float b[64];
+    float bC;
+    float D;        // state pass: log-decay of the later chunks of the segment
+    float base;     // output pass, factored route: log-decay from the reference point
+    float e1;       // output pass: exp(pre) if the reference moves before the chunk, else 1
+    float eC;       // output pass, exact route: exp(bC), else 1
+    uint32_t fast, moved, pad;
+};
+static_assert(sizeof(GateRec) == 288, "gate record size");
 
 // Bounded wait (if `need`) whose failure only sets the abort flag (see the epilogue loops).
 __device__ __forceinline__ void wait_nv(uint64_t *bar, uint32_t par, bool need,
@@ -209,6 +276,44 @@ __device__ __forceinline__ void store_row_scaled(uint8_t *dst, uint8_t *raw_dst,
     }
 }
 
+// Exact route, scores: row t of P' (already masked and rounded to bf16 in the SW128 tile at
+// pp) times exp(b_t - b_s) for every causal column s <= t (rare).
+__device__ __forceinline__ void exact_pp_weights(uint8_t *pp, const float *b, int t) {
+    const float bt = b[t] * kLog2e;
+    for (int c8 = 0; c8 < 8; ++c8) {
+        uint4 x = *reinterpret_cast<const uint4 *>(pp + sw(t, c8));
+        uint32_t *w = reinterpret_cast<uint32_t *>(&x);
+        for (int e = 0; e < 4; ++e) {
+            // only the causal entries s <= t carry a weight (past t the factor may overflow)
+            const int s = 8 * c8 + 2 * e;
+            const float2 f = bf16x2_to_float2(w[e]);
+            w[e] = float2_to_bf16x2(s <= t ? f.x * tc::ex2(bt - b[s] * kLog2e) : 0.f,
+                                    s + 1 <= t ? f.y * tc::ex2(bt - b[s + 1] * kLog2e) : 0.f);
+        }
+        *reinterpret_cast<uint4 *>(pp + sw(t, c8)) = x;
+    }
+}
+
+// Exact route, queries: row `row` (columns 64 half .. + 63) of the Q tile at qt becomes
+// exp(b_row) q_row, read from global memory (the tile has been consumed by M1).
+__device__ __forceinline__ void exact_q_scale(uint8_t *qt, const uint16_t *q, int64_t c0, int row, int half,
+                                           int nv, int H, int h, float b_row) {
+    uint4 x[8];
+    if (row < nv) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(q + ((c0 + row) * H + h) * kD + 64 * half);
+        for (int c8 = 0; c8 < 8; ++c8) x[c8] = src[c8];
+    } else {
+        for (int c8 = 0; c8 < 8; ++c8) x[c8] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    store_row_scaled<false>(qt, nullptr, row, x, tc::ex2(b_row * kLog2e));
+}
+
+// Per-warp arrival: the warp's lanes have finished their part; lane 0 arrives for the warp.
+__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) tc::mbar_arrive(bar);
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -216,14 +321,17 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-    __shared__ uint64_t full[kStages], empty[kStages], unit_full[2], unit_empty[2];
-    __shared__ uint64_t kp_ready[2], kp_free[2], ka_ready[kStages], drain;
-    __shared__ uint64_t ds_full[2], ds_free[2], p_full, p_free, pp_ready[2], pp_free[2];
-    __shared__ uint64_t o_full[2], o_free[2], sb_ready, sb_free;
-    __shared__ uint64_t d_ready, d_free;
+    __shared__ uint64_t full[kStages], empty[kStages], ka_ready[kStages];
+    __shared__ uint64_t unit_full[2], unit_empty[2], kp_ready[2], kp_free[2];
+    __shared__ uint64_t p_full, p_free, pp_ready, pp_free;
+    __shared__ uint64_t ga_full[kRecA], ga_empty[kRecA], gc_full[kRecC], gc_empty[kRecC];
+    __shared__ uint64_t z_full, z_free, zb_ready[2], zb_free[2], o_full[2], o_free[2];
+    __shared__ uint64_t ds_full, ds_free, d_ready, d_free, pub_ready, pub_free, drain;
     __shared__ UnitInfo units[2];
     __shared__ int kfast[2];
-    __shared__ float unit_D;   // total log-decay of the current unit's segment
+    __shared__ float unit_D;         // total log-decay of the current unit's segment
+    __shared__ uint32_t *pub_flag;   // the flag the publisher releases next
+    __shared__ int pub_cmd;          // 0: nothing this unit, 1: release pub_flag, 2: stop
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 #ifdef SALA_TRACE
@@ -236,33 +344,44 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            tc::mbar_init(&full[s], 1);    // expect_tx arrival
-            tc::mbar_init(&empty[s], 1);   // MMA commit
+            tc::mbar_init(&full[s], 1);       // expect_tx arrival
+            tc::mbar_init(&empty[s], 1);      // MMA commit
+            tc::mbar_init(&ka_ready[s], 1);   // the state-pass K' tile of this stage is scaled
+                                              // (phases count this stage's state-pass jobs)
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&unit_full[i], 1);
-            tc::mbar_init(&unit_empty[i], 4);   // MMA, scaler, two state groups
+            tc::mbar_init(&unit_empty[i], 5);   // MMA, gate, scaling, converting, output warps
             tc::mbar_init(&kp_ready[i], 1);
             tc::mbar_init(&kp_free[i], 1);
-            tc::mbar_init(&ds_full[i], 1);
-            tc::mbar_init(&ds_free[i], 2);
             tc::mbar_init(&o_full[i], 1);
-            tc::mbar_init(&o_free[i], 2);
+            tc::mbar_init(&o_free[i], 4);       // one arrival per output warp
         }
         tc::mbar_init(&p_full, 1);
         tc::mbar_init(&p_free, 1);
-        for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&pp_ready[i], 1);
-            tc::mbar_init(&pp_free[i], 1);
+        tc::mbar_init(&pp_ready, 1);
+        tc::mbar_init(&pp_free, 1);
+        for (int i = 0; i < kRecA; ++i) {
+            tc::mbar_init(&ga_full[i], 1);
+            tc::mbar_init(&ga_empty[i], 4);    // one arrival per scaling warp
         }
-        tc::mbar_init(&sb_ready, 2);
-        tc::mbar_init(&sb_free, 1);
-        tc::mbar_init(&drain, 1);
-        for (int s = 0; s < kStages; ++s)
-            tc::mbar_init(&ka_ready[s], 1);   // the state-pass K' tile of this stage is scaled
-                                              // (phases count this stage's state-pass jobs)
+        for (int i = 0; i < kRecC; ++i) {
+            tc::mbar_init(&gc_full[i], 1);
+            tc::mbar_init(&gc_empty[i], 12);   // scaling, converting and output warps
+        }
+        tc::mbar_init(&z_full, 1);       // MMA commit after M4 into Z
+        tc::mbar_init(&z_free, 4);       // converting warps: Z read (and rescaled)
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&zb_ready[i], 4);   // converting warps: bf16 Z written
+            tc::mbar_init(&zb_free[i], 1);    // MMA commit after M2
+        }
+        tc::mbar_init(&ds_full, 1);
+        tc::mbar_init(&ds_free, 4);
         tc::mbar_init(&d_ready, 1);
-        tc::mbar_init(&d_free, 2);      // both state groups have read unit_D
+        tc::mbar_init(&d_free, 4);
+        tc::mbar_init(&pub_ready, 4);
+        tc::mbar_init(&pub_free, 1);
+        tc::mbar_init(&drain, 1);
         abort_flag = 0;
         tc::fence_barrier_init();
     }
@@ -363,22 +482,24 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         // =============================== MMA issuer ===============================
         if (lane == 0) {
             const uint32_t sb = tc::smem_u32(sm);
-            uint32_t job = 0, us = 0, kpc = 0, dsc = 0, cc = 0, sbc = 0;
+            uint32_t job = 0, us = 0, kpc = 0, cc = 0, zbc = 0, zfc = 0;
             uint32_t ka_par = 0;   // bit st: phase parity of ka_ready[st] (state-pass jobs only)
             auto W = [&](uint64_t *bar, uint32_t par) { return wait_or_abort(bar, par & 1, abort_v, status); };
+#ifdef SALA_TRACE
+            unsigned long long wacc_[16] = {};
+#endif
             for (;;) {
                 const uint32_t slot = us & 1;
-                if (!W(&unit_full[slot], us >> 1)) break;
+                if (!TIMED(0, W(&unit_full[slot], us >> 1))) break;
                 const UnitInfo info = units[slot];
                 tc::mbar_arrive(&unit_empty[slot]);
                 if (!info.valid) break;
                 bool ok = true;
                 // ---- A: dS^T = sum over chunks of V^T K', one accumulator
-                const uint32_t dA = dsc & 1;
-                if (dsc >= 2) ok = W(&ds_free[dA], (dsc >> 1) - 1);
+                if (us >= 1) ok = TIMED(1, W(&ds_free, us - 1));
                 for (int r = 0; r < info.nch && ok; ++r) {
                     const uint32_t st = job % kStages;
-                    ok = W(&full[st], job / kStages) && W(&ka_ready[st], (ka_par >> st) & 1);
+                    ok = TIMED(2, W(&full[st], job / kStages)) && TIMED(3, W(&ka_ready[st], (ka_par >> st) & 1));
                     if (!ok) break;
                     ka_par ^= 1u << st;
                     TRACE(1, 1, r);
@@ -386,17 +507,15 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                     const uint32_t k_s = sb + st * kStage, v_s = k_s + kTile;   // K' scaled in place
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        tc::umma_bf16(tmem + kTdS + 128 * dA, desc_mn8(v_s + ks * 2048),
+                        tc::umma_bf16(tmem + kTdS, desc_mn8(v_s + ks * 2048),
                                       desc_mn8(k_s + ks * 2048), kIdescS, (r > 0 || ks > 0) ? 1u : 0u);
                     tc::umma_commit(&empty[st]);
                     ++job;
                 }
                 if (!ok) break;
-                tc::umma_commit(&ds_full[dA]);
-                ++dsc;
+                tc::umma_commit(&ds_full);
                 // ---- C, software-pipelined: M1 of chunk c+1 goes out right after M2 of chunk c
                 // (before M3 of chunk c), so the scores of c+1 are made while chunk c finishes
-                const uint32_t sb_base = sbc;
                 auto issue_m1 = [&](uint32_t q_s, uint32_t kb, bool fast) {
                     const uint32_t k1 = sb + (fast ? kKp : kKr) + kb * kTile;
                     tc::tc_fence_after();
@@ -407,12 +526,12 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                     }
                     tc::umma_commit(&p_full);
                 };
-                // M1 of chunk 0: P = Q K''^T (factored route) or Q K^T (exact route)
+                // M1 of chunk 0: P = Q K~^T (factored route) or Q K^T (exact route)
                 uint32_t kb = kpc & 1;
                 {
                     const uint32_t st = job % kStages;
-                    ok = W(&full[st], job / kStages) && W(&kp_ready[kb], kpc >> 1) &&
-                         (cc == 0 || W(&p_free, cc - 1));
+                    ok = TIMED(4, W(&full[st], job / kStages) && W(&kp_ready[kb], kpc >> 1) &&
+                         (cc == 0 || W(&p_free, cc - 1)));
                     if (ok) {
                         ++kpc;
                         TRACE(1, 2, 0);
@@ -422,66 +541,184 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 for (int c = 0; c < info.nch && ok; ++c) {
                     const uint32_t st = job % kStages;
                     const uint32_t q_s = sb + st * kStage, v_s = q_s + kTile;
-                    const uint32_t ob = cc & 1, pb = cc & 1;
+                    const uint32_t ob = cc & 1;
                     const bool fast = kfast[kb] != 0;
-                    // M4: dS^T = V^T K~ (not needed after the last chunk)
+                    // M4: Z^T += V^T K~ (not needed after the last chunk), once the converting
+                    // warps have read Z (and rescaled it, if the reference moved)
                     if (c + 1 < info.nch) {
-                        const uint32_t db = dsc & 1;
-                        if (dsc >= 2 && !W(&ds_free[db], (dsc >> 1) - 1)) { ok = false; break; }
+                        if (!TIMED(5, W(&z_free, zfc))) { ok = false; break; }
                         TRACE(1, 3, c);
+#ifdef SALA_TRACE
+                        const long long ti0 = clock64();
+#endif
                         tc::tc_fence_after();
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-                            tc::umma_bf16(tmem + kTdS + 128 * db, desc_mn8(v_s + ks * 2048),
-                                          desc_mn8(sb + kKp + kb * kTile + ks * 2048), kIdescS, ks > 0);
-                        tc::umma_commit(&ds_full[db]);
-                        ++dsc;
+                            tc::umma_bf16(tmem + kTZ, desc_mn8(v_s + ks * 2048),
+                                          desc_mn8(sb + kKp + kb * kTile + ks * 2048), kIdescS, 1u);
+                        tc::umma_commit(&z_full);
+#ifdef SALA_TRACE
+                        wacc_[13] += clock64() - ti0;
+#endif
+                        ++zfc;
                     }
-                    // M2: O^T = S^T Q^T (Q scaled in place first on the exact route)
-                    if (!W(&sb_ready, sb_base + c)) { ok = false; break; }
-                    if (cc >= 2 && !W(&o_free[ob], (cc >> 1) - 1)) { ok = false; break; }
-                    if (!fast && !W(&pp_ready[pb], cc >> 1)) { ok = false; break; }
+                    // M2: O^T = Z^T Q^T (Q scaled in place first on the exact route)
+                    const uint32_t zb = zbc & 1;
+                    if (!TIMED(6, W(&zb_ready[zb], zbc >> 1))) { ok = false; break; }
+                    if (cc >= 2 && !TIMED(7, W(&o_free[ob], (cc >> 1) - 1))) { ok = false; break; }
+                    if (!fast && !TIMED(8, W(&pp_ready, cc))) { ok = false; break; }
                     TRACE(1, 4, c);
+#ifdef SALA_TRACE
+                    const long long ti1 = clock64();
+#endif
                     tc::tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
-                        tc::umma_bf16_ta(tmem + kTO + 64 * ob, tmem + kTSb + 8 * ks, desc_k(q_s + off),
+                        tc::umma_bf16_ta(tmem + kTO + 64 * ob, tmem + zb_col(zb) + 8 * ks, desc_k(q_s + off),
                                          kIdescO2, ks > 0);
                     }
-                    tc::umma_commit(&sb_free);
+                    tc::umma_commit(&zb_free[zb]);
                     tc::umma_commit(&kp_free[kb]);   // M1, M4 and M2 of chunk c have read its set
+#ifdef SALA_TRACE
+                    wacc_[14] += clock64() - ti1;
+#endif
+                    ++zbc;
                     // M1 of chunk c+1, once the scores of chunk c have been read
                     if (c + 1 < info.nch) {
                         const uint32_t st1 = (job + 1) % kStages;
                         kb = kpc & 1;
-                        if (!W(&full[st1], (job + 1) / kStages) || !W(&kp_ready[kb], kpc >> 1) ||
-                            !W(&p_free, cc)) { ok = false; break; }
+                        if (!TIMED(9, W(&full[st1], (job + 1) / kStages)) || !TIMED(10, W(&kp_ready[kb], kpc >> 1)) ||
+                            !TIMED(11, W(&p_free, cc))) { ok = false; break; }
                         ++kpc;
                         TRACE(1, 2, c + 1);
                         issue_m1(sb + st1 * kStage, kb, kfast[kb] != 0);
                     }
                     // M3: O^T += V^T P'^T
-                    if (fast && !W(&pp_ready[pb], cc >> 1)) { ok = false; break; }
+                    if (fast && !TIMED(12, W(&pp_ready, cc))) { ok = false; break; }
                     TRACE(1, 5, c);
+#ifdef SALA_TRACE
+                    const long long ti2 = clock64();
+#endif
                     tc::tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
                         tc::umma_bf16(tmem + kTO + 64 * ob, desc_mn8(v_s + ks * 2048),
-                                      desc_k(sb + kPp + pb * kRegion + ks * 32), kIdescO3, 1u);
+                                      desc_k(sb + kPp + ks * 32), kIdescO3, 1u);
                     tc::umma_commit(&o_full[ob]);
-                    tc::umma_commit(&pp_free[pb]);
+                    tc::umma_commit(&pp_free);
                     tc::umma_commit(&empty[st]);
+#ifdef SALA_TRACE
+                    wacc_[15] += clock64() - ti2;
+#endif
                     ++job;
                     ++cc;
                 }
                 if (!ok) break;
-                sbc += info.nch;
                 ++us;
             }
+#ifdef SALA_TRACE
+            if (blockIdx.x == 0)
+                for (int i = 0; i < 16; ++i) g_wait_acc[i] = wacc_[i];
+#endif
             // no MMA may still run when the tensor memory is freed
             tc::umma_commit(&drain);
             tc::mbar_wait(&drain, 0, kWaitNs);
+        }
+    } else if (warp == 2) {
+        // =============================== flag publisher ===============================
+        // Releases a unit's hand-off flag once the converting warps have stored its S_out:
+        // their mbarrier arrivals order the stores before this thread's device-scope fence, so
+        // the fence's latency stays off the converting warps.
+        // One command per unit, so that no wait here spans more than one unit.
+        if (lane == 0) {
+            for (uint32_t n = 0;; ++n) {
+                if (!wait_or_abort(&pub_ready, n & 1, abort_v, status)) break;
+                const int cmd = pub_cmd;
+                if (cmd == 2) break;
+                if (cmd == 1) {
+                    __threadfence();
+                    tc::st_release_gpu(pub_flag, f.epoch);
+                }
+                tc::mbar_arrive(&pub_free);
+            }
+        }
+    } else if (warp == 3) {
+        // =============================== gate warp ===============================
+        // Loads the log-decays g of every chunk (a few chunks ahead), takes their in-warp prefix
+        // sums and publishes one record per chunk: for the state pass (chunks last to first)
+        // with the total of the later chunks, then for the output pass (chunks first to last)
+        // with each chunk's plan. One warp decides every plan, so all roles follow the same one.
+        GateRec *recA = reinterpret_cast<GateRec *>(sm + kGate);
+        GateRec *recC = recA + kRecA;
+        uint32_t us = 0, ja = 0, jc = 0;
+        for (;;) {
+            const uint32_t slot = us & 1;
+            bool bad = !wait_or_abort(&unit_full[slot], (us >> 1) & 1, abort_v, status);
+            if (__any_sync(0xffffffffu, bad)) break;
+            const UnitInfo info = units[slot];
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&unit_empty[slot]);
+            if (!info.valid) break;
+            const int h = info.h, nch = info.nch;
+            auto c0_of = [&](int c) { return info.t0 + int64_t(c) * kChunk; };
+            auto nv_of = [&](int c) { return static_cast<int>(min(int64_t(kChunk), info.t1 - c0_of(c))); };
+            // wait until the record slot is free again (its consumers have read the record of
+            // kRec chunks before)
+            auto claim = [&](uint64_t *empty_b, uint32_t n, int R) {
+                const bool b = n >= static_cast<uint32_t>(R) &&
+                               !wait_or_abort(&empty_b[n % R], ((n / R) - 1) & 1, abort_v, status);
+                return !__any_sync(0xffffffffu, b);
+            };
+            bool ok = true;
+            // state pass: chunks last to first
+            float2 g0 = load_gate(a.g, c0_of(nch - 1), nv_of(nch - 1), H, h);
+            float2 g1 = nch > 1 ? load_gate(a.g, c0_of(nch - 2), nv_of(nch - 2), H, h) : make_float2(0.f, 0.f);
+            float D = 0.f;
+            for (int r = 0; r < nch; ++r) {
+                const int c = nch - 1 - r;
+                const Gate G = scan_gate(g0, nv_of(c));
+                g0 = g1;
+                if (r + 2 < nch) g1 = load_gate(a.g, c0_of(c - 2), nv_of(c - 2), H, h);
+                if (!(ok = claim(ga_empty, ja, kRecA))) break;
+                GateRec *R = recA + ja % kRecA;
+                *reinterpret_cast<float2 *>(&R->b[2 * lane]) = make_float2(G.b0, G.b1);
+                if (lane == 0) {
+                    R->bC = G.bC;
+                    R->D = D;
+                }
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&ga_full[ja % kRecA]);
+                D += G.bC;
+                ++ja;
+            }
+            if (!ok) break;
+            // output pass: chunks first to last
+            float run = 0.f;
+            g0 = load_gate(a.g, c0_of(0), nv_of(0), H, h);
+            g1 = nch > 1 ? load_gate(a.g, c0_of(1), nv_of(1), H, h) : make_float2(0.f, 0.f);
+            for (int c = 0; c < nch; ++c) {
+                const Gate G = scan_gate(g0, nv_of(c));
+                g0 = g1;
+                if (c + 2 < nch) g1 = load_gate(a.g, c0_of(c + 2), nv_of(c + 2), H, h);
+                const Plan P = plan_chunk(G, run);
+                if (!(ok = claim(gc_empty, jc, kRecC))) break;
+                GateRec *R = recC + jc % kRecC;
+                *reinterpret_cast<float2 *>(&R->b[2 * lane]) = make_float2(G.b0, G.b1);
+                if (lane == 0) {
+                    R->bC = G.bC;
+                    R->base = P.base;
+                    R->e1 = P.moved ? tc::ex2(P.pre * kLog2e) : 1.f;
+                    R->eC = P.fast ? 1.f : tc::ex2(G.bC * kLog2e);
+                    R->fast = P.fast;
+                    R->moved = P.moved;
+                }
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&gc_full[jc % kRecC]);
+                ++jc;
+            }
+            if (!ok) break;
+            ++us;
         }
     } else if (warp >= 4 && warp < 8) {
         // =============================== scaling warps ===============================
@@ -490,45 +727,59 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         const int srow = wtid & 63, shalf = wtid >> 6;
         const int quarter = warp & 3;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        constexpr int kBar = 1;
-        const uint64_t keep = tc::policy_evict_last(), drop = tc::policy_evict_first();
+        constexpr int kBar = kBarScale;
+        const uint64_t drop = tc::policy_evict_first();
+        const GateRec *recA = reinterpret_cast<const GateRec *>(sm + kGate);
+        const GateRec *recC = recA + kRecA;
         uint32_t us = 0, kpc = 0, cc = 0, job = 0;   // job: stage counter as the producer's
+        uint32_t ja = 0, jc = 0;                     // gate records consumed
+#ifdef SALA_TRACE
+        unsigned long long wacc_[8] = {};
+#endif
 
-        // K rows and raw g of the output-pass chunk still to scale, loaded one chunk ahead into
-        // registers (the scores of the current chunk are done in between); raw g of the
-        // state-pass jobs, two jobs ahead
+        // K rows of the output-pass chunk still to scale, loaded one chunk ahead into registers
+        // (the scores of the current chunk are done in between)
         uint4 kx[8];
-        float2 graw = make_float2(0.f, 0.f), gry = make_float2(0.f, 0.f);
-        auto prefetch = [&](int64_t c0, int nv, int h, bool state_pass) {
-            graw = load_gate(a.g, c0, nv, H, h);
+        auto prefetch = [&](int64_t c0, int nv, int h) {
             if (srow < nv) {
                 const uint8_t *src = reinterpret_cast<const uint8_t *>(
                     a.k + ((c0 + srow) * H + h) * kD + 64 * shalf);
-                const uint64_t pol = state_pass ? keep : drop;
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) kx[c8] = tc::ldg_nc_hint(src + 16 * c8, pol);
+                for (int c8 = 0; c8 < 8; ++c8) kx[c8] = tc::ldg_nc_hint(src + 16 * c8, drop);
             } else {
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) kx[c8] = make_uint4(0u, 0u, 0u, 0u);
             }
         };
-        // K~ = K exp(base - b_s) into buffer kpc & 1 (and raw K if `raw`); rows >= nv zero.
-        auto make_k = [&](const uint4 (&x)[8], const Gate &G, float base, int nv, bool raw,
-                          int fast_flag) {
+        // K~ of the chunk whose gate record is R into buffer kpc & 1: k exp(-(base + b_s))
+        // (factored route) or k exp(b_C - b_s) plus the raw rows (exact route); rows >= nv zero.
+        auto make_k = [&](const uint4 (&x)[8], const GateRec *R, int nv) {
             const uint32_t kb = kpc & 1;
+#ifdef SALA_TRACE
+            long long tw0 = clock64();
+#endif
             wait_nv(&kp_free[kb], (kpc >> 1) - 1, kpc >= 2, abort_v, status);
+#ifdef SALA_TRACE
+            wacc_[0] += clock64() - tw0;
+            tw0 = clock64();
+#endif
             if (wtid == 0) TRACE(2, 9, kpc);
-            const float bs = gate_at(G, srow);
-            const float fac = srow < nv ? tc::ex2((base - bs) * kLog2e) : 0.f;
+            const bool fast = R->fast != 0;
+            const float bs = R->b[srow];
+            const float e = fast ? -(R->base + bs) : R->bC - bs;
+            const float fac = srow < nv ? tc::ex2(e * kLog2e) : 0.f;
             store_row_scaled<false>(sm + kKp + kb * kTile + shalf * kRegion,
-                             raw ? sm + kKr + kb * kTile + shalf * kRegion : nullptr, srow, x, fac);
+                             fast ? nullptr : sm + kKr + kb * kTile + shalf * kRegion, srow, x, fac);
             if (wtid == 0) TRACE(2, 10, kpc);
             tc::fence_proxy_async_smem();
             named_sync(kBar, 128);
             if (wtid == 0) {
-                kfast[kb] = fast_flag;
+                kfast[kb] = fast;
                 tc::mbar_arrive(&kp_ready[kb]);
             }
+#ifdef SALA_TRACE
+            wacc_[1] += clock64() - tw0;
+#endif
             ++kpc;
         };
 
@@ -548,23 +799,21 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             // ---------------- A: K' = K exp(B_end - B_s), chunks last to first ----------------
             // job r is chunk nch - 1 - r; its K tile arrived by TMA in the first tile of the
             // stage and is scaled there in place (ordinary shared-memory loads are cheap here:
-            // the tensor core only runs the short state-pass products). The log-decays are
-            // loaded two jobs ahead.
-            auto job_c0 = [&](int r) { return chunk_c0(nch - 1 - r); };
-            auto job_nv = [&](int r) { return chunk_nv(nch - 1 - r); };
-            graw = load_gate(a.g, job_c0(0), job_nv(0), H, h);
-            if (nch > 1) gry = load_gate(a.g, job_c0(1), job_nv(1), H, h);
-            float D = 0.f;   // total log-decay of the chunks already visited (the later ones)
-            auto a_job = [&](int r, float2 &gb) {
-                const int nv = job_nv(r);
+            // the tensor core only runs the short state-pass products).
+            float D = 0.f;   // total log-decay of the segment
+            for (int r = 0; r < nch; ++r) {
+                const int nv = chunk_nv(nch - 1 - r);
                 const uint32_t st = job % kStages;
                 if (wtid == 0) TRACE(2, 1, r);
-                const Gate G = scan_gate(gb, nv);
-                if (r + 2 < nch) gb = load_gate(a.g, job_c0(r + 2), job_nv(r + 2), H, h);
+                wait_nv(&ga_full[ja % kRecA], ja / kRecA, true, abort_v, status);
+                const GateRec *R = recA + ja % kRecA;
+                const float e = R->bC + R->D - R->b[srow];
+                const float bC = R->bC;
+                warp_arrive(&ga_empty[ja % kRecA]);
+                ++ja;
+                const float fac = srow < nv ? tc::ex2(e * kLog2e) : 0.f;
                 wait_nv(&full[st], job / kStages, true, abort_v, status);
                 if (wtid == 0) TRACE(2, 7, r);
-                const float bs = gate_at(G, srow);
-                const float fac = srow < nv ? tc::ex2((G.bC + D - bs) * kLog2e) : 0.f;
                 uint8_t *kt = sm + st * kStage + shalf * kRegion;
                 uint4 x[8];
 #pragma unroll
@@ -576,14 +825,10 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                     tc::mbar_arrive(&ka_ready[st]);
                     TRACE(2, 8, r);
                 }
-                D += G.bC;
+                D += bC;
                 ++job;
-            };
-            for (int r = 0; r < nch; r += 2) {
-                a_job(r, graw);
-                if (r + 1 < nch) a_job(r + 1, gry);
             }
-            prefetch(chunk_c0(0), chunk_nv(0), h, false);
+            prefetch(chunk_c0(0), chunk_nv(0), h);
             wait_nv(&d_free, us - 1, us >= 1, abort_v, status);
             if (wtid == 0) {
                 unit_D = D;
@@ -594,52 +839,63 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             // K~ of chunk 0; then per chunk: K~ of the next chunk, P' of this one. The scaling
             // warps wait on every stage phase (mbarrier waits compare parity only, so a waiter
             // must not skip phases), although here they read K with ordinary global loads.
-            const uint32_t job_c = job;
+            const uint32_t job_c = job, jc0 = jc;
             auto wait_stage = [&](int c) {
+#ifdef SALA_TRACE
+                const long long tw2 = clock64();
+#endif
                 wait_nv(&full[(job_c + c) % kStages], (job_c + c) / kStages, true, abort_v, status);
+#ifdef SALA_TRACE
+                wacc_[5] += clock64() - tw2;
+#endif
             };
-            Gate Gc = scan_gate(graw, chunk_nv(0));
-            wait_stage(0);
-            make_k(kx, Gc, Gc.fast ? 0.f : Gc.bC, chunk_nv(0), !Gc.fast, Gc.fast);
-            if (nch > 1) prefetch(chunk_c0(1), chunk_nv(1), h, false);
-            for (int c = 0; c < nch; ++c) {
-                const int64_t c0 = chunk_c0(c);
-                const int nv = chunk_nv(c);
-                const Gate G = Gc;
+            // the gate record of chunk c (held from its K~ until its P' is done)
+            auto rec = [&](int c) { return recC + (jc0 + c) % kRecC; };
+            auto wait_rec = [&](int c) {
+                wait_nv(&gc_full[(jc0 + c) % kRecC], (jc0 + c) / kRecC, true, abort_v, status);
+            };
+            for (int c = -1; c < nch; ++c) {
                 if (c + 1 < nch) {
-                    const int nv1 = chunk_nv(c + 1);
-                    Gc = scan_gate(graw, nv1);
+                    wait_rec(c + 1);
                     wait_stage(c + 1);
-                    make_k(kx, Gc, Gc.fast ? 0.f : Gc.bC, nv1, !Gc.fast, Gc.fast);
-                    if (c + 2 < nch) prefetch(chunk_c0(c + 2), chunk_nv(c + 2), h, false);
+                    make_k(kx, rec(c + 1), chunk_nv(c + 1));
+                    if (c + 2 < nch) prefetch(chunk_c0(c + 2), chunk_nv(c + 2), h);
                     if (wtid == 0) TRACE(2, 3, c);
                 }
+                if (c < 0) continue;
+                const int nv = chunk_nv(c);
+                const GateRec *R = rec(c);
                 // scores -> P' (bf16, K-major rows t): mask s <= t < nv; exact route weights
-                const uint32_t pb = cc & 1;
+                const bool fast = R->fast != 0;
+#ifdef SALA_TRACE
+                long long tw1 = clock64();
+#endif
                 wait_nv(&p_full, cc, true, abort_v, status);
-                wait_nv(&pp_free[pb], (cc >> 1) - 1, cc >= 2, abort_v, status);
+#ifdef SALA_TRACE
+                wacc_[2] += clock64() - tw1;
+                tw1 = clock64();
+#endif
+                wait_nv(&pp_free, cc - 1, cc >= 1, abort_v, status);
+#ifdef SALA_TRACE
+                wacc_[3] += clock64() - tw1;
+                tw1 = clock64();
+#endif
                 if (wtid == 0) TRACE(2, 5, c);
                 tc::tc_fence_after();
                 // M=64 accumulator layout: row t = 16 * quarter + lane in lanes 0-15
                 const int tr = quarter * 16 + (lane & 15);
-                const float bt = gate_at(G, tr) * kLog2e;
-                uint8_t *pp = sm + kPp + pb * kRegion;
-#pragma unroll
+                uint8_t *pp = sm + kPp;
+#pragma unroll 1
                 for (int half = 0; half < 2; ++half) {
                     uint32_t p[32];
                     tc::tmem_ld_32x32b_x32(tmem + lane_base + kTP + 32 * half, p);
                     tc::tmem_ld_wait();
+                    if (wtid == 0) TRACE(2, 20 + half, c);
                     if (half == 1) {
                         tc::tc_fence_before();
                         named_sync(kBar, 128);
                         if (wtid == 0) tc::mbar_arrive(&p_free);
-                    }
-                    if (!G.fast) {
-                        // exact route: P'[t, s] = P[t, s] exp(b_t - b_s)
-#pragma unroll
-                        for (int s = 0; s < 32; ++s)
-                            p[s] = __float_as_uint(__uint_as_float(p[s]) *
-                                                   tc::ex2(bt - gate_at(G, 32 * half + s) * kLog2e));
+                        if (wtid == 0) TRACE(2, 22, c);
                     }
                     if (lane < 16) {
                         const bool live = tr < nv;
@@ -657,86 +913,96 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                                 make_uint4(w[0], w[1], w[2], w[3]);
                         }
                     }
+                    if (wtid == 0) TRACE(2, 23 + half, c);
                 }
-                if (!G.fast) {
-                    // exact route: q_t <- exp(b_t) q_t in place (M1 has read Q already); the
-                    // rows come from global memory, not from the tile
-                    uint8_t *qt = sm + ((job_c + c) % kStages) * kStage + shalf * kRegion;
-                    uint4 x[8];
-                    if (srow < nv) {
-                        const uint8_t *src = reinterpret_cast<const uint8_t *>(
-                            a.q + ((c0 + srow) * H + h) * kD + 64 * shalf);
-#pragma unroll
-                        for (int c8 = 0; c8 < 8; ++c8) x[c8] = tc::ldg_nc_hint(src + 16 * c8, drop);
-                    } else {
-#pragma unroll
-                        for (int c8 = 0; c8 < 8; ++c8) x[c8] = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    store_row_scaled<false>(qt, nullptr, srow, x, tc::ex2(gate_at(G, srow) * kLog2e));
+                if (!fast) {
+                    // exact route: P'[t, s] *= exp(b_t - b_s); q_t <- exp(b_t) q_t in place (M1
+                    // has read Q already; the rows come from global memory, not from the tile)
+                    if (lane < 16 && tr < nv) exact_pp_weights(pp, R->b, tr);
+                    exact_q_scale(sm + ((job_c + c) % kStages) * kStage + shalf * kRegion,
+                                  reinterpret_cast<const uint16_t *>(a.q), chunk_c0(c), srow, shalf,
+                                  nv, H, h, R->b[srow]);
                 }
+                warp_arrive(&gc_empty[(jc0 + c) % kRecC]);   // done with chunk c's record
                 tc::fence_proxy_async_smem();
+                if (wtid == 0) TRACE(2, 25, c);
                 named_sync(kBar, 128);
                 if (wtid == 0) {
-                    tc::mbar_arrive(&pp_ready[pb]);
+                    tc::mbar_arrive(&pp_ready);
                     TRACE(2, 6, c);
                 }
+#ifdef SALA_TRACE
+                wacc_[4] += clock64() - tw1;
+#endif
                 ++cc;
             }
             // one uniform decision per unit (after an abort every wait returns at once, so all
             // threads still pass the same barriers inside the unit)
             if (named_any(kBar, 128, *abort_v != 0)) break;
             job = job_c + nch;
+            jc = jc0 + nch;
             ++us;
         }
-    } else if (warp >= 8) {
-        // =============================== state warps ===============================
-        // Waits inside a unit do not vote: a thread whose wait gives up has set the abort
-        // flag, and every later wait returns at once, so all threads still pass the same
-        // barriers; one OR-vote per hand-off and per unit, taken over both groups together
-        // (they also share a barrier in the hand-off), then ends the loop uniformly.
-        constexpr int kBarBoth = 4;
-        const int wg = (warp - 8) >> 2;
-        const int wtid = threadIdx.x - 256 - 128 * wg;
+#ifdef SALA_TRACE
+        if (blockIdx.x == 0 && wtid == 0)
+            for (int i = 0; i < 6; ++i) g_wait_acc[16 + i] = wacc_[i];
+#endif
+    } else if (warp >= 8 && warp < 12) {
+        // =============================== converting warps ===============================
+        // Thread j (= TMEM lane) owns row j of Z^T: all 128 keys i, handled 32 at a time.
+        // Waits inside a unit do not vote: a thread whose wait gives up has set the abort flag,
+        // and every later wait returns at once, so all threads still pass the same barriers;
+        // one OR-vote per hand-off and per unit then ends the loop uniformly.
+        const int wtid = threadIdx.x - 256;
         const int quarter = warp & 3;
         const int j = quarter * 32 + lane;     // value column = TMEM lane
-        const int i0 = 64 * wg;                // my key rows i0 .. i0 + 63
-        const int bar_id = 2 + wg;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        uint32_t us = 0, dsc = 0, cc = 0, sbc = 0;
-        float S[64];   // S^T[j][i0 + i] = S[i0 + i][j]
+        uint32_t us = 0, zfc = 0, zbc = 0, npub = 0, jc = 0;
+        const GateRec *recC = reinterpret_cast<const GateRec *>(sm + kGate) + kRecA;
+        // the plan of the next chunk from its gate record (released at once)
+        struct ConvPlan {
+            float e1, eC;
+            bool fast, moved;
+        };
+        auto next_plan = [&]() {
+            wait_nv(&gc_full[jc % kRecC], jc / kRecC, true, abort_v, status);
+            const GateRec *R = recC + jc % kRecC;
+            ConvPlan cp{R->e1, R->eC, R->fast != 0, R->moved != 0};
+            warp_arrive(&gc_empty[jc % kRecC]);
+            ++jc;
+            return cp;
+        };
 
-        // bf16 copy of S^T for M2: my 64 keys -> 32 packed columns of the A operand
-        auto write_sb = [&]() {
-            wait_nv(&sb_free, sbc - 1, sbc >= 1, abort_v, status);
+        // bf16 copy of 32 keys (one quarter of the row) into the A operand of M2
+        auto store_zb = [&](int k4, const float (&x)[32], float fac) {
+            uint32_t w[16];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) w[m] = float2_to_bf16x2(x[2 * m] * fac, x[2 * m + 1] * fac);
+            tc::tmem_st_32x32b_x16(tmem + lane_base + zb_col(zbc & 1) + 16 * k4, w);
+        };
+        auto store_z = [&](int k4, const float (&x)[32], float fac) {
             uint32_t w[32];
 #pragma unroll
-            for (int m = 0; m < 32; ++m) w[m] = float2_to_bf16x2(S[2 * m], S[2 * m + 1]);
-            tc::tmem_st_32x32b_x32(tmem + lane_base + kTSb + 32 * wg, w);
-            tc::tmem_st_wait();
-            tc::tc_fence_before();
-            named_sync(bar_id, 128);
-            if (wtid == 0) tc::mbar_arrive(&sb_ready);
-            ++sbc;
+            for (int m = 0; m < 32; ++m) w[m] = __float_as_uint(x[m] * fac);
+            tc::tmem_st_32x32b_x32(tmem + lane_base + kTZ + 32 * k4, w);
         };
 
         for (;;) {
             const uint32_t slot = us & 1;
-            if (!wg_wait(&unit_full[slot], us >> 1, true, kBarBoth, abort_v, status, 256)) break;
+            if (!wg_wait(&unit_full[slot], us >> 1, true, kBarConv, abort_v, status)) break;
             const UnitInfo info = units[slot];
-            named_sync(bar_id, 128);
+            named_sync(kBarConv, 128);
             if (wtid == 0) tc::mbar_arrive(&unit_empty[slot]);
             if (!info.valid) break;
             const int h = info.h, nch = info.nch;
-            if (wtid == 0) TRACE(3 + wg, 1, us);
+            if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 1, us);
 
-            // ---------------- hand-off: S_in, bf16 S_in for M2, publish S_out ----------------
+            // ---------------- hand-off: S_in, Z = S_in and its bf16 copy, publish S_out ----------------
             {
-                const uint32_t db = dsc & 1;
-                bool bad = !wait_or_abort(&ds_full[db], (dsc >> 1) & 1, abort_v, status);
-                if (wtid == 0) TRACE(3 + wg, 11, us);
+                bool bad = !wait_or_abort(&ds_full, us & 1, abort_v, status);
+                if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 15, us);
                 bad = bad || !wait_or_abort(&d_ready, us & 1, abort_v, status);
-                if (wtid == 0) TRACE(3 + wg, 12, us);
-                ++dsc;
+                if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 11, us);
                 if (!bad && !info.first && wtid == 0) {
                     const uint32_t *flag = f.flags + (info.sigma - 1) * H + h;
                     const uint64_t t0ns = tc::global_timer_ns();
@@ -750,148 +1016,258 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                         }
                     }
                 }
-                if (named_any(kBarBoth, 256, bad || *abort_v)) break;
-                if (wtid == 0) TRACE(3 + wg, 2, 0);
+                if (named_any(kBarConv, 128, bad || *abort_v)) break;
+                if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 2, 0);
                 tc::tc_fence_after();
-                if (info.first) {
-                    if (f.h0) {
-                        const float *src = f.h0 + ((info.n * H + h) * kD + i0) * kD + j;
-#pragma unroll
-                        for (int i = 0; i < 64; ++i) S[i] = __ldg(src + i * kD);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 64; ++i) S[i] = 0.f;
-                    }
-                } else {
-                    // the predecessor's S_out, written by another SM: read through L2
-                    const float *src = f.incl + ((static_cast<size_t>(info.sigma - 1) * H + h) * kD + i0) * kD + j;
-#pragma unroll
-                    for (int i = 0; i < 64; ++i) S[i] = __ldcg(src + i * kD);
-                }
-                if (wtid == 0) TRACE(3 + wg, 13, us);
+                // chunk 0 starts at the reference point (pre = 0); the exact route keeps the
+                // state scaled to the chunk end
+                const float zfac = next_plan().eC;
                 const float eB = tc::ex2(unit_D * kLog2e);
-                named_sync(bar_id, 128);
-                if (wtid == 0) tc::mbar_arrive(&d_free);
-                write_sb();   // bf16 S_in for the first chunk's M2 first: the output pass can start
-                // S_out = exp(B) S_in + dS: to hT (last segment) or to the successor; each warp
-                // store covers one 128-byte row segment (32 consecutive j)
+                warp_arrive(&d_free);
                 float *dst = info.last ? (f.hT ? f.hT + (info.n * H + h) * kD * kD : nullptr)
                                        : f.incl + (static_cast<size_t>(info.sigma) * H + h) * kD * kD;
+                const float *src = info.first
+                    ? (f.h0 ? f.h0 + (info.n * H + h) * kD * kD : nullptr)
+                    : f.incl + (static_cast<size_t>(info.sigma - 1) * H + h) * kD * kD;
+                // (the second bf16 buffer overlays dS^T columns 0-63: quarter k4 writes columns
+                // 16 k4 .. + 15, which quarters 0 and 1 have read already)
+                wait_nv(&zb_free[zbc & 1], (zbc >> 1) - 1, zbc >= 2, abort_v, status);
+#pragma unroll 1
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    // S_in[i][j] for i = 32 k4 .. + 31: another SM wrote it, so read through L2
+                    float s[32];
+                    if (src) {
+                        const float *p = src + (32 * k4) * kD + j;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                        for (int i = 0; i < 32; ++i) s[i] = info.first ? __ldg(p + i * kD) : __ldcg(p + i * kD);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) s[i] = 0.f;
+                    }
                     uint32_t d[32];
-                    tc::tmem_ld_32x32b_x32(tmem + lane_base + kTdS + 128 * db + i0 + 32 * half, d);
+                    tc::tmem_ld_32x32b_x32(tmem + lane_base + kTdS + 32 * k4, d);
                     tc::tmem_ld_wait();
                     if (dst) {
-                        float *p = dst + (i0 + 32 * half) * kD + j;
+                        // S_out = exp(B) S_in + dS: each warp store covers one 128-byte row segment
+                        float *p = dst + (32 * k4) * kD + j;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            p[i * kD] = fmaf(eB, S[32 * half + i], __uint_as_float(d[i]));
+                        for (int i = 0; i < 32; ++i) p[i * kD] = fmaf(eB, s[i], __uint_as_float(d[i]));
                     }
+                    store_z(k4, s, zfac);
+                    store_zb(k4, s, 1.f);
                 }
-                if (wtid == 0) TRACE(3 + wg, 14, us);
+                tc::tmem_st_wait();
                 tc::tc_fence_before();
-                named_sync(kBarBoth, 256);   // both state groups have stored S_out and read dS
-                if (wtid == 0) tc::mbar_arrive(&ds_free[db]);
-                if (wg == 0 && wtid == 0 && !info.last) {
-                    // publish for the successor: the barrier orders the groups' stores before
-                    // this thread's device-scope fence and release of the flag
-                    __threadfence();
-                    tc::st_release_gpu(f.flags + info.sigma * H + h, f.epoch);
+                warp_arrive(&ds_free);
+                if (nch > 1) warp_arrive(&z_free);
+                warp_arrive(&zb_ready[zbc & 1]);
+                ++zbc;
+                // the publisher releases the flag once all four warps have stored S_out
+                wait_nv(&pub_free, npub - 1, npub >= 1, abort_v, status);
+                if (wtid == 0) {
+                    pub_cmd = info.last ? 0 : 1;
+                    pub_flag = f.flags + info.sigma * H + h;
                 }
-                if (wtid == 0) TRACE(3 + wg, 3, 0);
-            }
+                warp_arrive(&pub_ready);
+                ++npub;
+                if (wtid == 0) TRACE(3, 3, 0);
 
-            // ---------------- C ----------------
-            float2 graw = load_gate(a.g, info.t0, static_cast<int>(min(int64_t(kChunk), info.t1 - info.t0)), H, h);
+                // ---------------- C: the state entering each later chunk ----------------
+                for (int c = 1; c < nch; ++c) {
+                    const ConvPlan P = next_plan();
+                    if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 12, c);
+                    wait_nv(&z_full, zfc, true, abort_v, status);   // M4 of chunk c - 1 is done
+                    ++zfc;
+                    if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 4, c);
+                    tc::tc_fence_after();
+                    // stored state -> true state at the chunk start: exp(pre); the stored state
+                    // keeps that (moved reference) or goes on to the chunk end (exact route).
+                    // Z is read (and rescaled) first and released to the next M4 at once; the
+                    // bf16 copy waits for M2 of the previous chunk to have read the old one.
+                    const float e1 = P.e1, eC = P.eC;
+                    // keys 64 k2 .. + 63 of Z, as the true state at the chunk start
+                    auto load_half = [&](int k2, uint32_t (&d0)[32], uint32_t (&d1)[32]) {
+                        tc::tmem_ld_32x32b_x32(tmem + lane_base + kTZ + 64 * k2, d0);
+                        tc::tmem_ld_32x32b_x32(tmem + lane_base + kTZ + 64 * k2 + 32, d1);
+                        tc::tmem_ld_wait();
+                        if (P.moved) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                d0[i] = __float_as_uint(__uint_as_float(d0[i]) * e1);
+                                d1[i] = __float_as_uint(__uint_as_float(d1[i]) * e1);
+                            }
+                        }
+                    };
+                    auto store_z_half = [&](int k2, const uint32_t (&d0)[32], const uint32_t (&d1)[32]) {
+                        tc::tmem_st_32x32b_x32(tmem + lane_base + kTZ + 64 * k2, d0);
+                        tc::tmem_st_32x32b_x32(tmem + lane_base + kTZ + 64 * k2 + 32, d1);
+                    };
+                    // bf16 copy of a half (2 keys per word) into the A operand of M2
+                    auto store_zb_half = [&](int k2, const uint32_t (&d0)[32], const uint32_t (&d1)[32]) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int m = 0; m < 16; ++m)
+                            w[m] = float2_to_bf16x2(__uint_as_float(d0[2 * m]), __uint_as_float(d0[2 * m + 1]));
+                        tc::tmem_st_32x32b_x16(tmem + lane_base + zb_col(zbc & 1) + 32 * k2, w);
+#pragma unroll
+                        for (int m = 0; m < 16; ++m)
+                            w[m] = float2_to_bf16x2(__uint_as_float(d1[2 * m]), __uint_as_float(d1[2 * m + 1]));
+                        tc::tmem_st_32x32b_x16(tmem + lane_base + zb_col(zbc & 1) + 32 * k2 + 16, w);
+                    };
+                    if (P.fast) {
+                        // Z is read (and, if the reference moved, rescaled) and released to the
+                        // next M4 as soon as its second half is in registers; the bf16 copy
+                        // goes to the buffer M2 of two chunks before has read
+                        {
+                            uint32_t d0[32], d1[32];
+                            load_half(0, d0, d1);
+                            if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 13, c);
+                            if (P.moved) store_z_half(0, d0, d1);
+                            wait_nv(&zb_free[zbc & 1], (zbc >> 1) - 1, zbc >= 2, abort_v, status);
+                            tc::tc_fence_after();
+                            store_zb_half(0, d0, d1);
+                            if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 14, c);
+                        }
+                        uint32_t d0[32], d1[32];
+                        load_half(1, d0, d1);
+                        if (P.moved) {
+                            store_z_half(1, d0, d1);
+                            tc::tmem_st_wait();
+                        }
+                        tc::tc_fence_before();
+                        if (c + 1 < nch) warp_arrive(&z_free);
+                        if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 5, c);
+                        store_zb_half(1, d0, d1);
+                    } else {
+                        // exact route (rare): Z goes on to the chunk end
+                        wait_nv(&zb_free[zbc & 1], (zbc >> 1) - 1, zbc >= 2, abort_v, status);
+                        tc::tc_fence_after();
+#pragma unroll 1
+                        for (int k2 = 0; k2 < 2; ++k2) {
+                            uint32_t d0[32], d1[32];
+                            load_half(k2, d0, d1);
+                            store_zb_half(k2, d0, d1);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                d0[i] = __float_as_uint(__uint_as_float(d0[i]) * eC);
+                                d1[i] = __float_as_uint(__uint_as_float(d1[i]) * eC);
+                            }
+                            store_z_half(k2, d0, d1);
+                        }
+                        tc::tmem_st_wait();
+                        tc::tc_fence_before();
+                        if (c + 1 < nch) warp_arrive(&z_free);
+                    }
+                    tc::tmem_st_wait();
+                    tc::tc_fence_before();
+                    warp_arrive(&zb_ready[zbc & 1]);
+                    ++zbc;
+                    if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 8, c);
+                }
+            }
+            if (named_any(kBarConv, 128, *abort_v != 0)) break;
+            ++us;
+        }
+        // stop the publisher (after an abort it stops by itself)
+        if (!named_any(kBarConv, 128, *abort_v != 0)) {
+            wait_nv(&pub_free, npub - 1, npub >= 1, abort_v, status);
+            if (wtid == 0) pub_cmd = 2;
+            warp_arrive(&pub_ready);
+        }
+    } else if (warp >= 12) {
+        // =============================== output warps ===============================
+        // Warp quarter q writes value columns j = 32 q + lane of every token: o_t = factor_t
+        // O^T[j][t], staged as a [64 t x 32 j] bf16 tile and written by one TMA store per warp
+        // (direct stores when the chunk is ragged: the rows past it belong to another sequence).
+        const int wtid = threadIdx.x - 384;
+        const int quarter = warp & 3;
+        const int j = quarter * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        uint8_t *stg = sm + kOst + quarter * kOstWarp;
+        const GateRec *recC = reinterpret_cast<const GateRec *>(sm + kGate) + kRecA;
+        uint32_t us = 0, cc = 0, jc = 0;
+        for (;;) {
+            const uint32_t slot = us & 1;
+            if (!wg_wait(&unit_full[slot], us >> 1, true, kBarOut, abort_v, status)) break;
+            const UnitInfo info = units[slot];
+            named_sync(kBarOut, 128);
+            if (wtid == 0) tc::mbar_arrive(&unit_empty[slot]);
+            if (!info.valid) break;
+            const int h = info.h, nch = info.nch;
             for (int c = 0; c < nch; ++c) {
                 const int64_t c0 = info.t0 + int64_t(c) * kChunk;
                 const int nv = static_cast<int>(min(int64_t(kChunk), info.t1 - c0));
-                const Gate G = scan_gate(graw, nv);
-                if (c + 1 < nch)
-                    graw = load_gate(a.g, c0 + kChunk, static_cast<int>(min(int64_t(kChunk), info.t1 - c0 - kChunk)), H, h);
-                if (wtid == 0) TRACE(3 + wg, 4, c);
-
-                // state carry for my 64 keys; bf16 copy for the next chunk's M2
-                if (c + 1 < nch) {
-                    const uint32_t db = dsc & 1;
-                    wait_nv(&ds_full[db], dsc >> 1, true, abort_v, status);
-                    ++dsc;
-                    if (wtid == 0) TRACE(3 + wg, 7, c);
-                    tc::tc_fence_after();
-                    const float eC = tc::ex2(G.bC * kLog2e);
+                // lane l's factors for tokens l and 32 + l (broadcast below), from the chunk's
+                // gate record
+                wait_nv(&gc_full[jc % kRecC], jc / kRecC, true, abort_v, status);
+                const GateRec *R = recC + jc % kRecC;
+                const bool fast = R->fast != 0;
+                const float b_lo = R->b[lane], b_hi = R->b[32 + lane], base = R->base;
+                warp_arrive(&gc_empty[jc % kRecC]);
+                ++jc;
+                const float f_lo = fast ? a.scale * tc::ex2((base + b_lo) * kLog2e) : a.scale;
+                const float f_hi = fast ? a.scale * tc::ex2((base + b_hi) * kLog2e) : a.scale;
+                const uint32_t ob = cc & 1;
+                wait_nv(&o_full[ob], cc >> 1, true, abort_v, status);
+                if (wtid == 0) TRACE(4, 9, c);
+                tc::tc_fence_after();
+                uint32_t o0[32], o1[32];
+                tc::tmem_ld_32x32b_x32(tmem + lane_base + kTO + 64 * ob, o0);
+                tc::tmem_ld_32x32b_x32(tmem + lane_base + kTO + 64 * ob + 32, o1);
+                tc::tmem_ld_wait();
+                tc::tc_fence_before();
+                warp_arrive(&o_free[ob]);
+                // Stage [64 t][32 j] bf16: neighbouring lanes swap one value per token pair, so
+                // that each lane holds two adjacent columns of one token (even lane: token t,
+                // odd lane: token t + 1), scales them and writes one 32-bit word.
+                if (lane == 0) tc::tma_store_wait_read<0>();   // staging tile free again
+                __syncwarp();
+                const bool odd = lane & 1;
+                uint8_t *col = stg + 4 * (lane >> 1);
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t d[32];
-                        tc::tmem_ld_32x32b_x32(tmem + lane_base + kTdS + 128 * db + i0 + 32 * half, d);
-                        tc::tmem_ld_wait();
-                        if (G.fast) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) S[32 * half + i] = eC * (S[32 * half + i] + __uint_as_float(d[i]));
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) S[32 * half + i] = fmaf(eC, S[32 * half + i], __uint_as_float(d[i]));
-                        }
-                    }
-                    tc::tc_fence_before();
-                    named_sync(bar_id, 128);
-                    if (wtid == 0) tc::mbar_arrive(&ds_free[db]);
-                    write_sb();
-                    if (wtid == 0) TRACE(3 + wg, 8, c);
+                for (int tp = 0; tp < 32; tp += 2) {
+                    const int tk = tp + (lane & 1);
+                    const float ft = __shfl_sync(0xffffffffu, f_lo, tk);
+                    const float mine = __uint_as_float(odd ? o0[tp + 1] : o0[tp]);
+                    const float give = __uint_as_float(odd ? o0[tp] : o0[tp + 1]);
+                    const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+                    *reinterpret_cast<uint32_t *>(col + tk * 64) =
+                        odd ? float2_to_bf16x2(got * ft, mine * ft) : float2_to_bf16x2(mine * ft, got * ft);
                 }
-
-                // o_t = factor_t O^T[j][t] for my 32 tokens t = 32 wg + tt: staged as a
-                // [32 t x 128 j] bf16 tile and written by one TMA store (direct stores when the
-                // group has rows past the chunk's valid tokens, which belong to another sequence)
-                {
-                    const uint32_t ob = cc & 1;
-                    wait_nv(&o_full[ob], cc >> 1, true, abort_v, status);
-                    if (wtid == 0) TRACE(3 + wg, 9, c);
-                    tc::tc_fence_after();
-                    uint32_t o[32];
-                    tc::tmem_ld_32x32b_x32(tmem + lane_base + kTO + 64 * ob + 32 * wg, o);
-                    tc::tmem_ld_wait();
-                    tc::tc_fence_before();
-                    if (wtid == 0) tc::tma_store_wait_read<0>();   // staging buffer free again
-                    named_sync(bar_id, 128);
-                    if (wtid == 0) tc::mbar_arrive(&o_free[ob]);
-                    // lane l's factor for token 32 wg + l, then broadcast
-                    const float bl = gate_at(G, 32 * wg + lane);
-                    const float fl = G.fast ? a.scale * tc::ex2(bl * kLog2e) : a.scale;
-                    if (32 * wg + 32 <= nv) {
-                        uint8_t *stg = sm + kOst + wg * kOstBytes + 2 * j;
 #pragma unroll
-                        for (int tt = 0; tt < 32; ++tt) {
-                            const float ft = __shfl_sync(0xffffffffu, fl, tt);
-                            *reinterpret_cast<uint16_t *>(stg + tt * 256) =
-                                __bfloat16_as_ushort(__float2bfloat16_rn(ft * __uint_as_float(o[tt])));
-                        }
-                        tc::fence_proxy_async_smem();
-                        named_sync(bar_id, 128);
-                        if (wtid == 0) {
-                            tc::tma_store_3d(&maps.o, 0, h, static_cast<int32_t>(c0 + 32 * wg),
-                                             sm + kOst + wg * kOstBytes);
-                            tc::tma_store_commit();
-                        }
-                    } else {
-                        uint16_t *orow = a.o + (c0 * H + h) * kD + j;
-#pragma unroll
-                        for (int tt = 0; tt < 32; ++tt) {
-                            const float ft = __shfl_sync(0xffffffffu, fl, tt);
-                            const int tk = 32 * wg + tt;
-                            if (tk < nv)
-                                orow[static_cast<size_t>(tk) * H * kD] =
-                                    __bfloat16_as_ushort(__float2bfloat16_rn(ft * __uint_as_float(o[tt])));
-                        }
-                    }
-                    if (wtid == 0) TRACE(3 + wg, 10, c);
+                for (int tp = 0; tp < 32; tp += 2) {
+                    const int tk = tp + (lane & 1);
+                    const float ft = __shfl_sync(0xffffffffu, f_hi, tk);
+                    const float mine = __uint_as_float(odd ? o1[tp + 1] : o1[tp]);
+                    const float give = __uint_as_float(odd ? o1[tp] : o1[tp + 1]);
+                    const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+                    *reinterpret_cast<uint32_t *>(col + (32 + tk) * 64) =
+                        odd ? float2_to_bf16x2(got * ft, mine * ft) : float2_to_bf16x2(mine * ft, got * ft);
                 }
+                if (nv == kChunk) {
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tc::tma_store_3d(&maps.o, 32 * quarter, h, static_cast<int32_t>(c0), stg);
+                        tc::tma_store_commit();
+                    }
+                } else {
+                    // ragged chunk: only its nv rows go out (the rows past it belong to another
+                    // sequence), 64 bytes per row
+                    __syncwarp();
+                    uint16_t *orow = a.o + (c0 * H + h) * kD + 32 * quarter + lane;
+#pragma unroll 1
+                    for (int tt = 0; tt < nv; ++tt)
+                        orow[static_cast<size_t>(tt) * H * kD] =
+                            *reinterpret_cast<const uint16_t *>(stg + tt * 64 + 2 * lane);
+                }
+                if (wtid == 0) TRACE(4, 10, c);
                 ++cc;
             }
-            if (named_any(kBarBoth, 256, *abort_v != 0)) break;
+            if (named_any(kBarOut, 128, *abort_v != 0)) break;
             ++us;
         }
-        if (wtid == 0) tc::tma_store_wait_all<0>();
+        if (lane == 0) tc::tma_store_wait_all<0>();
     }
 
     tc::tc_fence_before();
@@ -938,7 +1314,7 @@ cudaError_t encode_map(CUtensorMap *map, const void *base, int64_t T_total, int 
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H),
                           static_cast<cuuint64_t>(T_total)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(H) * kD * 2};
-    cuuint32_t box_load[3] = {64, 1, 64}, box_store[3] = {128, 1, 32};
+    cuuint32_t box_load[3] = {64, 1, 64}, box_store[3] = {32, 1, 64};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                           strides, store ? box_store : box_load, estr,
@@ -999,13 +1375,20 @@ cudaError_t launch_prefill_fused(const ChunkArgs &a, const SegTable &t, int64_t 
 }  // namespace sala
 
 #ifdef SALA_TRACE
+extern "C" int sala_gla_debug_wait_acc(unsigned long long *out) {
+    return cudaMemcpyFromSymbol(out, sala::g_wait_acc, sizeof(sala::g_wait_acc)) == cudaSuccess ? 0 : -1;
+}
+extern "C" void sala_gla_debug_wait_reset() {
+    static unsigned long long z[32] = {};
+    cudaMemcpyToSymbol(sala::g_wait_acc, z, sizeof(z));
+}
 extern "C" int sala_gla_debug_trace(unsigned long long *out, int max) {
-    unsigned int n[5];
+    unsigned int n[8];
     if (cudaMemcpyFromSymbol(n, sala::g_trace_n, sizeof(n)) != cudaSuccess) return -1;
-    static unsigned long long buf[5][sala::kTraceN];
+    static unsigned long long buf[8][sala::kTraceN];
     if (cudaMemcpyFromSymbol(buf, sala::g_trace, sizeof(buf)) != cudaSuccess) return -1;
     int k = 0;
-    for (int r = 0; r < 5; ++r)
+    for (int r = 0; r < 8; ++r)
         for (unsigned i = 0; i < n[r] && i < static_cast<unsigned>(sala::kTraceN) && k < max; ++i)
             out[k++] = buf[r][i];
     return k;

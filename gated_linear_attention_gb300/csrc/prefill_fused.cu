@@ -249,13 +249,12 @@ __device__ __forceinline__ bool wg_wait(uint64_t *bar, uint32_t par, bool need, 
     return !named_any(bar_id, n, bad);
 }
 
-// 64 bf16 of one row, scaled by f, to a [64 x 128 B] SW128 region row (and, if raw_dst, also
-// unscaled to a second tile). kExact: product in fp32, rounded once; otherwise f is rounded to
-// bf16 and each pair takes one packed multiply (about 5x fewer instructions, one more
-// rounding of the factor: used for the output pass, whose tolerance has more room).
+// 64 bf16 of one row, scaled by f, to a [64 x 128 B] SW128 region row. kExact: product in
+// fp32, rounded once; otherwise f is rounded to bf16 and each pair takes one packed multiply
+// (about 5x fewer instructions, one more rounding of the factor: used for the output pass,
+// whose tolerance has more room).
 template <bool kExact>
-__device__ __forceinline__ void store_row_scaled(uint8_t *dst, uint8_t *raw_dst, int row,
-                                                 const uint4 (&x)[8], float f) {
+__device__ __forceinline__ void store_row_scaled(uint8_t *dst, int row, const uint4 (&x)[8], float f) {
     const __nv_bfloat162 f2 = __float2bfloat162_rn(f);
 #pragma unroll
     for (int c8 = 0; c8 < 8; ++c8) {
@@ -272,14 +271,20 @@ __device__ __forceinline__ void store_row_scaled(uint8_t *dst, uint8_t *raw_dst,
             y.w = mul_bf16x2(x[c8].w, f2);
         }
         *reinterpret_cast<uint4 *>(dst + sw(row, c8)) = y;
-        if (raw_dst) *reinterpret_cast<uint4 *>(raw_dst + sw(row, c8)) = x[c8];
     }
+}
+
+// The same row unscaled (exact route: raw K for M1).
+__device__ __forceinline__ void store_row(uint8_t *dst, int row, const uint4 (&x)[8]) {
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8) *reinterpret_cast<uint4 *>(dst + sw(row, c8)) = x[c8];
 }
 
 // Exact route, scores: row t of P' (already masked and rounded to bf16 in the SW128 tile at
 // pp) times exp(b_t - b_s) for every causal column s <= t (rare).
 __device__ __forceinline__ void exact_pp_weights(uint8_t *pp, const float *b, int t) {
     const float bt = b[t] * kLog2e;
+#pragma unroll 1
     for (int c8 = 0; c8 < 8; ++c8) {
         uint4 x = *reinterpret_cast<const uint4 *>(pp + sw(t, c8));
         uint32_t *w = reinterpret_cast<uint32_t *>(&x);
@@ -305,7 +310,7 @@ __device__ __forceinline__ void exact_q_scale(uint8_t *qt, const uint16_t *q, in
     } else {
         for (int c8 = 0; c8 < 8; ++c8) x[c8] = make_uint4(0u, 0u, 0u, 0u);
     }
-    store_row_scaled<false>(qt, nullptr, row, x, tc::ex2(b_row * kLog2e));
+    store_row_scaled<false>(qt, row, x, tc::ex2(b_row * kLog2e));
 }
 
 // Per-warp arrival: the warp's lanes have finished their part; lane 0 arrives for the warp.
@@ -464,13 +469,12 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             }
             __syncwarp();
             if (!info.valid) break;
-            for (int r = 0; r < info.nch && ok; ++r) {
-                const int64_t c0 = info.t0 + int64_t(info.nch - 1 - r) * kChunk;
-                ok = load_job(c0, static_cast<int>(min(int64_t(kChunk), info.t1 - c0)), info.h, false);
-            }
-            for (int c = 0; c < info.nch && ok; ++c) {
+            // state pass (K, V; chunks last to first), then output pass (Q, V; first to last)
+#pragma unroll 1
+            for (int j = 0; j < 2 * info.nch && ok; ++j) {
+                const int c = j < info.nch ? info.nch - 1 - j : j - info.nch;
                 const int64_t c0 = info.t0 + int64_t(c) * kChunk;
-                ok = load_job(c0, static_cast<int>(min(int64_t(kChunk), info.t1 - c0)), info.h, true);
+                ok = load_job(c0, static_cast<int>(min(int64_t(kChunk), info.t1 - c0)), info.h, j >= info.nch);
             }
             ++us;
         }
@@ -516,84 +520,77 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 tc::umma_commit(&ds_full);
                 // ---- C, software-pipelined: M1 of chunk c+1 goes out right after M2 of chunk c
                 // (before M3 of chunk c), so the scores of c+1 are made while chunk c finishes
-                auto issue_m1 = [&](uint32_t q_s, uint32_t kb, bool fast) {
-                    const uint32_t k1 = sb + (fast ? kKp : kKr) + kb * kTile;
-                    tc::tc_fence_after();
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
-                        tc::umma_bf16(tmem + kTP, desc_k(q_s + off), desc_k(k1 + off), kIdescP, ks > 0);
-                    }
-                    tc::umma_commit(&p_full);
-                };
-                // M1 of chunk 0: P = Q K~^T (factored route) or Q K^T (exact route)
-                uint32_t kb = kpc & 1;
-                {
-                    const uint32_t st = job % kStages;
-                    ok = TIMED(4, W(&full[st], job / kStages) && W(&kp_ready[kb], kpc >> 1) &&
-                         (cc == 0 || W(&p_free, cc - 1)));
-                    if (ok) {
-                        ++kpc;
-                        TRACE(1, 2, 0);
-                        issue_m1(sb + st * kStage, kb, kfast[kb] != 0);
-                    }
-                }
-                for (int c = 0; c < info.nch && ok; ++c) {
+                // per chunk c: M4(c), M2(c), M1(c+1), M3(c); the first pass (c = -1) issues M1(0)
+                uint32_t kb = kpc & 1;   // K~ set of the chunk in flight
+                for (int c = -1; c < info.nch && ok; ++c) {
                     const uint32_t st = job % kStages;
                     const uint32_t q_s = sb + st * kStage, v_s = q_s + kTile;
                     const uint32_t ob = cc & 1;
                     const bool fast = kfast[kb] != 0;
-                    // M4: Z^T += V^T K~ (not needed after the last chunk), once the converting
-                    // warps have read Z (and rescaled it, if the reference moved)
-                    if (c + 1 < info.nch) {
-                        if (!TIMED(5, W(&z_free, zfc))) { ok = false; break; }
-                        TRACE(1, 3, c);
+                    if (c >= 0) {
+                        // M4: Z^T += V^T K~ (not needed after the last chunk), once the converting
+                        // warps have read Z (and rescaled it, if the reference moved)
+                        if (c + 1 < info.nch) {
+                            if (!TIMED(5, W(&z_free, zfc))) { ok = false; break; }
+                            TRACE(1, 3, c);
 #ifdef SALA_TRACE
-                        const long long ti0 = clock64();
+                            const long long ti0 = clock64();
+#endif
+                            tc::tc_fence_after();
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks)
+                                tc::umma_bf16(tmem + kTZ, desc_mn8(v_s + ks * 2048),
+                                              desc_mn8(sb + kKp + kb * kTile + ks * 2048), kIdescS, 1u);
+                            tc::umma_commit(&z_full);
+#ifdef SALA_TRACE
+                            wacc_[13] += clock64() - ti0;
+#endif
+                            ++zfc;
+                        }
+                        // M2: O^T = Z^T Q^T (Q scaled in place first on the exact route)
+                        const uint32_t zb = zbc & 1;
+                        if (!TIMED(6, W(&zb_ready[zb], zbc >> 1))) { ok = false; break; }
+                        if (cc >= 2 && !TIMED(7, W(&o_free[ob], (cc >> 1) - 1))) { ok = false; break; }
+                        if (!fast && !TIMED(8, W(&pp_ready, cc))) { ok = false; break; }
+                        TRACE(1, 4, c);
+#ifdef SALA_TRACE
+                        const long long ti1 = clock64();
 #endif
                         tc::tc_fence_after();
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)
-                            tc::umma_bf16(tmem + kTZ, desc_mn8(v_s + ks * 2048),
-                                          desc_mn8(sb + kKp + kb * kTile + ks * 2048), kIdescS, 1u);
-                        tc::umma_commit(&z_full);
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
+                            tc::umma_bf16_ta(tmem + kTO + 64 * ob, tmem + zb_col(zb) + 8 * ks, desc_k(q_s + off),
+                                             kIdescO2, ks > 0);
+                        }
+                        tc::umma_commit(&zb_free[zb]);
+                        tc::umma_commit(&kp_free[kb]);   // M1, M4 and M2 of chunk c have read its set
 #ifdef SALA_TRACE
-                        wacc_[13] += clock64() - ti0;
+                        wacc_[14] += clock64() - ti1;
 #endif
-                        ++zfc;
+                        ++zbc;
                     }
-                    // M2: O^T = Z^T Q^T (Q scaled in place first on the exact route)
-                    const uint32_t zb = zbc & 1;
-                    if (!TIMED(6, W(&zb_ready[zb], zbc >> 1))) { ok = false; break; }
-                    if (cc >= 2 && !TIMED(7, W(&o_free[ob], (cc >> 1) - 1))) { ok = false; break; }
-                    if (!fast && !TIMED(8, W(&pp_ready, cc))) { ok = false; break; }
-                    TRACE(1, 4, c);
-#ifdef SALA_TRACE
-                    const long long ti1 = clock64();
-#endif
-                    tc::tc_fence_after();
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
-                        tc::umma_bf16_ta(tmem + kTO + 64 * ob, tmem + zb_col(zb) + 8 * ks, desc_k(q_s + off),
-                                         kIdescO2, ks > 0);
-                    }
-                    tc::umma_commit(&zb_free[zb]);
-                    tc::umma_commit(&kp_free[kb]);   // M1, M4 and M2 of chunk c have read its set
-#ifdef SALA_TRACE
-                    wacc_[14] += clock64() - ti1;
-#endif
-                    ++zbc;
-                    // M1 of chunk c+1, once the scores of chunk c have been read
+                    // M1 of the next chunk (P = Q K~^T, or Q K^T on the exact route), once the
+                    // scores of the chunk before it have been read
                     if (c + 1 < info.nch) {
-                        const uint32_t st1 = (job + 1) % kStages;
-                        kb = kpc & 1;
-                        if (!TIMED(9, W(&full[st1], (job + 1) / kStages)) || !TIMED(10, W(&kp_ready[kb], kpc >> 1)) ||
-                            !TIMED(11, W(&p_free, cc))) { ok = false; break; }
+                        const uint32_t jn = c < 0 ? job : job + 1, gn = c < 0 ? cc : cc + 1;
+                        const uint32_t kn = kpc & 1;
+                        if (!TIMED(9, W(&full[jn % kStages], jn / kStages)) || !TIMED(10, W(&kp_ready[kn], kpc >> 1)) ||
+                            (gn >= 1 && !TIMED(11, W(&p_free, gn - 1)))) { ok = false; break; }
                         ++kpc;
                         TRACE(1, 2, c + 1);
-                        issue_m1(sb + st1 * kStage, kb, kfast[kb] != 0);
+                        const uint32_t k1 = sb + (kfast[kn] != 0 ? kKp : kKr) + kn * kTile;
+                        const uint32_t q1 = sb + (jn % kStages) * kStage;
+                        tc::tc_fence_after();
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
+                            tc::umma_bf16(tmem + kTP, desc_k(q1 + off), desc_k(k1 + off), kIdescP, ks > 0);
+                        }
+                        tc::umma_commit(&p_full);
+                        if (c < 0) kb = kn;
                     }
+                    if (c < 0) continue;
                     // M3: O^T += V^T P'^T
                     if (fast && !TIMED(12, W(&pp_ready, cc))) { ok = false; break; }
                     TRACE(1, 5, c);
@@ -611,6 +608,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
 #ifdef SALA_TRACE
                     wacc_[15] += clock64() - ti2;
 #endif
+                    kb = (kpc - 1) & 1;   // the set M1 of the next chunk has taken
                     ++job;
                     ++cc;
                 }
@@ -670,52 +668,46 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                                !wait_or_abort(&empty_b[n % R], ((n / R) - 1) & 1, abort_v, status);
                 return !__any_sync(0xffffffffu, b);
             };
+            // jobs 0 .. nch-1: state pass, chunks last to first; jobs nch .. 2 nch-1: output
+            // pass, chunks first to last (log-decays loaded two jobs ahead)
+            auto chunk_of = [&](int j) { return j < nch ? nch - 1 - j : j - nch; };
             bool ok = true;
-            // state pass: chunks last to first
-            float2 g0 = load_gate(a.g, c0_of(nch - 1), nv_of(nch - 1), H, h);
-            float2 g1 = nch > 1 ? load_gate(a.g, c0_of(nch - 2), nv_of(nch - 2), H, h) : make_float2(0.f, 0.f);
-            float D = 0.f;
-            for (int r = 0; r < nch; ++r) {
-                const int c = nch - 1 - r;
+            float2 g0 = load_gate(a.g, c0_of(chunk_of(0)), nv_of(chunk_of(0)), H, h);
+            float2 g1 = load_gate(a.g, c0_of(chunk_of(1)), nv_of(chunk_of(1)), H, h);
+            float D = 0.f, run = 0.f;
+#pragma unroll 1
+            for (int j = 0; j < 2 * nch; ++j) {
+                const int c = chunk_of(j);
                 const Gate G = scan_gate(g0, nv_of(c));
                 g0 = g1;
-                if (r + 2 < nch) g1 = load_gate(a.g, c0_of(c - 2), nv_of(c - 2), H, h);
-                if (!(ok = claim(ga_empty, ja, kRecA))) break;
-                GateRec *R = recA + ja % kRecA;
-                *reinterpret_cast<float2 *>(&R->b[2 * lane]) = make_float2(G.b0, G.b1);
-                if (lane == 0) {
-                    R->bC = G.bC;
-                    R->D = D;
+                if (j + 2 < 2 * nch) g1 = load_gate(a.g, c0_of(chunk_of(j + 2)), nv_of(chunk_of(j + 2)), H, h);
+                const bool state = j < nch;
+                uint64_t *empty_b = state ? ga_empty : gc_empty;
+                const uint32_t n = state ? ja : jc;
+                const int R = state ? kRecA : kRecC;
+                if (!(ok = claim(empty_b, n, R))) break;
+                GateRec *rec = (state ? recA : recC) + n % R;
+                *reinterpret_cast<float2 *>(&rec->b[2 * lane]) = make_float2(G.b0, G.b1);
+                if (state) {
+                    if (lane == 0) {
+                        rec->bC = G.bC;
+                        rec->D = D;
+                    }
+                    D += G.bC;
+                } else {
+                    const Plan P = plan_chunk(G, run);
+                    if (lane == 0) {
+                        rec->bC = G.bC;
+                        rec->base = P.base;
+                        rec->e1 = P.moved ? tc::ex2(P.pre * kLog2e) : 1.f;
+                        rec->eC = P.fast ? 1.f : tc::ex2(G.bC * kLog2e);
+                        rec->fast = P.fast;
+                        rec->moved = P.moved;
+                    }
                 }
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&ga_full[ja % kRecA]);
-                D += G.bC;
-                ++ja;
-            }
-            if (!ok) break;
-            // output pass: chunks first to last
-            float run = 0.f;
-            g0 = load_gate(a.g, c0_of(0), nv_of(0), H, h);
-            g1 = nch > 1 ? load_gate(a.g, c0_of(1), nv_of(1), H, h) : make_float2(0.f, 0.f);
-            for (int c = 0; c < nch; ++c) {
-                const Gate G = scan_gate(g0, nv_of(c));
-                g0 = g1;
-                if (c + 2 < nch) g1 = load_gate(a.g, c0_of(c + 2), nv_of(c + 2), H, h);
-                const Plan P = plan_chunk(G, run);
-                if (!(ok = claim(gc_empty, jc, kRecC))) break;
-                GateRec *R = recC + jc % kRecC;
-                *reinterpret_cast<float2 *>(&R->b[2 * lane]) = make_float2(G.b0, G.b1);
-                if (lane == 0) {
-                    R->bC = G.bC;
-                    R->base = P.base;
-                    R->e1 = P.moved ? tc::ex2(P.pre * kLog2e) : 1.f;
-                    R->eC = P.fast ? 1.f : tc::ex2(G.bC * kLog2e);
-                    R->fast = P.fast;
-                    R->moved = P.moved;
-                }
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&gc_full[jc % kRecC]);
-                ++jc;
+                if (lane == 0) tc::mbar_arrive(state ? &ga_full[n % R] : &gc_full[n % R]);
+                if (state) ++ja; else ++jc;
             }
             if (!ok) break;
             ++us;
@@ -768,8 +760,8 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             const float bs = R->b[srow];
             const float e = fast ? -(R->base + bs) : R->bC - bs;
             const float fac = srow < nv ? tc::ex2(e * kLog2e) : 0.f;
-            store_row_scaled<false>(sm + kKp + kb * kTile + shalf * kRegion,
-                             fast ? nullptr : sm + kKr + kb * kTile + shalf * kRegion, srow, x, fac);
+            store_row_scaled<false>(sm + kKp + kb * kTile + shalf * kRegion, srow, x, fac);
+            if (!fast) store_row(sm + kKr + kb * kTile + shalf * kRegion, srow, x);
             if (wtid == 0) TRACE(2, 10, kpc);
             tc::fence_proxy_async_smem();
             named_sync(kBar, 128);
@@ -818,7 +810,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 uint4 x[8];
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) x[c8] = *reinterpret_cast<const uint4 *>(kt + sw(srow, c8));
-                store_row_scaled<true>(kt, nullptr, srow, x, fac);
+                store_row_scaled<true>(kt, srow, x, fac);
                 tc::fence_proxy_async_smem();
                 named_sync(kBar, 128);
                 if (wtid == 0) {
@@ -1039,7 +1031,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                     if (src) {
                         const float *p = src + (32 * k4) * kD + j;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) s[i] = info.first ? __ldg(p + i * kD) : __ldcg(p + i * kD);
+                        for (int i = 0; i < 32; ++i) s[i] = __ldcg(p + i * kD);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) s[i] = 0.f;
@@ -1086,80 +1078,43 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                     // bf16 copy waits for M2 of the previous chunk to have read the old one.
                     const float e1 = P.e1, eC = P.eC;
                     // keys 64 k2 .. + 63 of Z, as the true state at the chunk start
-                    auto load_half = [&](int k2, uint32_t (&d0)[32], uint32_t (&d1)[32]) {
+                    // keys 64 k2 .. + 63 of Z: to the true state at the chunk start (times e1),
+                    // its bf16 copy into the A operand of M2 (the buffer M2 of two chunks before
+                    // has read), and, if the reference moved, the stored state itself (times eC on
+                    // the exact route: on to the chunk end). One path for every route.
+                    const uint32_t zb_base = tmem + lane_base + zb_col(zbc & 1);
+                    wait_nv(&zb_free[zbc & 1], (zbc >> 1) - 1, zbc >= 2, abort_v, status);
+                    tc::tc_fence_after();
+#pragma unroll 1
+                    for (int k2 = 0; k2 < 2; ++k2) {
+                        uint32_t d0[32], d1[32];
                         tc::tmem_ld_32x32b_x32(tmem + lane_base + kTZ + 64 * k2, d0);
                         tc::tmem_ld_32x32b_x32(tmem + lane_base + kTZ + 64 * k2 + 32, d1);
                         tc::tmem_ld_wait();
-                        if (P.moved) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                d0[i] = __float_as_uint(__uint_as_float(d0[i]) * e1);
-                                d1[i] = __float_as_uint(__uint_as_float(d1[i]) * e1);
-                            }
-                        }
-                    };
-                    auto store_z_half = [&](int k2, const uint32_t (&d0)[32], const uint32_t (&d1)[32]) {
-                        tc::tmem_st_32x32b_x32(tmem + lane_base + kTZ + 64 * k2, d0);
-                        tc::tmem_st_32x32b_x32(tmem + lane_base + kTZ + 64 * k2 + 32, d1);
-                    };
-                    // bf16 copy of a half (2 keys per word) into the A operand of M2
-                    auto store_zb_half = [&](int k2, const uint32_t (&d0)[32], const uint32_t (&d1)[32]) {
                         uint32_t w[16];
 #pragma unroll
                         for (int m = 0; m < 16; ++m)
-                            w[m] = float2_to_bf16x2(__uint_as_float(d0[2 * m]), __uint_as_float(d0[2 * m + 1]));
-                        tc::tmem_st_32x32b_x16(tmem + lane_base + zb_col(zbc & 1) + 32 * k2, w);
+                            w[m] = float2_to_bf16x2(__uint_as_float(d0[2 * m]) * e1, __uint_as_float(d0[2 * m + 1]) * e1);
+                        tc::tmem_st_32x32b_x16(zb_base + 32 * k2, w);
 #pragma unroll
                         for (int m = 0; m < 16; ++m)
-                            w[m] = float2_to_bf16x2(__uint_as_float(d1[2 * m]), __uint_as_float(d1[2 * m + 1]));
-                        tc::tmem_st_32x32b_x16(tmem + lane_base + zb_col(zbc & 1) + 32 * k2 + 16, w);
-                    };
-                    if (P.fast) {
-                        // Z is read (and, if the reference moved, rescaled) and released to the
-                        // next M4 as soon as its second half is in registers; the bf16 copy
-                        // goes to the buffer M2 of two chunks before has read
-                        {
-                            uint32_t d0[32], d1[32];
-                            load_half(0, d0, d1);
-                            if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 13, c);
-                            if (P.moved) store_z_half(0, d0, d1);
-                            wait_nv(&zb_free[zbc & 1], (zbc >> 1) - 1, zbc >= 2, abort_v, status);
-                            tc::tc_fence_after();
-                            store_zb_half(0, d0, d1);
-                            if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 14, c);
-                        }
-                        uint32_t d0[32], d1[32];
-                        load_half(1, d0, d1);
+                            w[m] = float2_to_bf16x2(__uint_as_float(d1[2 * m]) * e1, __uint_as_float(d1[2 * m + 1]) * e1);
+                        tc::tmem_st_32x32b_x16(zb_base + 32 * k2 + 16, w);
                         if (P.moved) {
-                            store_z_half(1, d0, d1);
-                            tc::tmem_st_wait();
-                        }
-                        tc::tc_fence_before();
-                        if (c + 1 < nch) warp_arrive(&z_free);
-                        if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 5, c);
-                        store_zb_half(1, d0, d1);
-                    } else {
-                        // exact route (rare): Z goes on to the chunk end
-                        wait_nv(&zb_free[zbc & 1], (zbc >> 1) - 1, zbc >= 2, abort_v, status);
-                        tc::tc_fence_after();
-#pragma unroll 1
-                        for (int k2 = 0; k2 < 2; ++k2) {
-                            uint32_t d0[32], d1[32];
-                            load_half(k2, d0, d1);
-                            store_zb_half(k2, d0, d1);
+                            const float e2 = e1 * eC;
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
-                                d0[i] = __float_as_uint(__uint_as_float(d0[i]) * eC);
-                                d1[i] = __float_as_uint(__uint_as_float(d1[i]) * eC);
+                                d0[i] = __float_as_uint(__uint_as_float(d0[i]) * e2);
+                                d1[i] = __float_as_uint(__uint_as_float(d1[i]) * e2);
                             }
-                            store_z_half(k2, d0, d1);
+                            tc::tmem_st_32x32b_x32(tmem + lane_base + kTZ + 64 * k2, d0);
+                            tc::tmem_st_32x32b_x32(tmem + lane_base + kTZ + 64 * k2 + 32, d1);
                         }
-                        tc::tmem_st_wait();
-                        tc::tc_fence_before();
-                        if (c + 1 < nch) warp_arrive(&z_free);
                     }
                     tc::tmem_st_wait();
                     tc::tc_fence_before();
+                    if (c + 1 < nch) warp_arrive(&z_free);
+                    if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 5, c);
                     warp_arrive(&zb_ready[zbc & 1]);
                     ++zbc;
                     if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 8, c);

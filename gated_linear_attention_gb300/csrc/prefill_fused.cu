@@ -280,12 +280,12 @@ __device__ __forceinline__ void store_row(uint8_t *dst, int row, const uint4 (&x
     for (int c8 = 0; c8 < 8; ++c8) *reinterpret_cast<uint4 *>(dst + sw(row, c8)) = x[c8];
 }
 
-// Exact route, scores: row t of P' (already masked and rounded to bf16 in the SW128 tile at
-// pp) times exp(b_t - b_s) for every causal column s <= t (rare).
-__device__ __forceinline__ void exact_pp_weights(uint8_t *pp, const float *b, int t) {
+// Exact route, scores: columns 32 half .. + 31 of row t of P' (already masked and rounded to
+// bf16 in the SW128 tile at pp) times exp(b_t - b_s) for every causal column s <= t (rare).
+__device__ __forceinline__ void exact_pp_weights(uint8_t *pp, const float *b, int t, int half) {
     const float bt = b[t] * kLog2e;
 #pragma unroll 1
-    for (int c8 = 0; c8 < 8; ++c8) {
+    for (int c8 = 4 * half; c8 < 4 * half + 4; ++c8) {
         uint4 x = *reinterpret_cast<const uint4 *>(pp + sw(t, c8));
         uint32_t *w = reinterpret_cast<uint32_t *>(&x);
         for (int e = 0; e < 4; ++e) {
@@ -363,8 +363,8 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             tc::mbar_init(&o_free[i], 4);       // one arrival per output warp
         }
         tc::mbar_init(&p_full, 1);
-        tc::mbar_init(&p_free, 1);
-        tc::mbar_init(&pp_ready, 1);
+        tc::mbar_init(&p_free, 4);     // one arrival per scaling warp
+        tc::mbar_init(&pp_ready, 4);
         tc::mbar_init(&pp_free, 1);
         for (int i = 0; i < kRecA; ++i) {
             tc::mbar_init(&ga_full[i], 1);
@@ -874,55 +874,45 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
 #endif
                 if (wtid == 0) TRACE(2, 5, c);
                 tc::tc_fence_after();
-                // M=64 accumulator layout: row t = 16 * quarter + lane in lanes 0-15
-                const int tr = quarter * 16 + (lane & 15);
+                // M=64 accumulator layout: rows t = 16 quarter + (lane & 15) in lanes 0-15 of the
+                // quarter; the 16-lane load gives lanes 0-15 columns s = 0-31 of those rows and
+                // lanes 16-31 columns 32-63
+                const int tr = quarter * 16 + (lane & 15), sh = lane >> 4;
                 uint8_t *pp = sm + kPp;
-#pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
+                {
                     uint32_t p[32];
-                    tc::tmem_ld_32x32b_x32(tmem + lane_base + kTP + 32 * half, p);
+                    tc::tmem_ld_16x32bx2_x32(tmem + lane_base + kTP, p);
                     tc::tmem_ld_wait();
-                    if (wtid == 0) TRACE(2, 20 + half, c);
-                    if (half == 1) {
-                        tc::tc_fence_before();
-                        named_sync(kBar, 128);
-                        if (wtid == 0) tc::mbar_arrive(&p_free);
-                        if (wtid == 0) TRACE(2, 22, c);
-                    }
-                    if (lane < 16) {
-                        const bool live = tr < nv;
+                    if (wtid == 0) TRACE(2, 20, c);
+                    tc::tc_fence_before();
+                    warp_arrive(&p_free);
+                    const bool live = tr < nv;
 #pragma unroll
-                        for (int c4 = 0; c4 < 4; ++c4) {
-                            uint32_t w[4];
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        uint32_t w[4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int si = 8 * c4 + 2 * e, s = 32 * half + si;
-                                const float f0 = (live && s <= tr) ? __uint_as_float(p[si]) : 0.f;
-                                const float f1 = (live && s + 1 <= tr) ? __uint_as_float(p[si + 1]) : 0.f;
-                                w[e] = float2_to_bf16x2(f0, f1);
-                            }
-                            *reinterpret_cast<uint4 *>(pp + sw(tr, 4 * half + c4)) =
-                                make_uint4(w[0], w[1], w[2], w[3]);
+                        for (int e = 0; e < 4; ++e) {
+                            const int si = 8 * c4 + 2 * e, s = 32 * sh + si;
+                            const float f0 = (live && s <= tr) ? __uint_as_float(p[si]) : 0.f;
+                            const float f1 = (live && s + 1 <= tr) ? __uint_as_float(p[si + 1]) : 0.f;
+                            w[e] = float2_to_bf16x2(f0, f1);
                         }
+                        *reinterpret_cast<uint4 *>(pp + sw(tr, 4 * sh + c4)) = make_uint4(w[0], w[1], w[2], w[3]);
                     }
-                    if (wtid == 0) TRACE(2, 23 + half, c);
+                    if (wtid == 0) TRACE(2, 23, c);
                 }
                 if (!fast) {
                     // exact route: P'[t, s] *= exp(b_t - b_s); q_t <- exp(b_t) q_t in place (M1
                     // has read Q already; the rows come from global memory, not from the tile)
-                    if (lane < 16 && tr < nv) exact_pp_weights(pp, R->b, tr);
+                    if (tr < nv) exact_pp_weights(pp, R->b, tr, sh);
                     exact_q_scale(sm + ((job_c + c) % kStages) * kStage + shalf * kRegion,
                                   reinterpret_cast<const uint16_t *>(a.q), chunk_c0(c), srow, shalf,
                                   nv, H, h, R->b[srow]);
                 }
                 warp_arrive(&gc_empty[(jc0 + c) % kRecC]);   // done with chunk c's record
                 tc::fence_proxy_async_smem();
-                if (wtid == 0) TRACE(2, 25, c);
-                named_sync(kBar, 128);
-                if (wtid == 0) {
-                    tc::mbar_arrive(&pp_ready);
-                    TRACE(2, 6, c);
-                }
+                warp_arrive(&pp_ready);
+                if (wtid == 0) TRACE(2, 6, c);
 #ifdef SALA_TRACE
                 wacc_[4] += clock64() - tw1;
 #endif

@@ -195,7 +195,7 @@ def summarise_clocks(rows):
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of
 # each kernel as it stands, on the workload the bench times (profiles/prefill_fused_sala_layer.md,
 # profiles/recurrent_step_decode.md); retaken whenever a kernel changes.
-MEASURED_TRAFFIC = {"prefill_fused": None, "recurrent_step": 1_023_500_000}
+MEASURED_TRAFFIC = {"prefill_fused": 255_998_720, "recurrent_step": 1_023_500_000}
 
 
 def prefill_bytes(T, H, nseq, has_h0, has_hT):

@@ -313,6 +313,24 @@ __device__ __forceinline__ void exact_q_scale(uint8_t *qt, const uint16_t *q, in
     store_row_scaled<false>(qt, row, x, tc::ex2(b_row * kLog2e));
 }
 
+// State pass: columns 32 q .. + 31 of row `row` of the K tile at kt scaled in place by f (the
+// scaling and converting warps share each tile, a quarter of its columns per half-group).
+__device__ __forceinline__ void scale_k_quarter(uint8_t *kt, int row, int q, float f) {
+    uint8_t *base = kt + (q >> 1) * kRegion;
+    uint4 x[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) x[k] = *reinterpret_cast<const uint4 *>(base + sw(row, (q & 1) * 4 + k));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint4 y;
+        y.x = mul_bf16x2(x[k].x, f);
+        y.y = mul_bf16x2(x[k].y, f);
+        y.z = mul_bf16x2(x[k].z, f);
+        y.w = mul_bf16x2(x[k].w, f);
+        *reinterpret_cast<uint4 *>(base + sw(row, (q & 1) * 4 + k)) = y;
+    }
+}
+
 // Per-warp arrival: the warp's lanes have finished their part; lane 0 arrives for the warp.
 __device__ __forceinline__ void warp_arrive(uint64_t *bar) {
     __syncwarp();
@@ -326,15 +344,14 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-    __shared__ uint64_t full[kStages], empty[kStages], ka_ready[kStages];
+    __shared__ uint64_t full[kStages], ka_full[kStages], empty[kStages], ka_ready[kStages];
     __shared__ uint64_t unit_full[2], unit_empty[2], kp_ready[2], kp_free[2];
     __shared__ uint64_t p_full, p_free, pp_ready, pp_free;
     __shared__ uint64_t ga_full[kRecA], ga_empty[kRecA], gc_full[kRecC], gc_empty[kRecC];
     __shared__ uint64_t z_full, z_free, zb_ready[2], zb_free[2], o_full[2], o_free[2];
-    __shared__ uint64_t ds_full, ds_free, d_ready, d_free, pub_ready, pub_free, drain;
+    __shared__ uint64_t ds_full, ds_free, pub_ready, pub_free, drain;
     __shared__ UnitInfo units[2];
     __shared__ int kfast[2];
-    __shared__ float unit_D;         // total log-decay of the current unit's segment
     __shared__ uint32_t *pub_flag;   // the flag the publisher releases next
     __shared__ int pub_cmd;          // 0: nothing this unit, 1: release pub_flag, 2: stop
     __shared__ uint32_t tmem_slot;
@@ -349,10 +366,12 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            tc::mbar_init(&full[s], 1);       // expect_tx arrival
+            tc::mbar_init(&full[s], 1);       // output-pass job: Q and V landed (expect_tx)
+            tc::mbar_init(&ka_full[s], 1);    // state-pass job: K and V landed (expect_tx)
             tc::mbar_init(&empty[s], 1);      // MMA commit
-            tc::mbar_init(&ka_ready[s], 1);   // the state-pass K' tile of this stage is scaled
-                                              // (phases count this stage's state-pass jobs)
+            tc::mbar_init(&ka_ready[s], 8);   // the state-pass K' tile of this stage is scaled
+                                              // (scaling and converting warps; phases count
+                                              // this stage's state-pass jobs)
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&unit_full[i], 1);
@@ -368,7 +387,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         tc::mbar_init(&pp_free, 1);
         for (int i = 0; i < kRecA; ++i) {
             tc::mbar_init(&ga_full[i], 1);
-            tc::mbar_init(&ga_empty[i], 4);    // one arrival per scaling warp
+            tc::mbar_init(&ga_empty[i], 8);    // scaling and converting warps
         }
         for (int i = 0; i < kRecC; ++i) {
             tc::mbar_init(&gc_full[i], 1);
@@ -382,8 +401,6 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         }
         tc::mbar_init(&ds_full, 1);
         tc::mbar_init(&ds_free, 4);
-        tc::mbar_init(&d_ready, 1);
-        tc::mbar_init(&d_free, 4);
         tc::mbar_init(&pub_ready, 4);
         tc::mbar_init(&pub_free, 1);
         tc::mbar_init(&drain, 1);
@@ -412,10 +429,12 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             tc::tma_prefetch_desc(&maps.o);
         }
         uint32_t job = 0, us = 0;
+        uint32_t fpar = 0, kfpar = 0;   // bit st: next phase of full[st] / ka_full[st]
+        uint32_t a_mask = 0, lpar = 0;  // bit st: last load of stage st was a state-pass job; its phase
         bool ok = true;
-        // one job: K and V (state pass; K goes to the first tile of the stage) or Q and V
-        // (output pass) of the chunk at token c0, with L2 prefetches of the chunk's log-decays
-        // (read by other warps a little later)
+        // one job: K and V (state pass -> ka_full; K goes to the first tile of the stage) or Q
+        // and V (output pass -> full) of the chunk at token c0, with L2 prefetches of the
+        // chunk's log-decays (read by other warps a little later)
         auto load_job = [&](int64_t c0, int nv, int h, bool with_q) -> bool {
             const uint32_t st = job % kStages;
             bool bad = false;
@@ -428,18 +447,23 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 TRACE(0, with_q ? 2 : 1, job);
                 uint8_t *base = sm + st * kStage;
                 const int32_t x0 = static_cast<int32_t>(c0);
-                tc::mbar_arrive_expect_tx(&full[st], 2 * kTile);
+                uint64_t *bar = with_q ? &full[st] : &ka_full[st];
+                tc::mbar_arrive_expect_tx(bar, 2 * kTile);
                 const CUtensorMap *first = with_q ? &maps.q : &maps.k;
-                tc::tma_load_3d_hint(base, first, 0, h, x0, &full[st], with_q ? drop : keep);
-                tc::tma_load_3d_hint(base + kRegion, first, 64, h, x0, &full[st], with_q ? drop : keep);
+                tc::tma_load_3d_hint(base, first, 0, h, x0, bar, with_q ? drop : keep);
+                tc::tma_load_3d_hint(base + kRegion, first, 64, h, x0, bar, with_q ? drop : keep);
                 const uint64_t pol = with_q ? drop : keep;
-                tc::tma_load_3d_hint(base + kTile, &maps.v, 0, h, x0, &full[st], pol);
-                tc::tma_load_3d_hint(base + kTile + kRegion, &maps.v, 64, h, x0, &full[st], pol);
+                tc::tma_load_3d_hint(base + kTile, &maps.v, 0, h, x0, bar, pol);
+                tc::tma_load_3d_hint(base + kTile + kRegion, &maps.v, 64, h, x0, bar, pol);
                 // the scaling warps read this chunk's K rows with ordinary loads a little later
                 tc::tma_prefetch_l2_3d(&maps.k, 0, h, x0, pol);
                 tc::tma_prefetch_l2_3d(&maps.k, 64, h, x0, pol);
             }
             __syncwarp();
+            const uint32_t ph = with_q ? (fpar >> st) & 1 : (kfpar >> st) & 1;
+            lpar = (lpar & ~(1u << st)) | (ph << st);
+            if (with_q) fpar ^= 1u << st; else kfpar ^= 1u << st;
+            a_mask = with_q ? (a_mask & ~(1u << st)) : (a_mask | (1u << st));
             ++job;
             return true;
         };
@@ -480,14 +504,17 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         }
         // drain: the copies of the last stages must land before the CTA may exit
         if (lane == 0)
-            for (uint32_t j = job > kStages ? job - kStages : 0; j < job; ++j)
-                tc::mbar_wait(&full[j % kStages], (j / kStages) & 1, kWaitNs);
+            for (uint32_t j = job > kStages ? job - kStages : 0; j < job; ++j) {
+                const uint32_t st = j % kStages;
+                tc::mbar_wait((a_mask >> st) & 1 ? &ka_full[st] : &full[st], (lpar >> st) & 1, kWaitNs);
+            }
     } else if (warp == 1) {
         // =============================== MMA issuer ===============================
         if (lane == 0) {
             const uint32_t sb = tc::smem_u32(sm);
             uint32_t job = 0, us = 0, kpc = 0, cc = 0, zbc = 0, zfc = 0;
             uint32_t ka_par = 0;   // bit st: phase parity of ka_ready[st] (state-pass jobs only)
+            uint32_t cpar = 0;     // bit st: phase parity of full[st] (output-pass jobs only)
             auto W = [&](uint64_t *bar, uint32_t par) { return wait_or_abort(bar, par & 1, abort_v, status); };
 #ifdef SALA_TRACE
             unsigned long long wacc_[16] = {};
@@ -503,7 +530,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 if (us >= 1) ok = TIMED(1, W(&ds_free, us - 1));
                 for (int r = 0; r < info.nch && ok; ++r) {
                     const uint32_t st = job % kStages;
-                    ok = TIMED(2, W(&full[st], job / kStages)) && TIMED(3, W(&ka_ready[st], (ka_par >> st) & 1));
+                    ok = TIMED(3, W(&ka_ready[st], (ka_par >> st) & 1));
                     if (!ok) break;
                     ka_par ^= 1u << st;
                     TRACE(1, 1, r);
@@ -575,8 +602,10 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                     if (c + 1 < info.nch) {
                         const uint32_t jn = c < 0 ? job : job + 1, gn = c < 0 ? cc : cc + 1;
                         const uint32_t kn = kpc & 1;
-                        if (!TIMED(9, W(&full[jn % kStages], jn / kStages)) || !TIMED(10, W(&kp_ready[kn], kpc >> 1)) ||
+                        const uint32_t sn = jn % kStages;
+                        if (!TIMED(9, W(&full[sn], (cpar >> sn) & 1)) || !TIMED(10, W(&kp_ready[kn], kpc >> 1)) ||
                             (gn >= 1 && !TIMED(11, W(&p_free, gn - 1)))) { ok = false; break; }
+                        cpar ^= 1u << sn;
                         ++kpc;
                         TRACE(1, 2, c + 1);
                         const uint32_t k1 = sb + (kfast[kn] != 0 ? kKp : kKr) + kn * kTile;
@@ -724,6 +753,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         const GateRec *recA = reinterpret_cast<const GateRec *>(sm + kGate);
         const GateRec *recC = recA + kRecA;
         uint32_t us = 0, kpc = 0, cc = 0, job = 0;   // job: stage counter as the producer's
+        uint32_t kfpar = 0;                          // bit st: phase parity of ka_full[st]
         uint32_t ja = 0, jc = 0;                     // gate records consumed
 #ifdef SALA_TRACE
         unsigned long long wacc_[8] = {};
@@ -791,8 +821,8 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             // ---------------- A: K' = K exp(B_end - B_s), chunks last to first ----------------
             // job r is chunk nch - 1 - r; its K tile arrived by TMA in the first tile of the
             // stage and is scaled there in place (ordinary shared-memory loads are cheap here:
-            // the tensor core only runs the short state-pass products).
-            float D = 0.f;   // total log-decay of the segment
+            // the tensor core only runs the short state-pass products). These warps take
+            // columns 0-63, the converting warps (idle until the hand-off) 64-127.
             for (int r = 0; r < nch; ++r) {
                 const int nv = chunk_nv(nch - 1 - r);
                 const uint32_t st = job % kStages;
@@ -800,47 +830,27 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 wait_nv(&ga_full[ja % kRecA], ja / kRecA, true, abort_v, status);
                 const GateRec *R = recA + ja % kRecA;
                 const float e = R->bC + R->D - R->b[srow];
-                const float bC = R->bC;
                 warp_arrive(&ga_empty[ja % kRecA]);
                 ++ja;
                 const float fac = srow < nv ? tc::ex2(e * kLog2e) : 0.f;
-                wait_nv(&full[st], job / kStages, true, abort_v, status);
+                wait_nv(&ka_full[st], (kfpar >> st) & 1, true, abort_v, status);
+                kfpar ^= 1u << st;
                 if (wtid == 0) TRACE(2, 7, r);
-                uint8_t *kt = sm + st * kStage + shalf * kRegion;
-                uint4 x[8];
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) x[c8] = *reinterpret_cast<const uint4 *>(kt + sw(srow, c8));
-                store_row_scaled<true>(kt, srow, x, fac);
+                scale_k_quarter(sm + st * kStage, srow, shalf, fac);
                 tc::fence_proxy_async_smem();
-                named_sync(kBar, 128);
-                if (wtid == 0) {
-                    tc::mbar_arrive(&ka_ready[st]);
-                    TRACE(2, 8, r);
-                }
-                D += bC;
+                warp_arrive(&ka_ready[st]);
+                if (wtid == 0) TRACE(2, 8, r);
                 ++job;
             }
             prefetch(chunk_c0(0), chunk_nv(0), h);
-            wait_nv(&d_free, us - 1, us >= 1, abort_v, status);
-            if (wtid == 0) {
-                unit_D = D;
-                tc::mbar_arrive(&d_ready);
-            }
 
             // ---------------- C ----------------
             // K~ of chunk 0; then per chunk: K~ of the next chunk, P' of this one. The scaling
             // warps wait on every stage phase (mbarrier waits compare parity only, so a waiter
             // must not skip phases), although here they read K with ordinary global loads.
+            // (these warps read K with ordinary global loads and wait on no stage: the scores of
+            // a chunk imply that its Q tile has landed)
             const uint32_t job_c = job, jc0 = jc;
-            auto wait_stage = [&](int c) {
-#ifdef SALA_TRACE
-                const long long tw2 = clock64();
-#endif
-                wait_nv(&full[(job_c + c) % kStages], (job_c + c) / kStages, true, abort_v, status);
-#ifdef SALA_TRACE
-                wacc_[5] += clock64() - tw2;
-#endif
-            };
             // the gate record of chunk c (held from its K~ until its P' is done)
             auto rec = [&](int c) { return recC + (jc0 + c) % kRecC; };
             auto wait_rec = [&](int c) {
@@ -849,7 +859,6 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             for (int c = -1; c < nch; ++c) {
                 if (c + 1 < nch) {
                     wait_rec(c + 1);
-                    wait_stage(c + 1);
                     make_k(kx, rec(c + 1), chunk_nv(c + 1));
                     if (c + 2 < nch) prefetch(chunk_c0(c + 2), chunk_nv(c + 2), h);
                     if (wtid == 0) TRACE(2, 3, c);
@@ -940,7 +949,10 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         const int j = quarter * 32 + lane;     // value column = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         uint32_t us = 0, zfc = 0, zbc = 0, npub = 0, jc = 0;
+        uint32_t job = 0, ja = 0, kfpar = 0;   // stage jobs seen, state-pass records, ka_full parity
+        const int arow = wtid & 63;           // state-pass row (columns 64 + 32 (wtid >> 6) .. + 31)
         const GateRec *recC = reinterpret_cast<const GateRec *>(sm + kGate) + kRecA;
+        const GateRec *recA = reinterpret_cast<const GateRec *>(sm + kGate);
         // the plan of the next chunk from its gate record (released at once)
         struct ConvPlan {
             float e1, eC;
@@ -979,11 +991,31 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             const int h = info.h, nch = info.nch;
             if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 1, us);
 
+            // ---------------- state pass: columns 64-127 of every K' tile ----------------
+            // (the scaling warps take columns 0-63); and the segment's total log-decay
+            float D = 0.f;
+#pragma unroll 1
+            for (int r = 0; r < nch; ++r) {
+                const int64_t c0 = info.t0 + int64_t(nch - 1 - r) * kChunk;
+                const uint32_t st = (job + r) % kStages;
+                wait_nv(&ga_full[ja % kRecA], ja / kRecA, true, abort_v, status);
+                const GateRec *R = recA + ja % kRecA;
+                const float e = R->bC + R->D - R->b[arow];
+                D += R->bC;
+                warp_arrive(&ga_empty[ja % kRecA]);
+                ++ja;
+                const float fac = c0 + arow < info.t1 ? tc::ex2(e * kLog2e) : 0.f;
+                wait_nv(&ka_full[st], (kfpar >> st) & 1, true, abort_v, status);
+                kfpar ^= 1u << st;
+                scale_k_quarter(sm + st * kStage, arow, 2 + (wtid >> 6), fac);
+                tc::fence_proxy_async_smem();
+                warp_arrive(&ka_ready[st]);
+            }
+            job += 2 * nch;
+
             // ---------------- hand-off: S_in, Z = S_in and its bf16 copy, publish S_out ----------------
             {
                 bool bad = !wait_or_abort(&ds_full, us & 1, abort_v, status);
-                if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 15, us);
-                bad = bad || !wait_or_abort(&d_ready, us & 1, abort_v, status);
                 if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 11, us);
                 if (!bad && !info.first && wtid == 0) {
                     const uint32_t *flag = f.flags + (info.sigma - 1) * H + h;
@@ -1004,8 +1036,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 // chunk 0 starts at the reference point (pre = 0); the exact route keeps the
                 // state scaled to the chunk end
                 const float zfac = next_plan().eC;
-                const float eB = tc::ex2(unit_D * kLog2e);
-                warp_arrive(&d_free);
+                const float eB = tc::ex2(D * kLog2e);
                 float *dst = info.last ? (f.hT ? f.hT + (info.n * H + h) * kD * kD : nullptr)
                                        : f.incl + (static_cast<size_t>(info.sigma) * H + h) * kD * kD;
                 const float *src = info.first
@@ -1126,7 +1157,6 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         // (direct stores when the chunk is ragged: the rows past it belong to another sequence).
         const int wtid = threadIdx.x - 384;
         const int quarter = warp & 3;
-        const int j = quarter * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         uint8_t *stg = sm + kOst + quarter * kOstWarp;
         const GateRec *recC = reinterpret_cast<const GateRec *>(sm + kGate) + kRecA;

@@ -97,10 +97,13 @@ void clear_records_locked() {
 
 }  // namespace
 
-// Tokens per segment: long enough that the per-unit overhead (hand-off state, chunk
-// pipeline fill) stays small, short enough that a segment's k and v are still in L2 when the
-// output pass re-reads them and that there are several units per SM. SALA_GLA_SEGMENT_TOKENS
-// overrides the choice (rounded up to a multiple of 64).
+// Tokens per segment. Each unit pays a fixed cost (its state pass ramp, the hand-off, the
+// output pipeline fill) worth several chunks, so long segments win when every SM gets many
+// units; when the whole job is only a few waves of units, the last wave's imbalance dominates
+// and shorter segments win. Measured on GB300 (H = 32): 8192 tokens (about 1.7K tokens per
+// SM) is fastest at 640; 65536 and 131072 tokens (14K and 28K per SM) at 1024, where 512
+// costs 25-30 % more. SALA_GLA_SEGMENT_TOKENS overrides the choice (rounded up to a multiple
+// of 64).
 int64_t choose_segment_tokens(int64_t T_total, int64_t H, int sm_count) {
     static const int64_t forced = []() -> int64_t {
         const char *e = getenv("SALA_GLA_SEGMENT_TOKENS");
@@ -109,9 +112,8 @@ int64_t choose_segment_tokens(int64_t T_total, int64_t H, int sm_count) {
         return v > 0 ? ((v + kChunk - 1) / kChunk) * kChunk : 0;
     }();
     if (forced) return forced;
-    (void)H;
-    (void)sm_count;
-    int64_t L = 512;
+    const int64_t per_sm = T_total * H / (sm_count > 0 ? sm_count : 1);
+    int64_t L = per_sm > 8192 ? 1024 : 640;
     if (T_total < L) L = ((T_total + kChunk - 1) / kChunk) * kChunk;
     return L < kChunk ? kChunk : L;
 }

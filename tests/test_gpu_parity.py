@@ -101,9 +101,10 @@ def test_prefill_varlen_with_empty_and_short(sg, lens):
 
 @pytest.mark.parametrize("seed", [11, 12, 13])
 def test_prefill_mixed_segment_shapes(sg, seed):
-    # Many packed sequences whose segments hold every chunk count from 1 to 8 plus ragged
-    # tails, with enough heads that units of different shapes run side by side on one CTA's
-    # pipeline in every order (state-pass and output-pass jobs interleave on the stages).
+    # Many packed sequences whose segments (640 tokens at this size) hold every chunk count
+    # from 1 to 10 plus ragged tails, with enough heads that units of different shapes run
+    # side by side on one CTA's pipeline in every order (state-pass and output-pass jobs
+    # interleave on the stages).
     lens = (1, 63, 64, 65, 128, 191, 256, 300, 448, 512, 513, 700, 1023, 1100, 1537, 2048)
     x = inputs.make_prefill("varlen", seqlens=lens, H=16, seed=seed)
     o, hT = run_prefill(sg, x)

@@ -510,148 +510,173 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             }
     } else if (warp == 1) {
         // =============================== MMA issuer ===============================
-        if (lane == 0) {
-            const uint32_t sb = tc::smem_u32(sm);
-            uint32_t job = 0, us = 0, kpc = 0, cc = 0, zbc = 0, zfc = 0;
-            uint32_t ka_par = 0;   // bit st: phase parity of ka_ready[st] (state-pass jobs only)
-            uint32_t cpar = 0;     // bit st: phase parity of full[st] (output-pass jobs only)
-            auto W = [&](uint64_t *bar, uint32_t par) { return wait_or_abort(bar, par & 1, abort_v, status); };
+        // The whole warp follows the schedule (every wait, counter and descriptor is
+        // warp-uniform, so it stays in the uniform datapath) and one elected lane issues the
+        // MMAs and commits (the same lane every time: a commit tracks its own thread's MMAs).
+        const uint32_t sb = tc::smem_u32(sm);
+        uint32_t job = 0, us = 0, kpc = 0, cc = 0, zbc = 0, zfc = 0;
+        uint32_t ka_par = 0;   // bit st: phase parity of ka_ready[st] (state-pass jobs only)
+        uint32_t cpar = 0;     // bit st: phase parity of full[st] (output-pass jobs only)
+        auto W = [&](uint64_t *bar, uint32_t par) {
+            return __all_sync(0xffffffffu, wait_or_abort(bar, par & 1, abort_v, status));
+        };
 #ifdef SALA_TRACE
-            unsigned long long wacc_[16] = {};
+        unsigned long long wacc_[16] = {};
 #endif
-            for (;;) {
-                const uint32_t slot = us & 1;
-                if (!TIMED(0, W(&unit_full[slot], us >> 1))) break;
-                const UnitInfo info = units[slot];
-                tc::mbar_arrive(&unit_empty[slot]);
-                if (!info.valid) break;
-                bool ok = true;
-                // ---- A: dS^T = sum over chunks of V^T K', one accumulator
-                if (us >= 1) ok = TIMED(1, W(&ds_free, us - 1));
-                for (int r = 0; r < info.nch && ok; ++r) {
-                    const uint32_t st = job % kStages;
-                    ok = TIMED(3, W(&ka_ready[st], (ka_par >> st) & 1));
-                    if (!ok) break;
-                    ka_par ^= 1u << st;
-                    TRACE(1, 1, r);
-                    tc::tc_fence_after();
-                    const uint32_t k_s = sb + st * kStage, v_s = k_s + kTile;   // K' scaled in place
+        for (;;) {
+            const uint32_t slot = us & 1;
+            if (!TIMED(0, W(&unit_full[slot], us >> 1))) break;
+            const UnitInfo info = units[slot];
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&unit_empty[slot]);
+            if (!info.valid) break;
+            bool ok = true;
+            // ---- A: dS^T = sum over chunks of V^T K', one accumulator
+            if (us >= 1) ok = TIMED(1, W(&ds_free, us - 1));
+            for (int r = 0; r < info.nch && ok; ++r) {
+                const uint32_t st = job % kStages;
+                ok = TIMED(3, W(&ka_ready[st], (ka_par >> st) & 1));
+                if (!ok) break;
+                ka_par ^= 1u << st;
+                TRACE(1, 1, r);
+                tc::tc_fence_after();
+                const uint32_t k_s = sb + st * kStage, v_s = k_s + kTile;   // K' scaled in place
+                const uint64_t da = desc_mn8(v_s), db = desc_mn8(k_s);
+                if (tc::elect_one()) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        tc::umma_bf16(tmem + kTdS, desc_mn8(v_s + ks * 2048),
-                                      desc_mn8(k_s + ks * 2048), kIdescS, (r > 0 || ks > 0) ? 1u : 0u);
+                        tc::umma_bf16(tmem + kTdS, da + ks * (2048 >> 4), db + ks * (2048 >> 4), kIdescS,
+                                      (r > 0 || ks > 0) ? 1u : 0u);
                     tc::umma_commit(&empty[st]);
-                    ++job;
                 }
-                if (!ok) break;
-                tc::umma_commit(&ds_full);
-                // ---- C, software-pipelined: M1 of chunk c+1 goes out right after M2 of chunk c
-                // (before M3 of chunk c), so the scores of c+1 are made while chunk c finishes
-                // per chunk c: M4(c), M2(c), M1(c+1), M3(c); the first pass (c = -1) issues M1(0)
-                uint32_t kb = kpc & 1;   // K~ set of the chunk in flight
-                for (int c = -1; c < info.nch && ok; ++c) {
-                    const uint32_t st = job % kStages;
-                    const uint32_t q_s = sb + st * kStage, v_s = q_s + kTile;
-                    const uint32_t ob = cc & 1;
-                    const bool fast = kfast[kb] != 0;
-                    if (c >= 0) {
-                        // M4: Z^T += V^T K~ (not needed after the last chunk), once the converting
-                        // warps have read Z (and rescaled it, if the reference moved)
-                        if (c + 1 < info.nch) {
-                            if (!TIMED(5, W(&z_free, zfc))) { ok = false; break; }
-                            TRACE(1, 3, c);
+                __syncwarp();
+                ++job;
+            }
+            if (!ok) break;
+            if (tc::elect_one()) tc::umma_commit(&ds_full);
+            __syncwarp();
+            // ---- C, software-pipelined: M1 of chunk c+1 goes out right after M2 of chunk c
+            // (before M3 of chunk c), so the scores of c+1 are made while chunk c finishes
+            // per chunk c: M4(c), M2(c), M1(c+1), M3(c); the first pass (c = -1) issues M1(0)
+            uint32_t kb = kpc & 1;   // K~ set of the chunk in flight
+            for (int c = -1; c < info.nch && ok; ++c) {
+                const uint32_t st = job % kStages;
+                const uint32_t q_s = sb + st * kStage, v_s = q_s + kTile;
+                const uint64_t dv = desc_mn8(v_s);
+                const uint32_t ob = cc & 1;
+                const bool fast = kfast[kb] != 0;
+                if (c >= 0) {
+                    // M4: Z^T += V^T K~ (not needed after the last chunk), once the converting
+                    // warps have read Z (and rescaled it, if the reference moved)
+                    if (c + 1 < info.nch) {
+                        if (!TIMED(5, W(&z_free, zfc))) { ok = false; break; }
+                        TRACE(1, 3, c);
 #ifdef SALA_TRACE
-                            const long long ti0 = clock64();
+                        const long long ti0 = clock64();
 #endif
-                            tc::tc_fence_after();
+                        tc::tc_fence_after();
+                        const uint64_t dk4 = desc_mn8(sb + kKp + kb * kTile);
+                        if (tc::elect_one()) {
 #pragma unroll
                             for (int ks = 0; ks < 4; ++ks)
-                                tc::umma_bf16(tmem + kTZ, desc_mn8(v_s + ks * 2048),
-                                              desc_mn8(sb + kKp + kb * kTile + ks * 2048), kIdescS, 1u);
+                                tc::umma_bf16(tmem + kTZ, dv + ks * (2048 >> 4), dk4 + ks * (2048 >> 4), kIdescS, 1u);
                             tc::umma_commit(&z_full);
-#ifdef SALA_TRACE
-                            wacc_[13] += clock64() - ti0;
-#endif
-                            ++zfc;
                         }
-                        // M2: O^T = Z^T Q^T (Q scaled in place first on the exact route)
-                        const uint32_t zb = zbc & 1;
-                        if (!TIMED(6, W(&zb_ready[zb], zbc >> 1))) { ok = false; break; }
-                        if (cc >= 2 && !TIMED(7, W(&o_free[ob], (cc >> 1) - 1))) { ok = false; break; }
-                        if (!fast && !TIMED(8, W(&pp_ready, cc))) { ok = false; break; }
-                        TRACE(1, 4, c);
+                        __syncwarp();
 #ifdef SALA_TRACE
-                        const long long ti1 = clock64();
+                        wacc_[13] += clock64() - ti0;
 #endif
-                        tc::tc_fence_after();
-#pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) {
-                            const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
-                            tc::umma_bf16_ta(tmem + kTO + 64 * ob, tmem + zb_col(zb) + 8 * ks, desc_k(q_s + off),
-                                             kIdescO2, ks > 0);
-                        }
-                        tc::umma_commit(&zb_free[zb]);
-                        tc::umma_commit(&kp_free[kb]);   // M1, M4 and M2 of chunk c have read its set
-#ifdef SALA_TRACE
-                        wacc_[14] += clock64() - ti1;
-#endif
-                        ++zbc;
+                        ++zfc;
                     }
-                    // M1 of the next chunk (P = Q K~^T, or Q K^T on the exact route), once the
-                    // scores of the chunk before it have been read
-                    if (c + 1 < info.nch) {
-                        const uint32_t jn = c < 0 ? job : job + 1, gn = c < 0 ? cc : cc + 1;
-                        const uint32_t kn = kpc & 1;
-                        const uint32_t sn = jn % kStages;
-                        if (!TIMED(9, W(&full[sn], (cpar >> sn) & 1)) || !TIMED(10, W(&kp_ready[kn], kpc >> 1)) ||
-                            (gn >= 1 && !TIMED(11, W(&p_free, gn - 1)))) { ok = false; break; }
-                        cpar ^= 1u << sn;
-                        ++kpc;
-                        TRACE(1, 2, c + 1);
-                        const uint32_t k1 = sb + (kfast[kn] != 0 ? kKp : kKr) + kn * kTile;
-                        const uint32_t q1 = sb + (jn % kStages) * kStage;
-                        tc::tc_fence_after();
-#pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) {
-                            const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
-                            tc::umma_bf16(tmem + kTP, desc_k(q1 + off), desc_k(k1 + off), kIdescP, ks > 0);
-                        }
-                        tc::umma_commit(&p_full);
-                        if (c < 0) kb = kn;
-                    }
-                    if (c < 0) continue;
-                    // M3: O^T += V^T P'^T
-                    if (fast && !TIMED(12, W(&pp_ready, cc))) { ok = false; break; }
-                    TRACE(1, 5, c);
+                    // M2: O^T = Z^T Q^T (Q scaled in place first on the exact route)
+                    const uint32_t zb = zbc & 1;
+                    if (!TIMED(6, W(&zb_ready[zb], zbc >> 1))) { ok = false; break; }
+                    if (cc >= 2 && !TIMED(7, W(&o_free[ob], (cc >> 1) - 1))) { ok = false; break; }
+                    if (!fast && !TIMED(8, W(&pp_ready, cc))) { ok = false; break; }
+                    TRACE(1, 4, c);
 #ifdef SALA_TRACE
-                    const long long ti2 = clock64();
+                    const long long ti1 = clock64();
 #endif
                     tc::tc_fence_after();
+                    const uint64_t dq = desc_k(q_s);
+                    const uint32_t za = tmem + zb_col(zb), od = tmem + kTO + 64 * ob;
+                    if (tc::elect_one()) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc::umma_bf16_ta(od, za + 8 * ks, dq + (((ks >> 2) * kRegion + (ks & 3) * 32) >> 4),
+                                             kIdescO2, ks > 0);
+                        tc::umma_commit(&zb_free[zb]);
+                        tc::umma_commit(&kp_free[kb]);   // M1, M4 and M2 of chunk c have read its set
+                    }
+                    __syncwarp();
+#ifdef SALA_TRACE
+                    wacc_[14] += clock64() - ti1;
+#endif
+                    ++zbc;
+                }
+                // M1 of the next chunk (P = Q K~^T, or Q K^T on the exact route), once the
+                // scores of the chunk before it have been read
+                if (c + 1 < info.nch) {
+                    const uint32_t jn = c < 0 ? job : job + 1, gn = c < 0 ? cc : cc + 1;
+                    const uint32_t kn = kpc & 1;
+                    const uint32_t sn = jn % kStages;
+                    if (!TIMED(9, W(&full[sn], (cpar >> sn) & 1)) || !TIMED(10, W(&kp_ready[kn], kpc >> 1)) ||
+                        (gn >= 1 && !TIMED(11, W(&p_free, gn - 1)))) { ok = false; break; }
+                    cpar ^= 1u << sn;
+                    ++kpc;
+                    TRACE(1, 2, c + 1);
+                    const uint64_t dk1 = desc_k(sb + (kfast[kn] != 0 ? kKp : kKr) + kn * kTile);
+                    const uint64_t dq1 = desc_k(sb + sn * kStage);
+                    tc::tc_fence_after();
+                    if (tc::elect_one()) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint32_t o4 = ((ks >> 2) * kRegion + (ks & 3) * 32) >> 4;
+                            tc::umma_bf16(tmem + kTP, dq1 + o4, dk1 + o4, kIdescP, ks > 0);
+                        }
+                        tc::umma_commit(&p_full);
+                    }
+                    __syncwarp();
+                    if (c < 0) kb = kn;
+                }
+                if (c < 0) continue;
+                // M3: O^T += V^T P'^T
+                if (fast && !TIMED(12, W(&pp_ready, cc))) { ok = false; break; }
+                TRACE(1, 5, c);
+#ifdef SALA_TRACE
+                const long long ti2 = clock64();
+#endif
+                tc::tc_fence_after();
+                const uint64_t dp = desc_k(sb + kPp);
+                if (tc::elect_one()) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        tc::umma_bf16(tmem + kTO + 64 * ob, desc_mn8(v_s + ks * 2048),
-                                      desc_k(sb + kPp + ks * 32), kIdescO3, 1u);
+                        tc::umma_bf16(tmem + kTO + 64 * ob, dv + ks * (2048 >> 4), dp + ks * (32 >> 4), kIdescO3, 1u);
                     tc::umma_commit(&o_full[ob]);
                     tc::umma_commit(&pp_free);
                     tc::umma_commit(&empty[st]);
-#ifdef SALA_TRACE
-                    wacc_[15] += clock64() - ti2;
-#endif
-                    kb = (kpc - 1) & 1;   // the set M1 of the next chunk has taken
-                    ++job;
-                    ++cc;
                 }
-                if (!ok) break;
-                ++us;
-            }
+                __syncwarp();
 #ifdef SALA_TRACE
-            if (blockIdx.x == 0)
-                for (int i = 0; i < 16; ++i) g_wait_acc[i] = wacc_[i];
+                wacc_[15] += clock64() - ti2;
 #endif
-            // no MMA may still run when the tensor memory is freed
+                kb = (kpc - 1) & 1;   // the set M1 of the next chunk has taken
+                ++job;
+                ++cc;
+            }
+            if (!ok) break;
+            ++us;
+        }
+#ifdef SALA_TRACE
+        if (blockIdx.x == 0 && lane == 0)
+            for (int i = 0; i < 16; ++i) g_wait_acc[i] = wacc_[i];
+#endif
+        // no MMA may still run when the tensor memory is freed
+        if (tc::elect_one()) {
             tc::umma_commit(&drain);
             tc::mbar_wait(&drain, 0, kWaitNs);
         }
+        __syncwarp();
     } else if (warp == 2) {
         // =============================== flag publisher ===============================
         // Releases a unit's hand-off flag once the converting warps have stored its S_out:

@@ -262,6 +262,17 @@ __device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, u
         : "memory");
 }
 
+// True in exactly one lane of the (converged) warp: the lowest active lane.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r));
+    return r != 0;
+}
+
 // Arrive once on `bar` when all previously issued tcgen05.mma of this thread complete.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile(

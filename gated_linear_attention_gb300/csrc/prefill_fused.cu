@@ -274,12 +274,6 @@ __device__ __forceinline__ void store_row_scaled(uint8_t *dst, int row, const ui
     }
 }
 
-// The same row unscaled (exact route: raw K for M1).
-__device__ __forceinline__ void store_row(uint8_t *dst, int row, const uint4 (&x)[8]) {
-#pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) *reinterpret_cast<uint4 *>(dst + sw(row, c8)) = x[c8];
-}
-
 // Exact route, scores: columns 32 half .. + 31 of row t of P' (already masked and rounded to
 // bf16 in the SW128 tile at pp) times exp(b_t - b_s) for every causal column s <= t (rare).
 __device__ __forceinline__ void exact_pp_weights(uint8_t *pp, const float *b, int t, int half) {
@@ -785,21 +779,21 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
 #endif
 
         // K rows of the output-pass chunk still to scale, loaded one chunk ahead into registers
-        // (the scores of the current chunk are done in between)
+        // (the scores of the current chunk are done in between). Thread wtid holds 16-byte
+        // column kc16 of rows krow + 8 i, so that each load instruction of a warp reads two
+        // whole 256-byte rows.
+        const int krow = wtid >> 4, kc16 = wtid & 15;
         uint4 kx[8];
         auto prefetch = [&](int64_t c0, int nv, int h) {
-            if (srow < nv) {
-                const uint8_t *src = reinterpret_cast<const uint8_t *>(
-                    a.k + ((c0 + srow) * H + h) * kD + 64 * shalf);
+            const uint8_t *src = reinterpret_cast<const uint8_t *>(a.k + ((c0 + krow) * H + h) * kD) + 16 * kc16;
+            const size_t step = static_cast<size_t>(8) * H * kD * sizeof(uint16_t);   // 8 rows
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) kx[c8] = tc::ldg_nc_hint(src + 16 * c8, drop);
-            } else {
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) kx[c8] = make_uint4(0u, 0u, 0u, 0u);
-            }
+            for (int i = 0; i < 8; ++i)
+                kx[i] = krow + 8 * i < nv ? tc::ldg_nc_hint(src + i * step, drop) : make_uint4(0u, 0u, 0u, 0u);
         };
         // K~ of the chunk whose gate record is R into buffer kpc & 1: k exp(-(base + b_s))
         // (factored route) or k exp(b_C - b_s) plus the raw rows (exact route); rows >= nv zero.
+        // The factor is rounded to bf16 and each pair takes one packed multiply.
         auto make_k = [&](const uint4 (&x)[8], const GateRec *R, int nv) {
             const uint32_t kb = kpc & 1;
 #ifdef SALA_TRACE
@@ -812,11 +806,22 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
 #endif
             if (wtid == 0) TRACE(2, 9, kpc);
             const bool fast = R->fast != 0;
-            const float bs = R->b[srow];
-            const float e = fast ? -(R->base + bs) : R->bC - bs;
-            const float fac = srow < nv ? tc::ex2(e * kLog2e) : 0.f;
-            store_row_scaled<false>(sm + kKp + kb * kTile + shalf * kRegion, srow, x, fac);
-            if (!fast) store_row(sm + kKr + kb * kTile + shalf * kRegion, srow, x);
+            const float off = fast ? -R->base : R->bC;
+            uint8_t *dst = sm + kKp + kb * kTile + (kc16 >> 3) * kRegion;
+            uint8_t *raw = sm + kKr + kb * kTile + (kc16 >> 3) * kRegion;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int row = krow + 8 * i;
+                const float fac = row < nv ? tc::ex2((off - R->b[row]) * kLog2e) : 0.f;
+                const __nv_bfloat162 f2 = __float2bfloat162_rn(fac);
+                uint4 y;
+                y.x = mul_bf16x2(x[i].x, f2);
+                y.y = mul_bf16x2(x[i].y, f2);
+                y.z = mul_bf16x2(x[i].z, f2);
+                y.w = mul_bf16x2(x[i].w, f2);
+                *reinterpret_cast<uint4 *>(dst + sw(row, kc16 & 7)) = y;
+                if (!fast) *reinterpret_cast<uint4 *>(raw + sw(row, kc16 & 7)) = x[i];
+            }
             if (wtid == 0) TRACE(2, 10, kpc);
             tc::fence_proxy_async_smem();
             named_sync(kBar, 128);

@@ -77,8 +77,7 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 std::atomic<uint32_t> g_epoch{0};
 
 // ---- timing instrumentation -------------------------------------------------------------
-const char *const kKernelNames[kKernelCount] = {"seg_table", "prefill_fused", "empty_seq_state",
-                                                "recurrent_step"};
+const char *const kKernelNames[kKernelCount] = {"seg_table", "prefill_fused", "recurrent_step"};
 struct TimingRecord {
     int id;
     cudaEvent_t start, stop;
@@ -309,7 +308,7 @@ int sala_gla_chunk_fwd(const void *q, const void *k, const void *v, const float 
     float *incl = reinterpret_cast<float *>(ws + off_bytes + tick_bytes + flag_bytes);
 
     int rc = SALA_OK;
-    if (launch_seg_table(tab, T_total, ticket, flags, max_units, d->status, st) != cudaSuccess ||
+    if (launch_seg_table(tab, T_total, ticket, flags, max_units, H, h0, hT, d->status, st) != cudaSuccess ||
         launch_prefill_fused(a, tab, T_total, max_units, h0, hT, incl, flags, ticket,
                              next_prefill_epoch(), d->sm_count, d->status, st) != cudaSuccess)
         rc = SALA_ERR_CUDA;

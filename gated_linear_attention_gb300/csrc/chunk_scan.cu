@@ -6,13 +6,18 @@ namespace sala {
 
 // ---------------------------------------------------------------------------------------
 // Segment table: seg_off[n] = sum over m < n of ceil(len_m / seg_len); validates cu_seqlens.
-// One block; each thread owns a contiguous range of sequences.
+// One block; each thread owns a contiguous range of sequences. Once the table is known to be
+// valid, the block also writes hT of every empty sequence (its initial state, or zeros): the
+// prefill kernel only visits sequences with tokens.
 constexpr int kPrepThreads = 1024;
 
 __global__ void __launch_bounds__(kPrepThreads)
 seg_table_kernel(SegTable t, int64_t T_total, uint32_t *ticket, uint32_t *flags, int64_t nflags,
-                 int *status) {
+                 int H, const float *__restrict__ h0, float *__restrict__ hT, int *status) {
     __shared__ int64_t part[kPrepThreads];
+    // the prefill kernel launched after this one may start its set-up now; it waits for this
+    // grid to complete before it reads anything written here
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int64_t i = threadIdx.x; i < nflags; i += kPrepThreads) flags[i] = 0u;
     if (threadIdx.x == 0 && ticket) *ticket = 0u;
     __shared__ int bad;
@@ -49,12 +54,23 @@ seg_table_kernel(SegTable t, int64_t T_total, uint32_t *ticket, uint32_t *flags,
         t.seg_off[t.nseq + 1] = bad ? 0 : 1;
         if (bad) record_status(status, SALA_ERR_BAD_SEQLENS);
     }
+    if (bad || !hT) return;
+    // hT of empty sequences (the block-wide flag `bad` is final after the barrier above)
+    constexpr int kVec = kD * kD / 4;   // float4 per (sequence, head)
+    for (int64_t n = 0; n < t.nseq; ++n) {
+        if (seq_begin(t, n + 1) != seq_begin(t, n)) continue;
+        float4 *dst = reinterpret_cast<float4 *>(hT + n * H * kD * kD);
+        const float4 *src = h0 ? reinterpret_cast<const float4 *>(h0 + n * H * kD * kD) : nullptr;
+        for (int64_t i = threadIdx.x; i < static_cast<int64_t>(H) * kVec; i += kPrepThreads)
+            dst[i] = src ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 }
 
 cudaError_t launch_seg_table(const SegTable &t, int64_t T_total, uint32_t *ticket,
-                             uint32_t *flags, int64_t nflags, int *status, cudaStream_t st) {
+                             uint32_t *flags, int64_t nflags, int H, const float *h0, float *hT,
+                             int *status, cudaStream_t st) {
     LaunchTimer timer(kKSegTable, st);
-    seg_table_kernel<<<1, kPrepThreads, 0, st>>>(t, T_total, ticket, flags, nflags, status);
+    seg_table_kernel<<<1, kPrepThreads, 0, st>>>(t, T_total, ticket, flags, nflags, H, h0, hT, status);
     return cudaGetLastError();
 }
 

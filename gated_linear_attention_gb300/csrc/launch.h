@@ -11,7 +11,6 @@ namespace sala {
 enum KernelId {
     kKSegTable = 0,
     kKPrefillFused,
-    kKEmptySeq,
     kKRecurrentStep,
     kKernelCount
 };
@@ -38,12 +37,13 @@ cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, c
                                   cudaStream_t stream);
 
 // Segment table from cu_seqlens (or B equal rows); also zeroes the work ticket and the
-// hand-off flags of the fused prefill.
+// hand-off flags of the fused prefill, and writes hT (= h0, or zeros) of empty sequences.
 cudaError_t launch_seg_table(const SegTable &t, int64_t T_total, uint32_t *ticket,
-                             uint32_t *flags, int64_t nflags, int *status, cudaStream_t st);
+                             uint32_t *flags, int64_t nflags, int H, const float *h0, float *hT,
+                             int *status, cudaStream_t st);
 
-// The fused tensor-core prefill (prefill_fused.cu): one persistent launch of `grid` CTAs,
-// then the final state of empty sequences. `incl` holds [max_units, 128, 128] fp32 hand-off
+// The fused tensor-core prefill (prefill_fused.cu): one persistent launch of `grid` CTAs
+// (the final state of empty sequences is written by the segment-table kernel). `incl` holds [max_units, 128, 128] fp32 hand-off
 // states, `flags` [max_units] words, `ticket` one word; `epoch` is nonzero and differs from
 // the previous call's. `status` receives SALA_ERR_TIMEOUT if a bounded wait gives up.
 cudaError_t setup_fused_kernel();

@@ -150,7 +150,7 @@ extern "C" int sala_gla_chunk_fwd_noalloc(const void *q, const void *k, const vo
     uint32_t *flags = reinterpret_cast<uint32_t *>(ws + table);
     float *incl = reinterpret_cast<float *>(ws + table + flag_bytes);
 
-    if (launch_seg_table(tab, T_total, ticket, flags, max_units, d->status, st) != cudaSuccess ||
+    if (launch_seg_table(tab, T_total, ticket, flags, max_units, H, h0, hT, d->status, st) != cudaSuccess ||
         launch_prefill_fused(a, tab, T_total, max_units, h0, hT, incl, flags, ticket,
                              next_prefill_epoch(), d->sm_count, d->status, st) != cudaSuccess)
         return SALA_ERR_CUDA;

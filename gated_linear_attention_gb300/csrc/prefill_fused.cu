@@ -410,6 +410,9 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
     tc::tc_fence_after();
     const uint32_t tmem = tmem_slot;
     volatile int *abort_v = &abort_flag;
+    // launched as a programmatic dependent of the segment-table kernel: the set-up above
+    // overlaps it; nothing that kernel writes (table, ticket, flags, hT) is touched before this
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const bool table_ok = t.seg_off[t.nseq + 1] == 1;
     const int64_t total_units = table_ok ? t.seg_off[t.nseq] * H : 0;
 
@@ -1283,20 +1286,6 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
     }
 }
 // ---------------------------------------------------------------------------------------
-// hT of empty sequences: the initial state (or zeros). One block per (sequence, head).
-__global__ void __launch_bounds__(256)
-empty_seq_state_kernel(SegTable t, int H, const float *__restrict__ h0, float *__restrict__ hT) {
-    if (t.seg_off[t.nseq + 1] != 1) return;
-    const int64_t nh = blockIdx.x;
-    const int64_t n = nh / H;
-    if (seq_begin(t, n + 1) != seq_begin(t, n)) return;
-    float4 *dst = reinterpret_cast<float4 *>(hT + nh * kD * kD);
-    const float4 *src = h0 ? reinterpret_cast<const float4 *>(h0 + nh * kD * kD) : nullptr;
-    for (int i = threadIdx.x; i < kD * kD / 4; i += blockDim.x)
-        dst[i] = src ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-}
-
-// ---------------------------------------------------------------------------------------
 // host side
 
 namespace tck {
@@ -1364,15 +1353,20 @@ cudaError_t launch_prefill_fused(const ChunkArgs &a, const SegTable &t, int64_t 
         f.epoch = epoch;
         if (grid > max_units) grid = static_cast<int>(max_units);
         LaunchTimer timer(kKPrefillFused, st);
-        prefill_fused_kernel<<<grid, kThreads, kSmemAlloc, st>>>(maps, f, t, status);
-        e = cudaGetLastError();
+        // programmatic dependent launch: the kernel's set-up may overlap the segment-table
+        // kernel before it on the stream (griddepcontrol.wait orders the rest)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemAlloc;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, prefill_fused_kernel, maps, f, t, status);
         if (e != cudaSuccess) return e;
-    }
-    if (hT && t.nseq > 0) {
-        const int64_t blocks = t.nseq * a.H;
-        LaunchTimer timer(kKEmptySeq, st);
-        empty_seq_state_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(t, a.H, h0, hT);
-        return cudaGetLastError();
     }
     return cudaSuccess;
 }

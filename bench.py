@@ -213,6 +213,11 @@ def decode_bytes(N, H):
     return N * H * (2 * D * D * 4 + 3 * D * 2 + 4 + D * 2)
 
 
+def decode_pool_bytes(N, H, state_bytes):
+    # the N addressed states read and written, q, k, v, g read, o written, the slot indices
+    return N * H * (2 * D * D * state_bytes + 3 * D * 2 + 4 + D * 2) + N * 4
+
+
 # ---------------------------------------------------------------------------------------
 # the oracle on the host cores (reference arm and CPU baseline)
 
@@ -410,6 +415,7 @@ def run_ours(args, dist):
     if not args.no_decode:
         decode = run_decode(args, dist, dev, peaks, sala_gla, inputs)
         launches_decode = decode.pop("_launches")
+        launches_decode += decode["pooled"].pop("_launches")
     else:
         launches_decode = 0
 
@@ -479,7 +485,9 @@ def run_decode(args, dist, dev, peaks, sala_gla, inputs):
     per_step = decode_bytes(w.nseq, w.H)
     gbs = per_step * w.steps / (ms / 1e3) / 1e9 * dist.world
     k_ach = per_step / (kern[0] / kern[1] / 1e3) / 1e9
+    pooled = run_decode_pool(args, dist, peaks, sala_gla, inputs, w, q, k, v, g, o, scale)
     return {
+        "pooled": pooled,
         "metric": "decode HBM GB/s", "value": gbs, "unit": "GB/s",
         "ms_per_step": ms / w.steps, "tokens_per_s": w.nseq * w.steps / (ms / 1e3) * dist.world,
         "config": {"workload": w.name, "N": w.nseq, "H": w.H, "d": D, "steps": w.steps,
@@ -488,6 +496,57 @@ def run_decode(args, dist, dev, peaks, sala_gla, inputs):
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": k_ach / peaks["hbm_gbs"],
                      "traffic": MEASURED_TRAFFIC["recurrent_step"] if w.nseq == 256 else None,
                      "peak_source": peaks["source"], "mean_launch_us": 1e3 * kern[0] / kern[1]},
+        "_launches": kern[1],
+    }
+
+
+def run_decode_pool(args, dist, peaks, sala_gla, inputs, wd, q, k, v, g, o, scale):
+    """The same decode steps on states kept in a pool of 512 slots stored in bf16 and
+    addressed through a slot permutation (sala_gla_recurrent_step_indexed). The per-step
+    tokens are the decode workload's, already resident."""
+    import dataclasses
+    import torch
+    w = dataclasses.replace(inputs.WORKLOADS["decode_pool"], steps=wd.steps)
+    p = inputs.make_decode_pool(w)
+    dev = q.device
+    pool, idx = p["pool"].to(dev), p["indices"].to(dev)
+    for s in range(max(3, args.warmup)):
+        sala_gla.recurrent_step_indexed(q[s], k[s], v[s], g[s], scale, pool, idx, o=o)
+    torch.cuda.synchronize()
+    pool.copy_(p["pool"])
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for s in range(w.steps):
+        sala_gla.recurrent_step_indexed(q[s], k[s], v[s], g[s], scale, pool, idx, o=o)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist.max(ev0.elapsed_time(ev1))
+    # per-kernel events in a second pass of the same steps
+    sala_gla.timing_enable(True)
+    for s in range(w.steps):
+        sala_gla.recurrent_step_indexed(q[s], k[s], v[s], g[s], scale, pool, idx, o=o)
+    torch.cuda.synchronize()
+    sala_gla.timing_enable(False)
+    kern = sala_gla.timing_read()["recurrent_step_indexed"]
+    assert sala_gla.get_device_status() == 0
+    per_step = decode_pool_bytes(w.nseq, w.H, 2 if w.storage == "bf16" else 4)
+    gbs = per_step * w.steps / (ms / 1e3) / 1e9 * dist.world
+    k_ach = per_step / (kern[0] / kern[1] / 1e3) / 1e9
+    return {
+        "metric": "pooled decode HBM GB/s", "value": gbs, "unit": "GB/s",
+        "ms_per_step": ms / w.steps, "tokens_per_s": w.nseq * w.steps / (ms / 1e3) * dist.world,
+        "config": {"workload": w.name, "N": w.nseq, "H": w.H, "d": D, "steps": w.steps,
+                   "pool_slots": w.pool, "state_storage": w.storage,
+                   "pool_bytes": w.pool * w.H * D * D * (2 if w.storage == "bf16" else 4),
+                   "bytes_per_step": per_step,
+                   "tokens": "the decode workload's per-step q, k, v, g"},
+        "roofline": {"kernel": "recurrent_step_indexed", "bound": "hbm", "achieved": k_ach,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": k_ach / peaks["hbm_gbs"],
+                     "traffic": None, "peak_source": peaks["source"],
+                     "mean_launch_us": 1e3 * kern[0] / kern[1]},
         "_launches": kern[1],
     }
 

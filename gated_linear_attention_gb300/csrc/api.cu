@@ -77,7 +77,8 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 std::atomic<uint32_t> g_epoch{0};
 
 // ---- timing instrumentation -------------------------------------------------------------
-const char *const kKernelNames[kKernelCount] = {"seg_table", "prefill_fused", "recurrent_step"};
+const char *const kKernelNames[kKernelCount] = {"seg_table", "prefill_fused", "recurrent_step",
+                                                "recurrent_step_indexed"};
 struct TimingRecord {
     int id;
     cudaEvent_t start, stop;
@@ -202,6 +203,7 @@ const char *sala_gla_status_string(int status) {
     case SALA_ERR_BAD_SEQLENS: return "cu_seqlens is not monotone from 0 to T";
     case SALA_ERR_TOO_LARGE:
         return "problem needs more scratch than the no-allocation entry point's fixed buffer";
+    case SALA_ERR_BAD_INDEX: return "a state index is at or past the pool size";
     default: return "unknown status";
     }
 }
@@ -241,6 +243,37 @@ int sala_gla_recurrent_step(const void *q, const void *k, const void *v, const f
     if (!device_state(&err)) return err;
     if (launch_recurrent_step(q, k, v, g, scale, S_inout, o, static_cast<int64_t>(units),
                               static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SALA_ERR_CUDA;
+    return SALA_OK;
+}
+
+int sala_gla_recurrent_step_indexed(const void *q, const void *k, const void *v, const float *g,
+                                    float scale, void *state_pool, int32_t state_dtype,
+                                    const int32_t *state_indices, int64_t P, void *o, int64_t N,
+                                    int32_t H, void *stream) {
+    if (N < 0 || H < 1 || P < 1) return SALA_ERR_INVALID_ARG;
+    if (state_dtype != SALA_STATE_F32 && state_dtype != SALA_STATE_BF16) return SALA_ERR_INVALID_ARG;
+    if (N == 0) return SALA_OK;
+    if (N > (int64_t(1) << 31) / H || P > (int64_t(1) << 40) / H) return SALA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !g || !state_pool || !state_indices || !o) return SALA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(state_pool) ||
+        !aligned16(state_indices) || !aligned16(o))
+        return SALA_ERR_MISALIGNED;
+    const size_t units = static_cast<size_t>(N) * H;
+    const size_t vec = units * kD * 2, gb = units * 4, ib = static_cast<size_t>(N) * 4;
+    const size_t pb = static_cast<size_t>(P) * H * kD * kD * (state_dtype == SALA_STATE_BF16 ? 2 : 4);
+    const void *ins[5] = {q, k, v, g, state_indices};
+    const size_t in_sz[5] = {vec, vec, vec, gb, ib};
+    for (int i = 0; i < 5; ++i)
+        if (overlaps(state_pool, pb, ins[i], in_sz[i]) || overlaps(o, vec, ins[i], in_sz[i]))
+            return SALA_ERR_INVALID_ARG;
+    if (overlaps(state_pool, pb, o, vec)) return SALA_ERR_INVALID_ARG;
+    int err = SALA_OK;
+    DeviceState *d = device_state(&err);
+    if (!d) return err;
+    if (launch_recurrent_step_indexed(q, k, v, g, scale, state_pool, state_dtype == SALA_STATE_BF16,
+                                      state_indices, P, o, N, H, d->status,
+                                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SALA_ERR_CUDA;
     return SALA_OK;
 }

@@ -12,6 +12,7 @@ enum KernelId {
     kKSegTable = 0,
     kKPrefillFused,
     kKRecurrentStep,
+    kKRecurrentStepIndexed,
     kKernelCount
 };
 
@@ -35,6 +36,13 @@ cudaError_t device_status_address(int **out);
 cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, const float *g,
                                   float scale, float *S, void *o, int64_t units,
                                   cudaStream_t stream);
+
+// The same step on states in a pool [P, H, 128, 128] (fp32, or bf16 if `bf16`) addressed by
+// idx[N] (negative: padding row, o = 0; >= P: SALA_ERR_BAD_INDEX recorded in `status`).
+cudaError_t launch_recurrent_step_indexed(const void *q, const void *k, const void *v,
+                                          const float *g, float scale, void *pool, bool bf16,
+                                          const int32_t *idx, int64_t P, void *o, int64_t N,
+                                          int H, int *status, cudaStream_t stream);
 
 // Segment table from cu_seqlens (or B equal rows); also zeroes the work ticket and the
 // hand-off flags of the fused prefill, and writes hT (= h0, or zeros) of empty sequences.

@@ -7,12 +7,18 @@
 // Bandwidth": GLA recurrence = state R/W), so the kernel is a single streaming pass over
 // the fp32 state: every byte of S is loaded once and stored once.
 //
+// The same kernel serves a state pool addressed through per-sequence slot indices, with the
+// states stored in fp32 or bf16 (the Blueprint's "Memory Architecture": per-request temporal
+// states in a pool, 1 MB each in bf16 for 32 heads); bf16 storage halves the bytes moved.
+//
 // Work split: one CTA of 256 threads (8 warps) per (sequence, head) unit. Warp w owns state
 // rows [16w, 16w + 16); lane l owns columns [4l, 4l + 4), so each warp instruction moves
 // one whole 512-byte row with 128-bit accesses. All 16 row loads of a thread are issued
 // before any arithmetic (64 KB in flight per CTA), with the streaming cache hint since the
 // state is touched exactly once per step. The q S reduction over rows is split: each thread
 // accumulates its 16 rows, then the 8 warp partials are summed through shared memory.
+#include <type_traits>
+
 #include "launch.h"
 
 namespace sala {
@@ -20,25 +26,68 @@ namespace sala {
 constexpr int kDecodeThreads = 256;
 constexpr int kRowsPerWarp = kD / (kDecodeThreads / 32);  // 16
 
+// Where one unit's state lives and how it is stored: a dense [N, H, 128, 128] fp32 array
+// (unit n * H + h at offset unit * 128 * 128), or a pool [P, H, 128, 128] of fp32 or bf16
+// addressed through the slot index of the unit's sequence.
+struct StateRef {
+    void *base;
+    const int32_t *idx;   // null: dense
+    int64_t P;
+    int H;
+};
+
+// kBf16: states stored as bf16 (4 columns of a row per lane = 8 bytes), else fp32 (16 bytes).
+template <bool kBf16>
+__device__ __forceinline__ float4 load_state4(const void *row, int lane) {
+    if constexpr (kBf16) {
+        const uint2 w = __ldcs(reinterpret_cast<const uint2 *>(row) + lane);
+        const float2 a = bf16x2_to_float2(w.x), b = bf16x2_to_float2(w.y);
+        return make_float4(a.x, a.y, b.x, b.y);
+    } else {
+        return __ldcs(reinterpret_cast<const float4 *>(row) + lane);
+    }
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void store_state4(void *row, int lane, float4 x) {
+    if constexpr (kBf16)
+        __stcs(reinterpret_cast<uint2 *>(row) + lane, make_uint2(float2_to_bf16x2(x.x, x.y), float2_to_bf16x2(x.z, x.w)));
+    else
+        __stcs(reinterpret_cast<float4 *>(row) + lane, x);
+}
+
+template <bool kBf16>
 __global__ void __launch_bounds__(kDecodeThreads)
 recurrent_step_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
                       const uint16_t *__restrict__ v, const float *__restrict__ g, float scale,
-                      float *__restrict__ S, uint16_t *__restrict__ o) {
+                      StateRef ref, uint16_t *__restrict__ o, int *status) {
+    using StateT = typename std::conditional<kBf16, uint16_t, float>::type;
     const int unit = blockIdx.x;  // n * H + h
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float *Su = S + static_cast<size_t>(unit) * kD * kD;
+    const size_t vec = static_cast<size_t>(unit) * kD;
+    size_t slot_unit = unit;
+    if (ref.idx) {
+        const int n = unit / ref.H, h = unit - n * ref.H;
+        const int32_t slot = __ldg(ref.idx + n);
+        if (slot < 0 || slot >= ref.P) {
+            // padding row (or a slot past the pool, reported): o = 0, no state touched
+            if (slot >= ref.P && h == 0 && threadIdx.x == 0) record_status(status, SALA_ERR_BAD_INDEX);
+            if (threadIdx.x < kD / 2) reinterpret_cast<uint32_t *>(o + vec)[threadIdx.x] = 0u;
+            return;
+        }
+        slot_unit = static_cast<size_t>(slot) * ref.H + h;
+    }
+    StateT *Su = static_cast<StateT *>(ref.base) + slot_unit * kD * kD;
     const int row0 = warp * kRowsPerWarp;
 
     // 1. stream the state rows in (issued first: nothing depends on them yet)
     float4 s[kRowsPerWarp];
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r)
-        s[r] = __ldcs(reinterpret_cast<const float4 *>(Su + (row0 + r) * kD) + lane);
+    for (int r = 0; r < kRowsPerWarp; ++r) s[r] = load_state4<kBf16>(Su + (row0 + r) * kD, lane);
 
     // 2. the token's q, k (for my rows) and v (for my columns)
     __shared__ float q_s[kD], k_s[kD];
     __shared__ float part[kDecodeThreads / 32][kD];
-    const size_t vec = static_cast<size_t>(unit) * kD;
     if (threadIdx.x < kD) {
         q_s[threadIdx.x] = bf16_bits_to_float(q[vec + threadIdx.x]);
         k_s[threadIdx.x] = bf16_bits_to_float(k[vec + threadIdx.x]);
@@ -48,7 +97,8 @@ recurrent_step_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict
     const float alpha = expf(g[unit]);
     __syncthreads();
 
-    // 3. decay + rank-1 update, store back, and accumulate q S for my 4 columns
+    // 3. decay + rank-1 update, store back, and accumulate q S for my 4 columns (from the
+    //    updated state before any storage rounding)
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
@@ -58,7 +108,7 @@ recurrent_step_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict
         x.y = fmaf(alpha, x.y, ki * v01.y);
         x.z = fmaf(alpha, x.z, ki * v23.x);
         x.w = fmaf(alpha, x.w, ki * v23.y);
-        __stcs(reinterpret_cast<float4 *>(Su + (row0 + r) * kD) + lane, x);
+        store_state4<kBf16>(Su + (row0 + r) * kD, lane, x);
         acc.x = fmaf(qi, x.x, acc.x);
         acc.y = fmaf(qi, x.y, acc.y);
         acc.z = fmaf(qi, x.z, acc.z);
@@ -85,9 +135,28 @@ cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, c
                                   cudaStream_t stream) {
     if (units == 0) return cudaSuccess;
     LaunchTimer timer(kKRecurrentStep, stream);
-    recurrent_step_kernel<<<static_cast<unsigned>(units), kDecodeThreads, 0, stream>>>(
+    recurrent_step_kernel<false><<<static_cast<unsigned>(units), kDecodeThreads, 0, stream>>>(
         static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k),
-        static_cast<const uint16_t *>(v), g, scale, S, static_cast<uint16_t *>(o));
+        static_cast<const uint16_t *>(v), g, scale, StateRef{S, nullptr, 0, 1},
+        static_cast<uint16_t *>(o), nullptr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_recurrent_step_indexed(const void *q, const void *k, const void *v,
+                                          const float *g, float scale, void *pool, bool bf16,
+                                          const int32_t *idx, int64_t P, void *o, int64_t N,
+                                          int H, int *status, cudaStream_t stream) {
+    if (N == 0) return cudaSuccess;
+    LaunchTimer timer(kKRecurrentStepIndexed, stream);
+    const unsigned blocks = static_cast<unsigned>(N * H);
+    const StateRef ref{pool, idx, P, H};
+    const auto *qb = static_cast<const uint16_t *>(q), *kb = static_cast<const uint16_t *>(k),
+               *vb = static_cast<const uint16_t *>(v);
+    auto *ob = static_cast<uint16_t *>(o);
+    if (bf16)
+        recurrent_step_kernel<true><<<blocks, kDecodeThreads, 0, stream>>>(qb, kb, vb, g, scale, ref, ob, status);
+    else
+        recurrent_step_kernel<false><<<blocks, kDecodeThreads, 0, stream>>>(qb, kb, vb, g, scale, ref, ob, status);
     return cudaGetLastError();
 }
 

@@ -27,7 +27,7 @@ D = 128
 BLOCK_TOKENS = 1024
 
 # stream ids
-_Q, _K, _V, _U, _H0 = 1, 2, 3, 4, 5
+_Q, _K, _V, _U, _H0, _SLOT = 1, 2, 3, 4, 5, 6
 
 
 @dataclass(frozen=True)
@@ -43,6 +43,8 @@ class Workload:
     varlen: bool = False
     nseq: int = 0               # decode: number of sequences
     steps: int = 0              # decode: consecutive steps
+    pool: int = 0               # pooled decode: slots in the state pool
+    storage: str = "f32"        # pooled decode: state storage type ("f32" or "bf16")
     description: str = field(default="", compare=False)
 
     @property
@@ -73,6 +75,13 @@ WORKLOADS = {
         nseq=256, steps=1000, description="batched recurrent decode: 256 sequences x 1 token, "
         "H=32; q,k L2-normalised; g=logsigmoid(u), u~U(2,6); S~N(0,0.02) [256,32,128,128] "
         "fp32 updated in place; 1000 consecutive steps"),
+    "decode_pool": Workload(
+        "decode_pool", "decode", H=32, seqlens=(), qk_norm="l2", gate="logsigmoid", h0=True,
+        seed=4, nseq=256, steps=1000, pool=512, storage="bf16",
+        description="pooled recurrent decode: 256 sequences x 1 token, H=32, states in a "
+        "pool of 512 slots [512,32,128,128] stored in bf16 (256 MB read+written per step), "
+        "slots of the batch = a seeded permutation of the pool; per-step q, k, v, g those of "
+        "the decode workload (same seed); S~N(0,0.02); 1000 consecutive steps"),
 }
 
 SCALE = 1.0 / math.sqrt(D)     # 1/sqrt(128) = 0.08839...
@@ -224,3 +233,27 @@ def make_decode_steps(w: Workload | str = "decode", start: int = 0, count: int |
     with ThreadPoolExecutor(_threads()) as pool:
         list(pool.map(one, range(count)))
     return dict(q=q, k=k, v=v, g=g, scale=SCALE, workload=w)
+
+
+def make_decode_pool(w: Workload | str = "decode_pool", *, nseq=None, H=None, pool=None,
+                     storage=None, pad=()) -> dict:
+    """Pool and slot indices of a pooled decode workload.
+
+    Returns pool [P, H, 128, 128] (states ~ N(0, 0.02^2) drawn in float32; cast to bfloat16
+    for bf16 storage) and indices int32 [nseq]: the first nseq entries of a seeded
+    permutation of the P slots, with the rows listed in ``pad`` set to -1 (padding). The
+    per-step q, k, v, g come from :func:`make_decode_steps` with the same workload.
+    """
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    n, Hh, P = nseq or w.nseq, H or w.H, pool or w.pool
+    st = storage or w.storage
+    assert n <= P
+    with ThreadPoolExecutor(_threads()) as tp:
+        S = _states(w.seed, _H0, P, Hh, tp)
+    perm = np.random.default_rng([w.seed, _SLOT, 0]).permutation(P)[:n]
+    idx = torch.from_numpy(perm.astype(np.int32))
+    for r in pad:
+        idx[r] = -1
+    return dict(pool=S.to(torch.bfloat16) if st == "bf16" else S, indices=idx, storage=st,
+                workload=w)

@@ -20,8 +20,9 @@ SALA_OK = 0
 STATUS_NAMES = {
     0: "SALA_OK", 1: "SALA_ERR_INVALID_ARG", 2: "SALA_ERR_MISALIGNED",
     3: "SALA_ERR_UNSUPPORTED", 4: "SALA_ERR_CUDA", 5: "SALA_ERR_TIMEOUT",
-    6: "SALA_ERR_BAD_SEQLENS", 7: "SALA_ERR_TOO_LARGE",
+    6: "SALA_ERR_BAD_SEQLENS", 7: "SALA_ERR_TOO_LARGE", 8: "SALA_ERR_BAD_INDEX",
 }
+SALA_STATE_F32, SALA_STATE_BF16 = 0, 1
 
 # exported symbols and their ctypes signatures (must match include/sala_gla.h)
 _p, _i64, _i32, _f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
@@ -29,6 +30,8 @@ SIGNATURES = {
     "sala_gla_chunk_fwd": ([_p, _p, _p, _p, _f32, _p, _p, _p, _p, _i64, _i64, _i32, _i64, _p],
                            ctypes.c_int),
     "sala_gla_recurrent_step": ([_p, _p, _p, _p, _f32, _p, _p, _i64, _i32, _p], ctypes.c_int),
+    "sala_gla_recurrent_step_indexed": ([_p, _p, _p, _p, _f32, _p, _i32, _p, _i64, _p, _i64, _i32,
+                                         _p], ctypes.c_int),
     "sala_gla_chunk_fwd_noalloc": ([_p, _p, _p, _p, _f32, _p, _p, _p, _p, _i64, _i64, _i32,
                                     _i64, _p], ctypes.c_int),
     "sala_gla_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -175,6 +178,36 @@ def recurrent_step(q, k, v, g, scale, S, o=None, stream=None):
     rc = load().sala_gla_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), float(scale),
                                         _ptr(S), _ptr(o), N, H, _stream(stream))
     _check(rc, "sala_gla_recurrent_step")
+    return o
+
+
+def recurrent_step_indexed(q, k, v, g, scale, pool, indices, o=None, stream=None):
+    """One decode step on pooled states, ``sala_gla_recurrent_step_indexed``: row n uses (and
+    updates in place) ``pool[indices[n]]``; a negative index is a padding row (o = 0).
+    q, k, v: bf16 [N, H, 128]; g: fp32 [N, H]; pool: fp32 or bf16 [P, H, 128, 128] (its dtype
+    is the storage type); indices: int32 [N]. Returns o (bf16 [N, H, 128])."""
+    N, H, D = q.shape
+    if D != 128:
+        raise ValueError("head dimension must be 128")
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16, q.shape)
+    _need(v, "v", torch.bfloat16, q.shape)
+    _need(g, "g", torch.float32, (N, H))
+    if pool.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError(f"pool must be float32 or bfloat16, got {pool.dtype}")
+    _need(pool, "pool", pool.dtype)
+    if pool.dim() != 4 or tuple(pool.shape[1:]) != (H, 128, 128):
+        raise ValueError(f"pool has shape {tuple(pool.shape)}, expected (P, {H}, 128, 128)")
+    _need(indices, "indices", torch.int32, (N,))
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _need(o, "o", torch.bfloat16, q.shape)
+    dt = SALA_STATE_BF16 if pool.dtype == torch.bfloat16 else SALA_STATE_F32
+    rc = load().sala_gla_recurrent_step_indexed(_ptr(q), _ptr(k), _ptr(v), _ptr(g), float(scale),
+                                                _ptr(pool), dt, _ptr(indices), pool.shape[0],
+                                                _ptr(o), N, H, _stream(stream))
+    _check(rc, "sala_gla_recurrent_step_indexed")
     return o
 
 

@@ -49,8 +49,16 @@ typedef enum {
     SALA_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, allocation) */
     SALA_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up */
     SALA_ERR_BAD_SEQLENS = 6, /* device-detected: cu_seqlens not monotone or last != T */
-    SALA_ERR_TOO_LARGE = 7    /* sala_gla_chunk_fwd_noalloc: problem exceeds its fixed scratch */
+    SALA_ERR_TOO_LARGE = 7,   /* sala_gla_chunk_fwd_noalloc: problem exceeds its fixed scratch */
+    SALA_ERR_BAD_INDEX = 8    /* device-detected: a state index at or past the pool size */
 } sala_status;
+
+/* Storage type of the states in a state pool (sala_gla_recurrent_step_indexed). The
+ * arithmetic is fp32 either way. */
+typedef enum {
+    SALA_STATE_F32 = 0,  /* fp32 states, 64 KB per (slot, head) */
+    SALA_STATE_BF16 = 1  /* bf16 states, 32 KB per (slot, head); rounded to nearest even on store */
+} sala_state_dtype;
 
 /*
  * Chunked prefill (chunk size 64).
@@ -108,6 +116,37 @@ int sala_gla_chunk_fwd(const void *q, const void *k, const void *v, const float 
 int sala_gla_recurrent_step(const void *q, const void *k, const void *v, const float *g,
                             float scale, float *S_inout, void *o, int64_t N, int32_t H,
                             void *stream);
+
+/*
+ * One-token recurrent decode on states kept in a pool and addressed through an index array.
+ *
+ * A serving engine keeps each request's recurrent state in a slot of a per-layer pool and
+ * hands the layer the slot of every request in the batch ("MiniCPM-SALA — Complete
+ * Blueprint", "Memory Architecture": MambaPool temporal states, one per request and layer,
+ * 1 MB each in bf16 for 32 heads; the decode step loads the state from the pool, updates it
+ * and saves it back in place). For each sequence n of the batch and head h, with
+ * i = state_indices[n]:
+ *     S = state_pool[i, h];  S = exp(g[n,h]) S + k[n,h]^T v[n,h];  o[n,h] = scale q[n,h] S;
+ *     state_pool[i, h] = S
+ * A negative index marks a padding row: its o is written as zeros and no state is touched.
+ *
+ *   q, k, v        bf16 [N, H, 128];  g fp32 [N, H]
+ *   state_pool     [P, H, 128, 128] of state_dtype (SALA_STATE_F32: fp32; SALA_STATE_BF16:
+ *                  bf16, widened to fp32 for the arithmetic and rounded to nearest even when
+ *                  stored). Only the N addressed slots are read and written.
+ *   state_indices  int32 [N] DEVICE array of slots (< P), or negative for padding. Two rows
+ *                  with the same slot race (the result is one of them); the caller must not
+ *                  do that. A slot >= P is recorded as SALA_ERR_BAD_INDEX in the device
+ *                  status word and its row is treated as padding.
+ *   o              bf16 [N, H, 128] output.
+ *   P, N, H        P >= 1, N >= 0 (0 is a no-op), H >= 1.
+ * Errors: SALA_ERR_INVALID_ARG (also for an unknown state_dtype or a pool that overlaps
+ * another argument), SALA_ERR_MISALIGNED, SALA_ERR_UNSUPPORTED, SALA_ERR_CUDA.
+ */
+int sala_gla_recurrent_step_indexed(const void *q, const void *k, const void *v, const float *g,
+                                    float scale, void *state_pool, int32_t state_dtype,
+                                    const int32_t *state_indices, int64_t P, void *o, int64_t N,
+                                    int32_t H, void *stream);
 
 /*
  * Chunked prefill that allocates nothing: same arguments, layouts, results and errors as

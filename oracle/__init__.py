@@ -22,7 +22,11 @@ Three independent statements of the same computation:
   o_t = scale * [ sum_{j<=t} exp(G_t - G_j) (q_t . k_j) v_j + exp(G_t) q_t h0 ],
   G_t = sum_{i<=t} g_i within the sequence. For tiny inputs only.
 
-All three take the exact values the GPU receives (bf16 q/k/v, fp32 g, fp32 h0) and compute
+Beside them, :func:`recurrent_step_indexed` is one decode step on states gathered from and
+written back to a pool through slot indices (fp32 or bf16 storage), built on
+:func:`recurrent`.
+
+All of them take the exact values the GPU receives (bf16 q/k/v, fp32 g, fp32 h0) and compute
 in float64.
 """
 from __future__ import annotations
@@ -223,6 +227,57 @@ def bruteforce(q, k, v, g, scale, h0=None, cu_seqlens=None):
             w_end = np.exp(GL - G) if L else np.zeros(0)
             hT[n, h] = np.exp(GL) * S0 + (kd[s:e, h] * w_end[:, None]).T @ vd[s:e, h]
     return o, hT
+
+
+# ----------------------------------------------------------------------------------------
+# one decode step on states held in a pool (fp64)
+
+
+def round_bf16(x) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 value (ties to even), returned as
+    float64. bfloat16 keeps 8 significant bits (the leading one included) and float32's
+    exponent range; valid for values in the normal range of bfloat16 and for zero."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                    # x = m 2^e with 0.5 <= |m| < 1
+    return np.ldexp(np.round(m * 256.0) / 256.0, e)   # numpy rounds halves to even
+
+
+def recurrent_step_indexed(q, k, v, g, scale, pool, indices, storage: str = "f32"):
+    """One decode step on states kept in a pool and addressed by slot, in float64.
+
+    "MiniCPM-SALA — Complete Blueprint", section "Memory Architecture": every request keeps
+    its temporal state in a slot of a per-layer pool (1 MB per request in bf16 for 32
+    heads); the decode step loads the state from its slot, applies the recurrence of
+    section "B2 lightning-attn (Simple GLA)" (decay, k^T v update, o = scale q S) and saves
+    the updated state back to the same slot. Row n uses slot indices[n]; a negative slot is
+    a padding row (o = 0, no state read or written). With ``storage="bf16"`` the pool holds
+    bfloat16 values: they are widened exactly, o reads the updated state before rounding,
+    and the stored state is the updated state rounded to the nearest bfloat16.
+
+    q, k, v: bf16 [N, H, dk|dv]; g: fp32 [N, H]; pool: [P, H, dk, dv] (float32/float64, or
+    bfloat16 for "bf16"); indices: ints [N]. Returns (o [N, H, dv] float64, new pool
+    [P, H, dk, dv] float64 holding the stored values). The recurrence itself is
+    :func:`recurrent`, run on one-token sequences.
+    """
+    idx = np.asarray(indices.cpu() if isinstance(indices, torch.Tensor) else indices,
+                     dtype=np.int64)
+    P = pool.shape[0]
+    if np.any(idx >= P):
+        raise ValueError("slot index at or past the pool size")
+    live = np.nonzero(idx >= 0)[0]
+    if len(set(idx[live].tolist())) != len(live):
+        raise ValueError("two rows name the same slot")
+    new = _as_f64(pool).copy()
+    N, H, dv = v.shape
+    o = np.zeros((N, H, dv), dtype=np.float64)
+    if len(live):
+        sel = torch.as_tensor(live)
+        cu = torch.arange(len(live) + 1, dtype=torch.int64)
+        o_live, S = recurrent(q[sel], k[sel], v[sel], g[sel], scale, h0=new[idx[live]],
+                              cu_seqlens=cu)
+        o[live] = o_live
+        new[idx[live]] = round_bf16(S) if storage == "bf16" else S
+    return o, new
 
 
 def rel_fro(x, ref) -> float:

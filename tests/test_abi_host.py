@@ -63,7 +63,7 @@ def test_library_is_sm103a_only_and_links_cudart_statically(lib):
 def test_status_strings(lib):
     from gated_linear_attention_gb300 import sala_gla
     assert sala_gla.status_string(0) == "success"
-    for s in range(1, 8):
+    for s in range(1, 9):
         assert sala_gla.status_string(s) not in ("", "unknown status")
     assert sala_gla.status_string(99) == "unknown status"
     assert sala_gla.version().count(".") == 2
@@ -117,11 +117,38 @@ def test_recurrent_step_argument_errors(lib):
     assert _step(lib, S=0x10000) == INVALID                        # S overlaps q
 
 
+def _istep(lib, q=0x10000, k=0x20000, v=0x30000, g=0x40000, pool=0x100000, dt=0, idx=0x48000,
+           Pn=4, o=0x50000, N=2, H=2):
+    return lib.sala_gla_recurrent_step_indexed(P(q), P(k), P(v), P(g), 0.1, P(pool), dt,
+                                               P(idx) if idx else None, Pn, P(o), N, H, None)
+
+
+@no_gpu
+def test_recurrent_step_indexed_argument_errors(lib):
+    INVALID, MISALIGNED = 1, 2
+    assert _istep(lib, N=-1) == INVALID
+    assert _istep(lib, H=0) == INVALID
+    assert _istep(lib, Pn=0) == INVALID
+    assert _istep(lib, dt=2) == INVALID                            # unknown storage type
+    assert _istep(lib, N=0) == 0                                   # empty batch is a no-op
+    assert _istep(lib, idx=0) == INVALID
+    assert _istep(lib, pool=0) == INVALID
+    assert _istep(lib, idx=0x48004) == MISALIGNED
+    assert _istep(lib, pool=0x100008) == MISALIGNED
+    # pool of 4 slots x 2 heads: 512 KB fp32, 256 KB bf16
+    assert _istep(lib, o=0x100000 + 300 * 1024) == INVALID           # o inside the fp32 pool
+    assert _istep(lib, dt=1, o=0x100000 + 300 * 1024) != INVALID     # past the bf16 pool
+    assert _istep(lib, pool=0x40000) == INVALID                      # pool overlaps g
+    assert _istep(lib, idx=0x100000 + 4096) == INVALID               # indices inside the pool
+
+
 @no_gpu
 def test_valid_arguments_without_a_gpu_report_cuda_error(lib):
     # validation passes, then the runtime finds no device: nothing is launched
     assert _chunk(lib) == 4
     assert _step(lib) == 4
+    assert _istep(lib) == 4
+    assert _istep(lib, dt=1) == 4
 
 
 def test_binding_refuses_cpu_tensors(lib):

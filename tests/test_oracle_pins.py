@@ -272,3 +272,102 @@ def test_oracle_rejects_bad_arguments():
         oracle.recurrent(q, q, q, g, 1.0, cu_seqlens=torch.tensor([0, 3, 2]))
     with pytest.raises(ValueError):
         oracle.recurrent(q, q, q, g, 1.0, heads=[1])
+
+
+# ---------------------------------------------------------------------------------------
+# one decode step on pooled states ("MiniCPM-SALA — Complete Blueprint", "Memory
+# Architecture": per-request temporal states in a per-layer pool, loaded, updated and saved
+# back in place; 1 MB per request in bf16 for 32 heads)
+
+
+def _pool_case(N, H, dk, dv, P, seed, pad=()):
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn((N, H, dk), generator=gen).to(torch.bfloat16)
+    k = torch.randn((N, H, dk), generator=gen).to(torch.bfloat16)
+    v = torch.randn((N, H, dv), generator=gen).to(torch.bfloat16)
+    g = -0.5 * torch.rand((N, H), generator=gen)
+    pool = torch.randn((P, H, dk, dv), generator=gen) * 0.5
+    idx = torch.randperm(P, generator=gen)[:N].to(torch.int32)
+    for n in pad:
+        idx[n] = -1
+    return q, k, v, g, pool, idx
+
+
+def _pool_step_numpy(q, k, v, g, scale, pool, idx):
+    """The step written out per row with numpy outer products (no oracle code)."""
+    new = pool.double().numpy().copy()
+    N, H, _ = q.shape
+    o = np.zeros((N, H, v.shape[-1]))
+    for n in range(N):
+        i = int(idx[n])
+        if i < 0:
+            continue
+        for h in range(H):
+            S = math.exp(float(g[n, h])) * new[i, h] + np.outer(k[n, h].double().numpy(),
+                                                                v[n, h].double().numpy())
+            o[n, h] = scale * (q[n, h].double().numpy() @ S)
+            new[i, h] = S
+    return o, new
+
+
+def test_pool_step_matches_outer_product_restatement():
+    q, k, v, g, pool, idx = _pool_case(N=5, H=3, dk=7, dv=4, P=9, seed=41, pad=(2,))
+    o, new = oracle.recurrent_step_indexed(q, k, v, g, 0.61, pool, idx)
+    o_ref, new_ref = _pool_step_numpy(q, k, v, g, 0.61, pool, idx)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(new, new_ref, rtol=1e-12, atol=1e-12)
+    # the padding row reads nothing and writes zeros; slots nobody names are untouched
+    assert np.all(o[2] == 0.0)
+    named = set(int(i) for i in idx if i >= 0)
+    for i in range(9):
+        if i not in named:
+            assert np.array_equal(new[i], pool[i].double().numpy())
+
+
+def test_pool_step_permutation_invariance():
+    # relabelling the pool's slots (and the indices with them) changes nothing else
+    q, k, v, g, pool, idx = _pool_case(N=4, H=2, dk=5, dv=6, P=7, seed=42, pad=(1,))
+    perm = torch.randperm(7, generator=torch.Generator().manual_seed(7))
+    inv = torch.argsort(perm)
+    o1, new1 = oracle.recurrent_step_indexed(q, k, v, g, 0.3, pool, idx)
+    idx2 = torch.where(idx >= 0, inv[idx.clamp(min=0).long()].to(torch.int32), idx)
+    o2, new2 = oracle.recurrent_step_indexed(q, k, v, g, 0.3, pool[perm], idx2)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(new1[perm.numpy()], new2)
+
+
+def test_round_bf16_matches_library_rounding():
+    # on values exactly representable in float32, rounding to bfloat16 directly equals
+    # torch's float32 -> bfloat16 conversion (round to nearest even)
+    x = np.random.default_rng(5).standard_normal(200000).astype(np.float32)
+    x = np.concatenate([x, x * 1e-20, x * 1e20, np.float32([0.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8])])
+    want = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(oracle.round_bf16(x.astype(np.float64)), want)
+    # ties go to even: 1 + 2^-8 is halfway between 1 and 1 + 2^-7
+    assert oracle.round_bf16(1.0 + 2 ** -8) == 1.0
+    assert oracle.round_bf16(1.0 + 3 * 2 ** -8) == 1.0 + 2 ** -6
+
+
+def test_pool_step_bf16_storage():
+    q, k, v, g, pool32, idx = _pool_case(N=4, H=2, dk=6, dv=5, P=6, seed=43, pad=(0,))
+    pool = pool32.to(torch.bfloat16)
+    o, new = oracle.recurrent_step_indexed(q, k, v, g, 0.5, pool, idx, storage="bf16")
+    o_ref, S_ref = _pool_step_numpy(q, k, v, g, 0.5, pool.float(), idx)
+    # o reads the updated state before rounding
+    np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12)
+    # stored values are bfloat16 numbers within half a unit in the last place of the state
+    assert np.array_equal(torch.from_numpy(new).to(torch.bfloat16).double().numpy(), new)
+    live = [int(i) for i in idx if i >= 0]
+    err = np.abs(new[live] - S_ref[live])
+    assert np.all(err <= np.abs(S_ref[live]) * 2.0 ** -8)
+    # the slot of the padding row is untouched
+    pad_slot = [i for i in range(6) if i not in live]
+    np.testing.assert_array_equal(new[pad_slot], pool[pad_slot].double().numpy())
+
+
+def test_pool_step_rejects_bad_indices():
+    q, k, v, g, pool, idx = _pool_case(N=3, H=1, dk=4, dv=4, P=5, seed=44)
+    with pytest.raises(ValueError):
+        oracle.recurrent_step_indexed(q, k, v, g, 0.5, pool, torch.tensor([0, 5, 1], dtype=torch.int32))
+    with pytest.raises(ValueError):
+        oracle.recurrent_step_indexed(q, k, v, g, 0.5, pool, torch.tensor([2, 2, 1], dtype=torch.int32))

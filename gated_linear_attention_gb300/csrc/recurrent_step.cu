@@ -17,8 +17,6 @@
 // before any arithmetic (64 KB in flight per CTA), with the streaming cache hint since the
 // state is touched exactly once per step. The q S reduction over rows is split: each thread
 // accumulates its 16 rows, then the 8 warp partials are summed through shared memory.
-#include <type_traits>
-
 #include "launch.h"
 
 namespace sala {
@@ -36,32 +34,16 @@ struct StateRef {
     int H;
 };
 
-// kBf16: states stored as bf16 (4 columns of a row per lane = 8 bytes), else fp32 (16 bytes).
-template <bool kBf16>
-__device__ __forceinline__ float4 load_state4(const void *row, int lane) {
-    if constexpr (kBf16) {
-        const uint2 w = __ldcs(reinterpret_cast<const uint2 *>(row) + lane);
-        const float2 a = bf16x2_to_float2(w.x), b = bf16x2_to_float2(w.y);
-        return make_float4(a.x, a.y, b.x, b.y);
-    } else {
-        return __ldcs(reinterpret_cast<const float4 *>(row) + lane);
-    }
-}
-
-template <bool kBf16>
-__device__ __forceinline__ void store_state4(void *row, int lane, float4 x) {
-    if constexpr (kBf16)
-        __stcs(reinterpret_cast<uint2 *>(row) + lane, make_uint2(float2_to_bf16x2(x.x, x.y), float2_to_bf16x2(x.z, x.w)));
-    else
-        __stcs(reinterpret_cast<float4 *>(row) + lane, x);
-}
-
+// One CTA per (sequence, head): the state S [128 x 128] is streamed in once, updated and
+// streamed back out. fp32 storage: warp w owns rows [16w, 16w + 16) and lane l the 4 columns
+// [4l, 4l + 4) of each (one 512-byte row per warp instruction). bf16 storage: the same rows,
+// two per warp instruction, lane l holding the 8 columns [8 (l % 16), + 8) of row
+// 2i + l / 16 (16-byte accesses, 512 bytes per warp instruction as well).
 template <bool kBf16>
 __global__ void __launch_bounds__(kDecodeThreads)
 recurrent_step_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
                       const uint16_t *__restrict__ v, const float *__restrict__ g, float scale,
                       StateRef ref, uint16_t *__restrict__ o, int *status) {
-    using StateT = typename std::conditional<kBf16, uint16_t, float>::type;
     const int unit = blockIdx.x;  // n * H + h
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t vec = static_cast<size_t>(unit) * kD;
@@ -77,44 +59,96 @@ recurrent_step_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict
         }
         slot_unit = static_cast<size_t>(slot) * ref.H + h;
     }
-    StateT *Su = static_cast<StateT *>(ref.base) + slot_unit * kD * kD;
     const int row0 = warp * kRowsPerWarp;
-
-    // 1. stream the state rows in (issued first: nothing depends on them yet)
-    float4 s[kRowsPerWarp];
-#pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) s[r] = load_state4<kBf16>(Su + (row0 + r) * kD, lane);
-
-    // 2. the token's q, k (for my rows) and v (for my columns)
     __shared__ float q_s[kD], k_s[kD];
     __shared__ float part[kDecodeThreads / 32][kD];
-    if (threadIdx.x < kD) {
-        q_s[threadIdx.x] = bf16_bits_to_float(q[vec + threadIdx.x]);
-        k_s[threadIdx.x] = bf16_bits_to_float(k[vec + threadIdx.x]);
-    }
-    const uint2 vw = *reinterpret_cast<const uint2 *>(v + vec + 4 * lane);
-    const float2 v01 = bf16x2_to_float2(vw.x), v23 = bf16x2_to_float2(vw.y);
-    const float alpha = expf(g[unit]);
-    __syncthreads();
 
-    // 3. decay + rank-1 update, store back, and accumulate q S for my 4 columns (from the
-    //    updated state before any storage rounding)
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (kBf16) {
+        uint16_t *Su = static_cast<uint16_t *>(ref.base) + slot_unit * kD * kD;
+        const int half = lane >> 4, c0 = 8 * (lane & 15);
+        // 1. stream the state rows in (8 x 16 bytes per thread)
+        uint4 s[kRowsPerWarp / 2];
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-        const float ki = k_s[row0 + r], qi = q_s[row0 + r];
-        float4 x = s[r];
-        x.x = fmaf(alpha, x.x, ki * v01.x);
-        x.y = fmaf(alpha, x.y, ki * v01.y);
-        x.z = fmaf(alpha, x.z, ki * v23.x);
-        x.w = fmaf(alpha, x.w, ki * v23.y);
-        store_state4<kBf16>(Su + (row0 + r) * kD, lane, x);
-        acc.x = fmaf(qi, x.x, acc.x);
-        acc.y = fmaf(qi, x.y, acc.y);
-        acc.z = fmaf(qi, x.z, acc.z);
-        acc.w = fmaf(qi, x.w, acc.w);
+        for (int i = 0; i < kRowsPerWarp / 2; ++i)
+            s[i] = __ldcs(reinterpret_cast<const uint4 *>(Su + (row0 + 2 * i + half) * kD + c0));
+        // 2. q, k (rows) and v (my 8 columns)
+        if (threadIdx.x < kD) {
+            q_s[threadIdx.x] = bf16_bits_to_float(q[vec + threadIdx.x]);
+            k_s[threadIdx.x] = bf16_bits_to_float(k[vec + threadIdx.x]);
+        }
+        const uint4 vw = *reinterpret_cast<const uint4 *>(v + vec + c0);
+        float vf[8];
+        {
+            const uint32_t w4[4] = {vw.x, vw.y, vw.z, vw.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float2 f = bf16x2_to_float2(w4[m]);
+                vf[2 * m] = f.x;
+                vf[2 * m + 1] = f.y;
+            }
+        }
+        const float alpha = expf(g[unit]);
+        __syncthreads();
+        // 3. decay + rank-1 update, store back rounded to bf16, q S from the unrounded values
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp / 2; ++i) {
+            const int r = row0 + 2 * i + half;
+            const float ki = k_s[r], qi = q_s[r];
+            const uint32_t w4[4] = {s[i].x, s[i].y, s[i].z, s[i].w};
+            uint32_t out[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float2 f = bf16x2_to_float2(w4[m]);
+                const float x0 = fmaf(alpha, f.x, ki * vf[2 * m]);
+                const float x1 = fmaf(alpha, f.y, ki * vf[2 * m + 1]);
+                acc[2 * m] = fmaf(qi, x0, acc[2 * m]);
+                acc[2 * m + 1] = fmaf(qi, x1, acc[2 * m + 1]);
+                out[m] = float2_to_bf16x2(x0, x1);
+            }
+            __stcs(reinterpret_cast<uint4 *>(Su + r * kD + c0), make_uint4(out[0], out[1], out[2], out[3]));
+        }
+        // the two half-warps hold the even and odd rows of the same columns
+#pragma unroll
+        for (int m = 0; m < 8; ++m) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], 16);
+        if (half == 0) {
+            *reinterpret_cast<float4 *>(&part[warp][c0]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            *reinterpret_cast<float4 *>(&part[warp][c0 + 4]) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+    } else {
+        float *Su = static_cast<float *>(ref.base) + slot_unit * kD * kD;
+        // 1. stream the state rows in (issued first: nothing depends on them yet)
+        float4 s[kRowsPerWarp];
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r)
+            s[r] = __ldcs(reinterpret_cast<const float4 *>(Su + (row0 + r) * kD) + lane);
+        // 2. the token's q, k (for my rows) and v (for my columns)
+        if (threadIdx.x < kD) {
+            q_s[threadIdx.x] = bf16_bits_to_float(q[vec + threadIdx.x]);
+            k_s[threadIdx.x] = bf16_bits_to_float(k[vec + threadIdx.x]);
+        }
+        const uint2 vw = *reinterpret_cast<const uint2 *>(v + vec + 4 * lane);
+        const float2 v01 = bf16x2_to_float2(vw.x), v23 = bf16x2_to_float2(vw.y);
+        const float alpha = expf(g[unit]);
+        __syncthreads();
+        // 3. decay + rank-1 update, store back, and accumulate q S for my 4 columns
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+            const float ki = k_s[row0 + r], qi = q_s[row0 + r];
+            float4 x = s[r];
+            x.x = fmaf(alpha, x.x, ki * v01.x);
+            x.y = fmaf(alpha, x.y, ki * v01.y);
+            x.z = fmaf(alpha, x.z, ki * v23.x);
+            x.w = fmaf(alpha, x.w, ki * v23.y);
+            __stcs(reinterpret_cast<float4 *>(Su + (row0 + r) * kD) + lane, x);
+            acc.x = fmaf(qi, x.x, acc.x);
+            acc.y = fmaf(qi, x.y, acc.y);
+            acc.z = fmaf(qi, x.z, acc.z);
+            acc.w = fmaf(qi, x.w, acc.w);
+        }
+        *reinterpret_cast<float4 *>(&part[warp][4 * lane]) = acc;
     }
-    *reinterpret_cast<float4 *>(&part[warp][4 * lane]) = acc;
     __syncthreads();
 
     // 4. o_j = scale * sum over the 8 warp partials

@@ -419,6 +419,12 @@ def run_ours(args, dist):
     else:
         launches_decode = 0
 
+    # the layer's output RMSNorm and sigmoid gate on the prefill's output shape
+    gate = None
+    if not args.no_decode:
+        gate = run_output_gate(args, dist, dev, peaks, sala_gla, inputs, T_total, w.H)
+        launches_decode += gate.pop("_launches")
+
     rows = clocks.stop()
 
     cpu = None
@@ -445,6 +451,7 @@ def run_ours(args, dist):
             "cpu_baseline": cpu,
             "clocks": summarise_clocks(rows),
             "decode": decode,
+            "output_gate": gate,
             "gpu_launches_decode": launches_decode,
         }
         print(json.dumps(line), flush=True)
@@ -544,6 +551,53 @@ def run_decode_pool(args, dist, peaks, sala_gla, inputs, wd, q, k, v, g, o, scal
                    "bytes_per_step": per_step,
                    "tokens": "the decode workload's per-step q, k, v, g"},
         "roofline": {"kernel": "recurrent_step_indexed", "bound": "hbm", "achieved": k_ach,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": k_ach / peaks["hbm_gbs"],
+                     "traffic": None, "peak_source": peaks["source"],
+                     "mean_launch_us": 1e3 * kern[0] / kern[1]},
+        "_launches": kern[1],
+    }
+
+
+def run_output_gate(args, dist, dev, peaks, sala_gla, inputs, T, H):
+    """sala_gla_output_norm_gate on [T, H * 128] (the prefill's output shape), two input sets
+    alternated (each 3 x 67 MB at T = 8192, H = 32: larger than L2 together)."""
+    import torch
+    sets = []
+    for sd in (6, 7):
+        x = inputs.make_output_gate(T, H, seed=sd)
+        sets.append((x["o"].to(dev), x["z"].to(dev), x["w"].to(dev), torch.empty_like(x["o"], device=dev)))
+    eps = 1e-6
+    for i in range(max(3, args.warmup)):
+        o, z, wt, out = sets[i % 2]
+        sala_gla.output_norm_gate(o, z, wt, eps, out=out)
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for i in range(args.steps):
+        o, z, wt, out = sets[i % 2]
+        sala_gla.output_norm_gate(o, z, wt, eps, out=out)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist.max(ev0.elapsed_time(ev1))
+    sala_gla.timing_enable(True)
+    for i in range(args.steps):
+        o, z, wt, out = sets[i % 2]
+        sala_gla.output_norm_gate(o, z, wt, eps, out=out)
+    torch.cuda.synchronize()
+    sala_gla.timing_enable(False)
+    kern = sala_gla.timing_read()["output_norm_gate"]
+    F = H * D
+    per_call = 3 * T * F * 2 + F * 2
+    k_ach = per_call / (kern[0] / kern[1] / 1e3) / 1e9
+    return {
+        "metric": "output norm+gate HBM GB/s", "value": per_call * args.steps / (ms / 1e3) / 1e9 * dist.world,
+        "unit": "GB/s", "us_per_call": 1e3 * ms / args.steps,
+        "tokens_per_s": T * args.steps / (ms / 1e3) * dist.world,
+        "config": {"workload": "output_gate", "T": T, "H": H, "features": F, "bytes_per_call": per_call,
+                   "inputs": "o ~ N(0,1), z ~ N(0,4) bf16, w = 1 + 0.1 N(0,1) bf16; two sets alternated"},
+        "roofline": {"kernel": "output_norm_gate", "bound": "hbm", "achieved": k_ach,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": k_ach / peaks["hbm_gbs"],
                      "traffic": None, "peak_source": peaks["source"],
                      "mean_launch_us": 1e3 * kern[0] / kern[1]},

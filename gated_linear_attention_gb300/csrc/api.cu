@@ -78,7 +78,7 @@ std::atomic<uint32_t> g_epoch{0};
 
 // ---- timing instrumentation -------------------------------------------------------------
 const char *const kKernelNames[kKernelCount] = {"seg_table", "prefill_fused", "recurrent_step",
-                                                "recurrent_step_indexed"};
+                                                "recurrent_step_indexed", "output_norm_gate"};
 struct TimingRecord {
     int id;
     cudaEvent_t start, stop;
@@ -274,6 +274,25 @@ int sala_gla_recurrent_step_indexed(const void *q, const void *k, const void *v,
     if (launch_recurrent_step_indexed(q, k, v, g, scale, state_pool, state_dtype == SALA_STATE_BF16,
                                       state_indices, P, o, N, H, d->status,
                                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SALA_ERR_CUDA;
+    return SALA_OK;
+}
+
+int sala_gla_output_norm_gate(const void *o, const void *z, const void *w, float eps, void *out,
+                              int64_t T, int32_t H, void *stream) {
+    if (T < 0 || H < 1 || !(eps >= 0.f)) return SALA_ERR_INVALID_ARG;
+    if (T == 0) return SALA_OK;
+    if (T > (int64_t(1) << 31) - 1 || H > 4096) return SALA_ERR_INVALID_ARG;
+    if (!o || !z || !w || !out) return SALA_ERR_INVALID_ARG;
+    if (!aligned16(o) || !aligned16(z) || !aligned16(w) || !aligned16(out)) return SALA_ERR_MISALIGNED;
+    const size_t vec = static_cast<size_t>(T) * H * kD * 2, wb = static_cast<size_t>(H) * kD * 2;
+    // out may be o itself (in place), but may not overlap z, w or o partially
+    if (out != o && overlaps(out, vec, o, vec)) return SALA_ERR_INVALID_ARG;
+    if (overlaps(out, vec, z, vec) || overlaps(out, vec, w, wb)) return SALA_ERR_INVALID_ARG;
+    int err = SALA_OK;
+    if (!device_state(&err)) return err;
+    if (launch_output_norm_gate(o, z, w, eps, out, T, H, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
         return SALA_ERR_CUDA;
     return SALA_OK;
 }

@@ -13,6 +13,7 @@ enum KernelId {
     kKPrefillFused,
     kKRecurrentStep,
     kKRecurrentStepIndexed,
+    kKOutputNormGate,
     kKernelCount
 };
 
@@ -59,6 +60,11 @@ cudaError_t launch_prefill_fused(const ChunkArgs &a, const SegTable &t, int64_t 
                                  int64_t max_units, const float *h0, float *hT, float *incl,
                                  uint32_t *flags, uint32_t *ticket, uint32_t epoch, int grid,
                                  int *status, cudaStream_t st);
+
+// out[t] = RMSNorm(o[t]) * w * sigmoid(z[t]) over the H * 128 features of each of T tokens
+// (bf16 in and out, fp32 arithmetic); out may be o.
+cudaError_t launch_output_norm_gate(const void *o, const void *z, const void *w, float eps,
+                                    void *out, int64_t T, int H, cudaStream_t stream);
 
 // Nonzero tag of one prefill call for the hand-off flags (differs from the previous call's).
 uint32_t next_prefill_epoch();

@@ -27,7 +27,7 @@ D = 128
 BLOCK_TOKENS = 1024
 
 # stream ids
-_Q, _K, _V, _U, _H0, _SLOT = 1, 2, 3, 4, 5, 6
+_Q, _K, _V, _U, _H0, _SLOT, _Z, _W = 1, 2, 3, 4, 5, 6, 7, 8
 
 
 @dataclass(frozen=True)
@@ -257,3 +257,23 @@ def make_decode_pool(w: Workload | str = "decode_pool", *, nseq=None, H=None, po
         idx[r] = -1
     return dict(pool=S.to(torch.bfloat16) if st == "bf16" else S, indices=idx, storage=st,
                 workload=w)
+
+
+def make_output_gate(T: int = 8192, H: int = 32, seed: int = 6) -> dict:
+    """Inputs of the output norm and gate: o ~ N(0, 1) and gate logits z ~ N(0, 2^2) as bf16
+    [T, H, 128], norm weight w = 1 + 0.1 N(0, 1) as bf16 [H * 128]. The defaults are the
+    lightning layer's prefill shape (8192 tokens, 32 heads)."""
+    o = torch.empty((T, H, D), dtype=torch.bfloat16)
+    z = torch.empty_like(o)
+    nblk = (T + BLOCK_TOKENS - 1) // BLOCK_TOKENS
+
+    def one(b):
+        t0 = b * BLOCK_TOKENS
+        n = min(BLOCK_TOKENS, T - t0)
+        o[t0:t0 + n] = torch.from_numpy(_normal(seed, _Q, b, (n, H, D))).to(torch.bfloat16)
+        z[t0:t0 + n] = (2.0 * torch.from_numpy(_normal(seed, _Z, b, (n, H, D)))).to(torch.bfloat16)
+
+    with ThreadPoolExecutor(_threads()) as pool:
+        list(pool.map(one, range(nblk)))
+    w = (1.0 + 0.1 * torch.from_numpy(_normal(seed, _W, 0, (H * D,)))).to(torch.bfloat16)
+    return dict(o=o, z=z, w=w, eps=1e-6)

@@ -32,6 +32,7 @@ SIGNATURES = {
     "sala_gla_recurrent_step": ([_p, _p, _p, _p, _f32, _p, _p, _i64, _i32, _p], ctypes.c_int),
     "sala_gla_recurrent_step_indexed": ([_p, _p, _p, _p, _f32, _p, _i32, _p, _i64, _p, _i64, _i32,
                                          _p], ctypes.c_int),
+    "sala_gla_output_norm_gate": ([_p, _p, _p, _f32, _p, _i64, _i32, _p], ctypes.c_int),
     "sala_gla_chunk_fwd_noalloc": ([_p, _p, _p, _p, _f32, _p, _p, _p, _p, _i64, _i64, _i32,
                                     _i64, _p], ctypes.c_int),
     "sala_gla_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -209,6 +210,28 @@ def recurrent_step_indexed(q, k, v, g, scale, pool, indices, o=None, stream=None
                                                 _ptr(o), N, H, _stream(stream))
     _check(rc, "sala_gla_recurrent_step_indexed")
     return o
+
+
+def output_norm_gate(o, z, w, eps=1e-6, out=None, stream=None):
+    """``sala_gla_output_norm_gate``: out = RMSNorm(o) * w * sigmoid(z) per token over its
+    H * 128 features. o, z: bf16 [T, H, 128] or [T, H * 128]; w: bf16 [H * 128]. ``out=o``
+    works in place. Returns out (the shape of o)."""
+    if o.dim() not in (2, 3) or o.shape[-1] % 128 or (o.dim() == 3 and o.shape[-1] != 128):
+        raise ValueError("o must be [T, H, 128] or [T, H * 128]")
+    T = o.shape[0]
+    F = o.shape[1] * o.shape[2] if o.dim() == 3 else o.shape[1]
+    H = F // 128
+    _need(o, "o", torch.bfloat16)
+    _need(z, "z", torch.bfloat16, o.shape)
+    _need(w, "w", torch.bfloat16, (F,))
+    if out is None:
+        out = torch.empty_like(o)
+    else:
+        _need(out, "out", torch.bfloat16, o.shape)
+    rc = load().sala_gla_output_norm_gate(_ptr(o), _ptr(z), _ptr(w), float(eps), _ptr(out), T, H,
+                                          _stream(stream))
+    _check(rc, "sala_gla_output_norm_gate")
+    return out
 
 
 def get_device_status(stream=None) -> int:

@@ -149,6 +149,27 @@ int sala_gla_recurrent_step_indexed(const void *q, const void *k, const void *v,
                                     int32_t H, void *stream);
 
 /*
+ * Output norm and gate of a lightning layer, per token:
+ *     out[t] = RMSNorm(o[t]) * w * sigmoid(z[t]),   RMSNorm(x) = x / sqrt(mean(x^2) + eps)
+ * over the F = H * 128 features of the token (all heads together), fp32 arithmetic.
+ * "MiniCPM-SALA — Complete Blueprint", section "B2 lightning-attn (Simple GLA)", block
+ * "Output Norm + Gate + Projection" (o_norm with a 4096-wide weight, then the z_proj gate
+ * sigmoid(h W_z^T)); RMSNorm as the page's input_layernorm block defines it (eps = 1e-6). The
+ * gate logits z = h W_z^T are computed by the caller.
+ *
+ *   o     bf16 [T, H * 128] attention output (e.g. the o of sala_gla_chunk_fwd, [T, H, 128])
+ *   z     bf16 [T, H * 128] gate logits (before the sigmoid)
+ *   w     bf16 [H * 128] norm weight
+ *   eps   >= 0, typically 1e-6
+ *   out   bf16 [T, H * 128] (round to nearest even); may be o itself (in place), must not
+ *         overlap z, w or part of o.
+ *   T, H  T >= 0 (0 is a no-op), 1 <= H <= 4096.
+ * Errors: SALA_ERR_INVALID_ARG, SALA_ERR_MISALIGNED, SALA_ERR_UNSUPPORTED, SALA_ERR_CUDA.
+ */
+int sala_gla_output_norm_gate(const void *o, const void *z, const void *w, float eps, void *out,
+                              int64_t T, int32_t H, void *stream);
+
+/*
  * Chunked prefill that allocates nothing: same arguments, layouts, results and errors as
  * sala_gla_chunk_fwd, plus SALA_ERR_TOO_LARGE. The pages have no counterpart to this entry
  * point; it exists for callers that cannot allocate device memory while they run the layer:

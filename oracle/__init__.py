@@ -22,7 +22,8 @@ Three independent statements of the same computation:
   o_t = scale * [ sum_{j<=t} exp(G_t - G_j) (q_t . k_j) v_j + exp(G_t) q_t h0 ],
   G_t = sum_{i<=t} g_i within the sequence. For tiny inputs only.
 
-Beside them, :func:`recurrent_step_indexed` is one decode step on states gathered from and
+Beside them, :func:`output_norm_gate` is the layer's output RMSNorm and sigmoid gate, and
+:func:`recurrent_step_indexed` is one decode step on states gathered from and
 written back to a pool through slot indices (fp32 or bf16 storage), built on
 :func:`recurrent`.
 
@@ -278,6 +279,28 @@ def recurrent_step_indexed(q, k, v, g, scale, pool, indices, storage: str = "f32
         o[live] = o_live
         new[idx[live]] = round_bf16(S) if storage == "bf16" else S
     return o, new
+
+
+# ----------------------------------------------------------------------------------------
+# output norm and gate (numpy, fp64)
+
+
+def output_norm_gate(o, z, w, eps: float = 1e-6) -> np.ndarray:
+    """Per token: RMSNorm over all its features, times the weight, times sigmoid(z), fp64.
+
+    "MiniCPM-SALA — Complete Blueprint", section "B2 lightning-attn (Simple GLA)", block
+    "Output Norm + Gate + Projection": o = RMSNorm(o, w) over the 4096 features of a token,
+    then o * sigmoid(z) with z = h W_z^T; RMSNorm as the page's input_layernorm block gives
+    it: rms = sqrt(sum of squares / n + eps), x / rms, times the weight element-wise.
+
+    o, z: [T, F] (or [T, H, 128], flattened per token); w: [F]. Returns [T, F] float64.
+    """
+    od = _as_f64(o)
+    od = od.reshape(od.shape[0], -1)
+    zd = _as_f64(z).reshape(od.shape)
+    wd = _as_f64(w).reshape(-1)
+    rms = np.sqrt((od * od).sum(axis=1) / od.shape[1] + eps)
+    return od / rms[:, None] * wd[None, :] * (1.0 / (1.0 + np.exp(-zd)))
 
 
 def rel_fro(x, ref) -> float:

@@ -142,6 +142,24 @@ def test_recurrent_step_indexed_argument_errors(lib):
     assert _istep(lib, idx=0x100000 + 4096) == INVALID               # indices inside the pool
 
 
+def _gate(lib, o=0x10000, z=0x20000, w=0x30000, eps=1e-6, out=0x40000, T=2, H=2):
+    return lib.sala_gla_output_norm_gate(P(o), P(z), P(w), eps, P(out) if out else None, T, H, None)
+
+
+@no_gpu
+def test_output_norm_gate_argument_errors(lib):
+    INVALID, MISALIGNED = 1, 2
+    assert _gate(lib, T=-1) == INVALID
+    assert _gate(lib, H=0) == INVALID
+    assert _gate(lib, eps=-1.0) == INVALID
+    assert _gate(lib, T=0) == 0
+    assert _gate(lib, out=0) == INVALID
+    assert _gate(lib, z=0x20008) == MISALIGNED
+    assert _gate(lib, out=0x20000) == INVALID                 # out overlaps z
+    assert _gate(lib, out=0x10000 + 256) == INVALID           # out overlaps part of o
+    assert _gate(lib, out=0x10000) == 4                       # in place is allowed (no GPU here)
+
+
 @no_gpu
 def test_valid_arguments_without_a_gpu_report_cuda_error(lib):
     # validation passes, then the runtime finds no device: nothing is launched

@@ -371,3 +371,39 @@ def test_pool_step_rejects_bad_indices():
         oracle.recurrent_step_indexed(q, k, v, g, 0.5, pool, torch.tensor([0, 5, 1], dtype=torch.int32))
     with pytest.raises(ValueError):
         oracle.recurrent_step_indexed(q, k, v, g, 0.5, pool, torch.tensor([2, 2, 1], dtype=torch.int32))
+
+
+# ---------------------------------------------------------------------------------------
+# output norm and gate ("MiniCPM-SALA — Complete Blueprint", "Output Norm + Gate +
+# Projection": RMSNorm over the token's 4096 features with a weight, times sigmoid(z))
+
+
+def test_output_gate_matches_library_rms_norm_and_sigmoid():
+    gen = torch.Generator().manual_seed(51)
+    o = torch.randn((9, 3, 128), generator=gen, dtype=torch.float64)
+    z = 3 * torch.randn((9, 3, 128), generator=gen, dtype=torch.float64)
+    w = 1 + 0.2 * torch.randn(384, generator=gen, dtype=torch.float64)
+    got = oracle.output_norm_gate(o, z, w, eps=1e-6)
+    want = (torch.nn.functional.rms_norm(o.reshape(9, 384), (384,), w, eps=1e-6) *
+            torch.sigmoid(z.reshape(9, 384))).numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-14)
+
+
+def test_output_gate_special_cases():
+    F = 256
+    # a constant row normalises to +-1 (up to eps); z = 0 halves it; w scales per feature
+    o = np.full((1, F), 3.0)
+    w = np.linspace(0.5, 1.5, F)
+    got = oracle.output_norm_gate(o, np.zeros((1, F)), w, eps=0.0)
+    np.testing.assert_allclose(got[0], 0.5 * w, rtol=1e-15)
+    # a very open gate passes RMSNorm(o) * w through; a closed one gives zeros
+    x = np.random.default_rng(3).standard_normal((2, F))
+    rms = np.sqrt((x * x).mean(axis=1, keepdims=True))
+    np.testing.assert_allclose(oracle.output_norm_gate(x, np.full((2, F), 60.0), w, eps=0.0),
+                               x / rms * w, rtol=1e-12)
+    assert np.all(np.abs(oracle.output_norm_gate(x, np.full((2, F), -80.0), w, eps=0.0)) < 1e-32)
+    # scaling o by a > 0 changes nothing when eps = 0
+    np.testing.assert_allclose(oracle.output_norm_gate(7.5 * x, x, w, eps=0.0),
+                               oracle.output_norm_gate(x, x, w, eps=0.0), rtol=1e-13)
+    # the page's printed epsilon: a zero row stays zero
+    assert np.all(oracle.output_norm_gate(np.zeros((1, F)), x[:1], w, eps=1e-6) == 0.0)

@@ -194,8 +194,10 @@ def summarise_clocks(rows):
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of
 # each kernel as it stands, on the workload the bench times (profiles/prefill_fused_sala_layer.md,
-# profiles/recurrent_step_decode.md); retaken whenever a kernel changes.
-MEASURED_TRAFFIC = {"prefill_fused": 255_998_720, "recurrent_step": 1_023_500_000}
+# profiles/recurrent_step_decode.md, profiles/output_norm_gate.md); retaken whenever a kernel
+# changes.
+MEASURED_TRAFFIC = {"prefill_fused": 251_769_600, "recurrent_step": 1_020_000_000,
+                    "recurrent_step_indexed": 482_800_000, "output_norm_gate": 171_900_000}
 
 
 def prefill_bytes(T, H, nseq, has_h0, has_hT):
@@ -552,8 +554,9 @@ def run_decode_pool(args, dist, peaks, sala_gla, inputs, wd, q, k, v, g, o, scal
                    "tokens": "the decode workload's per-step q, k, v, g"},
         "roofline": {"kernel": "recurrent_step_indexed", "bound": "hbm", "achieved": k_ach,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": k_ach / peaks["hbm_gbs"],
-                     "traffic": None, "peak_source": peaks["source"],
-                     "mean_launch_us": 1e3 * kern[0] / kern[1]},
+                     "traffic": MEASURED_TRAFFIC["recurrent_step_indexed"]
+                     if (w.nseq, w.H, w.pool, w.storage) == (256, 32, 512, "bf16") else None,
+                     "peak_source": peaks["source"], "mean_launch_us": 1e3 * kern[0] / kern[1]},
         "_launches": kern[1],
     }
 
@@ -599,7 +602,8 @@ def run_output_gate(args, dist, dev, peaks, sala_gla, inputs, T, H):
                    "inputs": "o ~ N(0,1), z ~ N(0,4) bf16, w = 1 + 0.1 N(0,1) bf16; two sets alternated"},
         "roofline": {"kernel": "output_norm_gate", "bound": "hbm", "achieved": k_ach,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": k_ach / peaks["hbm_gbs"],
-                     "traffic": None, "peak_source": peaks["source"],
+                     "traffic": MEASURED_TRAFFIC["output_norm_gate"] if (T, H) == (8192, 32) else None,
+                     "peak_source": peaks["source"],
                      "mean_launch_us": 1e3 * kern[0] / kern[1]},
         "_launches": kern[1],
     }

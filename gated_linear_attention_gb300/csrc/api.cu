@@ -78,7 +78,8 @@ std::atomic<uint32_t> g_epoch{0};
 
 // ---- timing instrumentation -------------------------------------------------------------
 const char *const kKernelNames[kKernelCount] = {"seg_table", "prefill_fused", "recurrent_step",
-                                                "recurrent_step_indexed", "output_norm_gate"};
+                                                "recurrent_step_indexed", "output_norm_gate",
+                                                "qk_prologue"};
 struct TimingRecord {
     int id;
     cudaEvent_t start, stop;
@@ -247,10 +248,25 @@ int sala_gla_recurrent_step(const void *q, const void *k, const void *v, const f
     return SALA_OK;
 }
 
+namespace {
+// Arguments of a q/k prologue: both weights present and 16-byte aligned, eps >= 0, theta > 0.
+int check_prologue(const sala_qk_prologue *p) {
+    if (!p) return SALA_OK;
+    if (!p->q_weight || !p->k_weight || !(p->eps >= 0.f) || !(p->rope_theta > 0.f))
+        return SALA_ERR_INVALID_ARG;
+    if (!aligned16(p->q_weight) || !aligned16(p->k_weight)) return SALA_ERR_MISALIGNED;
+    return SALA_OK;
+}
+}  // namespace
+
 int sala_gla_recurrent_step_indexed(const void *q, const void *k, const void *v, const float *g,
                                     float scale, void *state_pool, int32_t state_dtype,
                                     const int32_t *state_indices, int64_t P, void *o, int64_t N,
-                                    int32_t H, void *stream) {
+                                    int32_t H, const sala_qk_prologue *prologue,
+                                    const int64_t *positions, void *stream) {
+    if (const int e = check_prologue(prologue)) return e;
+    if (prologue && !positions) return SALA_ERR_INVALID_ARG;
+    if (prologue && (reinterpret_cast<uintptr_t>(positions) & 7u)) return SALA_ERR_MISALIGNED;
     if (N < 0 || H < 1 || P < 1) return SALA_ERR_INVALID_ARG;
     if (state_dtype != SALA_STATE_F32 && state_dtype != SALA_STATE_BF16) return SALA_ERR_INVALID_ARG;
     if (N == 0) return SALA_OK;
@@ -272,8 +288,42 @@ int sala_gla_recurrent_step_indexed(const void *q, const void *k, const void *v,
     DeviceState *d = device_state(&err);
     if (!d) return err;
     if (launch_recurrent_step_indexed(q, k, v, g, scale, state_pool, state_dtype == SALA_STATE_BF16,
-                                      state_indices, P, o, N, H, d->status,
-                                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+                                      state_indices, P, o, N, H, make_qk_prologue(prologue, positions),
+                                      d->status, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SALA_ERR_CUDA;
+    return SALA_OK;
+}
+
+int sala_gla_qk_prologue(void *q, void *k, const sala_qk_prologue *prologue,
+                         const int64_t *cu_seqlens, const int64_t *start_pos, int64_t B,
+                         int64_t T, int32_t H, int64_t num_seqs, void *stream) {
+    if (!prologue) return SALA_ERR_INVALID_ARG;
+    if (const int e = check_prologue(prologue)) return e;
+    if (B < 1 || T < 0 || H < 1) return SALA_ERR_INVALID_ARG;
+    if (cu_seqlens && (B != 1 || num_seqs < 1)) return SALA_ERR_INVALID_ARG;
+    const int64_t nseq = cu_seqlens ? num_seqs : B;
+    const int64_t T_total = B * T;
+    if (T_total > (int64_t(1) << 40) / H || nseq > (int64_t(1) << 31)) return SALA_ERR_INVALID_ARG;
+    if (T_total == 0) return SALA_OK;
+    if (!q || !k) return SALA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k)) return SALA_ERR_MISALIGNED;
+    if ((cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 7u)) ||
+        (start_pos && (reinterpret_cast<uintptr_t>(start_pos) & 7u)))
+        return SALA_ERR_MISALIGNED;
+    const size_t vec = static_cast<size_t>(T_total) * H * kD * 2;
+    if (overlaps(q, vec, k, vec)) return SALA_ERR_INVALID_ARG;
+    const size_t wb = kD * 2;
+    if (overlaps(q, vec, prologue->q_weight, wb) || overlaps(q, vec, prologue->k_weight, wb) ||
+        overlaps(k, vec, prologue->q_weight, wb) || overlaps(k, vec, prologue->k_weight, wb))
+        return SALA_ERR_INVALID_ARG;
+    int err = SALA_OK;
+    if (!device_state(&err)) return err;
+    SegTable tab{};
+    tab.cu = cu_seqlens;
+    tab.T_row = T;
+    tab.nseq = nseq;
+    if (launch_qk_prologue(q, k, make_qk_prologue(prologue, nullptr), tab, start_pos, T_total, H,
+                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SALA_ERR_CUDA;
     return SALA_OK;
 }

@@ -14,6 +14,7 @@ enum KernelId {
     kKRecurrentStep,
     kKRecurrentStepIndexed,
     kKOutputNormGate,
+    kKQkPrologue,
     kKernelCount
 };
 
@@ -38,12 +39,30 @@ cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, c
                                   float scale, float *S, void *o, int64_t units,
                                   cudaStream_t stream);
 
+// The q/k prologue in kernel-argument form (qw null: none). inv_freq[i] = float(theta^(-i/64)),
+// computed on the host in double precision and rounded once.
+struct QkPrologue {
+    const uint16_t *qw = nullptr, *kw = nullptr;   // bf16 [128] RMSNorm weights
+    const int64_t *pos = nullptr;                  // decode: [N] positions
+    float eps = 0.f;
+    float inv_freq[64] = {};
+};
+QkPrologue make_qk_prologue(const sala_qk_prologue *p, const int64_t *positions);
+
 // The same step on states in a pool [P, H, 128, 128] (fp32, or bf16 if `bf16`) addressed by
-// idx[N] (negative: padding row, o = 0; >= P: SALA_ERR_BAD_INDEX recorded in `status`).
+// idx[N] (negative: padding row, o = 0; >= P: SALA_ERR_BAD_INDEX recorded in `status`), with
+// the q/k prologue fused if pro.qw is set.
 cudaError_t launch_recurrent_step_indexed(const void *q, const void *k, const void *v,
                                           const float *g, float scale, void *pool, bool bf16,
                                           const int32_t *idx, int64_t P, void *o, int64_t N,
-                                          int H, int *status, cudaStream_t stream);
+                                          int H, const QkPrologue &pro, int *status,
+                                          cudaStream_t stream);
+
+// The q/k prologue in place on a prefill's q and k ([T_total, H, 128] rows; positions from
+// the segment table's sequence bounds plus start_pos).
+cudaError_t launch_qk_prologue(void *q, void *k, const QkPrologue &pro, const SegTable &t,
+                               const int64_t *start_pos, int64_t T_total, int H,
+                               cudaStream_t stream);
 
 // Segment table from cu_seqlens (or B equal rows); also zeroes the work ticket and the
 // hand-off flags of the fused prefill, and writes hT (= h0, or zeros) of empty sequences.

@@ -39,11 +39,64 @@ struct StateRef {
 // [4l, 4l + 4) of each (one 512-byte row per warp instruction). bf16 storage: the same rows,
 // two per warp instruction, lane l holding the 8 columns [8 (l % 16), + 8) of row
 // 2i + l / 16 (16-byte accesses, 512 bytes per warp instruction as well).
+__device__ __forceinline__ float round_bf16f(float x) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// The q/k prologue on the token's q and k held in shared memory (element i by thread i < 128):
+// per-head RMSNorm with its weight, rounded to bf16, then RoPE (rotate-half pairs (i, i + 64),
+// angle float(pos) * inv_freq[i % 64] in fp32), rounded to bf16. Called by the whole CTA.
+__device__ __forceinline__ void qk_prologue_smem(float *q_s, float *k_s, const QkPrologue &pro,
+                                                 int64_t pos) {
+    __shared__ float pss[2][kD / 32];
+    const int i = threadIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float xq = 0.f, xk = 0.f;
+    if (i < kD) {
+        xq = q_s[i];
+        xk = k_s[i];
+    }
+    float sq = xq * xq, sk = xk * xk;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, off);
+        sk += __shfl_xor_sync(0xffffffffu, sk, off);
+    }
+    if (lane == 0 && warp < kD / 32) {
+        pss[0][warp] = sq;
+        pss[1][warp] = sk;
+    }
+    __syncthreads();
+    float yq = 0.f, yk = 0.f;
+    if (i < kD) {
+        const float rq = 1.f / sqrtf((pss[0][0] + pss[0][1] + pss[0][2] + pss[0][3]) / kD + pro.eps);
+        const float rk = 1.f / sqrtf((pss[1][0] + pss[1][1] + pss[1][2] + pss[1][3]) / kD + pro.eps);
+        yq = round_bf16f(xq * rq * bf16_bits_to_float(pro.qw[i]));
+        yk = round_bf16f(xk * rk * bf16_bits_to_float(pro.kw[i]));
+        q_s[i] = yq;
+        k_s[i] = yk;
+    }
+    __syncthreads();
+    float oq = 0.f, ok = 0.f;
+    if (i < kD) {
+        const float a = static_cast<float>(pos) * pro.inv_freq[i & 63];
+        float sn, cs;
+        sincosf(a, &sn, &cs);
+        const float pq = q_s[i ^ 64], pk = k_s[i ^ 64];
+        oq = round_bf16f(i < 64 ? yq * cs - pq * sn : yq * cs + pq * sn);
+        ok = round_bf16f(i < 64 ? yk * cs - pk * sn : yk * cs + pk * sn);
+    }
+    __syncthreads();
+    if (i < kD) {
+        q_s[i] = oq;
+        k_s[i] = ok;
+    }
+}
+
 template <bool kBf16>
 __global__ void __launch_bounds__(kDecodeThreads)
 recurrent_step_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
                       const uint16_t *__restrict__ v, const float *__restrict__ g, float scale,
-                      StateRef ref, uint16_t *__restrict__ o, int *status) {
+                      StateRef ref, uint16_t *__restrict__ o, int *status, QkPrologue pro) {
     const int unit = blockIdx.x;  // n * H + h
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t vec = static_cast<size_t>(unit) * kD;
@@ -88,6 +141,7 @@ recurrent_step_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict
             }
         }
         const float alpha = expf(g[unit]);
+        if (pro.qw) qk_prologue_smem(q_s, k_s, pro, pro.pos[unit / ref.H]);
         __syncthreads();
         // 3. decay + rank-1 update, store back rounded to bf16, q S from the unrounded values
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -130,6 +184,7 @@ recurrent_step_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict
         const uint2 vw = *reinterpret_cast<const uint2 *>(v + vec + 4 * lane);
         const float2 v01 = bf16x2_to_float2(vw.x), v23 = bf16x2_to_float2(vw.y);
         const float alpha = expf(g[unit]);
+        if (pro.qw) qk_prologue_smem(q_s, k_s, pro, pro.pos[unit / ref.H]);
         __syncthreads();
         // 3. decay + rank-1 update, store back, and accumulate q S for my 4 columns
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -172,14 +227,15 @@ cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, c
     recurrent_step_kernel<false><<<static_cast<unsigned>(units), kDecodeThreads, 0, stream>>>(
         static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k),
         static_cast<const uint16_t *>(v), g, scale, StateRef{S, nullptr, 0, 1},
-        static_cast<uint16_t *>(o), nullptr);
+        static_cast<uint16_t *>(o), nullptr, QkPrologue{});
     return cudaGetLastError();
 }
 
 cudaError_t launch_recurrent_step_indexed(const void *q, const void *k, const void *v,
                                           const float *g, float scale, void *pool, bool bf16,
                                           const int32_t *idx, int64_t P, void *o, int64_t N,
-                                          int H, int *status, cudaStream_t stream) {
+                                          int H, const QkPrologue &pro, int *status,
+                                          cudaStream_t stream) {
     if (N == 0) return cudaSuccess;
     LaunchTimer timer(kKRecurrentStepIndexed, stream);
     const unsigned blocks = static_cast<unsigned>(N * H);
@@ -188,9 +244,9 @@ cudaError_t launch_recurrent_step_indexed(const void *q, const void *k, const vo
                *vb = static_cast<const uint16_t *>(v);
     auto *ob = static_cast<uint16_t *>(o);
     if (bf16)
-        recurrent_step_kernel<true><<<blocks, kDecodeThreads, 0, stream>>>(qb, kb, vb, g, scale, ref, ob, status);
+        recurrent_step_kernel<true><<<blocks, kDecodeThreads, 0, stream>>>(qb, kb, vb, g, scale, ref, ob, status, pro);
     else
-        recurrent_step_kernel<false><<<blocks, kDecodeThreads, 0, stream>>>(qb, kb, vb, g, scale, ref, ob, status);
+        recurrent_step_kernel<false><<<blocks, kDecodeThreads, 0, stream>>>(qb, kb, vb, g, scale, ref, ob, status, pro);
     return cudaGetLastError();
 }
 

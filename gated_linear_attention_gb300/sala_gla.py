@@ -24,14 +24,23 @@ STATUS_NAMES = {
 }
 SALA_STATE_F32, SALA_STATE_BF16 = 0, 1
 
+class QkPrologue(ctypes.Structure):
+    """``sala_qk_prologue``: RMSNorm weights of q and k (bf16 [128] device pointers), eps,
+    RoPE theta."""
+    _fields_ = [("q_weight", ctypes.c_void_p), ("k_weight", ctypes.c_void_p),
+                ("eps", ctypes.c_float), ("rope_theta", ctypes.c_float)]
+
+
 # exported symbols and their ctypes signatures (must match include/sala_gla.h)
 _p, _i64, _i32, _f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+_pro = ctypes.POINTER(QkPrologue)
 SIGNATURES = {
     "sala_gla_chunk_fwd": ([_p, _p, _p, _p, _f32, _p, _p, _p, _p, _i64, _i64, _i32, _i64, _p],
                            ctypes.c_int),
     "sala_gla_recurrent_step": ([_p, _p, _p, _p, _f32, _p, _p, _i64, _i32, _p], ctypes.c_int),
     "sala_gla_recurrent_step_indexed": ([_p, _p, _p, _p, _f32, _p, _i32, _p, _i64, _p, _i64, _i32,
-                                         _p], ctypes.c_int),
+                                         _pro, _p, _p], ctypes.c_int),
+    "sala_gla_qk_prologue": ([_p, _p, _pro, _p, _p, _i64, _i64, _i32, _i64, _p], ctypes.c_int),
     "sala_gla_output_norm_gate": ([_p, _p, _p, _f32, _p, _i64, _i32, _p], ctypes.c_int),
     "sala_gla_chunk_fwd_noalloc": ([_p, _p, _p, _p, _f32, _p, _p, _p, _p, _i64, _i64, _i32,
                                     _i64, _p], ctypes.c_int),
@@ -182,11 +191,20 @@ def recurrent_step(q, k, v, g, scale, S, o=None, stream=None):
     return o
 
 
-def recurrent_step_indexed(q, k, v, g, scale, pool, indices, o=None, stream=None):
+def _prologue(q_weight, k_weight, eps, rope_theta):
+    _need(q_weight, "q_weight", torch.bfloat16, (128,))
+    _need(k_weight, "k_weight", torch.bfloat16, (128,))
+    return QkPrologue(_ptr(q_weight), _ptr(k_weight), float(eps), float(rope_theta))
+
+
+def recurrent_step_indexed(q, k, v, g, scale, pool, indices, o=None, stream=None, prologue=None,
+                           positions=None):
     """One decode step on pooled states, ``sala_gla_recurrent_step_indexed``: row n uses (and
     updates in place) ``pool[indices[n]]``; a negative index is a padding row (o = 0).
     q, k, v: bf16 [N, H, 128]; g: fp32 [N, H]; pool: fp32 or bf16 [P, H, 128, 128] (its dtype
-    is the storage type); indices: int32 [N]. Returns o (bf16 [N, H, 128])."""
+    is the storage type); indices: int32 [N]. ``prologue=(q_weight, k_weight, eps, theta)``
+    applies the q/k RMSNorm and RoPE to the raw q, k in the kernel, with ``positions`` int64
+    [N]. Returns o (bf16 [N, H, 128])."""
     N, H, D = q.shape
     if D != 128:
         raise ValueError("head dimension must be 128")
@@ -205,11 +223,50 @@ def recurrent_step_indexed(q, k, v, g, scale, pool, indices, o=None, stream=None
     else:
         _need(o, "o", torch.bfloat16, q.shape)
     dt = SALA_STATE_BF16 if pool.dtype == torch.bfloat16 else SALA_STATE_F32
+    pro = None
+    if prologue is not None:
+        pro = ctypes.byref(_prologue(*prologue))
+        _need(positions, "positions", torch.int64, (N,))
     rc = load().sala_gla_recurrent_step_indexed(_ptr(q), _ptr(k), _ptr(v), _ptr(g), float(scale),
                                                 _ptr(pool), dt, _ptr(indices), pool.shape[0],
-                                                _ptr(o), N, H, _stream(stream))
+                                                _ptr(o), N, H, pro,
+                                                _ptr(positions) if prologue is not None else None,
+                                                _stream(stream))
     _check(rc, "sala_gla_recurrent_step_indexed")
     return o
+
+
+def qk_prologue(q, k, q_weight, k_weight, eps=1e-6, rope_theta=10000.0, cu_seqlens=None,
+                start_pos=None, stream=None):
+    """``sala_gla_qk_prologue``: the q/k RMSNorm and RoPE, in place on a prefill's q and k
+    (bf16 [B, T, H, 128], or packed [T, H, 128] with ``cu_seqlens``). ``start_pos`` int64
+    [Nseq]: position of each sequence's first token (default 0)."""
+    if q.dim() == 4:
+        Bn, T, H, D = q.shape
+        nseq = Bn
+    elif q.dim() == 3:
+        if cu_seqlens is None:
+            raise ValueError("packed q needs cu_seqlens")
+        Bn, (T, H, D) = 1, q.shape
+        nseq = cu_seqlens.numel() - 1
+    else:
+        raise ValueError("q must be [B, T, H, 128] or [T, H, 128]")
+    if D != 128:
+        raise ValueError("head dimension must be 128")
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16, q.shape)
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int64, (nseq + 1,))
+    if start_pos is not None:
+        _need(start_pos, "start_pos", torch.int64, (nseq,))
+    pro = _prologue(q_weight, k_weight, eps, rope_theta)
+    rc = load().sala_gla_qk_prologue(_ptr(q), _ptr(k), ctypes.byref(pro),
+                                     _ptr(cu_seqlens) if cu_seqlens is not None else None,
+                                     _ptr(start_pos) if start_pos is not None else None,
+                                     Bn, T, H, nseq if cu_seqlens is not None else 0,
+                                     _stream(stream))
+    _check(rc, "sala_gla_qk_prologue")
+    return q, k
 
 
 def output_norm_gate(o, z, w, eps=1e-6, out=None, stream=None):

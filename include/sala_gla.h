@@ -53,6 +53,23 @@ typedef enum {
     SALA_ERR_BAD_INDEX = 8    /* device-detected: a state index at or past the pool size */
 } sala_status;
 
+/*
+ * The q/k prologue of a lightning layer ("MiniCPM-SALA — Complete Blueprint", section "B2
+ * lightning-attn (Simple GLA)": per-head QK RMSNorm with a 128-wide weight, then RoPE with
+ * theta = 10000 computed in fp32 and rounded to bf16). For each head vector x of q (or k):
+ *     y = bf16( x / sqrt(mean(x^2) + eps) * weight )
+ *     for i < 64, with a = float(pos) * inv_freq[i], inv_freq[i] = float(theta^(-i/64)):
+ *         out[i]      = bf16( y[i] cos a - y[i + 64] sin a )
+ *         out[i + 64] = bf16( y[i + 64] cos a + y[i] sin a )
+ * (the rotate-half pairing (i, i + 64); pos is the token's position in its sequence).
+ */
+typedef struct {
+    const void *q_weight; /* bf16 [128] RMSNorm weight of q (shared by all heads) */
+    const void *k_weight; /* bf16 [128] RMSNorm weight of k */
+    float eps;            /* RMSNorm epsilon, e.g. 1e-6 */
+    float rope_theta;     /* RoPE base, e.g. 10000 */
+} sala_qk_prologue;
+
 /* Storage type of the states in a state pool (sala_gla_recurrent_step_indexed). The
  * arithmetic is fp32 either way. */
 typedef enum {
@@ -140,13 +157,37 @@ int sala_gla_recurrent_step(const void *q, const void *k, const void *v, const f
  *                  status word and its row is treated as padding.
  *   o              bf16 [N, H, 128] output.
  *   P, N, H        P >= 1, N >= 0 (0 is a no-op), H >= 1.
+ *   prologue       NULL: q and k are used as given. Otherwise q and k are the raw
+ *                  projections and the step first applies the q/k prologue (RMSNorm, RoPE;
+ *                  see sala_qk_prologue) to them, fused into the same kernel; q and k
+ *                  themselves are not modified.
+ *   positions      int64 [N] DEVICE array, the position of each row's token in its sequence
+ *                  (required with a prologue, ignored without).
  * Errors: SALA_ERR_INVALID_ARG (also for an unknown state_dtype or a pool that overlaps
  * another argument), SALA_ERR_MISALIGNED, SALA_ERR_UNSUPPORTED, SALA_ERR_CUDA.
  */
 int sala_gla_recurrent_step_indexed(const void *q, const void *k, const void *v, const float *g,
                                     float scale, void *state_pool, int32_t state_dtype,
                                     const int32_t *state_indices, int64_t P, void *o, int64_t N,
-                                    int32_t H, void *stream);
+                                    int32_t H, const sala_qk_prologue *prologue,
+                                    const int64_t *positions, void *stream);
+
+/*
+ * The q/k prologue (see sala_qk_prologue) in place on the q and k of a prefill, before
+ * sala_gla_chunk_fwd. A separate pass: the chunked prefill loads its q and k tiles straight
+ * into shared memory by TMA, so the prologue is not applied on that load.
+ *
+ *   q, k         bf16 [B, T, H, 128] (packed [T, H, 128] with cu_seqlens), rewritten in place.
+ *   cu_seqlens   int64 [num_seqs + 1] DEVICE array as for sala_gla_chunk_fwd, or NULL (B rows
+ *                of T tokens).
+ *   start_pos    int64 [Nseq] DEVICE array, the position of each sequence's first token here
+ *                (a continued sequence), or NULL for 0. A token's position is start_pos[n]
+ *                plus its index in sequence n.
+ * Errors: SALA_ERR_INVALID_ARG, SALA_ERR_MISALIGNED, SALA_ERR_UNSUPPORTED, SALA_ERR_CUDA.
+ */
+int sala_gla_qk_prologue(void *q, void *k, const sala_qk_prologue *prologue,
+                         const int64_t *cu_seqlens, const int64_t *start_pos, int64_t B,
+                         int64_t T, int32_t H, int64_t num_seqs, void *stream);
 
 /*
  * Output norm and gate of a lightning layer, per token:

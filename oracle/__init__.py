@@ -22,7 +22,8 @@ Three independent statements of the same computation:
   o_t = scale * [ sum_{j<=t} exp(G_t - G_j) (q_t . k_j) v_j + exp(G_t) q_t h0 ],
   G_t = sum_{i<=t} g_i within the sequence. For tiny inputs only.
 
-Beside them, :func:`output_norm_gate` is the layer's output RMSNorm and sigmoid gate, and
+Beside them, :func:`qk_prologue` is the layer's per-head q/k RMSNorm and RoPE,
+:func:`output_norm_gate` is the layer's output RMSNorm and sigmoid gate, and
 :func:`recurrent_step_indexed` is one decode step on states gathered from and
 written back to a pool through slot indices (fp32 or bf16 storage), built on
 :func:`recurrent`.
@@ -279,6 +280,40 @@ def recurrent_step_indexed(q, k, v, g, scale, pool, indices, storage: str = "f32
         o[live] = o_live
         new[idx[live]] = round_bf16(S) if storage == "bf16" else S
     return o, new
+
+
+# ----------------------------------------------------------------------------------------
+# q/k prologue: per-head RMSNorm and RoPE (numpy)
+
+
+def rope_inv_freq(theta: float = 10000.0, d: int = 128) -> np.ndarray:
+    """inv_freq[i] = theta^(-2i/d) for i < d/2, rounded to float32 (the RoPE of the Blueprint is
+    computed on float32 values: "RoPE(q.float(), k.float(), pos)")."""
+    return (theta ** (-np.arange(d // 2, dtype=np.float64) * 2.0 / d)).astype(np.float32)
+
+
+def qk_prologue(x, w, pos, eps: float = 1e-6, theta: float = 10000.0) -> np.ndarray:
+    """The q/k prologue of a lightning layer on head vectors x [..., 128].
+
+    "MiniCPM-SALA — Complete Blueprint", section "B2 lightning-attn (Simple GLA)": q =
+    RMSNorm(q, w = [128]) per head (the page's RMSNorm: x / sqrt(mean(x^2) + eps) times the
+    weight), in the model's bf16; then q = RoPE(q.float(), pos).bf16() with theta = 10000. The
+    rotation pairs element i with i + 64 (rotate-half) by the angle pos * inv_freq[i]; the
+    angle is the float32 product of float32 values, as a float32 RoPE computes it, and the
+    rest is float64. x: bf16/float values [..., 128]; w: [128]; pos: integer positions,
+    broadcast against x's leading shape. Returns float64 values that are bfloat16 numbers.
+    """
+    xd = _as_f64(x)
+    wd = _as_f64(w).reshape(-1)
+    d = xd.shape[-1]
+    rms = np.sqrt((xd * xd).sum(axis=-1, keepdims=True) / d + eps)
+    y = round_bf16(xd / rms * wd)
+    pos32 = np.asarray(pos, dtype=np.float32)[..., None]
+    ang = (pos32 * rope_inv_freq(theta, d)).astype(np.float64)      # float32 product
+    c, s = np.cos(ang), np.sin(ang)
+    h = d // 2
+    lo, hi = y[..., :h], y[..., h:]
+    return round_bf16(np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1))
 
 
 # ----------------------------------------------------------------------------------------

@@ -118,9 +118,45 @@ def test_recurrent_step_argument_errors(lib):
 
 
 def _istep(lib, q=0x10000, k=0x20000, v=0x30000, g=0x40000, pool=0x100000, dt=0, idx=0x48000,
-           Pn=4, o=0x50000, N=2, H=2):
+           Pn=4, o=0x50000, N=2, H=2, pro=None, pos=None):
     return lib.sala_gla_recurrent_step_indexed(P(q), P(k), P(v), P(g), 0.1, P(pool), dt,
-                                               P(idx) if idx else None, Pn, P(o), N, H, None)
+                                               P(idx) if idx else None, Pn, P(o), N, H,
+                                               ctypes.byref(pro) if pro is not None else None,
+                                               P(pos) if pos else None, None)
+
+
+def _pro(qw=0x60000, kw=0x60100, eps=1e-6, theta=10000.0):
+    from gated_linear_attention_gb300 import sala_gla
+    return sala_gla.QkPrologue(qw, kw, eps, theta)
+
+
+def _qkp(lib, q=0x10000, k=0x20000, pro=None, cu=None, sp=None, Bn=1, T=64, H=2, nseq=0):
+    pro = pro if pro is not None else _pro()
+    return lib.sala_gla_qk_prologue(P(q), P(k), ctypes.byref(pro), P(cu) if cu else None,
+                                    P(sp) if sp else None, Bn, T, H, nseq, None)
+
+
+@no_gpu
+def test_qk_prologue_argument_errors(lib):
+    INVALID, MISALIGNED = 1, 2
+    assert lib.sala_gla_qk_prologue(P(0x10000), P(0x20000), None, None, None, 1, 64, 2, 0, None) == INVALID
+    assert _qkp(lib, pro=_pro(qw=0)) == INVALID
+    assert _qkp(lib, pro=_pro(eps=-1.0)) == INVALID
+    assert _qkp(lib, pro=_pro(theta=0.0)) == INVALID
+    assert _qkp(lib, pro=_pro(kw=0x60108)) == MISALIGNED
+    assert _qkp(lib, Bn=0) == INVALID
+    assert _qkp(lib, cu=0x70000, nseq=0) == INVALID
+    assert _qkp(lib, q=0x10008) == MISALIGNED
+    assert _qkp(lib, sp=0x70004) == MISALIGNED
+    assert _qkp(lib, k=0x10000 + 1024) == INVALID                      # k overlaps q
+    assert _qkp(lib, pro=_pro(qw=0x20000 + 256)) == INVALID           # weight inside k
+    assert _qkp(lib, T=0) == 0
+    assert _qkp(lib) == 4                                              # no GPU here
+    # the decode step with a prologue needs positions
+    assert _istep(lib, pro=_pro()) == INVALID
+    assert _istep(lib, pro=_pro(), pos=0x70004) == MISALIGNED
+    assert _istep(lib, pro=_pro(theta=-1.0), pos=0x70000) == INVALID
+    assert _istep(lib, pro=_pro(), pos=0x70000) == 4
 
 
 @no_gpu

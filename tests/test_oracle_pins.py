@@ -407,3 +407,56 @@ def test_output_gate_special_cases():
                                oracle.output_norm_gate(x, x, w, eps=0.0), rtol=1e-13)
     # the page's printed epsilon: a zero row stays zero
     assert np.all(oracle.output_norm_gate(np.zeros((1, F)), x[:1], w, eps=1e-6) == 0.0)
+
+
+# ---------------------------------------------------------------------------------------
+# q/k prologue ("MiniCPM-SALA — Complete Blueprint", B2: QK RMSNorm per head with w = [128],
+# then RoPE with theta = 10000 on float32 values, rounded to bf16)
+
+
+def test_prologue_at_position_zero_is_rms_norm():
+    gen = torch.Generator().manual_seed(61)
+    x = torch.randn((5, 3, 128), generator=gen).to(torch.bfloat16)
+    w = (1 + 0.1 * torch.randn(128, generator=gen)).to(torch.bfloat16)
+    got = oracle.qk_prologue(x, w, np.zeros((5, 1)), eps=1e-6)
+    want = torch.nn.functional.rms_norm(x.double(), (128,), w.double(), eps=1e-6).numpy()
+    np.testing.assert_array_equal(got, oracle.round_bf16(want))
+
+
+def test_prologue_rotation_closed_form():
+    # a head vector along element 0: after the norm it is sqrt(128) e_0 (w = 1); element i = 0
+    # turns with element 64 by the angle pos * theta^0 = pos
+    x = np.zeros((1, 128))
+    x[0, 0] = 3.0
+    for pos in (1, 2, 7):
+        y = oracle.qk_prologue(x, np.ones(128), np.array([pos]), eps=0.0)[0]
+        r = math.sqrt(128.0)
+        assert abs(y[0] - r * math.cos(pos)) <= r * 2 ** -8
+        assert abs(y[64] - r * math.sin(pos)) <= r * 2 ** -8
+        assert np.all(y[1:64] == 0) and np.all(y[65:] == 0)
+    # element i = 32 turns by pos * theta^(-1/2) = pos / 100
+    x = np.zeros((1, 128))
+    x[0, 32] = 1.0
+    y = oracle.qk_prologue(x, np.ones(128), np.array([50]), eps=0.0)[0]
+    assert abs(y[32] - math.sqrt(128) * math.cos(0.5)) <= math.sqrt(128) * 2 ** -8
+    assert abs(y[96] - math.sqrt(128) * math.sin(0.5)) <= math.sqrt(128) * 2 ** -8
+
+
+def test_prologue_rotation_invariants():
+    gen = torch.Generator().manual_seed(62)
+    q = torch.randn((1, 128), generator=gen).to(torch.bfloat16)
+    k = torch.randn((1, 128), generator=gen).to(torch.bfloat16)
+    w = np.ones(128)
+    y0 = oracle.qk_prologue(q, w, np.array([0]))[0]
+    y = oracle.qk_prologue(q, w, np.array([37]))[0]
+    # each (i, i + 64) pair keeps its length (to the bf16 rounding)
+    n0 = np.hypot(y0[:64], y0[64:])
+    n1 = np.hypot(y[:64], y[64:])
+    np.testing.assert_allclose(n1, n0, rtol=2 ** -6, atol=1e-3)
+    # q . k depends on the positions' difference only
+    dots = []
+    for m, n in ((10, 3), (17, 10), (107, 100)):
+        a = oracle.qk_prologue(q, w, np.array([m]))[0]
+        b = oracle.qk_prologue(k, w, np.array([n]))[0]
+        dots.append(a @ b)
+    assert max(dots) - min(dots) <= 0.02 * abs(dots[0]) + 0.05

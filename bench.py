@@ -421,11 +421,14 @@ def run_ours(args, dist):
     else:
         launches_decode = 0
 
-    # the layer's output RMSNorm and sigmoid gate on the prefill's output shape
-    gate = None
+    # the layer's output RMSNorm and sigmoid gate on the prefill's output shape, and its q/k
+    # prologue (RMSNorm + RoPE) on the prefill's q and k
+    gate = prologue = None
     if not args.no_decode:
         gate = run_output_gate(args, dist, dev, peaks, sala_gla, inputs, T_total, w.H)
         launches_decode += gate.pop("_launches")
+        prologue = run_qk_prologue(args, dist, dev, peaks, sala_gla, inputs, T_total, w.H)
+        launches_decode += prologue.pop("_launches")
 
     rows = clocks.stop()
 
@@ -454,6 +457,7 @@ def run_ours(args, dist):
             "clocks": summarise_clocks(rows),
             "decode": decode,
             "output_gate": gate,
+            "qk_prologue": prologue,
             "gpu_launches_decode": launches_decode,
         }
         print(json.dumps(line), flush=True)
@@ -541,12 +545,28 @@ def run_decode_pool(args, dist, peaks, sala_gla, inputs, wd, q, k, v, g, o, scal
     sala_gla.timing_enable(False)
     kern = sala_gla.timing_read()["recurrent_step_indexed"]
     assert sala_gla.get_device_status() == 0
+    # the same steps with the q/k prologue fused (RMSNorm + RoPE on the token's q and k;
+    # positions 4096 + step)
+    gen = torch.Generator().manual_seed(10)
+    qw = (1 + 0.1 * torch.randn(D, generator=gen)).to(torch.bfloat16).to(dev)
+    kw = (1 + 0.1 * torch.randn(D, generator=gen)).to(torch.bfloat16).to(dev)
+    pos = [torch.full((w.nseq,), 4096 + s, dtype=torch.int64, device=dev) for s in range(w.steps)]
+    pool.copy_(p["pool"])
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for s in range(w.steps):
+        sala_gla.recurrent_step_indexed(q[s], k[s], v[s], g[s], scale, pool, idx, o=o,
+                                        prologue=(qw, kw, 1e-6, 10000.0), positions=pos[s])
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms_pro = dist.max(ev0.elapsed_time(ev1))
     per_step = decode_pool_bytes(w.nseq, w.H, 2 if w.storage == "bf16" else 4)
     gbs = per_step * w.steps / (ms / 1e3) / 1e9 * dist.world
     k_ach = per_step / (kern[0] / kern[1] / 1e3) / 1e9
     return {
         "metric": "pooled decode HBM GB/s", "value": gbs, "unit": "GB/s",
         "ms_per_step": ms / w.steps, "tokens_per_s": w.nseq * w.steps / (ms / 1e3) * dist.world,
+        "ms_per_step_with_qk_prologue": ms_pro / w.steps,
         "config": {"workload": w.name, "N": w.nseq, "H": w.H, "d": D, "steps": w.steps,
                    "pool_slots": w.pool, "state_storage": w.storage,
                    "pool_bytes": w.pool * w.H * D * D * (2 if w.storage == "bf16" else 4),
@@ -557,6 +577,55 @@ def run_decode_pool(args, dist, peaks, sala_gla, inputs, wd, q, k, v, g, o, scal
                      "traffic": MEASURED_TRAFFIC["recurrent_step_indexed"]
                      if (w.nseq, w.H, w.pool, w.storage) == (256, 32, 512, "bf16") else None,
                      "peak_source": peaks["source"], "mean_launch_us": 1e3 * kern[0] / kern[1]},
+        "_launches": kern[1],
+    }
+
+
+def run_qk_prologue(args, dist, dev, peaks, sala_gla, inputs, T, H):
+    """sala_gla_qk_prologue in place on q and k [T, H, 128] (the prefill's shape), one sequence
+    from position 0, two input sets alternated (each 2 x 67 MB at T = 8192, H = 32). Every call
+    rewrites its inputs, which is what it is timed on (the values stay normalised)."""
+    import torch
+    sets = []
+    for sd in (8, 9):
+        x = inputs.make_qk_prologue(T, H, seed=sd)
+        sets.append((x["q"].to(dev), x["k"].to(dev), x["q_weight"].to(dev), x["k_weight"].to(dev)))
+    cu = torch.tensor([0, T], dtype=torch.int64, device=dev)
+
+    def call(i):
+        q, k, qw, kw = sets[i % 2]
+        sala_gla.qk_prologue(q, k, qw, kw, 1e-6, 10000.0, cu_seqlens=cu)
+
+    for i in range(max(3, args.warmup)):
+        call(i)
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for i in range(args.steps):
+        call(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist.max(ev0.elapsed_time(ev1))
+    sala_gla.timing_enable(True)
+    for i in range(args.steps):
+        call(i)
+    torch.cuda.synchronize()
+    sala_gla.timing_enable(False)
+    kern = sala_gla.timing_read()["qk_prologue"]
+    per_call = 2 * 2 * T * H * D * 2 + 2 * D * 2
+    k_ach = per_call / (kern[0] / kern[1] / 1e3) / 1e9
+    return {
+        "metric": "q/k prologue HBM GB/s", "value": per_call * args.steps / (ms / 1e3) / 1e9 * dist.world,
+        "unit": "GB/s", "us_per_call": 1e3 * ms / args.steps,
+        "tokens_per_s": T * args.steps / (ms / 1e3) * dist.world,
+        "config": {"workload": "qk_prologue", "T": T, "H": H, "bytes_per_call": per_call,
+                   "inputs": "raw q, k ~ 3 N(0,1) bf16, weights 1 + 0.1 N(0,1); theta 10000; in place"},
+        "roofline": {"kernel": "qk_prologue", "bound": "hbm", "achieved": k_ach,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": k_ach / peaks["hbm_gbs"],
+                     "traffic": None, "peak_source": peaks["source"],
+                     "mean_launch_us": 1e3 * kern[0] / kern[1]},
         "_launches": kern[1],
     }
 

@@ -303,7 +303,7 @@ int sala_gla_qk_prologue(void *q, void *k, const sala_qk_prologue *prologue,
     if (cu_seqlens && (B != 1 || num_seqs < 1)) return SALA_ERR_INVALID_ARG;
     const int64_t nseq = cu_seqlens ? num_seqs : B;
     const int64_t T_total = B * T;
-    if (T_total > (int64_t(1) << 40) / H || nseq > (int64_t(1) << 31)) return SALA_ERR_INVALID_ARG;
+    if (T_total > (int64_t(1) << 31) - 1 || nseq > (int64_t(1) << 31)) return SALA_ERR_INVALID_ARG;
     if (T_total == 0) return SALA_OK;
     if (!q || !k) return SALA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k)) return SALA_ERR_MISALIGNED;

@@ -6,10 +6,11 @@
 // 10000. The pairing is rotate-half: element i < 64 turns with element i + 64 by the angle
 // pos * theta^(-i/64).
 //
-// One warp per (token, head): lane l holds elements 4l .. 4l + 3 of q and of k (8-byte
-// accesses, a whole 256-byte head vector per warp instruction), the sum of squares is a warp
-// reduction, and the RoPE partner of lane l's elements sits in lane l ^ 16. A token's
-// position is its index in its sequence plus the sequence's start position. HBM-bound:
+// One CTA per token, one warp per head at a time: lane l holds elements 4l .. 4l + 3 of q and
+// of k (8-byte accesses, a whole 256-byte head vector per warp instruction), the sum of
+// squares is a warp reduction, and the RoPE partner of lane l's elements sits in lane l ^ 16.
+// The angles depend only on the token's position (its index in its sequence plus the
+// sequence's start position), so their cos/sin are computed once per token. HBM-bound:
 // 2 x 256 B read and written per (token, head).
 #include "launch.h"
 
@@ -18,64 +19,94 @@
 namespace sala {
 
 constexpr int kProThreads = 256;
+constexpr int kProWarps = kProThreads / 32;
+constexpr int kProHeadsInFlight = 4;   // heads per warp whose loads are issued together
 
 __device__ __forceinline__ float round_bf16_f(float x) {
     return __bfloat162float(__float2bfloat16_rn(x));
 }
 
+// One head vector (4 elements per lane): RMSNorm with weight w, bf16, RoPE with the lane's
+// (cos, sin), bf16. The RoPE partner of lane l's elements is in lane l ^ 16.
+__device__ __forceinline__ uint2 prologue_head(uint2 xw, const float (&wv)[4], const float (&cs)[4],
+                                               const float (&sn)[4], float eps, bool low) {
+    const float2 a01 = bf16x2_to_float2(xw.x), a23 = bf16x2_to_float2(xw.y);
+    const float xs[4] = {a01.x, a01.y, a23.x, a23.y};
+    float ss = xs[0] * xs[0] + xs[1] * xs[1] + xs[2] * xs[2] + xs[3] * xs[3];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = 1.f / sqrtf(ss / kD + eps);
+    float out[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float y = round_bf16_f(xs[e] * r * wv[e]);
+        const float py = __shfl_xor_sync(0xffffffffu, y, 16);
+        out[e] = round_bf16_f(low ? y * cs[e] - py * sn[e] : y * cs[e] + py * sn[e]);
+    }
+    return make_uint2(float2_to_bf16x2(out[0], out[1]), float2_to_bf16x2(out[2], out[3]));
+}
+
+// One CTA per token: the token's position and the 64 rotation angles are found once (lane l
+// of every warp holds the cos/sin of elements 4l .. 4l + 3), then warp w rewrites heads
+// w, w + 8, ... of q and k, loading a group of heads before working on it.
 __global__ void __launch_bounds__(kProThreads)
 qk_prologue_kernel(uint16_t *q, uint16_t *k, QkPrologue pro, SegTable t, const int64_t *start_pos,
                    int64_t T_total, int H) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t pair = static_cast<int64_t>(blockIdx.x) * (kProThreads / 32) + warp;
-    if (pair >= T_total * H) return;
-    const int64_t tok = pair / H;
+    const int64_t tok = blockIdx.x;
+    const size_t row = static_cast<size_t>(tok) * H;
+    // the first group of heads is loaded before anything else (its latency overlaps the
+    // position lookup and the angles)
+    uint2 xq[kProHeadsInFlight], xk[kProHeadsInFlight];
+    auto load_group = [&](int h0) {
+#pragma unroll
+        for (int j = 0; j < kProHeadsInFlight; ++j) {
+            const int h = h0 + j * kProWarps;
+            if (h < H) {
+                const size_t off = (row + h) * kD + 4 * lane;
+                xq[j] = *reinterpret_cast<const uint2 *>(q + off);
+                xk[j] = *reinterpret_cast<const uint2 *>(k + off);
+            }
+        }
+    };
+    load_group(warp);
     // the token's sequence: largest n with begin(n) <= tok
     int64_t n = 0;
-    if (lane == 0) {
-        if (t.cu) {
-            int64_t lo = 0, hi = t.nseq - 1;
-            while (lo < hi) {
-                const int64_t mid = (lo + hi + 1) >> 1;
-                if (t.cu[mid] <= tok) lo = mid; else hi = mid - 1;
-            }
-            n = lo;
-        } else {
-            n = tok / t.T_row;
+    if (t.cu) {
+        int64_t lo = 0, hi = t.nseq - 1;
+        while (lo < hi) {
+            const int64_t mid = (lo + hi + 1) >> 1;
+            if (t.cu[mid] <= tok) lo = mid; else hi = mid - 1;
         }
+        n = lo;
+    } else {
+        n = tok / t.T_row;
     }
-    n = __shfl_sync(0xffffffffu, n, 0);
     const int64_t pos = tok - seq_begin(t, n) + (start_pos ? start_pos[n] : 0);
-    const float ang_pos = static_cast<float>(pos);
-    const size_t off = static_cast<size_t>(pair) * kD + 4 * lane;
-    const uint2 wq = *reinterpret_cast<const uint2 *>(pro.qw + 4 * lane);
-    const uint2 wk = *reinterpret_cast<const uint2 *>(pro.kw + 4 * lane);
+    const float fpos = static_cast<float>(pos);
+    float cs[4], sn[4], wq[4], wk[4];
+    {
+        const uint2 a = *reinterpret_cast<const uint2 *>(pro.qw + 4 * lane);
+        const uint2 b = *reinterpret_cast<const uint2 *>(pro.kw + 4 * lane);
+        const float2 a0 = bf16x2_to_float2(a.x), a1 = bf16x2_to_float2(a.y);
+        const float2 b0 = bf16x2_to_float2(b.x), b1 = bf16x2_to_float2(b.y);
+        wq[0] = a0.x; wq[1] = a0.y; wq[2] = a1.x; wq[3] = a1.y;
+        wk[0] = b0.x; wk[1] = b0.y; wk[2] = b1.x; wk[3] = b1.y;
+    }
 #pragma unroll
-    for (int which = 0; which < 2; ++which) {
-        uint16_t *x = which ? k : q;
-        const uint2 ww = which ? wk : wq;
-        const uint2 xw = *reinterpret_cast<const uint2 *>(x + off);
-        const float2 a01 = bf16x2_to_float2(xw.x), a23 = bf16x2_to_float2(xw.y);
-        const float w01x = bf16x2_to_float2(ww.x).x, w01y = bf16x2_to_float2(ww.x).y;
-        const float w23x = bf16x2_to_float2(ww.y).x, w23y = bf16x2_to_float2(ww.y).y;
-        const float xs[4] = {a01.x, a01.y, a23.x, a23.y}, wv[4] = {w01x, w01y, w23x, w23y};
-        float ss = xs[0] * xs[0] + xs[1] * xs[1] + xs[2] * xs[2] + xs[3] * xs[3];
+    for (int e = 0; e < 4; ++e) sincosf(fpos * pro.inv_freq[(4 * lane + e) & 63], &sn[e], &cs[e]);
+    const bool low = lane < 16;
+    for (int h0 = warp; h0 < H; h0 += kProWarps * kProHeadsInFlight) {
+        if (h0 != warp) load_group(h0);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float r = 1.f / sqrtf(ss / kD + pro.eps);
-        float y[4], out[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) y[e] = round_bf16_f(xs[e] * r * wv[e]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float py = __shfl_xor_sync(0xffffffffu, y[e], 16);
-            const int i = 4 * lane + e;
-            float sn, cs;
-            sincosf(ang_pos * pro.inv_freq[i & 63], &sn, &cs);
-            out[e] = round_bf16_f(lane < 16 ? y[e] * cs - py * sn : y[e] * cs + py * sn);
+        for (int j = 0; j < kProHeadsInFlight; ++j) {
+            const int h = h0 + j * kProWarps;
+            if (h < H) {
+                const size_t off = (row + h) * kD + 4 * lane;
+                *reinterpret_cast<uint2 *>(q + off) = prologue_head(xq[j], wq, cs, sn, pro.eps, low);
+                *reinterpret_cast<uint2 *>(k + off) = prologue_head(xk[j], wk, cs, sn, pro.eps, low);
+            }
         }
-        *reinterpret_cast<uint2 *>(x + off) =
-            make_uint2(float2_to_bf16x2(out[0], out[1]), float2_to_bf16x2(out[2], out[3]));
     }
 }
 
@@ -96,9 +127,7 @@ cudaError_t launch_qk_prologue(void *q, void *k, const QkPrologue &pro, const Se
                                cudaStream_t stream) {
     if (T_total == 0) return cudaSuccess;
     LaunchTimer timer(kKQkPrologue, stream);
-    const int64_t pairs = T_total * H;
-    const int64_t blocks = (pairs + kProThreads / 32 - 1) / (kProThreads / 32);
-    qk_prologue_kernel<<<static_cast<unsigned>(blocks), kProThreads, 0, stream>>>(
+    qk_prologue_kernel<<<static_cast<unsigned>(T_total), kProThreads, 0, stream>>>(
         static_cast<uint16_t *>(q), static_cast<uint16_t *>(k), pro, t, start_pos, T_total, H);
     return cudaGetLastError();
 }

@@ -27,7 +27,7 @@ D = 128
 BLOCK_TOKENS = 1024
 
 # stream ids
-_Q, _K, _V, _U, _H0, _SLOT, _Z, _W = 1, 2, 3, 4, 5, 6, 7, 8
+_Q, _K, _V, _U, _H0, _SLOT, _Z, _W, _QW, _KW = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10
 
 
 @dataclass(frozen=True)
@@ -277,3 +277,24 @@ def make_output_gate(T: int = 8192, H: int = 32, seed: int = 6) -> dict:
         list(pool.map(one, range(nblk)))
     w = (1.0 + 0.1 * torch.from_numpy(_normal(seed, _W, 0, (H * D,)))).to(torch.bfloat16)
     return dict(o=o, z=z, w=w, eps=1e-6)
+
+
+def make_qk_prologue(T: int = 8192, H: int = 32, seed: int = 8) -> dict:
+    """Raw (before the prologue) q, k ~ 3 N(0, 1) as bf16 [T, H, 128] and the RMSNorm weights
+    q_weight, k_weight = 1 + 0.1 N(0, 1) as bf16 [128]; eps 1e-6, theta 10000. The defaults
+    are the lightning layer's prefill shape."""
+    q = torch.empty((T, H, D), dtype=torch.bfloat16)
+    k = torch.empty_like(q)
+    nblk = (T + BLOCK_TOKENS - 1) // BLOCK_TOKENS
+
+    def one(b):
+        t0 = b * BLOCK_TOKENS
+        n = min(BLOCK_TOKENS, T - t0)
+        q[t0:t0 + n] = (3.0 * torch.from_numpy(_normal(seed, _Q, b, (n, H, D)))).to(torch.bfloat16)
+        k[t0:t0 + n] = (3.0 * torch.from_numpy(_normal(seed, _K, b, (n, H, D)))).to(torch.bfloat16)
+
+    with ThreadPoolExecutor(_threads()) as pool:
+        list(pool.map(one, range(nblk)))
+    qw = (1.0 + 0.1 * torch.from_numpy(_normal(seed, _QW, 0, (D,)))).to(torch.bfloat16)
+    kw = (1.0 + 0.1 * torch.from_numpy(_normal(seed, _KW, 0, (D,)))).to(torch.bfloat16)
+    return dict(q=q, k=k, q_weight=qw, k_weight=kw, eps=1e-6, theta=10000.0)

@@ -418,6 +418,7 @@ def run_ours(args, dist):
         decode = run_decode(args, dist, dev, peaks, sala_gla, inputs)
         launches_decode = decode.pop("_launches")
         launches_decode += decode["pooled"].pop("_launches")
+        launches_decode += decode["gdn"].pop("_launches")
     else:
         launches_decode = 0
 
@@ -499,8 +500,10 @@ def run_decode(args, dist, dev, peaks, sala_gla, inputs):
     gbs = per_step * w.steps / (ms / 1e3) / 1e9 * dist.world
     k_ach = per_step / (kern[0] / kern[1] / 1e3) / 1e9
     pooled = run_decode_pool(args, dist, peaks, sala_gla, inputs, w, q, k, v, g, o, scale)
+    gdn = run_gdn_decode(args, dist, peaks, sala_gla, inputs, w, q, k, v, g, o, scale, S0)
     return {
         "pooled": pooled,
+        "gdn": gdn,
         "metric": "decode HBM GB/s", "value": gbs, "unit": "GB/s",
         "ms_per_step": ms / w.steps, "tokens_per_s": w.nseq * w.steps / (ms / 1e3) * dist.world,
         "config": {"workload": w.name, "N": w.nseq, "H": w.H, "d": D, "steps": w.steps,
@@ -509,6 +512,50 @@ def run_decode(args, dist, dev, peaks, sala_gla, inputs):
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": k_ach / peaks["hbm_gbs"],
                      "traffic": MEASURED_TRAFFIC["recurrent_step"] if w.nseq == 256 else None,
                      "peak_source": peaks["source"], "mean_launch_us": 1e3 * kern[0] / kern[1]},
+        "_launches": kern[1],
+    }
+
+
+def run_gdn_decode(args, dist, peaks, sala_gla, inputs, wd, q, k, v, g, o, scale, S0):
+    """The same decode steps under the gated delta rule (sala_gla_gdn_recurrent_step): the
+    decode workload's tokens and initial states, write strengths beta = sigmoid(N(0, 1)) of
+    the gdn_decode workload; the state flows step to step."""
+    import torch
+    w = inputs.WORKLOADS["gdn_decode"]
+    beta = inputs.make_gdn_beta(w, 0, wd.steps, nseq=wd.nseq, H=wd.H).to(q.device)
+    S = S0.to(q.device)
+    Sw = S.clone()
+    for s in range(max(3, args.warmup)):
+        sala_gla.gdn_recurrent_step(q[s], k[s], v[s], g[s], beta[s], scale, Sw, o=o)
+    torch.cuda.synchronize()
+    del Sw
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    sala_gla.timing_enable(True)
+    ev0.record(stream)
+    for s in range(wd.steps):
+        sala_gla.gdn_recurrent_step(q[s], k[s], v[s], g[s], beta[s], scale, S, o=o)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sala_gla.timing_enable(False)
+    kern = sala_gla.timing_read()["gdn_step"]
+    assert sala_gla.get_device_status() == 0
+    ms = dist.max(ev0.elapsed_time(ev1))
+    per_step = decode_bytes(wd.nseq, wd.H) + wd.nseq * wd.H * 4     # + beta
+    k_ach = per_step / (kern[0] / kern[1] / 1e3) / 1e9
+    return {
+        "metric": "gated-delta-rule decode HBM GB/s", "value": per_step * wd.steps / (ms / 1e3) / 1e9 * dist.world,
+        "unit": "GB/s", "ms_per_step": ms / wd.steps,
+        "tokens_per_s": wd.nseq * wd.steps / (ms / 1e3) * dist.world,
+        "config": {"workload": w.name, "N": wd.nseq, "H": wd.H, "d": D, "steps": wd.steps,
+                   "bytes_per_step": per_step,
+                   "tokens": "the decode workload's q, k, v, g and initial states; beta of gdn_decode"},
+        "roofline": {"kernel": "gdn_step", "bound": "hbm", "achieved": k_ach,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": k_ach / peaks["hbm_gbs"],
+                     "traffic": None, "peak_source": peaks["source"],
+                     "mean_launch_us": 1e3 * kern[0] / kern[1]},
         "_launches": kern[1],
     }
 

@@ -79,7 +79,7 @@ std::atomic<uint32_t> g_epoch{0};
 // ---- timing instrumentation -------------------------------------------------------------
 const char *const kKernelNames[kKernelCount] = {"seg_table", "prefill_fused", "recurrent_step",
                                                 "recurrent_step_indexed", "output_norm_gate",
-                                                "qk_prologue"};
+                                                "qk_prologue", "gdn_step"};
 struct TimingRecord {
     int id;
     cudaEvent_t start, stop;
@@ -343,6 +343,32 @@ int sala_gla_output_norm_gate(const void *o, const void *z, const void *w, float
     if (!device_state(&err)) return err;
     if (launch_output_norm_gate(o, z, w, eps, out, T, H, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
+        return SALA_ERR_CUDA;
+    return SALA_OK;
+}
+
+int sala_gla_gdn_recurrent_step(const void *q, const void *k, const void *v, const float *g,
+                                const float *beta, float scale, float *S_inout, void *o,
+                                int64_t N, int32_t H, void *stream) {
+    if (N < 0 || H < 1) return SALA_ERR_INVALID_ARG;
+    if (N == 0) return SALA_OK;
+    if (N > (int64_t(1) << 31) / H) return SALA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !g || !beta || !S_inout || !o) return SALA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
+        !aligned16(S_inout) || !aligned16(o))
+        return SALA_ERR_MISALIGNED;
+    const size_t units = static_cast<size_t>(N) * H;
+    const size_t vec = units * kD * 2, gb = units * 4, sb = units * kD * kD * 4;
+    const void *ins[5] = {q, k, v, g, beta};
+    const size_t in_sz[5] = {vec, vec, vec, gb, gb};
+    for (int i = 0; i < 5; ++i)
+        if (overlaps(S_inout, sb, ins[i], in_sz[i]) || overlaps(o, vec, ins[i], in_sz[i]))
+            return SALA_ERR_INVALID_ARG;
+    if (overlaps(S_inout, sb, o, vec)) return SALA_ERR_INVALID_ARG;
+    int err = SALA_OK;
+    if (!device_state(&err)) return err;
+    if (launch_gdn_step(q, k, v, g, beta, scale, S_inout, o, static_cast<int64_t>(units),
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SALA_ERR_CUDA;
     return SALA_OK;
 }

@@ -15,6 +15,7 @@ enum KernelId {
     kKRecurrentStepIndexed,
     kKOutputNormGate,
     kKQkPrologue,
+    kKGdnStep,
     kKernelCount
 };
 
@@ -84,6 +85,11 @@ cudaError_t launch_prefill_fused(const ChunkArgs &a, const SegTable &t, int64_t 
 // (bf16 in and out, fp32 arithmetic); out may be o.
 cudaError_t launch_output_norm_gate(const void *o, const void *z, const void *w, float eps,
                                     void *out, int64_t T, int H, cudaStream_t stream);
+
+// One gated-delta-rule step on [units] dense fp32 states (one CTA per (sequence, head)).
+cudaError_t launch_gdn_step(const void *q, const void *k, const void *v, const float *g,
+                            const float *beta, float scale, float *S, void *o, int64_t units,
+                            cudaStream_t stream);
 
 // Nonzero tag of one prefill call for the hand-off flags (differs from the previous call's).
 uint32_t next_prefill_epoch();

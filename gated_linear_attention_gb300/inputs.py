@@ -27,7 +27,7 @@ D = 128
 BLOCK_TOKENS = 1024
 
 # stream ids
-_Q, _K, _V, _U, _H0, _SLOT, _Z, _W, _QW, _KW = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10
+_Q, _K, _V, _U, _H0, _SLOT, _Z, _W, _QW, _KW, _BETA = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11
 
 
 @dataclass(frozen=True)
@@ -75,6 +75,11 @@ WORKLOADS = {
         nseq=256, steps=1000, description="batched recurrent decode: 256 sequences x 1 token, "
         "H=32; q,k L2-normalised; g=logsigmoid(u), u~U(2,6); S~N(0,0.02) [256,32,128,128] "
         "fp32 updated in place; 1000 consecutive steps"),
+    "gdn_decode": Workload(
+        "gdn_decode", "decode", H=32, seqlens=(), qk_norm="l2", gate="logsigmoid", h0=True, seed=12,
+        nseq=256, steps=1000, description="batched gated-delta-rule decode: 256 sequences x 1 "
+        "token, H=32; q,k L2-normalised; g=logsigmoid(u), u~U(2,6); beta=sigmoid(w), w~N(0,1); "
+        "S~N(0,0.02) [256,32,128,128] fp32 updated in place; 1000 consecutive steps"),
     "decode_pool": Workload(
         "decode_pool", "decode", H=32, seqlens=(), qk_norm="l2", gate="logsigmoid", h0=True,
         seed=4, nseq=256, steps=1000, pool=512, storage="bf16",
@@ -298,3 +303,17 @@ def make_qk_prologue(T: int = 8192, H: int = 32, seed: int = 8) -> dict:
     qw = (1.0 + 0.1 * torch.from_numpy(_normal(seed, _QW, 0, (D,)))).to(torch.bfloat16)
     kw = (1.0 + 0.1 * torch.from_numpy(_normal(seed, _KW, 0, (D,)))).to(torch.bfloat16)
     return dict(q=q, k=k, q_weight=qw, k_weight=kw, eps=1e-6, theta=10000.0)
+
+
+def make_gdn_beta(w: Workload | str = "gdn_decode", start: int = 0, count: int | None = None,
+                  *, nseq=None, H=None) -> torch.Tensor:
+    """Write strengths of the gated delta rule for decode steps [start, start+count):
+    beta = sigmoid(w), w ~ N(0, 1), fp32 [count, nseq, H] (stream 11, one block per step)."""
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    count = w.steps - start if count is None else count
+    n, Hh = nseq or w.nseq, H or w.H
+    b = torch.empty((count, n, Hh), dtype=torch.float32)
+    for i in range(count):
+        b[i] = torch.sigmoid(torch.from_numpy(_normal(w.seed, _BETA, start + i, (n, Hh))))
+    return b

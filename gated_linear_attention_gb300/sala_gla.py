@@ -40,6 +40,7 @@ SIGNATURES = {
     "sala_gla_recurrent_step": ([_p, _p, _p, _p, _f32, _p, _p, _i64, _i32, _p], ctypes.c_int),
     "sala_gla_recurrent_step_indexed": ([_p, _p, _p, _p, _f32, _p, _i32, _p, _i64, _p, _i64, _i32,
                                          _pro, _p, _p], ctypes.c_int),
+    "sala_gla_gdn_recurrent_step": ([_p, _p, _p, _p, _p, _f32, _p, _p, _i64, _i32, _p], ctypes.c_int),
     "sala_gla_qk_prologue": ([_p, _p, _pro, _p, _p, _i64, _i64, _i32, _i64, _p], ctypes.c_int),
     "sala_gla_output_norm_gate": ([_p, _p, _p, _f32, _p, _i64, _i32, _p], ctypes.c_int),
     "sala_gla_chunk_fwd_noalloc": ([_p, _p, _p, _p, _f32, _p, _p, _p, _p, _i64, _i64, _i32,
@@ -289,6 +290,28 @@ def output_norm_gate(o, z, w, eps=1e-6, out=None, stream=None):
                                           _stream(stream))
     _check(rc, "sala_gla_output_norm_gate")
     return out
+
+
+def gdn_recurrent_step(q, k, v, g, beta, scale, S, o=None, stream=None):
+    """One gated-delta-rule step, ``sala_gla_gdn_recurrent_step``; S [N, H, 128, 128] fp32 is
+    updated in place. q, k, v: bf16 [N, H, 128]; g, beta: fp32 [N, H]. Returns o."""
+    N, H, D = q.shape
+    if D != 128:
+        raise ValueError("head dimension must be 128")
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16, q.shape)
+    _need(v, "v", torch.bfloat16, q.shape)
+    _need(g, "g", torch.float32, (N, H))
+    _need(beta, "beta", torch.float32, (N, H))
+    _need(S, "S", torch.float32, (N, H, 128, 128))
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _need(o, "o", torch.bfloat16, q.shape)
+    rc = load().sala_gla_gdn_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                            float(scale), _ptr(S), _ptr(o), N, H, _stream(stream))
+    _check(rc, "sala_gla_gdn_recurrent_step")
+    return o
 
 
 def get_device_status(stream=None) -> int:

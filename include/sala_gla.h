@@ -211,6 +211,27 @@ int sala_gla_output_norm_gate(const void *o, const void *z, const void *w, float
                               int64_t T, int32_t H, void *stream);
 
 /*
+ * One-token recurrent step of the gated delta rule (GDN), the second linear-attention
+ * workload of "Formulas and Code for Adapting Inference to GDN/KDA Linear Modules", section
+ * 1.1. For each of the N sequences and H heads, with the [128 x 128] fp32 state S (row = key
+ * dimension):
+ *     S = exp(g) S;   v_new = beta (v - k S);   S = S + k^T v_new;   o = scale q S
+ * (the decay precedes the memory read, as the page's chunked form computes; k S is the
+ * vector over the value dimension read at key k). Normalising q and k (the page's l2norm)
+ * and forming g and beta happen before the call.
+ *
+ *   q, k, v    bf16 [N, H, 128]
+ *   g          fp32 [N, H] log-decay;  beta fp32 [N, H] write strength (typically in (0, 1))
+ *   S_inout    fp32 [N, H, 128, 128], read and overwritten. Must not overlap the inputs or o.
+ *   o          bf16 [N, H, 128] output.
+ *   N, H       N >= 0 (0 is a no-op), H >= 1.
+ * Errors: SALA_ERR_INVALID_ARG, SALA_ERR_MISALIGNED, SALA_ERR_UNSUPPORTED, SALA_ERR_CUDA.
+ */
+int sala_gla_gdn_recurrent_step(const void *q, const void *k, const void *v, const float *g,
+                                const float *beta, float scale, float *S_inout, void *o,
+                                int64_t N, int32_t H, void *stream);
+
+/*
  * Chunked prefill that allocates nothing: same arguments, layouts, results and errors as
  * sala_gla_chunk_fwd, plus SALA_ERR_TOO_LARGE. The pages have no counterpart to this entry
  * point; it exists for callers that cannot allocate device memory while they run the layer:

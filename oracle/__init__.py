@@ -22,7 +22,9 @@ Three independent statements of the same computation:
   o_t = scale * [ sum_{j<=t} exp(G_t - G_j) (q_t . k_j) v_j + exp(G_t) q_t h0 ],
   G_t = sum_{i<=t} g_i within the sequence. For tiny inputs only.
 
-Beside them, :func:`qk_prologue` is the layer's per-head q/k RMSNorm and RoPE,
+Beside them, :func:`gdn_recurrent` and :func:`gdn_chunkwise` state the gated delta rule
+(the second workload) in its two forms, :func:`qk_prologue` is the layer's per-head q/k
+RMSNorm and RoPE,
 :func:`output_norm_gate` is the layer's output RMSNorm and sigmoid gate, and
 :func:`recurrent_step_indexed` is one decode step on states gathered from and
 written back to a pool through slot indices (fp32 or bf16 storage), built on
@@ -280,6 +282,94 @@ def recurrent_step_indexed(q, k, v, g, scale, pool, indices, storage: str = "f32
         o[live] = o_live
         new[idx[live]] = round_bf16(S) if storage == "bf16" else S
     return o, new
+
+
+# ----------------------------------------------------------------------------------------
+# the gated delta rule (GDN), numpy fp64
+
+
+def gdn_recurrent(q, k, v, g, beta, scale, h0=None, cu_seqlens=None):
+    """Token-by-token gated delta rule, fp64.
+
+    "Formulas and Code for Adapting Inference to GDN/KDA Linear Modules", section 1.1: per
+    token the state decays by exp(g), the memory read at the key, kv = k S, is replaced by the
+    value: v_new = beta (v - kv), S <- S + k^T v_new, and o = scale q S. The decay is applied
+    before the memory read (the chunked form of section 1.2, whose W carries exp(g), computes
+    exactly this; see the pins). q, k: bf16 [T, H, dk] packed (with cu_seqlens) or [B, T, H,
+    dk]; v [.., dv]; g, beta fp32 [.., H]; h0 [nseq, H, dk, dv] or None. Returns (o [T, H, dv],
+    hT [nseq, H, dk, dv]) float64.
+    """
+    q, k, v, g, cu = _packed(q, k, v, g, cu_seqlens)
+    bd = _as_f64(beta).reshape(g.shape)
+    qd, kd, vd, gd = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(g)
+    T, H, dk = qd.shape
+    dv = vd.shape[-1]
+    nseq = len(cu) - 1
+    h0d = None if h0 is None else _as_f64(h0).reshape(nseq, H, dk, dv)
+    o = np.zeros((T, H, dv))
+    hT = np.zeros((nseq, H, dk, dv))
+    for n in range(nseq):
+        s, e = int(cu[n]), int(cu[n + 1])
+        for h in range(H):
+            S = np.zeros((dk, dv)) if h0d is None else h0d[n, h].copy()
+            for t in range(s, e):
+                S = np.exp(gd[t, h]) * S
+                v_new = bd[t, h] * (vd[t, h] - kd[t, h] @ S)
+                S = S + np.outer(kd[t, h], v_new)
+                o[t, h] = scale * (qd[t, h] @ S)
+            hT[n, h] = S
+    return o, hT
+
+
+def _gdn_chunk_one(q, k, v, g, beta, scale, S, C):
+    """One sequence and head in the chunked form (UT transform), fp64: q, k [L, dk], v [L, dv],
+    g, beta [L], S [dk, dv]. The steps of the GDN/KDA page's section 1.2 (formulas 11-17)."""
+    L = q.shape[0]
+    o = np.empty((L, v.shape[1]))
+    for c0 in range(0, L, C):
+        qi, ki, vi = q[c0:c0 + C], k[c0:c0 + C], v[c0:c0 + C]
+        n = qi.shape[0]
+        b = np.cumsum(g[c0:c0 + C])                         # chunk decay
+        gamma = np.exp(np.tril(b[:, None] - b[None, :]))    # masked difference, then exp
+        kb = ki * beta[c0:c0 + C, None]
+        vb = vi * beta[c0:c0 + C, None]
+        # formula 11: T = -(K_beta K^T * gamma).tril(-1), then row by row T[i, :i] += T[i, :] T[:, :i]
+        Tm = -np.tril(kb @ ki.T * gamma, -1)
+        for i in range(1, n):
+            Tm[i, :i] = Tm[i, :i] + Tm[i, :] @ Tm[:, :i]
+        Tm = Tm + np.eye(n)
+        W = Tm @ (kb * np.exp(b)[:, None])                  # formula 12
+        U = Tm @ vb                                         # formula 13
+        new_v = U - W @ S                                   # formula 15
+        o_inter = (qi * np.exp(b)[:, None]) @ S
+        o_intra = np.tril(qi @ ki.T * gamma) @ new_v
+        S = S * np.exp(b[-1]) + (ki * np.exp(b[-1] - b)[:, None]).T @ new_v   # formula 16
+        o[c0:c0 + C] = scale * (o_inter + o_intra)          # formula 17
+    return o, S
+
+
+def gdn_chunkwise(q, k, v, g, beta, scale, h0=None, cu_seqlens=None, chunk: int = 64):
+    """Chunked fp64 form of the gated delta rule; same arguments and results as
+    :func:`gdn_recurrent`."""
+    q, k, v, g, cu = _packed(q, k, v, g, cu_seqlens)
+    bd = _as_f64(beta).reshape(g.shape)
+    qd, kd, vd, gd = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(g)
+    T, H, dk = qd.shape
+    dv = vd.shape[-1]
+    nseq = len(cu) - 1
+    h0d = None if h0 is None else _as_f64(h0).reshape(nseq, H, dk, dv)
+    o = np.zeros((T, H, dv))
+    hT = np.zeros((nseq, H, dk, dv))
+    for n in range(nseq):
+        s, e = int(cu[n]), int(cu[n + 1])
+        for h in range(H):
+            S0 = np.zeros((dk, dv)) if h0d is None else h0d[n, h].copy()
+            if e > s:
+                o[s:e, h], hT[n, h] = _gdn_chunk_one(qd[s:e, h], kd[s:e, h], vd[s:e, h],
+                                                     gd[s:e, h], bd[s:e, h], scale, S0, chunk)
+            else:
+                hT[n, h] = S0
+    return o, hT
 
 
 # ----------------------------------------------------------------------------------------

@@ -196,6 +196,24 @@ def test_output_norm_gate_argument_errors(lib):
     assert _gate(lib, out=0x10000) == 4                       # in place is allowed (no GPU here)
 
 
+def _gstep(lib, q=0x10000, k=0x20000, v=0x30000, g=0x40000, b=0x44000, S=0x100000, o=0x50000, N=2, H=2):
+    return lib.sala_gla_gdn_recurrent_step(P(q), P(k), P(v), P(g), P(b) if b else None, 0.1, P(S),
+                                           P(o), N, H, None)
+
+
+@no_gpu
+def test_gdn_step_argument_errors(lib):
+    INVALID, MISALIGNED = 1, 2
+    assert _gstep(lib, N=-1) == INVALID
+    assert _gstep(lib, H=0) == INVALID
+    assert _gstep(lib, N=0) == 0
+    assert _gstep(lib, b=0) == INVALID
+    assert _gstep(lib, b=0x44004) == MISALIGNED
+    assert _gstep(lib, S=0x44000) == INVALID                    # S overlaps beta
+    assert _gstep(lib, o=0x100000 + 64) == INVALID              # o inside S
+    assert _gstep(lib) == 4                                     # no GPU here
+
+
 @no_gpu
 def test_valid_arguments_without_a_gpu_report_cuda_error(lib):
     # validation passes, then the runtime finds no device: nothing is launched

@@ -460,3 +460,74 @@ def test_prologue_rotation_invariants():
         b = oracle.qk_prologue(k, w, np.array([n]))[0]
         dots.append(a @ b)
     assert max(dots) - min(dots) <= 0.02 * abs(dots[0]) + 0.05
+
+
+# ---------------------------------------------------------------------------------------
+# gated delta rule ("Formulas and Code for Adapting Inference to GDN/KDA Linear Modules":
+# recurrent form, section 1.1; chunked form with the UT transform, section 1.2)
+
+
+def _gdn_case(T, H, dk, dv, seed, lens=None, h0=True):
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.nn.functional.normalize(torch.randn((T, H, dk), generator=gen), dim=-1).to(torch.bfloat16)
+    k = torch.nn.functional.normalize(torch.randn((T, H, dk), generator=gen), dim=-1).to(torch.bfloat16)
+    v = torch.randn((T, H, dv), generator=gen).to(torch.bfloat16)
+    g = -0.4 * torch.rand((T, H), generator=gen)
+    beta = torch.rand((T, H), generator=gen)
+    lens = lens or [T]
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int64)
+    hz = torch.randn((len(lens), H, dk, dv), generator=gen) * 0.3 if h0 else None
+    return q, k, v, g, beta, hz, cu
+
+
+@pytest.mark.parametrize("lens,chunk", [([37], 8), ([130, 0, 64, 5], 16), ([200], 64)])
+def test_gdn_chunked_form_equals_recurrence(lens, chunk):
+    # the page's chunked form (UT transform, W carrying exp(g)) reaches the recurrence with
+    # the decay applied before the memory read
+    q, k, v, g, beta, h0, cu = _gdn_case(sum(lens), 2, 12, 7, seed=sum(lens), lens=lens)
+    o1, h1 = oracle.gdn_recurrent(q, k, v, g, beta, 0.7, h0=h0, cu_seqlens=cu)
+    o2, h2 = oracle.gdn_chunkwise(q, k, v, g, beta, 0.7, h0=h0, cu_seqlens=cu, chunk=chunk)
+    assert oracle.rel_fro(o2, o1) < 1e-12
+    assert oracle.rel_fro(h2, h1) < 1e-12
+
+
+def test_gdn_delta_rule_retrieval():
+    # g = 0, beta = 1, unit-norm key: after the write, reading at that key returns its value
+    dk, dv = 16, 9
+    rng = np.random.default_rng(4)
+    S0 = rng.standard_normal((1, 1, dk, dv))
+    kk = rng.standard_normal(dk)
+    kk /= np.linalg.norm(kk)
+    vv = rng.standard_normal(dv)
+    k = torch.tensor(kk, dtype=torch.float64).reshape(1, 1, dk)
+    v = torch.tensor(vv, dtype=torch.float64).reshape(1, 1, dv)
+    _, hT = oracle.gdn_recurrent(k, k, v, torch.zeros((1, 1)), torch.ones((1, 1)), 1.0, h0=S0,
+                                 cu_seqlens=torch.tensor([0, 1]))
+    np.testing.assert_allclose(kk @ hT[0, 0], vv, rtol=1e-12, atol=1e-12)
+
+
+def test_gdn_beta_zero_only_decays():
+    q, k, v, g, beta, h0, cu = _gdn_case(40, 2, 8, 6, seed=5)
+    o, hT = oracle.gdn_recurrent(q, k, v, g, torch.zeros_like(beta), 0.5, h0=h0, cu_seqlens=cu)
+    G = np.cumsum(g.double().numpy(), axis=0)
+    for h in range(2):
+        want_o = 0.5 * np.exp(G[:, h])[:, None] * (q[:, h].double().numpy() @ h0[0, h].double().numpy())
+        np.testing.assert_allclose(o[:, h], want_o, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(hT[0, h], np.exp(G[-1, h]) * h0[0, h].double().numpy(), rtol=1e-12)
+
+
+def test_gdn_orthogonal_keys_reduce_to_simple_gla():
+    # keys along distinct coordinate axes never read back what an earlier token wrote, so
+    # with beta = 1 and no initial state the gated delta rule is Simple GLA
+    T, H, dk, dv = 20, 1, 24, 5
+    gen = torch.Generator().manual_seed(8)
+    k = torch.zeros((T, H, dk))
+    k[torch.arange(T), 0, torch.arange(T)] = 1.0
+    k = k.to(torch.bfloat16)
+    q = torch.randn((T, H, dk), generator=gen).to(torch.bfloat16)
+    v = torch.randn((T, H, dv), generator=gen).to(torch.bfloat16)
+    g = -0.3 * torch.rand((T, H), generator=gen)
+    cu = torch.tensor([0, T])
+    o1, h1 = oracle.gdn_recurrent(q, k, v, g, torch.ones((T, H)), 0.9, cu_seqlens=cu)
+    o2, h2 = oracle.recurrent(q, k, v, g, 0.9, cu_seqlens=cu)
+    assert oracle.rel_fro(o1, o2) < 1e-12 and oracle.rel_fro(h1, h2) < 1e-12

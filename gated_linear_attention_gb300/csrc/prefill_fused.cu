@@ -370,7 +370,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&unit_full[i], 1);
             tc::mbar_init(&unit_empty[i], 5);   // MMA, gate, scaling, converting, output warps
-            tc::mbar_init(&kp_ready[i], 1);
+            tc::mbar_init(&kp_ready[i], 4);     // one arrival per scaling warp
             tc::mbar_init(&kp_free[i], 1);
             tc::mbar_init(&o_full[i], 1);
             tc::mbar_init(&o_free[i], 4);       // one arrival per output warp
@@ -812,10 +812,15 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             const float off = fast ? -R->base : R->bC;
             uint8_t *dst = sm + kKp + kb * kTile + (kc16 >> 3) * kRegion;
             uint8_t *raw = sm + kKr + kb * kTile + (kc16 >> 3) * kRegion;
+            // the warp's 16 rows (krow parity p, i = 0..7) each get their factor from one lane:
+            // lane l computes row 2 (warp % 4) + (l & 1) + 8 ((l & 15) >> 1)
+            const int lr = 2 * quarter + (lane & 1) + 8 * ((lane & 15) >> 1);
+            const float myfac = lr < nv ? tc::ex2((off - R->b[lr]) * kLog2e) : 0.f;
+            const int par = lane >> 4;   // krow = 2 (warp % 4) + par
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int row = krow + 8 * i;
-                const float fac = row < nv ? tc::ex2((off - R->b[row]) * kLog2e) : 0.f;
+                const float fac = __shfl_sync(0xffffffffu, myfac, 2 * i + par);
                 const __nv_bfloat162 f2 = __float2bfloat162_rn(fac);
                 uint4 y;
                 y.x = mul_bf16x2(x[i].x, f2);
@@ -826,12 +831,9 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 if (!fast) *reinterpret_cast<uint4 *>(raw + sw(row, kc16 & 7)) = x[i];
             }
             if (wtid == 0) TRACE(2, 10, kpc);
+            if (wtid == 0) kfast[kb] = fast;
             tc::fence_proxy_async_smem();
-            named_sync(kBar, 128);
-            if (wtid == 0) {
-                kfast[kb] = fast;
-                tc::mbar_arrive(&kp_ready[kb]);
-            }
+            warp_arrive(&kp_ready[kb]);
 #ifdef SALA_TRACE
             wacc_[1] += clock64() - tw0;
 #endif

@@ -517,6 +517,17 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         auto W = [&](uint64_t *bar, uint32_t par) {
             return __all_sync(0xffffffffu, wait_or_abort(bar, par & 1, abort_v, status));
         };
+        // Several phases an MMA group needs: their tests go out together (each mbarrier test
+        // takes tens of cycles, and they are usually all complete already); only if one is
+        // not does the group wait for them one by one.
+        auto W3 = [&](uint64_t *b0, uint32_t p0, bool n0, uint64_t *b1, uint32_t p1, bool n1,
+                      uint64_t *b2, uint32_t p2, bool n2) {
+            const bool t0 = !n0 || tc::mbar_test_wait(b0, p0 & 1);
+            const bool t1 = !n1 || tc::mbar_test_wait(b1, p1 & 1);
+            const bool t2 = !n2 || tc::mbar_test_wait(b2, p2 & 1);
+            if (__all_sync(0xffffffffu, t0 && t1 && t2)) return true;
+            return (!n0 || W(b0, p0)) && (!n1 || W(b1, p1)) && (!n2 || W(b2, p2));
+        };
 #ifdef SALA_TRACE
         unsigned long long wacc_[16] = {};
 #endif
@@ -587,9 +598,8 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                     }
                     // M2: O^T = Z^T Q^T (Q scaled in place first on the exact route)
                     const uint32_t zb = zbc & 1;
-                    if (!TIMED(6, W(&zb_ready[zb], zbc >> 1))) { ok = false; break; }
-                    if (cc >= 2 && !TIMED(7, W(&o_free[ob], (cc >> 1) - 1))) { ok = false; break; }
-                    if (!fast && !TIMED(8, W(&pp_ready, cc))) { ok = false; break; }
+                    if (!TIMED(6, W3(&zb_ready[zb], zbc >> 1, true, &o_free[ob], (cc >> 1) - 1, cc >= 2,
+                                     &pp_ready, cc, !fast))) { ok = false; break; }
                     TRACE(1, 4, c);
 #ifdef SALA_TRACE
                     const long long ti1 = clock64();
@@ -617,8 +627,8 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                     const uint32_t jn = c < 0 ? job : job + 1, gn = c < 0 ? cc : cc + 1;
                     const uint32_t kn = kpc & 1;
                     const uint32_t sn = jn % kStages;
-                    if (!TIMED(9, W(&full[sn], (cpar >> sn) & 1)) || !TIMED(10, W(&kp_ready[kn], kpc >> 1)) ||
-                        (gn >= 1 && !TIMED(11, W(&p_free, gn - 1)))) { ok = false; break; }
+                    if (!TIMED(9, W3(&full[sn], (cpar >> sn) & 1, true, &kp_ready[kn], kpc >> 1, true,
+                                     &p_free, gn - 1, gn >= 1))) { ok = false; break; }
                     cpar ^= 1u << sn;
                     ++kpc;
                     TRACE(1, 2, c + 1);

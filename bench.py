@@ -196,8 +196,9 @@ def summarise_clocks(rows):
 # each kernel as it stands, on the workload the bench times (profiles/prefill_fused_sala_layer.md,
 # profiles/recurrent_step_decode.md, profiles/output_norm_gate.md); retaken whenever a kernel
 # changes.
-MEASURED_TRAFFIC = {"prefill_fused": 251_769_600, "recurrent_step": 1_020_000_000,
-                    "recurrent_step_indexed": 482_800_000, "output_norm_gate": 171_900_000}
+MEASURED_TRAFFIC = {"prefill_fused": 251_610_112, "recurrent_step": 1_019_700_000,
+                    "recurrent_step_indexed": 483_300_000, "output_norm_gate": 171_600_000,
+                    "qk_prologue": 204_000_000, "gdn_step": 1_019_300_000}
 
 
 def prefill_bytes(T, H, nseq, has_h0, has_hT):
@@ -579,8 +580,8 @@ def run_gdn_decode(args, dist, peaks, sala_gla, inputs, wd, q, k, v, g, o, scale
                    "tokens": "the decode workload's q, k, v, g and initial states; beta of gdn_decode"},
         "roofline": {"kernel": "gdn_step", "bound": "hbm", "achieved": k_ach,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": k_ach / peaks["hbm_gbs"],
-                     "traffic": None, "peak_source": peaks["source"],
-                     "mean_launch_us": 1e3 * kern[0] / kern[1]},
+                     "traffic": MEASURED_TRAFFIC["gdn_step"] if (wd.nseq, wd.H) == (256, 32) else None,
+                     "peak_source": peaks["source"], "mean_launch_us": 1e3 * kern[0] / kern[1]},
         "_launches": kern[1],
     }
 
@@ -696,7 +697,8 @@ def run_qk_prologue(args, dist, dev, peaks, sala_gla, inputs, T, H):
                    "inputs": "raw q, k ~ 3 N(0,1) bf16, weights 1 + 0.1 N(0,1); theta 10000; in place"},
         "roofline": {"kernel": "qk_prologue", "bound": "hbm", "achieved": k_ach,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": k_ach / peaks["hbm_gbs"],
-                     "traffic": None, "peak_source": peaks["source"],
+                     "traffic": MEASURED_TRAFFIC["qk_prologue"] if (T, H) == (8192, 32) else None,
+                     "peak_source": peaks["source"],
                      "mean_launch_us": 1e3 * kern[0] / kern[1]},
         "_launches": kern[1],
     }

@@ -450,12 +450,14 @@ def run_ours(args, dist):
 
     # the layer's output RMSNorm and sigmoid gate on the prefill's output shape, and its q/k
     # prologue (RMSNorm + RoPE) on the prefill's q and k
-    gate = prologue = None
+    gate = prologue = gdn_prefill = None
     if not args.no_decode:
         gate = run_output_gate(args, dist, dev, peaks, sala_gla, inputs, T_total, w.H)
         launches_decode += gate.pop("_launches")
         prologue = run_qk_prologue(args, dist, dev, peaks, sala_gla, inputs, T_total, w.H)
         launches_decode += prologue.pop("_launches")
+        gdn_prefill = run_gdn_prefill(args, dist, dev, peaks, sala_gla, inputs)
+        launches_decode += gdn_prefill.pop("_launches")
 
     rows = clocks.stop()
 
@@ -485,6 +487,7 @@ def run_ours(args, dist):
             "decode": decode,
             "output_gate": gate,
             "qk_prologue": prologue,
+            "gdn_prefill": gdn_prefill,
             "gpu_launches_decode": launches_decode,
         }
         print(json.dumps(line), flush=True)
@@ -650,6 +653,61 @@ def run_decode_pool(args, dist, peaks, sala_gla, inputs, wd, q, k, v, g, o, scal
                      "traffic": MEASURED_TRAFFIC["recurrent_step_indexed"]
                      if (w.nseq, w.H, w.pool, w.storage) == (256, 32, 512, "bf16") else None,
                      "peak_source": peaks["source"], "mean_launch_us": 1e3 * kern[0] / kern[1]},
+        "_launches": kern[1],
+    }
+
+
+def run_gdn_prefill(args, dist, dev, peaks, sala_gla, inputs):
+    """sala_gla_gdn_fwd, the gated delta rule's recurrent form over a batch of short sequences
+    (64 x 256 tokens, 32 heads; the form the GDN/KDA page uses for short prefills). It is bound
+    by fp32 FMA throughput, not by memory: 4 d^2 = 65,536 FMA per token and head, against the
+    CUDA cores' 152 SMs x 128 FMA per cycle at the 2.07 GHz clock."""
+    import torch
+    lens = (256,) * 64
+    H = 32
+    x = inputs.make_prefill("varlen", seqlens=lens, H=H, seed=13)
+    gen = torch.Generator().manual_seed(13)
+    beta = torch.sigmoid(torch.randn(x["g"].shape, generator=gen))
+    q, k, v, g, h0, cu = (x[n].to(dev) for n in ("q", "k", "v", "g", "h0", "cu_seqlens"))
+    b = beta.to(dev)
+    o = torch.empty_like(q)
+    hT = torch.empty_like(h0)
+
+    def call():
+        sala_gla.gdn_fwd(q, k, v, g, b, x["scale"], h0=h0, cu_seqlens=cu, o=o, hT=hT)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = max(3, min(args.steps, 10))
+    dist.barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(steps):
+        call()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist.max(ev0.elapsed_time(ev1))
+    sala_gla.timing_enable(True)
+    for _ in range(steps):
+        call()
+    torch.cuda.synchronize()
+    sala_gla.timing_enable(False)
+    kern = sala_gla.timing_read()["gdn_fwd"]
+    T = sum(lens)
+    flops = 2.0 * 4 * D * D * T * H
+    peak_tflops = 152 * 128 * 2 * 2.07e9 / 1e12
+    k_ach = flops / (kern[0] / kern[1] / 1e3) / 1e12
+    return {
+        "metric": "gated-delta-rule recurrent prefill tokens/s", "value": T * steps / (ms / 1e3) * dist.world,
+        "unit": "tokens/s", "ms_per_call": ms / steps,
+        "config": {"workload": "gdn_prefill", "seqlens": "64 x 256", "T": T, "H": H, "d": D,
+                   "inputs": "varlen recipe (q, k L2, g logsigmoid, h0 N(0, 0.02)), beta = sigmoid(N(0,1))"},
+        "roofline": {"kernel": "gdn_fwd", "bound": "alu", "achieved": k_ach, "peak": peak_tflops,
+                     "unit": "TFLOP/s", "frac": k_ach / peak_tflops, "traffic": None,
+                     "peak_source": "derived: 152 SMs x 128 fp32 FMA/cycle x 2 flop x 2.07 GHz",
+                     "mean_launch_us": 1e3 * kern[0] / kern[1]},
         "_launches": kern[1],
     }
 

@@ -79,7 +79,7 @@ std::atomic<uint32_t> g_epoch{0};
 // ---- timing instrumentation -------------------------------------------------------------
 const char *const kKernelNames[kKernelCount] = {"seg_table", "prefill_fused", "recurrent_step",
                                                 "recurrent_step_indexed", "output_norm_gate",
-                                                "qk_prologue", "gdn_step"};
+                                                "qk_prologue", "gdn_step", "gdn_fwd"};
 struct TimingRecord {
     int id;
     cudaEvent_t start, stop;
@@ -369,6 +369,41 @@ int sala_gla_gdn_recurrent_step(const void *q, const void *k, const void *v, con
     if (!device_state(&err)) return err;
     if (launch_gdn_step(q, k, v, g, beta, scale, S_inout, o, static_cast<int64_t>(units),
                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SALA_ERR_CUDA;
+    return SALA_OK;
+}
+
+int sala_gla_gdn_fwd(const void *q, const void *k, const void *v, const float *g,
+                     const float *beta, float scale, const float *h0, const int64_t *cu_seqlens,
+                     void *o, float *hT, int64_t B, int64_t T, int32_t H, int64_t num_seqs,
+                     void *stream) {
+    if (B < 1 || T < 0 || H < 1) return SALA_ERR_INVALID_ARG;
+    if (cu_seqlens && (B != 1 || num_seqs < 1)) return SALA_ERR_INVALID_ARG;
+    const int64_t nseq = cu_seqlens ? num_seqs : B;
+    const int64_t T_total = B * T;
+    if (T_total > (int64_t(1) << 40) || nseq * H > (int64_t(1) << 31) - 1) return SALA_ERR_INVALID_ARG;
+    if (T_total > 0 && (!q || !k || !v || !g || !beta || !o)) return SALA_ERR_INVALID_ARG;
+    const void *al[8] = {q, k, v, g, beta, o, h0, hT};
+    for (const void *p : al)
+        if (p && !aligned16(p)) return SALA_ERR_MISALIGNED;
+    if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 7u)) return SALA_ERR_MISALIGNED;
+    const size_t vec = static_cast<size_t>(T_total) * H * kD * 2, gb = static_cast<size_t>(T_total) * H * 4;
+    const size_t sb = static_cast<size_t>(nseq) * H * kD * kD * 4;
+    const void *ins[7] = {q, k, v, g, beta, h0, cu_seqlens};
+    const size_t in_sz[7] = {vec, vec, vec, gb, gb, h0 ? sb : 0, cu_seqlens ? size_t(nseq + 1) * 8 : 0};
+    for (int i = 0; i < 7; ++i)
+        if (overlaps(o, vec, ins[i], in_sz[i]) || overlaps(hT, sb, ins[i], in_sz[i]))
+            return SALA_ERR_INVALID_ARG;
+    if (overlaps(o, vec, hT, sb)) return SALA_ERR_INVALID_ARG;
+    if (!hT && T_total == 0) return SALA_OK;
+    int err = SALA_OK;
+    if (!device_state(&err)) return err;
+    SegTable tab{};
+    tab.cu = cu_seqlens;
+    tab.T_row = T;
+    tab.nseq = nseq;
+    if (launch_gdn_fwd(q, k, v, g, beta, scale, h0, tab, T_total, o, hT, H,
+                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SALA_ERR_CUDA;
     return SALA_OK;
 }

@@ -117,3 +117,150 @@ cudaError_t launch_gdn_step(const void *q, const void *k, const void *v, const f
 }
 
 }  // namespace sala
+
+namespace sala {
+
+// ---------------------------------------------------------------------------------------
+// The recurrent form over whole sequences (the page's recurrent prefill, used for short
+// sequences): one CTA per (sequence, head) keeps the state in registers for all its tokens
+// (the decode kernel's layout: warp w rows [16w, 16w + 16), lane l columns [4l, 4l + 4)), so
+// the state is read once (h0) and written once (hT). Per token: the decay and this warp's part
+// of kv = k S, an exchange between the warps, the delta-rule update, and this warp's part of
+// q S; the token's output is summed after the next exchange. The next token's q, k, v, g, beta
+// are loaded while the current one is worked on.
+__global__ void __launch_bounds__(kGdnThreads, 2)
+gdn_fwd_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
+               const uint16_t *__restrict__ v, const float *__restrict__ g,
+               const float *__restrict__ beta, float scale, const float *__restrict__ h0,
+               SegTable t, int64_t T_total, uint16_t *__restrict__ o, float *__restrict__ hT, int H) {
+    const int nh = blockIdx.x;   // n * H + h
+    const int n = nh / H, h = nh - n * H;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = warp * kGdnRows;
+    // sequence bounds, kept inside the token range whatever cu_seqlens holds
+    const int64_t bos = min(max(seq_begin(t, n), int64_t(0)), T_total);
+    const int64_t eos = min(max(seq_begin(t, n + 1), bos), T_total);
+
+    float4 s[kGdnRows];
+    if (h0) {
+        const float *src = h0 + static_cast<size_t>(nh) * kD * kD;
+#pragma unroll
+        for (int r = 0; r < kGdnRows; ++r) s[r] = *(reinterpret_cast<const float4 *>(src + (row0 + r) * kD) + lane);
+    } else {
+#pragma unroll
+        for (int r = 0; r < kGdnRows; ++r) s[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
+    __shared__ float qk_s[2][2][kD];                    // [buffer][q, k][i]
+    __shared__ float part[kGdnThreads / 32][kD];         // kv partials
+    __shared__ float part_o[kGdnThreads / 32][kD];       // q S partials
+    // token inputs in registers: q_i, k_i (thread i < 128), v (my 4 columns), g, beta
+    float rq = 0.f, rk = 0.f, rg = 0.f, rb = 0.f;
+    uint2 rv = make_uint2(0u, 0u);
+    auto load_token = [&](int64_t tok) {
+        const size_t vec = (static_cast<size_t>(tok) * H + h) * kD;
+        if (threadIdx.x < kD) {
+            rq = bf16_bits_to_float(q[vec + threadIdx.x]);
+            rk = bf16_bits_to_float(k[vec + threadIdx.x]);
+        }
+        rv = *reinterpret_cast<const uint2 *>(v + vec + 4 * lane);
+        rg = g[static_cast<size_t>(tok) * H + h];
+        rb = beta[static_cast<size_t>(tok) * H + h];
+    };
+    if (bos < eos) load_token(bos);
+    for (int64_t tok = bos; tok < eos; ++tok) {
+        const int b = static_cast<int>(tok - bos) & 1;
+        if (threadIdx.x < kD) {
+            qk_s[b][0][threadIdx.x] = rq;
+            qk_s[b][1][threadIdx.x] = rk;
+        }
+        const float2 v01 = bf16x2_to_float2(rv.x), v23 = bf16x2_to_float2(rv.y);
+        const float alpha = expf(rg), bt = rb;
+        if (tok + 1 < eos) load_token(tok + 1);
+        __syncthreads();
+        // the previous token's output (its partials were written before this barrier)
+        if (tok > bos && threadIdx.x < kD / 2) {
+            const int j = 2 * threadIdx.x;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int w = 0; w < kGdnThreads / 32; ++w) {
+                a0 += part_o[w][j];
+                a1 += part_o[w][j + 1];
+            }
+            reinterpret_cast<uint32_t *>(o + (static_cast<size_t>(tok - 1) * H + h) * kD)[threadIdx.x] =
+                float2_to_bf16x2(scale * a0, scale * a1);
+        }
+        // decay and this warp's part of kv = k S
+        float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < kGdnRows; ++r) {
+            const float ki = qk_s[b][1][row0 + r];
+            s[r].x *= alpha;
+            s[r].y *= alpha;
+            s[r].z *= alpha;
+            s[r].w *= alpha;
+            kv.x = fmaf(ki, s[r].x, kv.x);
+            kv.y = fmaf(ki, s[r].y, kv.y);
+            kv.z = fmaf(ki, s[r].z, kv.z);
+            kv.w = fmaf(ki, s[r].w, kv.w);
+        }
+        *reinterpret_cast<float4 *>(&part[warp][4 * lane]) = kv;
+        __syncthreads();
+        float4 kvs = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kGdnThreads / 32; ++w) {
+            const float4 p = *reinterpret_cast<const float4 *>(&part[w][4 * lane]);
+            kvs.x += p.x;
+            kvs.y += p.y;
+            kvs.z += p.z;
+            kvs.w += p.w;
+        }
+        const float4 vn = make_float4(bt * (v01.x - kvs.x), bt * (v01.y - kvs.y),
+                                      bt * (v23.x - kvs.z), bt * (v23.y - kvs.w));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < kGdnRows; ++r) {
+            const float ki = qk_s[b][1][row0 + r], qi = qk_s[b][0][row0 + r];
+            s[r].x = fmaf(ki, vn.x, s[r].x);
+            s[r].y = fmaf(ki, vn.y, s[r].y);
+            s[r].z = fmaf(ki, vn.z, s[r].z);
+            s[r].w = fmaf(ki, vn.w, s[r].w);
+            acc.x = fmaf(qi, s[r].x, acc.x);
+            acc.y = fmaf(qi, s[r].y, acc.y);
+            acc.z = fmaf(qi, s[r].z, acc.z);
+            acc.w = fmaf(qi, s[r].w, acc.w);
+        }
+        *reinterpret_cast<float4 *>(&part_o[warp][4 * lane]) = acc;
+    }
+    __syncthreads();
+    if (eos > bos && threadIdx.x < kD / 2) {
+        const int j = 2 * threadIdx.x;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < kGdnThreads / 32; ++w) {
+            a0 += part_o[w][j];
+            a1 += part_o[w][j + 1];
+        }
+        reinterpret_cast<uint32_t *>(o + (static_cast<size_t>(eos - 1) * H + h) * kD)[threadIdx.x] =
+            float2_to_bf16x2(scale * a0, scale * a1);
+    }
+    if (hT) {
+        float *dst = hT + static_cast<size_t>(nh) * kD * kD;
+#pragma unroll
+        for (int r = 0; r < kGdnRows; ++r) *(reinterpret_cast<float4 *>(dst + (row0 + r) * kD) + lane) = s[r];
+    }
+}
+
+cudaError_t launch_gdn_fwd(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, float scale, const float *h0, const SegTable &t,
+                           int64_t T_total, void *o, float *hT, int H, cudaStream_t stream) {
+    if (t.nseq == 0) return cudaSuccess;
+    LaunchTimer timer(kKGdnFwd, stream);
+    gdn_fwd_kernel<<<static_cast<unsigned>(t.nseq * H), kGdnThreads, 0, stream>>>(
+        static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k),
+        static_cast<const uint16_t *>(v), g, beta, scale, h0, t, T_total, static_cast<uint16_t *>(o),
+        hT, H);
+    return cudaGetLastError();
+}
+
+}  // namespace sala

@@ -16,6 +16,7 @@ enum KernelId {
     kKOutputNormGate,
     kKQkPrologue,
     kKGdnStep,
+    kKGdnFwd,
     kKernelCount
 };
 
@@ -90,6 +91,12 @@ cudaError_t launch_output_norm_gate(const void *o, const void *z, const void *w,
 cudaError_t launch_gdn_step(const void *q, const void *k, const void *v, const float *g,
                             const float *beta, float scale, float *S, void *o, int64_t units,
                             cudaStream_t stream);
+
+// The gated delta rule over whole sequences (recurrent form), one CTA per (sequence, head);
+// sequence bounds from t.cu (or rows of t.T_row tokens); h0 / hT may be null.
+cudaError_t launch_gdn_fwd(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, float scale, const float *h0, const SegTable &t,
+                           int64_t T_total, void *o, float *hT, int H, cudaStream_t stream);
 
 // Nonzero tag of one prefill call for the hand-off flags (differs from the previous call's).
 uint32_t next_prefill_epoch();

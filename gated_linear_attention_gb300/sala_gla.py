@@ -41,6 +41,8 @@ SIGNATURES = {
     "sala_gla_recurrent_step_indexed": ([_p, _p, _p, _p, _f32, _p, _i32, _p, _i64, _p, _i64, _i32,
                                          _pro, _p, _p], ctypes.c_int),
     "sala_gla_gdn_recurrent_step": ([_p, _p, _p, _p, _p, _f32, _p, _p, _i64, _i32, _p], ctypes.c_int),
+    "sala_gla_gdn_fwd": ([_p, _p, _p, _p, _p, _f32, _p, _p, _p, _p, _i64, _i64, _i32, _i64, _p],
+                         ctypes.c_int),
     "sala_gla_qk_prologue": ([_p, _p, _pro, _p, _p, _i64, _i64, _i32, _i64, _p], ctypes.c_int),
     "sala_gla_output_norm_gate": ([_p, _p, _p, _f32, _p, _i64, _i32, _p], ctypes.c_int),
     "sala_gla_chunk_fwd_noalloc": ([_p, _p, _p, _p, _f32, _p, _p, _p, _p, _i64, _i64, _i32,
@@ -290,6 +292,43 @@ def output_norm_gate(o, z, w, eps=1e-6, out=None, stream=None):
                                           _stream(stream))
     _check(rc, "sala_gla_output_norm_gate")
     return out
+
+
+def gdn_fwd(q, k, v, g, beta, scale, h0=None, cu_seqlens=None, output_final_state=True,
+            o=None, hT=None, stream=None):
+    """``sala_gla_gdn_fwd``: the gated delta rule over whole sequences (recurrent form).
+    q, k, v: bf16 [B, T, H, 128] or packed [T, H, 128] with ``cu_seqlens``; g, beta: fp32
+    [B, T, H] / [T, H]. Returns (o, hT or None)."""
+    if q.dim() == 4:
+        Bn, T, H, D = q.shape
+        nseq, packed = Bn, False
+    elif q.dim() == 3 and cu_seqlens is not None:
+        (T, H, D), Bn = q.shape, 1
+        nseq, packed = cu_seqlens.numel() - 1, True
+    else:
+        raise ValueError("q must be [B, T, H, 128], or [T, H, 128] with cu_seqlens")
+    if D != 128:
+        raise ValueError("head dimension must be 128")
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16, q.shape)
+    _need(v, "v", torch.bfloat16, q.shape)
+    _need(g, "g", torch.float32, q.shape[:-1])
+    _need(beta, "beta", torch.float32, q.shape[:-1])
+    if h0 is not None:
+        _need(h0, "h0", torch.float32, (nseq, H, 128, 128))
+    if packed:
+        _need(cu_seqlens, "cu_seqlens", torch.int64, (nseq + 1,))
+    if o is None:
+        o = torch.empty_like(q)
+    if output_final_state and hT is None:
+        hT = torch.empty((nseq, H, 128, 128), dtype=torch.float32, device=q.device)
+    if not output_final_state:
+        hT = None
+    rc = load().sala_gla_gdn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                 _ptr(h0), _ptr(cu_seqlens) if packed else None, _ptr(o), _ptr(hT),
+                                 Bn, T, H, nseq if packed else 0, _stream(stream))
+    _check(rc, "sala_gla_gdn_fwd")
+    return o, hT
 
 
 def gdn_recurrent_step(q, k, v, g, beta, scale, S, o=None, stream=None):

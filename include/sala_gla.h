@@ -232,6 +232,28 @@ int sala_gla_gdn_recurrent_step(const void *q, const void *k, const void *v, con
                                 int64_t N, int32_t H, void *stream);
 
 /*
+ * The gated delta rule over whole sequences in its recurrent form (the page's prefill for
+ * short sequences: "Formulas and Code for Adapting Inference to GDN/KDA Linear Modules",
+ * section 1): for each sequence and head, token by token from h0, the update of
+ * sala_gla_gdn_recurrent_step. One CTA per (sequence, head) keeps the state in registers, so
+ * the work is parallel over sequences and heads only (a long single sequence runs on H SMs).
+ *
+ *   q, k, v    bf16 [B, T, H, 128] (packed [T, H, 128] with cu_seqlens, B = 1)
+ *   g, beta    fp32 [B, T, H]
+ *   h0         fp32 [Nseq, H, 128, 128] or NULL (zeros); hT fp32 [Nseq, H, 128, 128] or NULL
+ *   cu_seqlens int64 [num_seqs + 1] DEVICE array (0 = cu[0] <= ... <= cu[num_seqs] = T), or NULL
+ *   o          bf16 [B, T, H, 128]
+ * cu_seqlens is not validated here beyond keeping every sequence inside [0, T) (a malformed
+ * one gives meaningless results for the affected sequences, never an access outside the
+ * tensors); sala_gla_chunk_fwd reports a malformed one.
+ * Errors: SALA_ERR_INVALID_ARG, SALA_ERR_MISALIGNED, SALA_ERR_UNSUPPORTED, SALA_ERR_CUDA.
+ */
+int sala_gla_gdn_fwd(const void *q, const void *k, const void *v, const float *g,
+                     const float *beta, float scale, const float *h0, const int64_t *cu_seqlens,
+                     void *o, float *hT, int64_t B, int64_t T, int32_t H, int64_t num_seqs,
+                     void *stream);
+
+/*
  * Chunked prefill that allocates nothing: same arguments, layouts, results and errors as
  * sala_gla_chunk_fwd, plus SALA_ERR_TOO_LARGE. The pages have no counterpart to this entry
  * point; it exists for callers that cannot allocate device memory while they run the layer:

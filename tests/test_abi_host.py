@@ -214,6 +214,26 @@ def test_gdn_step_argument_errors(lib):
     assert _gstep(lib) == 4                                     # no GPU here
 
 
+def _gfwd(lib, q=0x10000, k=0x20000, v=0x30000, g=0x40000, b=0x44000, h0=None, cu=None,
+          o=0x50000, hT=0x60000, Bn=1, T=64, H=2, nseq=0):
+    return lib.sala_gla_gdn_fwd(P(q), P(k), P(v), P(g), P(b) if b else None, 0.1,
+                                P(h0) if h0 else None, P(cu) if cu else None, P(o),
+                                P(hT) if hT else None, Bn, T, H, nseq, None)
+
+
+@no_gpu
+def test_gdn_fwd_argument_errors(lib):
+    INVALID, MISALIGNED = 1, 2
+    assert _gfwd(lib, Bn=0) == INVALID
+    assert _gfwd(lib, b=0) == INVALID
+    assert _gfwd(lib, cu=0x70000, nseq=0) == INVALID
+    assert _gfwd(lib, b=0x44004) == MISALIGNED
+    assert _gfwd(lib, o=0x10000 + 64) == INVALID                # o overlaps q
+    assert _gfwd(lib, hT=0x44000) == INVALID                    # hT overlaps beta
+    assert _gfwd(lib, T=0, hT=None) == 0
+    assert _gfwd(lib) == 4                                      # no GPU here
+
+
 @no_gpu
 def test_valid_arguments_without_a_gpu_report_cuda_error(lib):
     # validation passes, then the runtime finds no device: nothing is launched

@@ -73,3 +73,62 @@ def test_gdn_full_size_sampled(sg):
     N = len(seqs)
     assert oracle.rel_fro(od[:, seqs].transpose(0, 1).reshape(N * steps, w.H, 128).float(), o_ref) <= O_TOL
     assert oracle.rel_fro(S[seqs], h_ref) <= S_TOL
+
+
+# ---------------------------------------------------------------------------------------
+# the recurrent form over whole sequences (sala_gla_gdn_fwd)
+
+
+def _gdn_prefill_inputs(lens, H, seed):
+    x = inputs.make_prefill("varlen", seqlens=tuple(lens), H=H, seed=seed)
+    gen = torch.Generator().manual_seed(seed)
+    beta = torch.sigmoid(torch.randn(x["g"].shape, generator=gen))
+    return x, beta
+
+
+@pytest.mark.parametrize("lens", [[1], [5, 0, 130, 64], [700, 300]])
+def test_gdn_prefill_packed(sg, lens):
+    x, beta = _gdn_prefill_inputs(lens, 4, seed=sum(lens))
+    cu = x["cu_seqlens"]
+    o, hT = sg.gdn_fwd(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["g"].cuda(), beta.cuda(),
+                       x["scale"], h0=x["h0"].cuda(), cu_seqlens=cu.cuda())
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle.gdn_chunkwise(x["q"], x["k"], x["v"], x["g"], beta, x["scale"],
+                                        h0=x["h0"], cu_seqlens=cu)
+    assert oracle.rel_fro(o.cpu().float(), o_ref) <= O_TOL
+    assert oracle.rel_fro(hT.cpu(), h_ref) <= S_TOL
+    for n, L in enumerate(lens):                 # an empty sequence returns h0
+        if L == 0:
+            assert torch.equal(hT[n].cpu(), x["h0"][n])
+
+
+def test_gdn_prefill_rows_without_state(sg):
+    x, beta = _gdn_prefill_inputs([96] * 3, 2, seed=21)
+    q, k, v = (x[n].reshape(3, 96, 2, 128) for n in ("q", "k", "v"))
+    g, b = x["g"].reshape(3, 96, 2), beta.reshape(3, 96, 2)
+    o, hT = sg.gdn_fwd(q.cuda(), k.cuda(), v.cuda(), g.cuda(), b.cuda(), x["scale"])
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle.gdn_recurrent(q, k, v, g, b, x["scale"])
+    assert oracle.rel_fro(o.cpu().float().reshape(o_ref.shape), o_ref) <= O_TOL
+    assert oracle.rel_fro(hT.cpu(), h_ref) <= S_TOL
+
+
+def test_gdn_prefill_then_decode_equals_longer_prefill(sg):
+    # prefill 50 tokens, then 10 decode steps from its final state == prefill of 60 tokens
+    x, beta = _gdn_prefill_inputs([60], 3, seed=33)
+    q, k, v, g = (x[n].cuda() for n in ("q", "k", "v", "g"))
+    b, cu = beta.cuda(), torch.tensor([0, 50], dtype=torch.int64, device="cuda")
+    o1, h1 = sg.gdn_fwd(q[:50].contiguous(), k[:50].contiguous(), v[:50].contiguous(), g[:50].contiguous(),
+                        b[:50].contiguous(), x["scale"], h0=x["h0"].cuda(), cu_seqlens=cu)
+    outs = []
+    for t in range(50, 60):
+        # (fresh copies: a row of g or beta alone is not 16-byte aligned for 3 heads)
+        outs.append(sg.gdn_recurrent_step(q[t:t + 1].clone(), k[t:t + 1].clone(),
+                                          v[t:t + 1].clone(), g[t:t + 1].clone(),
+                                          b[t:t + 1].clone(), x["scale"], h1))
+    o_all, h_all = sg.gdn_fwd(q, k, v, g, b, x["scale"], h0=x["h0"].cuda(),
+                              cu_seqlens=torch.tensor([0, 60], dtype=torch.int64, device="cuda"))
+    torch.cuda.synchronize()
+    od = torch.cat([o1] + outs)
+    assert oracle.rel_fro(od.cpu().float(), o_all.cpu().float()) <= 5e-3
+    assert oracle.rel_fro(h1.cpu(), h_all.cpu()) <= 1e-5

@@ -46,9 +46,10 @@ __device__ __forceinline__ uint2 prologue_head(uint2 xw, const float (&wv)[4], c
     return make_uint2(float2_to_bf16x2(out[0], out[1]), float2_to_bf16x2(out[2], out[3]));
 }
 
-// One CTA per token: the token's position and the 64 rotation angles are found once (lane l
-// of every warp holds the cos/sin of elements 4l .. 4l + 3), then warp w rewrites heads
-// w, w + 8, ... of q and k, loading a group of heads before working on it.
+// One CTA per token: the token's position and the cos / sin of the 64 rotation angles are
+// found once (into shared memory; lane l of every warp then holds those of elements
+// 4l .. 4l + 3), and warp w rewrites heads w, w + 8, ... of q and k, loading a group of heads
+// before working on it.
 __global__ void __launch_bounds__(kProThreads)
 qk_prologue_kernel(uint16_t *q, uint16_t *k, QkPrologue pro, SegTable t, const int64_t *start_pos,
                    int64_t T_total, int H) {
@@ -70,21 +71,27 @@ qk_prologue_kernel(uint16_t *q, uint16_t *k, QkPrologue pro, SegTable t, const i
         }
     };
     load_group(warp);
-    // the token's sequence: largest n with begin(n) <= tok
-    int64_t n = 0;
-    if (t.cu) {
-        int64_t lo = 0, hi = t.nseq - 1;
-        while (lo < hi) {
-            const int64_t mid = (lo + hi + 1) >> 1;
-            if (t.cu[mid] <= tok) lo = mid; else hi = mid - 1;
+    // the token's position and the 64 angles' cos / sin, once per token (thread i < 64 takes
+    // angle i; thread 0 finds the sequence: largest n with begin(n) <= tok)
+    __shared__ float cs_s[64], sn_s[64];
+    __shared__ float pos_s;
+    if (threadIdx.x == 0) {
+        int64_t n = 0;
+        if (t.cu) {
+            int64_t lo = 0, hi = t.nseq - 1;
+            while (lo < hi) {
+                const int64_t mid = (lo + hi + 1) >> 1;
+                if (t.cu[mid] <= tok) lo = mid; else hi = mid - 1;
+            }
+            n = lo;
+        } else {
+            n = tok / t.T_row;
         }
-        n = lo;
-    } else {
-        n = tok / t.T_row;
+        pos_s = static_cast<float>(tok - seq_begin(t, n) + (start_pos ? start_pos[n] : 0));
     }
-    const int64_t pos = tok - seq_begin(t, n) + (start_pos ? start_pos[n] : 0);
-    const float fpos = static_cast<float>(pos);
-    float cs[4], sn[4], wq[4], wk[4];
+    __syncthreads();
+    if (threadIdx.x < 64) sincosf(pos_s * pro.inv_freq[threadIdx.x], &sn_s[threadIdx.x], &cs_s[threadIdx.x]);
+    float wq[4], wk[4];
     {
         const uint2 a = *reinterpret_cast<const uint2 *>(pro.qw + 4 * lane);
         const uint2 b = *reinterpret_cast<const uint2 *>(pro.kw + 4 * lane);
@@ -93,8 +100,13 @@ qk_prologue_kernel(uint16_t *q, uint16_t *k, QkPrologue pro, SegTable t, const i
         wq[0] = a0.x; wq[1] = a0.y; wq[2] = a1.x; wq[3] = a1.y;
         wk[0] = b0.x; wk[1] = b0.y; wk[2] = b1.x; wk[3] = b1.y;
     }
+    __syncthreads();
+    float cs[4], sn[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) sincosf(fpos * pro.inv_freq[(4 * lane + e) & 63], &sn[e], &cs[e]);
+    for (int e = 0; e < 4; ++e) {
+        cs[e] = cs_s[(4 * lane + e) & 63];
+        sn[e] = sn_s[(4 * lane + e) & 63];
+    }
     const bool low = lane < 16;
     for (int h0 = warp; h0 < H; h0 += kProWarps * kProHeadsInFlight) {
         if (h0 != warp) load_group(h0);

@@ -198,7 +198,7 @@ def summarise_clocks(rows):
 # changes.
 MEASURED_TRAFFIC = {"prefill_fused": 251_610_112, "recurrent_step": 1_019_700_000,
                     "recurrent_step_indexed": 483_300_000, "output_norm_gate": 171_600_000,
-                    "qk_prologue": None, "gdn_step": 1_019_300_000}
+                    "qk_prologue": 204_000_000, "gdn_step": 1_019_300_000}
 
 
 def prefill_bytes(T, H, nseq, has_h0, has_hT):

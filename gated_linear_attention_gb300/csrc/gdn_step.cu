@@ -122,12 +122,68 @@ namespace sala {
 
 // ---------------------------------------------------------------------------------------
 // The recurrent form over whole sequences (the page's recurrent prefill, used for short
-// sequences): one CTA per (sequence, head) keeps the state in registers for all its tokens
-// (the decode kernel's layout: warp w rows [16w, 16w + 16), lane l columns [4l, 4l + 4)), so
-// the state is read once (h0) and written once (hT). Per token: the decay and this warp's part
-// of kv = k S, an exchange between the warps, the delta-rule update, and this warp's part of
-// q S; the token's output is summed after the next exchange. The next token's q, k, v, g, beta
-// are loaded while the current one is worked on.
+// sequences). One CTA of 8 warps per (sequence, head); warp w owns the 16 value columns
+// [16w, 16w + 16) of the state for all 128 key rows and runs the sequence alone: no barrier
+// and nothing shared with the other warps. Lane l = cg + 4 rg keeps rows [16 rg, 16 rg + 16)
+// of the columns 16w + 4 cg + [0, 4) in registers. The sums over rows (k S and q S) end in
+// three shuffle levels that also spread the four columns over the lanes: afterwards the lane
+// whose bits 4 and 3 read m holds column 16w + 4 cg + m. For that to need no selects, slot j
+// of a lane's four registers holds column 16w + 4 cg + (j xor m). The state is read once (h0)
+// and written once (hT).
+//
+// The decay is kept out of the stored state: the warp holds S~ with S = c S~, c the product
+// of the gates exp(g) since the last renormalisation. Then kv = c (k S~), the update adds
+// k^T (v_new / c) to S~, and o = scale c (q S~): three multiply-adds per state entry and
+// token instead of a multiply and three. When c leaves [2^-40, 2^40] (a gate of 0 included)
+// S~ is multiplied by c and c reset to 1 before the token's read, so S~ stays well inside the
+// fp32 range. Each warp copies its next tokens' inputs into shared memory asynchronously,
+// four tokens ahead, so the loads' latency stays off the token-to-token chain.
+constexpr float kGdnCLo = 0x1p-40f, kGdnCHi = 0x1p40f;
+constexpr int kGdnRing = 5;     // token slots per warp
+constexpr int kGdnSlot = 576;   // q 256 B, k 256 B, the warp's v 32 B, g, beta (16-byte multiple)
+
+// Asynchronous copy of 16 (or 4) bytes into shared memory, issued only where `on` is set.
+__device__ __forceinline__ void gdn_cp_async16(uint32_t dst, const void *src, bool on) {
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n @p cp.async.ca.shared.global [%0], [%1], 16;\n}\n"
+                 ::"r"(dst), "l"(src), "r"(static_cast<int>(on)) : "memory");
+}
+__device__ __forceinline__ void gdn_cp_async4(uint32_t dst, const void *src, bool on) {
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n @p cp.async.ca.shared.global [%0], [%1], 4;\n}\n"
+                 ::"r"(dst), "l"(src), "r"(static_cast<int>(on)) : "memory");
+}
+__device__ __forceinline__ float gdn_ex2(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Components reordered so that slot j holds component j xor m (its own inverse).
+__device__ __forceinline__ float4 gdn_perm(float4 f, int m) {
+    if (m & 2) f = make_float4(f.z, f.w, f.x, f.y);
+    if (m & 1) f = make_float4(f.y, f.x, f.w, f.z);
+    return f;
+}
+
+// Sum a lane's four column partials over the 8 row groups (lane bits 2..4). With slot j
+// holding column j xor m, the lane 16 apart holds the same two columns in its slots 2, 3 that
+// this lane keeps in slots 0, 1, and the lane 8 apart the kept column in its second place;
+// the result is column m (the same in the two lanes that differ in bit 2).
+__device__ __forceinline__ float gdn_rows_sum(float4 a) {
+    const float p0 = a.x + __shfl_xor_sync(0xffffffffu, a.z, 16);
+    const float p1 = a.y + __shfl_xor_sync(0xffffffffu, a.w, 16);
+    const float r = p0 + __shfl_xor_sync(0xffffffffu, p1, 8);
+    return r + __shfl_xor_sync(0xffffffffu, r, 4);
+}
+
+__device__ __forceinline__ void gdn_unpack8(uint4 x, float *f) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
 __global__ void __launch_bounds__(kGdnThreads, 2)
 gdn_fwd_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
                const uint16_t *__restrict__ v, const float *__restrict__ g,
@@ -136,118 +192,117 @@ gdn_fwd_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
     const int nh = blockIdx.x;   // n * H + h
     const int n = nh / H, h = nh - n * H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row0 = warp * kGdnRows;
+    const int cg = lane & 3, row0 = 16 * (lane >> 2), col0 = 16 * warp + 4 * cg;
+    const int m = (lane >> 3) & 3;   // this lane's column after gdn_rows_sum: col0 + m
     // sequence bounds, kept inside the token range whatever cu_seqlens holds
     const int64_t bos = min(max(seq_begin(t, n), int64_t(0)), T_total);
     const int64_t eos = min(max(seq_begin(t, n + 1), bos), T_total);
 
-    float4 s[kGdnRows];
+    float4 s[16];
     if (h0) {
-        const float *src = h0 + static_cast<size_t>(nh) * kD * kD;
+        const float *src = h0 + static_cast<size_t>(nh) * kD * kD + col0;
 #pragma unroll
-        for (int r = 0; r < kGdnRows; ++r) s[r] = *(reinterpret_cast<const float4 *>(src + (row0 + r) * kD) + lane);
+        for (int r = 0; r < 16; ++r) s[r] = gdn_perm(*reinterpret_cast<const float4 *>(src + (row0 + r) * kD), m);
     } else {
 #pragma unroll
-        for (int r = 0; r < kGdnRows; ++r) s[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = 0; r < 16; ++r) s[r] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    float c = 1.f;
 
-    __shared__ float qk_s[2][2][kD];                    // [buffer][q, k][i]
-    __shared__ float part[kGdnThreads / 32][kD];         // kv partials
-    __shared__ float part_o[kGdnThreads / 32][kD];       // q S partials
-    // token inputs in registers: q_i, k_i (thread i < 128), v (my 4 columns), g, beta
-    float rq = 0.f, rk = 0.f, rg = 0.f, rb = 0.f;
-    uint2 rv = make_uint2(0u, 0u);
-    auto load_token = [&](int64_t tok) {
-        const size_t vec = (static_cast<size_t>(tok) * H + h) * kD;
-        if (threadIdx.x < kD) {
-            rq = bf16_bits_to_float(q[vec + threadIdx.x]);
-            rk = bf16_bits_to_float(k[vec + threadIdx.x]);
-        }
-        rv = *reinterpret_cast<const uint2 *>(v + vec + 4 * lane);
-        rg = g[static_cast<size_t>(tok) * H + h];
-        rb = beta[static_cast<size_t>(tok) * H + h];
+    // Token inputs go through a ring of kGdnRing slots per warp, kGdnRing - 1 tokens ahead:
+    // lanes 0-15 copy 16 bytes of k each, lanes 16-31 of q, lanes 0-1 the warp's 16 values of
+    // v, lanes 2-3 g and beta.
+    __shared__ __align__(16) unsigned char ring_all[kGdnThreads / 32][kGdnRing][kGdnSlot];
+    const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(ring_all[warp]));
+    const uint16_t *qk_src = (lane < 16 ? k : q) + 8 * (lane & 15);
+    const uint32_t qk_dst = (lane < 16 ? 256u : 0u) + 16u * (lane & 15);
+    const uint16_t *v_src = v + 16 * warp + 8 * (lane & 1);
+    const float *gb_src = (lane & 1) ? beta : g;
+    const uint32_t x_dst = lane < 2 ? 512u + 16u * lane : 544u + 4u * (lane & 1);
+    const bool v_lane = lane < 2, gb_lane = lane == 2 || lane == 3;
+    size_t gi_fetch = static_cast<size_t>(bos) * H + h;   // token index x H + h of the next copy
+    int64_t tok_fetch = bos;
+    int ws = 0, rs = 0;
+    auto fetch = [&]() {
+        const bool in = tok_fetch < eos;
+        const uint32_t dst = ring + ws * kGdnSlot;
+        gdn_cp_async16(dst + qk_dst, qk_src + gi_fetch * kD, in);
+        gdn_cp_async16(dst + x_dst, v_src + gi_fetch * kD, in && v_lane);
+        gdn_cp_async4(dst + x_dst, gb_src + gi_fetch, in && gb_lane);
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+        ++tok_fetch;
+        gi_fetch += H;
+        ws = ws + 1 == kGdnRing ? 0 : ws + 1;
     };
-    if (bos < eos) load_token(bos);
+#pragma unroll
+    for (int i = 0; i < kGdnRing - 1; ++i) fetch();
+    const int sl0 = cg + 8 * m, sl1 = cg + 8 * (m ^ 1), sl2 = cg + 8 * (m ^ 2), sl3 = cg + 8 * (m ^ 3);
+    const unsigned char *ring_p = ring_all[warp][0];
+    uint16_t *o_p = o + (static_cast<size_t>(bos) * H + h) * kD + col0 + m;
+    const size_t o_step = static_cast<size_t>(H) * kD;
     for (int64_t tok = bos; tok < eos; ++tok) {
-        const int b = static_cast<int>(tok - bos) & 1;
-        if (threadIdx.x < kD) {
-            qk_s[b][0][threadIdx.x] = rq;
-            qk_s[b][1][threadIdx.x] = rk;
-        }
-        const float2 v01 = bf16x2_to_float2(rv.x), v23 = bf16x2_to_float2(rv.y);
-        const float alpha = expf(rg), bt = rb;
-        if (tok + 1 < eos) load_token(tok + 1);
-        __syncthreads();
-        // the previous token's output (its partials were written before this barrier)
-        if (tok > bos && threadIdx.x < kD / 2) {
-            const int j = 2 * threadIdx.x;
-            float a0 = 0.f, a1 = 0.f;
+        // this token's copies have landed (each lane waits for its own, the warp then meets)
+        asm volatile("cp.async.wait_group %0;\n" ::"n"(kGdnRing - 2) : "memory");
+        __syncwarp();
+        fetch();
+        const unsigned char *cur = ring_p + rs * kGdnSlot;
+        rs = rs + 1 == kGdnRing ? 0 : rs + 1;
+        const uint4 *cq = reinterpret_cast<const uint4 *>(cur);
+        float kf[16], qf[16];
+        gdn_unpack8(cq[16 + 2 * (lane >> 2)], kf);
+        gdn_unpack8(cq[17 + 2 * (lane >> 2)], kf + 8);
+        gdn_unpack8(cq[2 * (lane >> 2)], qf);
+        gdn_unpack8(cq[1 + 2 * (lane >> 2)], qf + 8);
+        const float vj = bf16_bits_to_float(reinterpret_cast<const uint16_t *>(cur + 512)[4 * cg + m]);
+        const float bt = *reinterpret_cast<const float *>(cur + 548);
+        c *= gdn_ex2(*reinterpret_cast<const float *>(cur + 544) * 1.4426950408889634f);
+        if (!(c >= kGdnCLo && c <= kGdnCHi)) {   // fold c into S~ (also a zero or NaN gate)
 #pragma unroll
-            for (int w = 0; w < kGdnThreads / 32; ++w) {
-                a0 += part_o[w][j];
-                a1 += part_o[w][j + 1];
+            for (int r = 0; r < 16; ++r) {
+                s[r].x *= c;
+                s[r].y *= c;
+                s[r].z *= c;
+                s[r].w *= c;
             }
-            reinterpret_cast<uint32_t *>(o + (static_cast<size_t>(tok - 1) * H + h) * kD)[threadIdx.x] =
-                float2_to_bf16x2(scale * a0, scale * a1);
+            c = 1.f;
         }
-        // decay and this warp's part of kv = k S
-        float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
+        // kv / c = k S~ over this lane's rows, then over all rows
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int r = 0; r < kGdnRows; ++r) {
-            const float ki = qk_s[b][1][row0 + r];
-            s[r].x *= alpha;
-            s[r].y *= alpha;
-            s[r].z *= alpha;
-            s[r].w *= alpha;
-            kv.x = fmaf(ki, s[r].x, kv.x);
-            kv.y = fmaf(ki, s[r].y, kv.y);
-            kv.z = fmaf(ki, s[r].z, kv.z);
-            kv.w = fmaf(ki, s[r].w, kv.w);
+        for (int r = 0; r < 16; ++r) {
+            a.x = fmaf(kf[r], s[r].x, a.x);
+            a.y = fmaf(kf[r], s[r].y, a.y);
+            a.z = fmaf(kf[r], s[r].z, a.z);
+            a.w = fmaf(kf[r], s[r].w, a.w);
         }
-        *reinterpret_cast<float4 *>(&part[warp][4 * lane]) = kv;
-        __syncthreads();
-        float4 kvs = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float kvc = gdn_rows_sum(a);
+        // v_new / c = beta (v / c - kv / c) at this lane's column, then at its four slots'
+        const float u = bt * (__fdividef(vj, c) - kvc);
+        const float u0 = __shfl_sync(0xffffffffu, u, sl0), u1 = __shfl_sync(0xffffffffu, u, sl1);
+        const float u2 = __shfl_sync(0xffffffffu, u, sl2), u3 = __shfl_sync(0xffffffffu, u, sl3);
+        // S~ += k^T (v_new / c); q S~ over this lane's rows
+        float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < kGdnThreads / 32; ++w) {
-            const float4 p = *reinterpret_cast<const float4 *>(&part[w][4 * lane]);
-            kvs.x += p.x;
-            kvs.y += p.y;
-            kvs.z += p.z;
-            kvs.w += p.w;
+        for (int r = 0; r < 16; ++r) {
+            s[r].x = fmaf(kf[r], u0, s[r].x);
+            s[r].y = fmaf(kf[r], u1, s[r].y);
+            s[r].z = fmaf(kf[r], u2, s[r].z);
+            s[r].w = fmaf(kf[r], u3, s[r].w);
+            b.x = fmaf(qf[r], s[r].x, b.x);
+            b.y = fmaf(qf[r], s[r].y, b.y);
+            b.z = fmaf(qf[r], s[r].z, b.z);
+            b.w = fmaf(qf[r], s[r].w, b.w);
         }
-        const float4 vn = make_float4(bt * (v01.x - kvs.x), bt * (v01.y - kvs.y),
-                                      bt * (v23.x - kvs.z), bt * (v23.y - kvs.w));
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int r = 0; r < kGdnRows; ++r) {
-            const float ki = qk_s[b][1][row0 + r], qi = qk_s[b][0][row0 + r];
-            s[r].x = fmaf(ki, vn.x, s[r].x);
-            s[r].y = fmaf(ki, vn.y, s[r].y);
-            s[r].z = fmaf(ki, vn.z, s[r].z);
-            s[r].w = fmaf(ki, vn.w, s[r].w);
-            acc.x = fmaf(qi, s[r].x, acc.x);
-            acc.y = fmaf(qi, s[r].y, acc.y);
-            acc.z = fmaf(qi, s[r].z, acc.z);
-            acc.w = fmaf(qi, s[r].w, acc.w);
-        }
-        *reinterpret_cast<float4 *>(&part_o[warp][4 * lane]) = acc;
-    }
-    __syncthreads();
-    if (eos > bos && threadIdx.x < kD / 2) {
-        const int j = 2 * threadIdx.x;
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int w = 0; w < kGdnThreads / 32; ++w) {
-            a0 += part_o[w][j];
-            a1 += part_o[w][j + 1];
-        }
-        reinterpret_cast<uint32_t *>(o + (static_cast<size_t>(eos - 1) * H + h) * kD)[threadIdx.x] =
-            float2_to_bf16x2(scale * a0, scale * a1);
+        const float oj = gdn_rows_sum(b) * (scale * c);
+        if (!(lane & 4)) *o_p = __bfloat16_as_ushort(__float2bfloat16_rn(oj));
+        o_p += o_step;
     }
     if (hT) {
-        float *dst = hT + static_cast<size_t>(nh) * kD * kD;
+        float *dst = hT + static_cast<size_t>(nh) * kD * kD + col0;
 #pragma unroll
-        for (int r = 0; r < kGdnRows; ++r) *(reinterpret_cast<float4 *>(dst + (row0 + r) * kD) + lane) = s[r];
+        for (int r = 0; r < 16; ++r)
+            *reinterpret_cast<float4 *>(dst + (row0 + r) * kD) =
+                gdn_perm(make_float4(s[r].x * c, s[r].y * c, s[r].z * c, s[r].w * c), m);
     }
 }
 

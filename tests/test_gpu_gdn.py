@@ -132,3 +132,30 @@ def test_gdn_prefill_then_decode_equals_longer_prefill(sg):
     od = torch.cat([o1] + outs)
     assert oracle.rel_fro(od.cpu().float(), o_all.cpu().float()) <= 5e-3
     assert oracle.rel_fro(h1.cpu(), h_all.cpu()) <= 1e-5
+
+
+def test_gdn_prefill_gates_leaving_the_range(sg):
+    # a gate of exactly 0 (g = -inf), single gates far below 2^-40, a run of strong decay and
+    # gates above 1: the kernel keeps the running product of the gates apart from the state
+    # and folds it in whenever it leaves [2^-40, 2^40]; the direct recurrence is the reference
+    x, beta = _gdn_prefill_inputs([200, 90], 2, seed=41)
+    g = x["g"].clone()
+    g[10] = float("-inf")
+    g[50, 0] = -60.0
+    g[100:140] = -3.0
+    g[150:160] = 0.7
+    g[230] = -200.0
+    cu = x["cu_seqlens"]
+    o, hT = sg.gdn_fwd(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), g.cuda(), beta.cuda(),
+                       x["scale"], h0=x["h0"].cuda(), cu_seqlens=cu.cuda())
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle.gdn_recurrent(x["q"], x["k"], x["v"], g, beta, x["scale"],
+                                        h0=x["h0"], cu_seqlens=cu)
+    assert torch.isfinite(o.cpu().float()).all() and torch.isfinite(hT.cpu()).all()
+    assert oracle.rel_fro(o.cpu().float(), o_ref) <= O_TOL
+    assert oracle.rel_fro(hT.cpu(), h_ref) <= S_TOL
+    # the output right after the zero gate sees only that token's own write
+    o10 = oracle.gdn_recurrent(x["q"][10:11], x["k"][10:11], x["v"][10:11], g[10:11],
+                               beta[10:11], x["scale"],
+                               cu_seqlens=torch.tensor([0, 1], dtype=torch.int64))[0]
+    assert oracle.rel_fro(o[10:11].cpu().float(), o10) <= O_TOL

@@ -137,7 +137,8 @@ namespace sala {
 // token instead of a multiply and three. When c leaves [2^-40, 2^40] (a gate of 0 included)
 // S~ is multiplied by c and c reset to 1 before the token's read, so S~ stays well inside the
 // fp32 range. Each warp copies its next tokens' inputs into shared memory asynchronously,
-// four tokens ahead, so the loads' latency stays off the token-to-token chain.
+// four tokens ahead, so the loads' latency stays off the token-to-token chain. The
+// multiply-adds are the packed two-wide fp32 kind, over pairs of adjacent rows.
 constexpr float kGdnCLo = 0x1p-40f, kGdnCHi = 0x1p40f;
 constexpr int kGdnRing = 5;     // token slots per warp
 constexpr int kGdnSlot = 576;   // q 256 B, k 256 B, the warp's v 32 B, g, beta (16-byte multiple)
@@ -175,13 +176,11 @@ __device__ __forceinline__ float gdn_rows_sum(float4 a) {
     return r + __shfl_xor_sync(0xffffffffu, r, 4);
 }
 
-__device__ __forceinline__ void gdn_unpack8(uint4 x, float *f) {
+// Eight bf16 -> four pairs of floats (element 2i, element 2i + 1).
+__device__ __forceinline__ void gdn_unpack8(uint4 x, float2 *f) {
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
+    for (int i = 0; i < 4; ++i) f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
 }
 
 __global__ void __launch_bounds__(kGdnThreads, 2)
@@ -198,14 +197,21 @@ gdn_fwd_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
     const int64_t bos = min(max(seq_begin(t, n), int64_t(0)), T_total);
     const int64_t eos = min(max(seq_begin(t, n + 1), bos), T_total);
 
-    float4 s[16];
-    if (h0) {
-        const float *src = h0 + static_cast<size_t>(nh) * kD * kD + col0;
+    // s[p][j] = (S~[row0 + 2p][col], S~[row0 + 2p + 1][col]), col the column of slot j: row
+    // pairs, so that packed two-wide multiply-adds take the key and query pairs as they unpack
+    float2 s[8][4];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) s[r] = gdn_perm(*reinterpret_cast<const float4 *>(src + (row0 + r) * kD), m);
-    } else {
-#pragma unroll
-        for (int r = 0; r < 16; ++r) s[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p = 0; p < 8; ++p) {
+        float4 e = make_float4(0.f, 0.f, 0.f, 0.f), f = e;
+        if (h0) {
+            const float *src = h0 + static_cast<size_t>(nh) * kD * kD + col0 + (row0 + 2 * p) * kD;
+            e = gdn_perm(*reinterpret_cast<const float4 *>(src), m);
+            f = gdn_perm(*reinterpret_cast<const float4 *>(src + kD), m);
+        }
+        s[p][0] = make_float2(e.x, f.x);
+        s[p][1] = make_float2(e.y, f.y);
+        s[p][2] = make_float2(e.z, f.z);
+        s[p][3] = make_float2(e.w, f.w);
     }
     float c = 1.f;
 
@@ -248,61 +254,61 @@ gdn_fwd_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
         const unsigned char *cur = ring_p + rs * kGdnSlot;
         rs = rs + 1 == kGdnRing ? 0 : rs + 1;
         const uint4 *cq = reinterpret_cast<const uint4 *>(cur);
-        float kf[16], qf[16];
-        gdn_unpack8(cq[16 + 2 * (lane >> 2)], kf);
-        gdn_unpack8(cq[17 + 2 * (lane >> 2)], kf + 8);
-        gdn_unpack8(cq[2 * (lane >> 2)], qf);
-        gdn_unpack8(cq[1 + 2 * (lane >> 2)], qf + 8);
+        float2 kp[8], qp[8];   // (k, q)[row0 + 2p], (k, q)[row0 + 2p + 1]
+        gdn_unpack8(cq[16 + 2 * (lane >> 2)], kp);
+        gdn_unpack8(cq[17 + 2 * (lane >> 2)], kp + 4);
+        gdn_unpack8(cq[2 * (lane >> 2)], qp);
+        gdn_unpack8(cq[1 + 2 * (lane >> 2)], qp + 4);
         const float vj = bf16_bits_to_float(reinterpret_cast<const uint16_t *>(cur + 512)[4 * cg + m]);
         const float bt = *reinterpret_cast<const float *>(cur + 548);
         c *= gdn_ex2(*reinterpret_cast<const float *>(cur + 544) * 1.4426950408889634f);
         if (!(c >= kGdnCLo && c <= kGdnCHi)) {   // fold c into S~ (also a zero or NaN gate)
+            const float2 cc = make_float2(c, c);
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                s[r].x *= c;
-                s[r].y *= c;
-                s[r].z *= c;
-                s[r].w *= c;
-            }
+            for (int p = 0; p < 8; ++p)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) s[p][j] = __fmul2_rn(s[p][j], cc);
             c = 1.f;
         }
         // kv / c = k S~ over this lane's rows, then over all rows
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        float2 a[4];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            a.x = fmaf(kf[r], s[r].x, a.x);
-            a.y = fmaf(kf[r], s[r].y, a.y);
-            a.z = fmaf(kf[r], s[r].z, a.z);
-            a.w = fmaf(kf[r], s[r].w, a.w);
-        }
-        const float kvc = gdn_rows_sum(a);
+        for (int j = 0; j < 4; ++j) a[j] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int p = 0; p < 8; ++p)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) a[j] = __ffma2_rn(kp[p], s[p][j], a[j]);
+        const float kvc = gdn_rows_sum(make_float4(a[0].x + a[0].y, a[1].x + a[1].y, a[2].x + a[2].y, a[3].x + a[3].y));
         // v_new / c = beta (v / c - kv / c) at this lane's column, then at its four slots'
         const float u = bt * (__fdividef(vj, c) - kvc);
         const float u0 = __shfl_sync(0xffffffffu, u, sl0), u1 = __shfl_sync(0xffffffffu, u, sl1);
         const float u2 = __shfl_sync(0xffffffffu, u, sl2), u3 = __shfl_sync(0xffffffffu, u, sl3);
         // S~ += k^T (v_new / c); q S~ over this lane's rows
-        float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float2 uu[4] = {make_float2(u0, u0), make_float2(u1, u1), make_float2(u2, u2), make_float2(u3, u3)};
+        float2 b[4];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            s[r].x = fmaf(kf[r], u0, s[r].x);
-            s[r].y = fmaf(kf[r], u1, s[r].y);
-            s[r].z = fmaf(kf[r], u2, s[r].z);
-            s[r].w = fmaf(kf[r], u3, s[r].w);
-            b.x = fmaf(qf[r], s[r].x, b.x);
-            b.y = fmaf(qf[r], s[r].y, b.y);
-            b.z = fmaf(qf[r], s[r].z, b.z);
-            b.w = fmaf(qf[r], s[r].w, b.w);
-        }
-        const float oj = gdn_rows_sum(b) * (scale * c);
+        for (int j = 0; j < 4; ++j) b[j] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int p = 0; p < 8; ++p)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                s[p][j] = __ffma2_rn(kp[p], uu[j], s[p][j]);
+                b[j] = __ffma2_rn(qp[p], s[p][j], b[j]);
+            }
+        const float oj = gdn_rows_sum(make_float4(b[0].x + b[0].y, b[1].x + b[1].y, b[2].x + b[2].y, b[3].x + b[3].y)) *
+                         (scale * c);
         if (!(lane & 4)) *o_p = __bfloat16_as_ushort(__float2bfloat16_rn(oj));
         o_p += o_step;
     }
     if (hT) {
         float *dst = hT + static_cast<size_t>(nh) * kD * kD + col0;
 #pragma unroll
-        for (int r = 0; r < 16; ++r)
-            *reinterpret_cast<float4 *>(dst + (row0 + r) * kD) =
-                gdn_perm(make_float4(s[r].x * c, s[r].y * c, s[r].z * c, s[r].w * c), m);
+        for (int p = 0; p < 8; ++p) {
+            *reinterpret_cast<float4 *>(dst + (row0 + 2 * p) * kD) =
+                gdn_perm(make_float4(s[p][0].x * c, s[p][1].x * c, s[p][2].x * c, s[p][3].x * c), m);
+            *reinterpret_cast<float4 *>(dst + (row0 + 2 * p + 1) * kD) =
+                gdn_perm(make_float4(s[p][0].y * c, s[p][1].y * c, s[p][2].y * c, s[p][3].y * c), m);
+        }
     }
 }
 

@@ -660,7 +660,8 @@ def run_decode_pool(args, dist, peaks, sala_gla, inputs, wd, q, k, v, g, o, scal
 def run_gdn_prefill(args, dist, dev, peaks, sala_gla, inputs):
     """sala_gla_gdn_fwd, the gated delta rule's recurrent form over a batch of short sequences
     (64 x 256 tokens, 32 heads; the form the GDN/KDA page uses for short prefills). It is bound
-    by fp32 FMA throughput, not by memory: 4 d^2 = 65,536 FMA per token and head, against the
+    by fp32 FMA throughput, not by memory: the recurrence's 4 d^2 = 65,536 multiply-adds per
+    token and head (the kernel executes 3 d^2, keeping the decay as a scalar), against the
     CUDA cores' 152 SMs x 128 FMA per cycle at the 2.07 GHz clock."""
     import torch
     lens = (256,) * 64

@@ -159,3 +159,24 @@ def test_gdn_prefill_gates_leaving_the_range(sg):
                                beta[10:11], x["scale"],
                                cu_seqlens=torch.tensor([0, 1], dtype=torch.int64))[0]
     assert oracle.rel_fro(o[10:11].cpu().float(), o10) <= O_TOL
+
+
+def test_gdn_prefill_bench_size_sampled(sg):
+    # the recurrent prefill at the benchmark's size and launch (64 sequences x 256 tokens,
+    # 32 heads, inputs as the benchmark draws them); three sequences checked against the oracle
+    lens = (256,) * 64
+    x = inputs.make_prefill("varlen", seqlens=lens, H=32, seed=13)
+    beta = torch.sigmoid(torch.randn(x["g"].shape, generator=torch.Generator().manual_seed(13)))
+    o, hT = sg.gdn_fwd(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["g"].cuda(), beta.cuda(),
+                       x["scale"], h0=x["h0"].cuda(), cu_seqlens=x["cu_seqlens"].cuda())
+    torch.cuda.synchronize()
+    o, hT = o.cpu().float(), hT.cpu()
+    cu = x["cu_seqlens"]
+    for n in (0, 37, 63):
+        a, b = int(cu[n]), int(cu[n + 1])
+        sl = lambda t: t[a:b].contiguous()
+        o_ref, h_ref = oracle.gdn_recurrent(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["g"]), sl(beta),
+                                            x["scale"], h0=x["h0"][n:n + 1],
+                                            cu_seqlens=torch.tensor([0, b - a], dtype=torch.int64))
+        assert oracle.rel_fro(o[a:b], o_ref) <= O_TOL
+        assert oracle.rel_fro(hT[n:n + 1], h_ref) <= S_TOL

@@ -21,7 +21,7 @@ def sg():
     return sala_gla
 
 
-@pytest.mark.parametrize("T,H", [(1, 1), (5, 3), (37, 8), (300, 32), (20, 72)])
+@pytest.mark.parametrize("T,H", [(1, 1), (5, 3), (37, 8), (41, 16), (300, 32), (19, 64), (20, 72)])
 def test_output_gate_small(sg, T, H):
     x = inputs.make_output_gate(T, H, seed=T + H)
     out = sg.output_norm_gate(x["o"].cuda(), x["z"].cuda(), x["w"].cuda(), x["eps"])

@@ -198,7 +198,8 @@ def summarise_clocks(rows):
 # changes.
 MEASURED_TRAFFIC = {"prefill_fused": 251_610_112, "recurrent_step": 1_019_700_000,
                     "recurrent_step_indexed": 483_300_000, "output_norm_gate": 171_600_000,
-                    "qk_prologue": 204_000_000, "gdn_step": 1_019_300_000}
+                    "qk_prologue": 204_000_000, "gdn_step": 1_019_300_000,
+                    "gdn_fwd": 775_600_000}
 
 
 def prefill_bytes(T, H, nseq, has_h0, has_hT):
@@ -706,7 +707,7 @@ def run_gdn_prefill(args, dist, dev, peaks, sala_gla, inputs):
         "config": {"workload": "gdn_prefill", "seqlens": "64 x 256", "T": T, "H": H, "d": D,
                    "inputs": "varlen recipe (q, k L2, g logsigmoid, h0 N(0, 0.02)), beta = sigmoid(N(0,1))"},
         "roofline": {"kernel": "gdn_fwd", "bound": "alu", "achieved": k_ach, "peak": peak_tflops,
-                     "unit": "TFLOP/s", "frac": k_ach / peak_tflops, "traffic": None,
+                     "unit": "TFLOP/s", "frac": k_ach / peak_tflops, "traffic": MEASURED_TRAFFIC["gdn_fwd"],
                      "peak_source": "derived: 152 SMs x 128 fp32 FMA/cycle x 2 flop x 2.07 GHz",
                      "mean_launch_us": 1e3 * kern[0] / kern[1]},
         "_launches": kern[1],

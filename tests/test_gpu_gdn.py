@@ -180,3 +180,18 @@ def test_gdn_prefill_bench_size_sampled(sg):
                                             cu_seqlens=torch.tensor([0, b - a], dtype=torch.int64))
         assert oracle.rel_fro(o[a:b], o_ref) <= O_TOL
         assert oracle.rel_fro(hT[n:n + 1], h_ref) <= S_TOL
+
+
+def test_gdn_prefill_no_tokens(sg):
+    # packed call whose sequences are all empty: no output rows, hT = h0 (zeros without h0)
+    H = 3
+    q = torch.empty((0, H, 128), dtype=torch.bfloat16, device="cuda")
+    g = torch.empty((0, H), dtype=torch.float32, device="cuda")
+    cu = torch.zeros(4, dtype=torch.int64, device="cuda")
+    h0 = inputs.make_decode_state("gdn_decode", nseq=3, H=H)
+    o, hT = sg.gdn_fwd(q, q.clone(), q.clone(), g, g.clone(), 0.088, h0=h0.cuda(), cu_seqlens=cu)
+    _, hz = sg.gdn_fwd(q, q.clone(), q.clone(), g, g.clone(), 0.088, cu_seqlens=cu)
+    torch.cuda.synchronize()
+    assert o.numel() == 0
+    assert torch.equal(hT.cpu(), h0)
+    assert torch.count_nonzero(hz).item() == 0

@@ -22,35 +22,35 @@ constexpr int kProThreads = 256;
 constexpr int kProWarps = kProThreads / 32;
 constexpr int kProHeadsInFlight = 4;   // heads per warp whose loads are issued together
 
-__device__ __forceinline__ float round_bf16_f(float x) {
-    return __bfloat162float(__float2bfloat16_rn(x));
-}
-
 // One head vector (4 elements per lane): RMSNorm with weight w, bf16, RoPE with the lane's
-// (cos, sin), bf16. The RoPE partner of lane l's elements is in lane l ^ 16.
+// (cos, sin), bf16. The normalised values are rounded to bf16 two to a word, and the RoPE
+// partners (lane l ^ 16) are exchanged in that packed form; ssn is -sin for the first half of
+// the vector (lanes 0-15) and +sin for the second.
 __device__ __forceinline__ uint2 prologue_head(uint2 xw, const float (&wv)[4], const float (&cs)[4],
-                                               const float (&sn)[4], float eps, bool low) {
+                                               const float (&ssn)[4], float eps) {
     const float2 a01 = bf16x2_to_float2(xw.x), a23 = bf16x2_to_float2(xw.y);
-    const float xs[4] = {a01.x, a01.y, a23.x, a23.y};
-    float ss = xs[0] * xs[0] + xs[1] * xs[1] + xs[2] * xs[2] + xs[3] * xs[3];
+    float ss = a01.x * a01.x;
+    ss = fmaf(a01.y, a01.y, ss);
+    ss = fmaf(a23.x, a23.x, ss);
+    ss = fmaf(a23.y, a23.y, ss);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float r = 1.f / sqrtf(ss / kD + eps);
-    float out[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float y = round_bf16_f(xs[e] * r * wv[e]);
-        const float py = __shfl_xor_sync(0xffffffffu, y, 16);
-        out[e] = round_bf16_f(low ? y * cs[e] - py * sn[e] : y * cs[e] + py * sn[e]);
-    }
-    return make_uint2(float2_to_bf16x2(out[0], out[1]), float2_to_bf16x2(out[2], out[3]));
+    const float r = rsqrtf(ss * (1.f / kD) + eps);
+    const uint32_t y01 = float2_to_bf16x2(a01.x * r * wv[0], a01.y * r * wv[1]);
+    const uint32_t y23 = float2_to_bf16x2(a23.x * r * wv[2], a23.y * r * wv[3]);
+    const uint32_t p01 = __shfl_xor_sync(0xffffffffu, y01, 16);
+    const uint32_t p23 = __shfl_xor_sync(0xffffffffu, y23, 16);
+    const float2 y0 = bf16x2_to_float2(y01), y1 = bf16x2_to_float2(y23);
+    const float2 q0 = bf16x2_to_float2(p01), q1 = bf16x2_to_float2(p23);
+    return make_uint2(float2_to_bf16x2(fmaf(q0.x, ssn[0], y0.x * cs[0]), fmaf(q0.y, ssn[1], y0.y * cs[1])),
+                      float2_to_bf16x2(fmaf(q1.x, ssn[2], y1.x * cs[2]), fmaf(q1.y, ssn[3], y1.y * cs[3])));
 }
 
 // One CTA per token: the token's position and the cos / sin of the 64 rotation angles are
 // found once (into shared memory; lane l of every warp then holds those of elements
 // 4l .. 4l + 3), and warp w rewrites heads w, w + 8, ... of q and k, loading a group of heads
 // before working on it.
-__global__ void __launch_bounds__(kProThreads)
+__global__ void __launch_bounds__(kProThreads, 5)
 qk_prologue_kernel(uint16_t *q, uint16_t *k, QkPrologue pro, SegTable t, const int64_t *start_pos,
                    int64_t T_total, int H) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -101,13 +101,12 @@ qk_prologue_kernel(uint16_t *q, uint16_t *k, QkPrologue pro, SegTable t, const i
         wk[0] = b0.x; wk[1] = b0.y; wk[2] = b1.x; wk[3] = b1.y;
     }
     __syncthreads();
-    float cs[4], sn[4];
+    float cs[4], ssn[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         cs[e] = cs_s[(4 * lane + e) & 63];
-        sn[e] = sn_s[(4 * lane + e) & 63];
+        ssn[e] = lane < 16 ? -sn_s[(4 * lane + e) & 63] : sn_s[(4 * lane + e) & 63];
     }
-    const bool low = lane < 16;
     for (int h0 = warp; h0 < H; h0 += kProWarps * kProHeadsInFlight) {
         if (h0 != warp) load_group(h0);
 #pragma unroll
@@ -115,8 +114,8 @@ qk_prologue_kernel(uint16_t *q, uint16_t *k, QkPrologue pro, SegTable t, const i
             const int h = h0 + j * kProWarps;
             if (h < H) {
                 const size_t off = (row + h) * kD + 4 * lane;
-                *reinterpret_cast<uint2 *>(q + off) = prologue_head(xq[j], wq, cs, sn, pro.eps, low);
-                *reinterpret_cast<uint2 *>(k + off) = prologue_head(xk[j], wk, cs, sn, pro.eps, low);
+                *reinterpret_cast<uint2 *>(q + off) = prologue_head(xq[j], wq, cs, ssn, pro.eps);
+                *reinterpret_cast<uint2 *>(k + off) = prologue_head(xk[j], wk, cs, ssn, pro.eps);
             }
         }
     }

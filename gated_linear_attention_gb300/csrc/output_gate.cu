@@ -74,7 +74,7 @@ output_norm_gate_kernel(const uint16_t *__restrict__ o, const uint16_t *__restri
         for (int i = 0; i < 4; ++i) {
             const float2 xf = bf16x2_to_float2(xs[i]), zf = bf16x2_to_float2(zs[i]),
                          wf = bf16x2_to_float2(ws[i]);
-            const float g0 = 1.f / (1.f + __expf(-zf.x)), g1 = 1.f / (1.f + __expf(-zf.y));
+            const float g0 = __fdividef(1.f, 1.f + __expf(-zf.x)), g1 = __fdividef(1.f, 1.f + __expf(-zf.y));
             r[i] = float2_to_bf16x2(xf.x * rinv * wf.x * g0, xf.y * rinv * wf.y * g1);
         }
         __stcs(reinterpret_cast<uint4 *>(out + tok + e), make_uint4(r[0], r[1], r[2], r[3]));
@@ -92,9 +92,10 @@ output_norm_gate_kernel(const uint16_t *__restrict__ o, const uint16_t *__restri
 
 // The common widths (H = 8, 16, 32, 64: F = 8 kIt kThr features): o, z and the weight of the
 // token are all loaded up front (kIt 16-byte pieces each per thread of kThr), so each CTA has
-// its whole token in flight at once, with up to 2048 threads resident per SM.
+// its whole token in flight at once, with up to 1536 threads resident per SM (the register
+// budget of 40 per thread that leaves holds a token without spilling more than a word).
 template <int kIt, int kThr>
-__global__ void __launch_bounds__(kThr, 2048 / kThr)
+__global__ void __launch_bounds__(kThr, 1536 / kThr)
 output_norm_gate_fixed_kernel(const uint16_t *__restrict__ o, const uint16_t *__restrict__ z,
                               const uint16_t *__restrict__ w, float eps, uint16_t *out) {
     constexpr int F = kIt * 8 * kThr;
@@ -137,7 +138,7 @@ output_norm_gate_fixed_kernel(const uint16_t *__restrict__ o, const uint16_t *__
         for (int i = 0; i < 4; ++i) {
             const float2 xf = bf16x2_to_float2(xs[i]), zf = bf16x2_to_float2(zs[i]),
                          wf = bf16x2_to_float2(ws[i]);
-            const float g0 = 1.f / (1.f + __expf(-zf.x)), g1 = 1.f / (1.f + __expf(-zf.y));
+            const float g0 = __fdividef(1.f, 1.f + __expf(-zf.x)), g1 = __fdividef(1.f, 1.f + __expf(-zf.y));
             r[i] = float2_to_bf16x2(xf.x * rinv * wf.x * g0, xf.y * rinv * wf.y * g1);
         }
         __stcs(reinterpret_cast<uint4 *>(out + tok + e), make_uint4(r[0], r[1], r[2], r[3]));

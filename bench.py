@@ -198,7 +198,7 @@ def summarise_clocks(rows):
 # changes.
 MEASURED_TRAFFIC = {"prefill_fused": 251_610_112, "recurrent_step": 1_019_700_000,
                     "recurrent_step_indexed": 483_300_000, "output_norm_gate": 167_600_000,
-                    "qk_prologue": None, "gdn_step": 1_019_300_000,
+                    "qk_prologue": 204_400_000, "gdn_step": 1_019_300_000,
                     "gdn_fwd": 775_600_000}
 
 

@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other prefill workloads (tiny, varlen, long)")
     ap.add_argument("--decode-steps", type=int, default=None,
                     help="decode steps to run (default: the workload's 1000; fewer for profiling)")
     return ap.parse_args()
@@ -193,9 +195,8 @@ def summarise_clocks(rows):
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of
-# each kernel as it stands, on the workload the bench times (profiles/prefill_fused_sala_layer.md,
-# profiles/recurrent_step_decode.md, profiles/output_norm_gate.md); retaken whenever a kernel
-# changes.
+# each kernel as it stands, on the workload the bench times; retaken whenever a kernel changes
+# (None: not measured since the last change).
 MEASURED_TRAFFIC = {"prefill_fused": 251_610_112, "recurrent_step": 1_019_700_000,
                     "recurrent_step_indexed": 483_300_000, "output_norm_gate": 167_600_000,
                     "qk_prologue": 204_400_000, "gdn_step": 1_019_300_000,
@@ -460,6 +461,15 @@ def run_ours(args, dist):
         gdn_prefill = run_gdn_prefill(args, dist, dev, peaks, sala_gla, inputs)
         launches_decode += gdn_prefill.pop("_launches")
 
+    # the other prefill workloads: varlen (8 packed sequences, 66,560 tokens, h0), long
+    # (131,072 tokens, h0) and tiny (256 tokens, 4 heads)
+    configs = None
+    if not args.no_configs:
+        configs = {}
+        for name in ("varlen", "long", "tiny"):
+            configs[name] = run_prefill_config(args, dist, dev, peaks, sala_gla, inputs, name)
+            launches_decode += configs[name].pop("_launches")
+
     rows = clocks.stop()
 
     cpu = None
@@ -489,10 +499,80 @@ def run_ours(args, dist):
             "output_gate": gate,
             "qk_prologue": prologue,
             "gdn_prefill": gdn_prefill,
+            "prefill_configs": configs,
             "gpu_launches_decode": launches_decode,
         }
         print(json.dumps(line), flush=True)
     dist.close()
+
+
+def run_prefill_config(args, dist, dev, peaks, sala_gla, inputs, name):
+    """One more prefill workload, timed like the headline one: inputs resident in HBM, W
+    warm-up calls, K timed calls between CUDA events on the launching stream (max over
+    ranks), then a second pass of K calls with the library's per-kernel events for the
+    dominant kernel's roofline. One input set: varlen (1.6 GB of q, k, v) and long (3.2 GB)
+    are far larger than L2 on their own; tiny (1 MB) stays in L2 and is a latency figure."""
+    import torch
+    w = inputs.WORKLOADS[name]
+    x = inputs.make_prefill(w, seed=w.seed + 1000 * dist.rank)
+    s = {n: (x[n].to(dev) if x[n] is not None else None)
+         for n in ("q", "k", "v", "g", "h0", "cu_seqlens")}
+    T_total = x["q"].shape[0] * x["q"].shape[1] if x["q"].dim() == 4 else x["q"].shape[0]
+    nseq = len(w.seqlens)
+    o = torch.empty_like(s["q"])
+    hT = torch.empty((nseq, w.H, D, D), device=dev)
+
+    def step():
+        sala_gla.chunk_fwd(s["q"], s["k"], s["v"], s["g"], x["scale"], h0=s["h0"],
+                           cu_seqlens=s["cu_seqlens"], o=o, hT=hT)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert sala_gla.get_device_status() == 0
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist.max(ev0.elapsed_time(ev1))
+    sala_gla.timing_enable(True)
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    sala_gla.timing_enable(False)
+    kern = sala_gla.timing_read()
+    assert sala_gla.get_device_status() == 0
+    has_h0 = x["h0"] is not None
+    nbytes = prefill_bytes(T_total, w.H, nseq, has_h0, True)
+    k_ms, k_n = kern["prefill_fused"]
+    k_ach = nbytes / (k_ms / k_n / 1e3) / 1e9
+    value = dist.sum(T_total * args.steps) / (ms / 1e3)
+    step_rate = T_total / (nbytes / (peaks["hbm_gbs"] * 1e9))
+    del s, o, hT
+    torch.cuda.empty_cache()
+    return {
+        "metric": "prefill tokens/s", "value": value, "unit": "tokens/s",
+        "ms_per_step": ms / args.steps,
+        "config": {"workload": w.name, "T": T_total, "H": w.H, "d": D, "sequences": nseq,
+                   "h0": has_h0, "bytes_per_step": nbytes,
+                   "l2": "L2-resident (latency)" if nbytes < 64e6 else "inputs larger than L2",
+                   "description": w.description},
+        "roofline": {"kernel": "prefill_fused", "bound": "hbm", "achieved": k_ach,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": k_ach / peaks["hbm_gbs"],
+                     "traffic": MEASURED_TRAFFIC.get("prefill_fused_" + w.name),
+                     "peak_source": peaks["source"], "mean_launch_us": 1e3 * k_ms / k_n},
+        "step_roofline": {"bytes_per_step": nbytes, "roofline_tokens_per_s": step_rate,
+                          "frac": (value / dist.world) / step_rate},
+        "kernels": {k: {"ms_total": v[0], "launches": v[1],
+                        "us_per_launch": (1e3 * v[0] / v[1]) if v[1] else None}
+                    for k, v in kern.items() if v[1]},
+        "_launches": sum(n for _, n in kern.values()),
+    }
 
 
 def run_decode(args, dist, dev, peaks, sala_gla, inputs):

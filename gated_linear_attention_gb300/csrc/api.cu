@@ -153,11 +153,28 @@ LaunchTimer::~LaunchTimer() {
     g_records.push_back({id_, start_, stop});
 }
 
+namespace {
+std::atomic<uint64_t> g_fault_wait_ns{0};
+std::atomic<int64_t> g_fault_withhold{-1};
+}  // namespace
+
+void prefill_fault_knobs(uint64_t *wait_ns, int64_t *withhold) {
+    *wait_ns = g_fault_wait_ns.load();
+    *withhold = g_fault_withhold.load();
+}
+
 }  // namespace sala
 
 using namespace sala;
 
 extern "C" {
+
+int sala_gla_debug_prefill_knobs(uint64_t flag_wait_ns, int64_t withhold_unit) {
+    if (withhold_unit < -1) return SALA_ERR_INVALID_ARG;
+    g_fault_wait_ns.store(flag_wait_ns);
+    g_fault_withhold.store(withhold_unit);
+    return SALA_OK;
+}
 
 const char *sala_gla_version(void) { return "0.1.0"; }
 

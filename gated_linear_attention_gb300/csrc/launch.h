@@ -98,6 +98,11 @@ cudaError_t launch_gdn_fwd(const void *q, const void *k, const void *v, const fl
                            const float *beta, float scale, const float *h0, const SegTable &t,
                            int64_t T_total, void *o, float *hT, int H, cudaStream_t stream);
 
+// Failure-path test settings of the fused prefill (sala_gla_debug_prefill_knobs): the limit
+// of the wait for a predecessor's state (0: the default 2 s) and a unit whose flag is withheld
+// (-1: none).
+void prefill_fault_knobs(uint64_t *wait_ns, int64_t *withhold);
+
 // Nonzero tag of one prefill call for the hand-off flags (differs from the previous call's).
 uint32_t next_prefill_epoch();
 

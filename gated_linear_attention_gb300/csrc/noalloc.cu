@@ -111,6 +111,7 @@ extern "C" int sala_gla_chunk_fwd_noalloc(const void *q, const void *k, const vo
     // tokens per segment there are at most T/L + nseq segments, so floor(T/L) may not exceed
     // r = (segments that fit) - nseq.
     const size_t table = round256(size_t(nseq + 2) * 8) + 256;   // segment table + ticket
+    // (this check also keeps the unsigned subtraction below from wrapping)
     if (table + 256 + H * kUnitBytes > kScratchBytes) return SALA_ERR_TOO_LARGE;
     const int64_t units_fit = static_cast<int64_t>((kScratchBytes - table - 256) / kUnitBytes);
     const int64_t r = units_fit / H - nseq;
@@ -126,6 +127,9 @@ extern "C" int sala_gla_chunk_fwd_noalloc(const void *q, const void *k, const vo
     if (seg_len < need) seg_len = need;
     const int64_t max_segs = T_total / seg_len + nseq;
     const int64_t max_units = max_segs * H;
+    // the same bound as sala_gla_chunk_fwd (unit indices are 32-bit in the kernels); the
+    // scratch size already implies it
+    if (max_units >= (int64_t(1) << 31)) return SALA_ERR_TOO_LARGE;
     const size_t flag_bytes = round256(size_t(max_units) * 4);
     if (table + flag_bytes + size_t(max_units) * kD * kD * 4 > kScratchBytes)
         return SALA_ERR_TOO_LARGE;

@@ -103,6 +103,8 @@ struct FusedArgs {
     uint32_t *flags;        // [units]: == epoch once incl of that unit is published
     uint32_t *ticket;       // work counter, zeroed by the table kernel
     uint32_t epoch;
+    uint64_t flag_wait_ns;  // limit of the wait for the predecessor's published state
+    const uint32_t *withheld;   // failure-path test: this unit's flag is never released (or null)
 };
 
 struct UnitInfo {
@@ -695,7 +697,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                 if (!wait_or_abort(&pub_ready, n & 1, abort_v, status)) break;
                 const int cmd = pub_cmd;
                 if (cmd == 2) break;
-                if (cmd == 1) {
+                if (cmd == 1 && pub_flag != f.withheld) {
                     __threadfence();
                     tc::st_release_gpu(pub_flag, f.epoch);
                 }
@@ -1067,7 +1069,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                     const uint64_t t0ns = tc::global_timer_ns();
                     while (tc::ld_acquire_gpu(flag) != f.epoch) {
                         if (*abort_v) { bad = true; break; }
-                        if (tc::global_timer_ns() - t0ns > kWaitNs) {
+                        if (tc::global_timer_ns() - t0ns > f.flag_wait_ns) {
                             *abort_v = 1;
                             record_status(status, SALA_ERR_TIMEOUT);
                             bad = true;
@@ -1158,14 +1160,25 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                         tc::tmem_ld_32x32b_x32(tmem + lane_base + kTZ + 64 * k2 + 32, d1);
                         tc::tmem_ld_wait();
                         uint32_t w[16];
+                        if (P.moved) {
 #pragma unroll
-                        for (int m = 0; m < 16; ++m)
-                            w[m] = float2_to_bf16x2(__uint_as_float(d0[2 * m]) * e1, __uint_as_float(d0[2 * m + 1]) * e1);
-                        tc::tmem_st_32x32b_x16(zb_base + 32 * k2, w);
+                            for (int m = 0; m < 16; ++m)
+                                w[m] = float2_to_bf16x2(__uint_as_float(d0[2 * m]) * e1, __uint_as_float(d0[2 * m + 1]) * e1);
+                            tc::tmem_st_32x32b_x16(zb_base + 32 * k2, w);
 #pragma unroll
-                        for (int m = 0; m < 16; ++m)
-                            w[m] = float2_to_bf16x2(__uint_as_float(d1[2 * m]) * e1, __uint_as_float(d1[2 * m + 1]) * e1);
-                        tc::tmem_st_32x32b_x16(zb_base + 32 * k2 + 16, w);
+                            for (int m = 0; m < 16; ++m)
+                                w[m] = float2_to_bf16x2(__uint_as_float(d1[2 * m]) * e1, __uint_as_float(d1[2 * m + 1]) * e1);
+                            tc::tmem_st_32x32b_x16(zb_base + 32 * k2 + 16, w);
+                        } else {
+#pragma unroll
+                            for (int m = 0; m < 16; ++m)
+                                w[m] = float2_to_bf16x2(__uint_as_float(d0[2 * m]), __uint_as_float(d0[2 * m + 1]));
+                            tc::tmem_st_32x32b_x16(zb_base + 32 * k2, w);
+#pragma unroll
+                            for (int m = 0; m < 16; ++m)
+                                w[m] = float2_to_bf16x2(__uint_as_float(d1[2 * m]), __uint_as_float(d1[2 * m + 1]));
+                            tc::tmem_st_32x32b_x16(zb_base + 32 * k2 + 16, w);
+                        }
                         if (P.moved) {
                             const float e2 = e1 * eC;
 #pragma unroll
@@ -1363,6 +1376,11 @@ cudaError_t launch_prefill_fused(const ChunkArgs &a, const SegTable &t, int64_t 
         f.flags = flags;
         f.ticket = ticket;
         f.epoch = epoch;
+        uint64_t wait_ns = 0;
+        int64_t withhold = -1;
+        prefill_fault_knobs(&wait_ns, &withhold);
+        f.flag_wait_ns = wait_ns ? wait_ns : kWaitNs;
+        f.withheld = (withhold >= 0 && withhold < max_units) ? flags + withhold : nullptr;
         if (grid > max_units) grid = static_cast<int>(max_units);
         LaunchTimer timer(kKPrefillFused, st);
         // programmatic dependent launch: the kernel's set-up may overlap the segment-table

@@ -55,6 +55,7 @@ SIGNATURES = {
                               ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
     "sala_gla_kernel_count": ([], ctypes.c_int),
     "sala_gla_kernel_name": ([ctypes.c_int], ctypes.c_char_p),
+    "sala_gla_debug_prefill_knobs": ([ctypes.c_uint64, _i64], ctypes.c_int),
 }
 
 
@@ -373,3 +374,11 @@ def timing_read() -> dict:
                "sala_gla_timing_read")
         out[lib.sala_gla_kernel_name(i).decode()] = (ms.value, n.value)
     return out
+
+
+def debug_prefill_knobs(flag_wait_ns: int = 0, withhold_unit: int = -1) -> None:
+    """Failure-path test settings of the prefill (``sala_gla_debug_prefill_knobs``): the limit of
+    the wait for a predecessor's state (0: the default) and a unit whose hand-off flag is never
+    raised (-1: none). ``debug_prefill_knobs()`` restores the defaults."""
+    _check(load().sala_gla_debug_prefill_knobs(int(flag_wait_ns), int(withhold_unit)),
+           "sala_gla_debug_prefill_knobs")

@@ -281,6 +281,25 @@ int sala_gla_chunk_fwd_noalloc(const void *q, const void *k, const void *v, cons
                                float *hT, int64_t B, int64_t T, int32_t H, int64_t num_seqs,
                                void *stream);
 
+/*
+ * Failure-path test settings of the chunked prefill (process-wide; for tests and diagnosis,
+ * not for production use). The prefill hands the state of each (segment, head) unit to the
+ * next segment through a flag that the successor waits for, and every such wait is bounded
+ * (2 s by default). With these settings a test can make one wait give up on purpose and check
+ * that the call still returns, that SALA_ERR_TIMEOUT is recorded in the device status word,
+ * and that the next call computes correct results (the aborted kernel released its tensor
+ * memory and drained its copies).
+ *
+ *   flag_wait_ns   limit of the wait for a predecessor's state, in nanoseconds (0: 2 s).
+ *   withhold_unit  index of a unit (segment * H + head in the segment table's numbering)
+ *                  whose state is computed but whose flag later calls never raise, so that
+ *                  the unit after it waits in vain; -1: none. Units past a call's last unit
+ *                  are ignored.
+ * Affects every later sala_gla_chunk_fwd / sala_gla_chunk_fwd_noalloc call until reset with
+ * (0, -1). Errors: SALA_ERR_INVALID_ARG (withhold_unit < -1).
+ */
+int sala_gla_debug_prefill_knobs(uint64_t flag_wait_ns, int64_t withhold_unit);
+
 /* Static English description of a sala_status value (never NULL). */
 const char *sala_gla_status_string(int status);
 

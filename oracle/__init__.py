@@ -437,3 +437,33 @@ def rel_fro(x, ref) -> float:
     if den == 0.0:
         return float(num)
     return float(num / den)
+
+
+def rel_fro_slices(x, ref, bounds) -> np.ndarray:
+    """Relative Frobenius error of every (slice, head) block.
+
+    ``x`` and ``ref`` are [R, H, ...] (rows, heads, then anything); ``bounds`` lists the row
+    ranges (start, end) of the slices: the token ranges of the sequences for an output
+    [T, H, d], or (n, n + 1) for each sequence of a state [N, H, d, d]. Returns a
+    [len(bounds), H] array whose entry (i, h) is :func:`rel_fro` of x[s:e, h] against
+    ref[s:e, h]. The tolerances are stated per sequence and head (each (sequence, head)
+    pair runs its own recurrence), so the largest entry is what a parity test bounds.
+    """
+    x = _as_f64(x)
+    ref = _as_f64(ref)
+    if x.shape != ref.shape:
+        raise ValueError(f"shape mismatch {x.shape} vs {ref.shape}")
+    out = np.zeros((len(bounds), ref.shape[1]))
+    for i, (s, e) in enumerate(bounds):
+        for h in range(ref.shape[1]):
+            out[i, h] = rel_fro(x[s:e, h], ref[s:e, h])
+    return out
+
+
+def seq_bounds(cu_seqlens, T: int | None = None):
+    """Token ranges of the sequences: from ``cu_seqlens`` ([N+1] offsets), or one range
+    [0, T) when it is None."""
+    if cu_seqlens is None:
+        return [(0, int(T))]
+    cu = [int(c) for c in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist") else cu_seqlens)]
+    return list(zip(cu[:-1], cu[1:]))

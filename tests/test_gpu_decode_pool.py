@@ -10,6 +10,7 @@ import pytest
 import torch
 
 import oracle
+from parity_report import record
 from gated_linear_attention_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -40,6 +41,19 @@ def _run_steps(sg, x, pool, idx, steps):
     return torch.stack(outs).cpu(), pd.cpu()
 
 
+def _check_slices(o, o_ref, S, S_ref):
+    """Worst (sequence, head) relative Frobenius errors of o [steps, N, H, d] over the steps,
+    and of the states [N, H, d, d], within tolerance."""
+    steps, N, H, d = o.shape
+    of = o.float().transpose(0, 1).reshape(N * steps, H, d)
+    orf = np.ascontiguousarray(np.asarray(o_ref).transpose(1, 0, 2, 3)).reshape(N * steps, H, d)
+    so = oracle.rel_fro_slices(of, orf, [(n * steps, (n + 1) * steps) for n in range(N)])
+    sh = oracle.rel_fro_slices(S.float(), S_ref, [(n, n + 1) for n in range(S.shape[0])])
+    assert so.max() <= O_TOL, f"worst (sequence, head) output error {so.max():.3e}"
+    assert sh.max() <= S_TOL, f"worst (sequence, head) state error {sh.max():.3e}"
+    record({"o_slice_max": float(so.max()), "hT_slice_max": float(sh.max())})
+
+
 def _ref_steps(x, pool, idx, steps, storage):
     ref = pool
     o_ref = []
@@ -65,6 +79,9 @@ def test_pool_decode_small(sg, storage, N, H, P, steps, pad):
     named = [int(i) for i in p["indices"] if i >= 0]
     if named:
         assert oracle.rel_fro(pool[named].float(), pool_ref[named]) <= S_TOL
+        live = [r for r in range(N) if int(p["indices"][r]) >= 0]
+        _check_slices(o[:, live], o_ref[:, live], pool[p["indices"][live].long()],
+                      pool_ref[p["indices"][live].long().numpy()])
     # padding rows give zeros; slots nobody names keep their bits
     for r in pad:
         assert torch.all(o[:, r] == 0)
@@ -120,3 +137,4 @@ def test_full_pool_decode_sampled_sequences(sg):
                                 steps, "bf16")
     assert oracle.rel_fro(o[:, seqs].float(), o_ref) <= O_TOL
     assert oracle.rel_fro(pool[slots].float(), sub_ref) <= S_TOL
+    _check_slices(o[:, seqs], o_ref, pool[slots], sub_ref)

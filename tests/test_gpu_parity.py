@@ -1,7 +1,15 @@
 """Parity of the CUDA path (through the C ABI) with the fp64 oracle.
 
 Tolerances: relative Frobenius error <= 1e-2 for outputs o (bf16) and <= 5e-3 for final
-states hT (fp32), over whole tensors, on identical seeded inputs.
+states hT (fp32), on identical seeded inputs, over whole tensors and over every (sequence,
+head) slice (each pair runs its own recurrence, so an error confined to one sequence, one head
+or one ragged tail is not diluted by the rest). Output slices of sequences shorter than one
+64-token chunk are bounded together, per head, as one block: the tensor cores take the
+scores q.k in bf16, and for a single token that one rounding, with the cancellation between
+the state term and the token's own term, puts about 3 % of random single-token slices above
+1e-2 in any bf16-score evaluation (checked by emulating the roundings in float64). Every state
+slice is bounded on its own. The largest slice errors are recorded (see ``parity_report``)
+when SALA_PARITY_REPORT names a file.
 """
 import numpy as np
 import pytest
@@ -9,11 +17,13 @@ import torch
 
 import oracle
 from gated_linear_attention_gb300 import inputs
+from parity_report import record
 
 pytestmark = pytest.mark.gpu
 
 O_TOL = 1e-2
 S_TOL = 5e-3
+CHUNK = 64
 
 
 @pytest.fixture(scope="module")
@@ -49,18 +59,54 @@ def _flat(o):
     return o.reshape(-1, o.shape[-2], o.shape[-1])
 
 
-def check(o, hT, o_ref, h_ref, heads=None):
+def bounds_of(x):
+    """Token ranges of the sequences of a prefill input (packed, or B rows of T)."""
+    if x["cu_seqlens"] is not None:
+        return oracle.seq_bounds(x["cu_seqlens"])
+    B, T = x["q"].shape[0], x["q"].shape[1]
+    return [(b * T, (b + 1) * T) for b in range(B)]
+
+
+def check(o, hT, o_ref, h_ref, heads=None, bounds=None):
+    """Whole-tensor and worst-(sequence, head) relative Frobenius errors within tolerance.
+    ``bounds``: token ranges of the sequences (None: one sequence)."""
     of = _flat(o).float()
     if heads is not None:
         of = of[:, heads]
     eo = oracle.rel_fro(of, o_ref)
     assert eo <= O_TOL, f"output rel err {eo:.3e}"
+    bounds = bounds or [(0, of.shape[0])]
+    long_b = [(a, b) for a, b in bounds if b - a >= CHUNK]
+    short_rows = [r for a, b in bounds if 0 < b - a < CHUNK for r in range(a, b)]
+    res = {"o": eo}
+    if long_b:
+        so = oracle.rel_fro_slices(of, o_ref, long_b)
+        i, h = np.unravel_index(int(so.argmax()), so.shape)
+        assert so.max() <= O_TOL, f"output rel err {so.max():.3e} in sequence {long_b[i]}, head {h}"
+        res["o_slice_max"] = float(so.max())
+    if short_rows:
+        ss = oracle.rel_fro_slices(of[short_rows], o_ref[short_rows], [(0, len(short_rows))])
+        assert ss.max() <= O_TOL, f"output rel err {ss.max():.3e} of the short sequences, head {int(ss.argmax())}"
+        res["o_short_block_max"] = float(ss.max())
     if h_ref is not None:
         hs = hT if heads is None else hT[:, heads]
         eh = oracle.rel_fro(hs, h_ref)
         assert eh <= S_TOL, f"state rel err {eh:.3e}"
-        return eo, eh
-    return eo, None
+        sh = oracle.rel_fro_slices(hs, h_ref, [(n, n + 1) for n in range(hs.shape[0])])
+        i, h = np.unravel_index(int(sh.argmax()), sh.shape)
+        assert sh.max() <= S_TOL, f"state rel err {sh.max():.3e} in sequence {i}, head {h}"
+        res.update(hT=eh, hT_slice_max=float(sh.max()))
+    record(res)
+    return res
+
+
+def check_states(hT, h_ref):
+    """hT [N, H, d, d] against the oracle: whole tensor and every (sequence, head)."""
+    eh = oracle.rel_fro(hT, h_ref)
+    sh = oracle.rel_fro_slices(hT, h_ref, [(n, n + 1) for n in range(hT.shape[0])])
+    i, h = np.unravel_index(int(sh.argmax()), sh.shape)
+    assert eh <= S_TOL and sh.max() <= S_TOL, f"state rel err {eh:.3e}, worst {sh.max():.3e} ({i}, {h})"
+    record({"hT": eh, "hT_slice_max": float(sh.max())})
 
 
 def small(seqlens, H=4, gate="logsigmoid", h0=True, seed=0, qk="l2"):
@@ -77,13 +123,13 @@ def small(seqlens, H=4, gate="logsigmoid", h0=True, seed=0, qk="l2"):
 def test_prefill_ragged_lengths(sg, T):
     x = small([T], H=3, seed=T)
     o, hT = run_prefill(sg, x)
-    check(o, hT, *ref_prefill(x))
+    check(o, hT, *ref_prefill(x), bounds=bounds_of(x))
 
 
 def test_prefill_tiny_workload(sg):
     x = inputs.make_prefill("tiny")
     o, hT = run_prefill(sg, x)
-    check(o, hT, *ref_prefill(x))
+    check(o, hT, *ref_prefill(x), bounds=bounds_of(x))
 
 
 @pytest.mark.parametrize("lens", [[0, 5, 1, 64, 0, 130], [1, 1, 1], [700, 0], [64] * 9,
@@ -92,7 +138,7 @@ def test_prefill_varlen_with_empty_and_short(sg, lens):
     x = small(lens, H=2, seed=len(lens))
     o, hT = run_prefill(sg, x)
     o_ref, h_ref = ref_prefill(x)
-    check(o, hT, o_ref, h_ref)
+    check(o, hT, o_ref, h_ref, bounds=bounds_of(x))
     # empty sequences return h0 exactly
     for n, L in enumerate(lens):
         if L == 0:
@@ -109,7 +155,7 @@ def test_prefill_mixed_segment_shapes(sg, seed):
     x = inputs.make_prefill("varlen", seqlens=lens, H=16, seed=seed)
     o, hT = run_prefill(sg, x)
     o_ref, h_ref = ref_prefill(x)
-    check(o, hT, o_ref, h_ref)
+    check(o, hT, o_ref, h_ref, bounds=bounds_of(x))
 
 
 def test_prefill_batched_rows(sg):
@@ -122,28 +168,28 @@ def test_prefill_batched_rows(sg):
     h0 = torch.randn((3, 2, 128, 128)) * 0.02
     xb = dict(q=q, k=k, v=v, g=g, h0=h0, cu_seqlens=None, scale=x["scale"])
     o, hT = run_prefill(sg, xb)
-    check(o, hT, *ref_prefill(xb))
+    check(o, hT, *ref_prefill(xb), bounds=bounds_of(xb))
 
 
 @pytest.mark.parametrize("H", [1, 3, 32])
 def test_prefill_head_counts(sg, H):
     x = small([333], H=H, seed=H, qk="rms", gate="const")
     o, hT = run_prefill(sg, x)
-    check(o, hT, *ref_prefill(x))
+    check(o, hT, *ref_prefill(x), bounds=bounds_of(x))
 
 
 def test_prefill_g_zero(sg):
     x = small([500], H=2, seed=9)
     x["g"] = torch.zeros_like(x["g"])
     o, hT = run_prefill(sg, x)
-    check(o, hT, *ref_prefill(x))
+    check(o, hT, *ref_prefill(x), bounds=bounds_of(x))
 
 
 def test_prefill_g_very_negative(sg):
     x = small([300], H=2, seed=10)
     x["g"] = torch.full_like(x["g"], -30.0)
     o, hT = run_prefill(sg, x)
-    check(o, hT, *ref_prefill(x))
+    check(o, hT, *ref_prefill(x), bounds=bounds_of(x))
 
 
 def test_prefill_h0_only(sg):
@@ -151,7 +197,7 @@ def test_prefill_h0_only(sg):
     x["k"] = torch.zeros_like(x["k"])
     x["v"] = torch.zeros_like(x["v"])
     o, hT = run_prefill(sg, x)
-    check(o, hT, *ref_prefill(x))
+    check(o, hT, *ref_prefill(x), bounds=bounds_of(x))
 
 
 def test_prefill_without_final_state(sg):
@@ -159,7 +205,7 @@ def test_prefill_without_final_state(sg):
     o, hT = run_prefill(sg, x, output_final_state=False)
     assert hT is None
     o_ref, _ = ref_prefill(x)
-    check(o, None, o_ref, None)
+    check(o, None, o_ref, None, bounds=bounds_of(x))
 
 
 def test_prefill_zero_tokens_returns_h0(sg):
@@ -252,8 +298,7 @@ def test_decode_small(sg, N, H, steps):
     cu = torch.arange(N + 1, dtype=torch.int64) * steps
     o_ref, h_ref = oracle.recurrent(q, k, v, g, x["scale"], h0=S0, cu_seqlens=cu)
     od = torch.stack(outs).transpose(0, 1).reshape(N * steps, H, 128)
-    assert oracle.rel_fro(od.float(), o_ref) <= O_TOL
-    assert oracle.rel_fro(S.cpu(), h_ref) <= S_TOL
+    check(od, S.cpu(), o_ref, h_ref, bounds=[(n * steps, (n + 1) * steps) for n in range(N)])
 
 
 def test_decode_empty_batch_is_noop(sg):
@@ -288,7 +333,7 @@ def test_bad_cu_seqlens_reported_and_skipped(sg, cu):
 def test_full_sala_layer(sg):
     x = inputs.make_prefill("sala_layer")
     o, hT = run_prefill(sg, x)
-    check(o, hT, *ref_prefill(x))
+    check(o, hT, *ref_prefill(x), bounds=bounds_of(x))
 
 
 def test_full_varlen(sg):
@@ -297,8 +342,8 @@ def test_full_varlen(sg):
     heads = [0, 5, 17, 31]
     o_ref, _ = ref_prefill(x, heads=heads)
     _, h_ref = ref_prefill(x, want_o=False)
-    check(o, hT, o_ref, None, heads=heads)
-    assert oracle.rel_fro(hT, h_ref) <= S_TOL
+    check(o, hT, o_ref, None, heads=heads, bounds=bounds_of(x))
+    check_states(hT, h_ref)
 
 
 def test_full_long(sg):
@@ -307,8 +352,8 @@ def test_full_long(sg):
     heads = [0, 13, 31]
     o_ref, _ = ref_prefill(x, heads=heads)
     _, h_ref = ref_prefill(x, want_o=False)
-    check(o, hT, o_ref, None, heads=heads)
-    assert oracle.rel_fro(hT, h_ref) <= S_TOL
+    check(o, hT, o_ref, None, heads=heads, bounds=bounds_of(x))
+    check_states(hT, h_ref)
 
 
 def test_full_decode_sampled_sequences(sg):
@@ -328,5 +373,4 @@ def test_full_decode_sampled_sequences(sg):
     o_ref, h_ref = oracle.recurrent(sel(x["q"]), sel(x["k"]), sel(x["v"]), sel(x["g"]),
                                     x["scale"], h0=S0[seqs], cu_seqlens=cu)
     od = o_all[:, seqs].cpu().transpose(0, 1).reshape(N * w.steps, H, 128)
-    assert oracle.rel_fro(od.float(), o_ref) <= O_TOL
-    assert oracle.rel_fro(S[seqs].cpu(), h_ref) <= S_TOL
+    check(od, S[seqs].cpu(), o_ref, h_ref, bounds=[(n * w.steps, (n + 1) * w.steps) for n in range(N)])

@@ -80,6 +80,22 @@ def test_noalloc_matches_allocating_entry_point_on_two_calls(lib):
     assert sala_gla.get_device_status() == 0
 
 
+def test_noalloc_lengthens_segments_to_fit_its_scratch(lib):
+    # 28 sequences x 2048 tokens x 32 heads: the allocating path cuts 1024-token segments
+    # (56 per head, 1792 units of 64 KB: 117 MB of hand-off states), which does not fit the
+    # 64 MiB array; the no-alloc path lengthens the segments until at most ~1000 units remain
+    # (here: one segment per sequence). The results agree within the parity tolerances.
+    x = inputs.make_prefill("varlen", seqlens=(2048,) * 28, seed=17)
+    o_ref, h_ref = _outputs(x)
+    assert _call(lib.sala_gla_chunk_fwd, x, o_ref, h_ref) == 0
+    o, hT = _outputs(x)
+    assert _call(lib.sala_gla_chunk_fwd_noalloc, x, o, hT) == 0
+    assert oracle.rel_fro(o.cpu().float(), o_ref.cpu().float()) <= 1e-2
+    assert oracle.rel_fro(hT.cpu(), h_ref.cpu()) <= 5e-3
+    from gated_linear_attention_gb300 import sala_gla
+    assert sala_gla.get_device_status() == 0
+
+
 def test_noalloc_repeated_call_is_stable(lib):
     x = inputs.make_prefill("tiny")
     o1, h1 = _outputs(x)

@@ -53,6 +53,8 @@ DeviceState *device_state(int *err) {
         d.init_error = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
         if (d.init_error != cudaSuccess) return;
         d.init_error = setup_fused_kernel();
+        if (d.init_error != cudaSuccess) return;
+        d.init_error = setup_gdn_chunk_kernel();
     });
     if (d.init_error != cudaSuccess) {
         *err = SALA_ERR_CUDA;
@@ -79,7 +81,8 @@ std::atomic<uint32_t> g_epoch{0};
 // ---- timing instrumentation -------------------------------------------------------------
 const char *const kKernelNames[kKernelCount] = {"seg_table", "prefill_fused", "recurrent_step",
                                                 "recurrent_step_indexed", "output_norm_gate",
-                                                "qk_prologue", "gdn_step", "gdn_fwd"};
+                                                "qk_prologue", "gdn_step", "gdn_fwd",
+                                                "gdn_newv"};
 struct TimingRecord {
     int id;
     cudaEvent_t start, stop;
@@ -423,6 +426,53 @@ int sala_gla_gdn_fwd(const void *q, const void *k, const void *v, const float *g
                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SALA_ERR_CUDA;
     return SALA_OK;
+}
+
+int sala_gla_gdn_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, float scale, const float *h0,
+                           const int64_t *cu_seqlens, void *o, float *hT, int64_t B, int64_t T,
+                           int32_t H, int64_t num_seqs, void *stream) {
+    if (B < 1 || T < 0 || H < 1) return SALA_ERR_INVALID_ARG;
+    if (cu_seqlens && (B != 1 || num_seqs < 1)) return SALA_ERR_INVALID_ARG;
+    const int64_t nseq = cu_seqlens ? num_seqs : B;
+    const int64_t T_total = B * T;
+    // TMA coordinates of the tiles are 32-bit token indices
+    if (T_total > (int64_t(1) << 31) - 64 || nseq * H > (int64_t(1) << 31) - 1) return SALA_ERR_INVALID_ARG;
+    if (T_total > 0 && (!q || !k || !v || !g || !beta || !o)) return SALA_ERR_INVALID_ARG;
+    const void *al[8] = {q, k, v, g, beta, o, h0, hT};
+    for (const void *p : al)
+        if (p && !aligned16(p)) return SALA_ERR_MISALIGNED;
+    if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 7u)) return SALA_ERR_MISALIGNED;
+    const size_t vec = static_cast<size_t>(T_total) * H * kD * 2, gb = static_cast<size_t>(T_total) * H * 4;
+    const size_t sb = static_cast<size_t>(nseq) * H * kD * kD * 4;
+    const void *ins[7] = {q, k, v, g, beta, h0, cu_seqlens};
+    const size_t in_sz[7] = {vec, vec, vec, gb, gb, h0 ? sb : 0, cu_seqlens ? size_t(nseq + 1) * 8 : 0};
+    for (int i = 0; i < 7; ++i)
+        if (overlaps(o, vec, ins[i], in_sz[i]) || overlaps(hT, sb, ins[i], in_sz[i]))
+            return SALA_ERR_INVALID_ARG;
+    if (overlaps(o, vec, hT, sb)) return SALA_ERR_INVALID_ARG;
+    if (!hT && T_total == 0) return SALA_OK;
+    int err = SALA_OK;
+    DeviceState *d = device_state(&err);
+    if (!d) return err;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // new_v of every token, then the Simple GLA chunked prefill with it in place of v
+    void *nv = nullptr;
+    if (T_total > 0 && cudaMallocFromPoolAsync(&nv, vec, d->pool, st) != cudaSuccess)
+        return SALA_ERR_CUDA;
+    SegTable tab{};
+    tab.cu = cu_seqlens;
+    tab.T_row = T;
+    tab.nseq = nseq;
+    int rc = SALA_OK;
+    if (T_total > 0 &&
+        launch_gdn_newv(k, v, g, beta, h0, tab, T_total, nv, H, d->status, st) != cudaSuccess)
+        rc = SALA_ERR_CUDA;
+    if (rc == SALA_OK)
+        rc = sala_gla_chunk_fwd(q, k, T_total > 0 ? nv : v, g, scale, h0, cu_seqlens, o, hT, B, T,
+                                H, num_seqs, stream);
+    if (nv && cudaFreeAsync(nv, st) != cudaSuccess && rc == SALA_OK) rc = SALA_ERR_CUDA;
+    return rc;
 }
 
 int sala_gla_chunk_fwd(const void *q, const void *k, const void *v, const float *g, float scale,

@@ -45,7 +45,7 @@ __device__ __forceinline__ bool named_any(int id, int n, bool x) {
 // Bounded wait that also gives up as soon as another role has aborted. The fast path (phase
 // already complete) is inline; the polling loop is a call, which keeps the many wait sites of
 // the persistent kernels small (their code shares one instruction cache).
-__device__ __noinline__ bool wait_or_abort_slow(uint64_t *bar, uint32_t parity,
+static __device__ __noinline__ bool wait_or_abort_slow(uint64_t *bar, uint32_t parity,
                                                 volatile int *abort_flag, int *status) {
     const uint64_t t0 = tc::global_timer_ns();
     while (!(SALA_WAIT_POLL_NS ? tc::mbar_test_wait(bar, parity) : tc::mbar_try_wait(bar, parity))) {

@@ -1,0 +1,522 @@
+// The gated delta rule (GDN) in its chunked form: the state-dependent value of every token.
+//
+// "Formulas and Code for Adapting Inference to GDN/KDA Linear Modules", section 1.2 (formulas
+// 11-17): per sequence and head, per 64-token chunk with in-chunk log-decay prefix sums b,
+// decay matrix Gamma[i][j] = exp(b_i - b_j), keys and values scaled by the write strengths
+// (K_beta = diag(beta) K, V_beta = diag(beta) V) and S the state entering the chunk:
+//   T     = (I + tril(K_beta K^T * Gamma, -1))^-1          (the UT transform, formula 11)
+//   W     = T (K_beta * exp(b)),  U = T V_beta              (formulas 12, 13)
+//   new_v = U - W S                                         (formula 15)
+//   S    <- exp(b_C) S + (K * exp(b_C - b))^T new_v         (formula 16)
+// The output (formula 17) and the state refresh are the Simple GLA chunk products with new_v
+// in place of v, so sala_gla_gdn_chunk_fwd runs this kernel for new_v and then the chunked
+// Simple GLA prefill on (q, k, new_v, g), which returns o and the final states.
+//
+// One CTA of 128 threads per (sequence, head) walks the chunks in order, the state in tensor
+// memory in fp32 (lane = key row, column = value index). Contractions (tcgen05.mma kind::f16,
+// bf16 operands, fp32 accumulators in tensor memory):
+//   X     = K K^T            M=64  N=64  K=128  (scores of the UT transform)
+//   W     = T (K_beta e^b)   M=64  N=128 K=64
+//   U     = T V_beta         M=64  N=128 K=64
+//   U    += (-W) S           M=64  N=128 K=128  (U becomes new_v)
+//   S    += K~^T new_v       M=128 N=128 K=64   (after S *= exp(b_C) in tensor memory)
+// T itself is inverted on the CUDA cores in fp32 (two diagonal 32 x 32 blocks by forward
+// substitution, then the off-diagonal block T21 = -T2 A21 T1). Every factor is at most 1
+// (b is non-increasing), so no range handling is needed. K and V tiles arrive by TMA, double
+// buffered (the next chunk's tiles load while this one is processed). Every wait is bounded
+// (2 s); a timeout records SALA_ERR_TIMEOUT and the CTA stops after draining its MMAs.
+#include "chunk_tc.cuh"
+
+namespace sala {
+namespace {
+
+using namespace tck;
+
+constexpr int kGThreads = 128;
+constexpr float kLog2eG = 1.4426950408889634f;
+constexpr int kAS = 68;   // row stride (floats) of the fp32 A and T matrices in shared memory
+
+// dynamic shared memory (offsets from a 1024-aligned base)
+constexpr uint32_t kGK = 0;                        // K tiles [2] (TMA)
+constexpr uint32_t kGV = kGK + 2 * kTile;          // V tiles [2] (TMA)
+constexpr uint32_t kGKbe = kGV + 2 * kTile;        // K * beta e^b (MN-major B of W)
+constexpr uint32_t kGVb = kGKbe + kTile;           // V * beta (MN-major B of U)
+constexpr uint32_t kGKt = kGVb + kTile;            // K * e^(bC - b) (MN-major A of the S update)
+constexpr uint32_t kGNv = kGKt + kTile;            // new_v bf16 (MN-major B of the S update)
+constexpr uint32_t kGW = kGNv + kTile;             // -W bf16 [t][k] (K-major A)
+constexpr uint32_t kGS = kGW + kTile;              // S bf16 [k][v] (MN-major B), 2 x 16 KB
+constexpr uint32_t kGT = kGS + 2 * kSRegion;       // T bf16 [t][s] (K-major A), one region
+constexpr uint32_t kGAf = kGT + kRegion;           // A fp32 [64][kAS]
+constexpr uint32_t kGTf = kGAf + 64 * kAS * 4;     // T fp32 [64][kAS]
+constexpr uint32_t kGY = kGTf + 64 * kAS * 4;      // Y = A21 T1 fp32 [32][33]
+constexpr uint32_t kGB = kGY + 32 * 33 * 4;        // b [64], beta [64]
+constexpr uint32_t kGBytes = kGB + 2 * 64 * 4;
+constexpr uint32_t kGSmem = kGBytes + 1024;
+static_assert(kGSmem <= 227 * 1024, "shared memory budget");
+
+// TMEM columns
+constexpr uint32_t kGtS = 0, kGtX = 128, kGtW = 192, kGtU = 320, kGtCols = 512;
+constexpr uint32_t kIdX = tc::idesc_bf16_f32(64, 64, 0, 0);
+constexpr uint32_t kIdWU = tc::idesc_bf16_f32(64, 128, 0, 1);
+constexpr uint32_t kIdS = tc::idesc_bf16_f32(128, 128, 1, 1);
+
+__device__ __forceinline__ uint64_t gdesc_k(uint32_t addr) {          // K-major, SW128
+    return tc::smem_desc_sw128(0, 16, 1024) | ((addr >> 4) & 0x3FFFu);
+}
+__device__ __forceinline__ uint64_t gdesc_mn64(uint32_t addr) {       // MN-major, 64-row tiles
+    return tc::smem_desc_sw128(0, kRegion, 1024) | ((addr >> 4) & 0x3FFFu);
+}
+__device__ __forceinline__ uint64_t gdesc_mn128(uint32_t addr) {      // MN-major, 128-row tiles
+    return tc::smem_desc_sw128(0, kSRegion, 1024) | ((addr >> 4) & 0x3FFFu);
+}
+
+struct GdnChunkArgs {
+    const float *g, *beta;    // [T_total, H]
+    const float *h0;          // [nseq, H, 128, 128] or null
+    uint16_t *nv;             // bf16 [T_total, H, 128], written
+    const int64_t *cu;        // [nseq + 1] or null (rows of T_row tokens)
+    int64_t T_row, nseq, T_total;
+    int H;
+};
+
+// bounded wait of every thread of the CTA on phase `par` of `bar`; false on timeout
+__device__ __forceinline__ bool gwait(uint64_t *bar, uint32_t par, int *status, volatile int *bad) {
+    if (*bad) return false;
+    if (tc::mbar_try_wait(bar, par & 1)) return true;
+    const uint64_t t0 = tc::global_timer_ns();
+    while (!tc::mbar_try_wait(bar, par & 1)) {
+        if (*bad) return false;
+        if (tc::global_timer_ns() - t0 > kWaitNs) {
+            *bad = 1;
+            record_status(status, SALA_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kGThreads, 1)
+gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+    __shared__ uint64_t full[2], bar_x, bar_wu, bar_nv, bar_s, drain;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int bad_flag;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = p.H;
+    const int unit = blockIdx.x;
+    const int64_t n = unit / H;
+    const int h = unit % H;
+    // sequence bounds, kept inside the tensors whatever cu holds
+    int64_t t0 = p.cu ? p.cu[n] : n * p.T_row;
+    int64_t t1 = p.cu ? p.cu[n + 1] : (n + 1) * p.T_row;
+    t0 = max(int64_t(0), min(t0, p.T_total));
+    t1 = max(t0, min(t1, p.T_total));
+    const int nch = static_cast<int>((t1 - t0 + kChunk - 1) / kChunk);
+
+    if (tid == 0) {
+        tc::mbar_init(&full[0], 1);
+        tc::mbar_init(&full[1], 1);
+        tc::mbar_init(&bar_x, 1);
+        tc::mbar_init(&bar_wu, 1);
+        tc::mbar_init(&bar_nv, 1);
+        tc::mbar_init(&bar_s, 1);
+        tc::mbar_init(&drain, 1);
+        bad_flag = 0;
+        tc::fence_barrier_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_slot, kGtCols);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    volatile int *bad = &bad_flag;
+    const uint32_t sb = tc::smem_u32(sm);
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    float *bsm = reinterpret_cast<float *>(sm + kGB);
+    float *betasm = bsm + 64;
+    float *Af = reinterpret_cast<float *>(sm + kGAf);
+    float *Tf = reinterpret_cast<float *>(sm + kGTf);
+    float *Yf = reinterpret_cast<float *>(sm + kGY);
+
+    // the state entering the sequence: row k (= TMEM lane = thread) of h0, or zeros
+    {
+        const float *src = p.h0 ? p.h0 + (static_cast<size_t>(n) * H + h) * kD * kD + tid * kD : nullptr;
+#pragma unroll 1
+        for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t r[32];
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                const float4 x = src ? *reinterpret_cast<const float4 *>(src + 32 * c4 + i)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                r[i] = __float_as_uint(x.x);
+                r[i + 1] = __float_as_uint(x.y);
+                r[i + 2] = __float_as_uint(x.z);
+                r[i + 3] = __float_as_uint(x.w);
+            }
+            tc::tmem_st_32x32b_x32(tmem + lane_base + kGtS + 32 * c4, r);
+        }
+        tc::tmem_st_wait();
+    }
+
+    auto load_chunk = [&](int c) {   // thread 0: TMA of chunk c's K and V tiles
+        const int buf = c & 1;
+        const int32_t x0 = static_cast<int32_t>(t0 + int64_t(c) * kChunk);
+        uint64_t *bar = &full[buf];
+        tc::mbar_arrive_expect_tx(bar, 2 * kTile);
+        uint8_t *kd = sm + kGK + buf * kTile, *vd = sm + kGV + buf * kTile;
+        tc::tma_load_3d(kd, &maps.k, 0, h, x0, bar);
+        tc::tma_load_3d(kd + kRegion, &maps.k, 64, h, x0, bar);
+        tc::tma_load_3d(vd, &maps.v, 0, h, x0, bar);
+        tc::tma_load_3d(vd + kRegion, &maps.v, 64, h, x0, bar);
+    };
+    if (tid == 0 && nch > 0) {
+        tc::tma_prefetch_desc(&maps.k);
+        tc::tma_prefetch_desc(&maps.v);
+        load_chunk(0);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+
+    uint32_t fpar = 0;      // bit b: next phase of full[b]
+    uint32_t pending = 0;   // bit b: a load into buffer b is issued and not yet waited for
+    if (nch > 0) pending = 1;
+#pragma unroll 1
+    for (int c = 0; c < nch; ++c) {
+        const int buf = c & 1;
+        const int64_t c0 = t0 + int64_t(c) * kChunk;
+        const int nv = static_cast<int>(min(int64_t(kChunk), t1 - c0));
+        if (c + 1 < nch) {   // its buffer was last read in chunk c - 1
+            if (tid == 0) {
+                tc::fence_proxy_async_smem();
+                load_chunk(c + 1);
+            }
+            pending |= 1u << ((c + 1) & 1);
+        }
+        // log-decays and write strengths of the chunk (zero past nv), prefix sums b
+        if (tid < 64) {
+            const bool live = tid < nv;
+            const float gv = live ? p.g[(c0 + tid) * H + h] : 0.f;
+            betasm[tid] = live ? p.beta[(c0 + tid) * H + h] : 0.f;
+            float run = gv;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, run, off);
+                if (lane >= off) run += y;
+            }
+            bsm[tid] = run;
+        }
+        __syncthreads();
+        if (tid >= 32 && tid < 64) bsm[tid] += bsm[31];
+        const bool ok_full = gwait(&full[buf], (fpar >> buf) & 1, status, bad);
+        fpar ^= 1u << buf;
+        pending &= ~(1u << buf);
+        if (__syncthreads_or(!ok_full)) break;
+        const float bC = bsm[nv - 1];
+        const uint32_t kt = sb + kGK + buf * kTile;
+
+        // X = K K^T
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t o4 = ((ks >> 2) * kRegion + (ks & 3) * 32) >> 4;
+                tc::umma_bf16(tmem + kGtX, gdesc_k(kt) + o4, gdesc_k(kt) + o4, kIdX, ks > 0);
+            }
+            tc::umma_commit(&bar_x);
+        }
+        // meanwhile: K * beta e^b, V * beta, K * e^(bC - b) from the tiles (row r, 64 columns
+        // per thread; rows >= nv zero)
+        {
+            const int r = tid & 63, half = tid >> 6;
+            const bool live = r < nv;
+            const float br = bsm[r], be = betasm[r];
+            const float fkb = live ? be * tc::ex2(br * kLog2eG) : 0.f;
+            const float fkt = live ? tc::ex2((bC - br) * kLog2eG) : 0.f;
+            const float fv = live ? be : 0.f;
+            const uint8_t *ksrc = sm + kGK + buf * kTile + half * kRegion;
+            const uint8_t *vsrc = sm + kGV + buf * kTile + half * kRegion;
+            uint8_t *dkb = sm + kGKbe + half * kRegion, *dkt = sm + kGKt + half * kRegion;
+            uint8_t *dvb = sm + kGVb + half * kRegion;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                const uint32_t off = sw(r, c8);
+                const uint4 kx = *reinterpret_cast<const uint4 *>(ksrc + off);
+                const uint4 vx = *reinterpret_cast<const uint4 *>(vsrc + off);
+                uint4 y;
+                y.x = mul_bf16x2(kx.x, fkb); y.y = mul_bf16x2(kx.y, fkb);
+                y.z = mul_bf16x2(kx.z, fkb); y.w = mul_bf16x2(kx.w, fkb);
+                *reinterpret_cast<uint4 *>(dkb + off) = y;
+                y.x = mul_bf16x2(kx.x, fkt); y.y = mul_bf16x2(kx.y, fkt);
+                y.z = mul_bf16x2(kx.z, fkt); y.w = mul_bf16x2(kx.w, fkt);
+                *reinterpret_cast<uint4 *>(dkt + off) = y;
+                y.x = mul_bf16x2(vx.x, fv); y.y = mul_bf16x2(vx.y, fv);
+                y.z = mul_bf16x2(vx.z, fv); y.w = mul_bf16x2(vx.w, fv);
+                *reinterpret_cast<uint4 *>(dvb + off) = y;
+            }
+        }
+        tc::fence_proxy_async_smem();
+        if (__syncthreads_or(!gwait(&bar_x, c, status, bad))) break;
+        tc::tc_fence_after();
+        // A[t][s] = beta_t exp(b_t - b_s) X[t][s] for s < t, else 0 (M=64 accumulator: rows
+        // t = 16 warp + (lane & 15) in lanes 0-15 of the quarter; lanes 0-15 get columns 0-31
+        // of those rows, lanes 16-31 columns 32-63)
+        {
+            uint32_t x[32];
+            tc::tmem_ld_16x32bx2_x32(tmem + lane_base + kGtX, x);
+            tc::tmem_ld_wait();
+            const int t = warp * 16 + (lane & 15), s0 = 32 * (lane >> 4);
+            const float bt = bsm[t] * kLog2eG, be = betasm[t];
+            float *arow = Af + t * kAS + s0;
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                float4 w;
+                w.x = (s0 + i < t) ? be * tc::ex2(bt - bsm[s0 + i] * kLog2eG) * __uint_as_float(x[i]) : 0.f;
+                w.y = (s0 + i + 1 < t) ? be * tc::ex2(bt - bsm[s0 + i + 1] * kLog2eG) * __uint_as_float(x[i + 1]) : 0.f;
+                w.z = (s0 + i + 2 < t) ? be * tc::ex2(bt - bsm[s0 + i + 2] * kLog2eG) * __uint_as_float(x[i + 2]) : 0.f;
+                w.w = (s0 + i + 3 < t) ? be * tc::ex2(bt - bsm[s0 + i + 3] * kLog2eG) * __uint_as_float(x[i + 3]) : 0.f;
+                *reinterpret_cast<float4 *>(arow + i) = w;
+            }
+        }
+        __syncthreads();
+        // T = (I + A)^-1. Diagonal blocks T1, T2 (32 x 32): thread (blk, j) solves column j by
+        // forward substitution, T[i][j] = -sum_{m < i} A[i][m] T[m][j] with T[j][j] = 1 (the
+        // column is zero above j, so the sum may run over every m < i)
+        if (tid < 64) {
+            const int blk = tid >> 5, j = tid & 31, o = 32 * blk;
+            float col[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) col[i] = (i == j) ? 1.f : 0.f;
+#pragma unroll
+            for (int i = 1; i < 32; ++i) {
+                const float *ar = Af + (o + i) * kAS + o;
+                float acc = 0.f;
+#pragma unroll
+                for (int m = 0; m < i; ++m) acc = fmaf(ar[m], col[m], acc);
+                if (i > j) col[i] = -acc;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) Tf[(o + i) * kAS + o + j] = col[i];
+        }
+        __syncthreads();
+        // Y = A21 T1 (rows 32-63, columns 0-31 of A times T1): thread: row i, columns 8 q8 .. + 7
+        {
+            const int i = tid >> 2, j0 = 8 * (tid & 3);
+            const float *ar = Af + (32 + i) * kAS;
+            float acc[8] = {};
+#pragma unroll 4
+            for (int m = 0; m < 32; ++m) {
+                const float am = ar[m];
+                const float *tr = Tf + m * kAS + j0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = fmaf(am, tr[e], acc[e]);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) Yf[i * 33 + j0 + e] = acc[e];
+        }
+        __syncthreads();
+        // T21 = -T2 Y
+        {
+            const int i = tid >> 2, j0 = 8 * (tid & 3);
+            const float *tr = Tf + (32 + i) * kAS + 32;
+            float acc[8] = {};
+#pragma unroll 4
+            for (int m = 0; m < 32; ++m) {
+                const float tm = tr[m];
+                const float *yr = Yf + m * 33 + j0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = fmaf(tm, yr[e], acc[e]);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) Tf[(32 + i) * kAS + j0 + e] = -acc[e];
+            // the upper off-diagonal block is zero
+#pragma unroll
+            for (int e = 0; e < 8; ++e) Tf[i * kAS + 32 + j0 + e] = 0.f;
+        }
+        __syncthreads();
+        // T to bf16, K-major [t][s] (one 64-column region): thread: row t, 32 columns
+        {
+            const int t = tid & 63, half = tid >> 6;
+            const float *tr = Tf + t * kAS + 32 * half;
+            uint8_t *dst = sm + kGT;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint4 w;
+                w.x = float2_to_bf16x2(tr[8 * c4], tr[8 * c4 + 1]);
+                w.y = float2_to_bf16x2(tr[8 * c4 + 2], tr[8 * c4 + 3]);
+                w.z = float2_to_bf16x2(tr[8 * c4 + 4], tr[8 * c4 + 5]);
+                w.w = float2_to_bf16x2(tr[8 * c4 + 6], tr[8 * c4 + 7]);
+                *reinterpret_cast<uint4 *>(dst + sw(t, 4 * half + c4)) = w;
+            }
+        }
+        tc::fence_proxy_async_smem();
+        __syncthreads();
+        // W = T (K beta e^b), U = T (V beta)
+        if (tid == 0) {
+            tc::tc_fence_after();
+            const uint64_t dt = gdesc_k(sb + kGT);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                tc::umma_bf16(tmem + kGtW, dt + ((ks * 32) >> 4), gdesc_mn64(sb + kGKbe) + ks * (2048 >> 4), kIdWU, ks > 0);
+                tc::umma_bf16(tmem + kGtU, dt + ((ks * 32) >> 4), gdesc_mn64(sb + kGVb) + ks * (2048 >> 4), kIdWU, ks > 0);
+            }
+            tc::umma_commit(&bar_wu);
+        }
+        // meanwhile: the state entering the chunk to bf16 [k][v] (MN-major B of W S), and S
+        // taken on by exp(bC) for the update at the end of the chunk (thread = key row k)
+        {
+            const float eC = tc::ex2(bC * kLog2eG);
+            uint8_t *dst = sm + kGS;
+#pragma unroll 1
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t r[32];
+                tc::tmem_ld_32x32b_x32(tmem + lane_base + kGtS + 32 * c4, r);
+                tc::tmem_ld_wait();
+                // columns v = 32 c4 .. + 31: region v / 64, 16-byte chunks 4 (c4 & 1) .. + 3
+                uint8_t *reg = dst + (c4 >> 1) * kSRegion;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint4 w;
+                    w.x = float2_to_bf16x2(__uint_as_float(r[8 * q4]), __uint_as_float(r[8 * q4 + 1]));
+                    w.y = float2_to_bf16x2(__uint_as_float(r[8 * q4 + 2]), __uint_as_float(r[8 * q4 + 3]));
+                    w.z = float2_to_bf16x2(__uint_as_float(r[8 * q4 + 4]), __uint_as_float(r[8 * q4 + 5]));
+                    w.w = float2_to_bf16x2(__uint_as_float(r[8 * q4 + 6]), __uint_as_float(r[8 * q4 + 7]));
+                    *reinterpret_cast<uint4 *>(reg + sw(tid, 4 * (c4 & 1) + q4)) = w;
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * eC);
+                tc::tmem_st_32x32b_x32(tmem + lane_base + kGtS + 32 * c4, r);
+            }
+            tc::tmem_st_wait();
+        }
+        tc::fence_proxy_async_smem();
+        if (__syncthreads_or(!gwait(&bar_wu, c, status, bad))) break;
+        tc::tc_fence_after();
+        // -W to bf16 [t][k] (K-major A of W S): thread: row t, columns 32 (lane >> 4) .. of each
+        // 64-column half
+        {
+            const int t = warp * 16 + (lane & 15), sh = lane >> 4;
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t x[32];
+                tc::tmem_ld_16x32bx2_x32(tmem + lane_base + kGtW + 64 * hf, x);
+                tc::tmem_ld_wait();
+                uint8_t *dst = sm + kGW + hf * kRegion;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint4 w;
+                    w.x = float2_to_bf16x2(-__uint_as_float(x[8 * c4]), -__uint_as_float(x[8 * c4 + 1]));
+                    w.y = float2_to_bf16x2(-__uint_as_float(x[8 * c4 + 2]), -__uint_as_float(x[8 * c4 + 3]));
+                    w.z = float2_to_bf16x2(-__uint_as_float(x[8 * c4 + 4]), -__uint_as_float(x[8 * c4 + 5]));
+                    w.w = float2_to_bf16x2(-__uint_as_float(x[8 * c4 + 6]), -__uint_as_float(x[8 * c4 + 7]));
+                    *reinterpret_cast<uint4 *>(dst + sw(t, 4 * sh + c4)) = w;
+                }
+            }
+        }
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        __syncthreads();
+        // new_v = U + (-W) S
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t oa = ((ks >> 2) * kRegion + (ks & 3) * 32) >> 4;
+                tc::umma_bf16(tmem + kGtU, gdesc_k(sb + kGW) + oa, gdesc_mn128(sb + kGS) + ks * (2048 >> 4), kIdWU, 1u);
+            }
+            tc::umma_commit(&bar_nv);
+        }
+        if (__syncthreads_or(!gwait(&bar_nv, c, status, bad))) break;
+        tc::tc_fence_after();
+        // new_v to bf16: the MN-major B of the state update [s][v], and out to global memory
+        {
+            const int t = warp * 16 + (lane & 15), sh = lane >> 4;
+            const bool live = t < nv;
+            uint16_t *grow = p.nv + ((c0 + t) * H + h) * kD;
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t x[32];
+                tc::tmem_ld_16x32bx2_x32(tmem + lane_base + kGtU + 64 * hf, x);
+                tc::tmem_ld_wait();
+                uint8_t *dst = sm + kGNv + hf * kRegion;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint4 w;
+                    w.x = float2_to_bf16x2(__uint_as_float(x[8 * c4]), __uint_as_float(x[8 * c4 + 1]));
+                    w.y = float2_to_bf16x2(__uint_as_float(x[8 * c4 + 2]), __uint_as_float(x[8 * c4 + 3]));
+                    w.z = float2_to_bf16x2(__uint_as_float(x[8 * c4 + 4]), __uint_as_float(x[8 * c4 + 5]));
+                    w.w = float2_to_bf16x2(__uint_as_float(x[8 * c4 + 6]), __uint_as_float(x[8 * c4 + 7]));
+                    *reinterpret_cast<uint4 *>(dst + sw(t, 4 * sh + c4)) = w;
+                    if (live)
+                        *reinterpret_cast<uint4 *>(grow + 64 * hf + 32 * sh + 8 * c4) = w;
+                }
+            }
+        }
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        __syncthreads();
+        // S += (K e^(bC - b))^T new_v
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                tc::umma_bf16(tmem + kGtS, gdesc_mn64(sb + kGKt) + ks * (2048 >> 4),
+                              gdesc_mn64(sb + kGNv) + ks * (2048 >> 4), kIdS, 1u);
+            tc::umma_commit(&bar_s);
+        }
+        if (__syncthreads_or(!gwait(&bar_s, c, status, bad))) break;
+        tc::tc_fence_after();
+    }
+
+    // no MMA or copy may be in flight when the CTA ends
+    tc::tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        tc::umma_commit(&drain);
+        if (!tc::mbar_wait(&drain, 0, kWaitNs)) record_status(status, SALA_ERR_TIMEOUT);
+        // tiles still landing if the loop stopped early: every load issued, but not waited for
+        for (int b = 0; b < 2; ++b)
+            if ((pending >> b) & 1) (void)tc::mbar_wait(&full[b], (fpar >> b) & 1, kWaitNs);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kGtCols);
+    }
+}
+
+cudaError_t setup_gdn_chunk_kernel() {
+    return cudaFuncSetAttribute(gdn_newv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(kGSmem));
+}
+
+cudaError_t launch_gdn_newv(const void *k, const void *v, const float *g, const float *beta,
+                            const float *h0, const SegTable &t, int64_t T_total, void *nv, int H,
+                            int *status, cudaStream_t st) {
+    if (t.nseq == 0 || T_total == 0) return cudaSuccess;
+    tck::TcMaps maps;
+    // the q and o maps are not used here: k and v stand in for them
+    cudaError_t e = tck::make_maps(&maps, k, k, v, nv, T_total, H);
+    if (e != cudaSuccess) return e;
+    GdnChunkArgs p;
+    p.g = g;
+    p.beta = beta;
+    p.h0 = h0;
+    p.nv = static_cast<uint16_t *>(nv);
+    p.cu = t.cu;
+    p.T_row = t.T_row;
+    p.nseq = t.nseq;
+    p.T_total = T_total;
+    p.H = H;
+    LaunchTimer timer(kKGdnNewv, st);
+    gdn_newv_kernel<<<static_cast<unsigned>(t.nseq * H), kGThreads, kGSmem, st>>>(maps, p, status);
+    return cudaGetLastError();
+}
+
+}  // namespace sala

@@ -17,6 +17,7 @@ enum KernelId {
     kKQkPrologue,
     kKGdnStep,
     kKGdnFwd,
+    kKGdnNewv,
     kKernelCount
 };
 
@@ -102,6 +103,14 @@ cudaError_t launch_gdn_fwd(const void *q, const void *k, const void *v, const fl
 // of the wait for a predecessor's state (0: the default 2 s) and a unit whose flag is withheld
 // (-1: none).
 void prefill_fault_knobs(uint64_t *wait_ns, int64_t *withhold);
+
+// The gated delta rule's chunked form: new_v = U - W S of every token (bf16 [T_total, H, 128]
+// into nv) for sala_gla_gdn_chunk_fwd, one CTA per (sequence, head); sequence bounds from t.cu
+// (or rows of t.T_row tokens), kept inside the tensors.
+cudaError_t setup_gdn_chunk_kernel();
+cudaError_t launch_gdn_newv(const void *k, const void *v, const float *g, const float *beta,
+                            const float *h0, const SegTable &t, int64_t T_total, void *nv, int H,
+                            int *status, cudaStream_t st);
 
 // Nonzero tag of one prefill call for the hand-off flags (differs from the previous call's).
 uint32_t next_prefill_epoch();

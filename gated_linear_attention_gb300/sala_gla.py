@@ -43,6 +43,8 @@ SIGNATURES = {
     "sala_gla_gdn_recurrent_step": ([_p, _p, _p, _p, _p, _f32, _p, _p, _i64, _i32, _p], ctypes.c_int),
     "sala_gla_gdn_fwd": ([_p, _p, _p, _p, _p, _f32, _p, _p, _p, _p, _i64, _i64, _i32, _i64, _p],
                          ctypes.c_int),
+    "sala_gla_gdn_chunk_fwd": ([_p, _p, _p, _p, _p, _f32, _p, _p, _p, _p, _i64, _i64, _i32, _i64,
+                                _p], ctypes.c_int),
     "sala_gla_qk_prologue": ([_p, _p, _pro, _p, _p, _i64, _i64, _i32, _i64, _p], ctypes.c_int),
     "sala_gla_output_norm_gate": ([_p, _p, _p, _f32, _p, _i64, _i32, _p], ctypes.c_int),
     "sala_gla_chunk_fwd_noalloc": ([_p, _p, _p, _p, _f32, _p, _p, _p, _p, _i64, _i64, _i32,
@@ -296,10 +298,11 @@ def output_norm_gate(o, z, w, eps=1e-6, out=None, stream=None):
 
 
 def gdn_fwd(q, k, v, g, beta, scale, h0=None, cu_seqlens=None, output_final_state=True,
-            o=None, hT=None, stream=None):
-    """``sala_gla_gdn_fwd``: the gated delta rule over whole sequences (recurrent form).
-    q, k, v: bf16 [B, T, H, 128] or packed [T, H, 128] with ``cu_seqlens``; g, beta: fp32
-    [B, T, H] / [T, H]. Returns (o, hT or None)."""
+            o=None, hT=None, stream=None, chunked=False):
+    """``sala_gla_gdn_fwd`` (recurrent form) or, with ``chunked=True``,
+    ``sala_gla_gdn_chunk_fwd`` (chunked form on the tensor cores): the gated delta rule over
+    whole sequences. q, k, v: bf16 [B, T, H, 128] or packed [T, H, 128] with ``cu_seqlens``;
+    g, beta: fp32 [B, T, H] / [T, H]. Returns (o, hT or None)."""
     if q.dim() == 4:
         Bn, T, H, D = q.shape
         nseq, packed = Bn, False
@@ -325,10 +328,11 @@ def gdn_fwd(q, k, v, g, beta, scale, h0=None, cu_seqlens=None, output_final_stat
         hT = torch.empty((nseq, H, 128, 128), dtype=torch.float32, device=q.device)
     if not output_final_state:
         hT = None
-    rc = load().sala_gla_gdn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
-                                 _ptr(h0), _ptr(cu_seqlens) if packed else None, _ptr(o), _ptr(hT),
-                                 Bn, T, H, nseq if packed else 0, _stream(stream))
-    _check(rc, "sala_gla_gdn_fwd")
+    name = "sala_gla_gdn_chunk_fwd" if chunked else "sala_gla_gdn_fwd"
+    rc = getattr(load(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                               _ptr(h0), _ptr(cu_seqlens) if packed else None, _ptr(o), _ptr(hT),
+                               Bn, T, H, nseq if packed else 0, _stream(stream))
+    _check(rc, name)
     return o, hT
 
 

@@ -254,6 +254,28 @@ int sala_gla_gdn_fwd(const void *q, const void *k, const void *v, const float *g
                      void *stream);
 
 /*
+ * The gated delta rule over whole sequences in its chunked form ("Formulas and Code for
+ * Adapting Inference to GDN/KDA Linear Modules", section 1.2, formulas 11-17; chunk size 64):
+ * the same results as sala_gla_gdn_fwd (decay first, then the delta-rule write and the read),
+ * computed chunk by chunk on the tensor cores. Per chunk the UT transform
+ * T = (I + tril(diag(beta) K K^T * Gamma, -1))^-1 gives W = T (diag(beta) K * exp(b)) and
+ * U = T diag(beta) V, and the state-dependent values new_v = U - W S; the output and the state
+ * refresh are then the Simple GLA chunk products with new_v in place of v, which this call
+ * computes with the chunked prefill of sala_gla_chunk_fwd (its segment-parallel state pass and
+ * hand-off included). The new_v pass runs one CTA per (sequence, head), so it is parallel over
+ * sequences and heads; the prefill that follows is parallel over segments as well.
+ *
+ * Arguments, layouts and errors as sala_gla_gdn_fwd; in addition T (B * T) must stay below
+ * 2^31 - 64 tokens. Scratch: the bf16 new_v [B * T, H, 128] and the prefill's scratch, from the
+ * library's stream-ordered pool (as sala_gla_chunk_fwd). A malformed cu_seqlens is reported as
+ * by sala_gla_chunk_fwd (SALA_ERR_BAD_SEQLENS; nothing written).
+ */
+int sala_gla_gdn_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, float scale, const float *h0,
+                           const int64_t *cu_seqlens, void *o, float *hT, int64_t B, int64_t T,
+                           int32_t H, int64_t num_seqs, void *stream);
+
+/*
  * Chunked prefill that allocates nothing: same arguments, layouts, results and errors as
  * sala_gla_chunk_fwd, plus SALA_ERR_TOO_LARGE. The pages have no counterpart to this entry
  * point; it exists for callers that cannot allocate device memory while they run the layer:

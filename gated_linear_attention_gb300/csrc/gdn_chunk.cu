@@ -12,7 +12,7 @@
 // in place of v, so sala_gla_gdn_chunk_fwd runs this kernel for new_v and then the chunked
 // Simple GLA prefill on (q, k, new_v, g), which returns o and the final states.
 //
-// One CTA of 128 threads per (sequence, head) walks the chunks in order, the state in tensor
+// One CTA of 256 threads per (sequence, head) walks the chunks in order, the state in tensor
 // memory in fp32 (lane = key row, column = value index). Contractions (tcgen05.mma kind::f16,
 // bf16 operands, fp32 accumulators in tensor memory):
 //   X     = K K^T            M=64  N=64  K=128  (scores of the UT transform)
@@ -32,7 +32,7 @@ namespace {
 
 using namespace tck;
 
-constexpr int kGThreads = 128;
+constexpr int kGThreads = 256;
 constexpr float kLog2eG = 1.4426950408889634f;
 constexpr int kAS = 68;   // row stride (floats) of the fp32 A and T matrices in shared memory
 
@@ -48,8 +48,8 @@ constexpr uint32_t kGS = kGW + kTile;              // S bf16 [k][v] (MN-major B)
 constexpr uint32_t kGT = kGS + 2 * kSRegion;       // T bf16 [t][s] (K-major A), one region
 constexpr uint32_t kGAf = kGT + kRegion;           // A fp32 [64][kAS]
 constexpr uint32_t kGTf = kGAf + 64 * kAS * 4;     // T fp32 [64][kAS]
-constexpr uint32_t kGY = kGTf + 64 * kAS * 4;      // Y = A21 T1 fp32 [32][33]
-constexpr uint32_t kGB = kGY + 32 * 33 * 4;        // b [64], beta [64]
+constexpr uint32_t kGY = kGTf + 64 * kAS * 4;      // Y = A21 T1 fp32 [32][36]
+constexpr uint32_t kGB = kGY + 32 * 36 * 4;        // b [64], beta [64]
 constexpr uint32_t kGBytes = kGB + 2 * 64 * 4;
 constexpr uint32_t kGSmem = kGBytes + 1024;
 static_assert(kGSmem <= 227 * 1024, "shared memory budget");
@@ -95,6 +95,17 @@ __device__ __forceinline__ bool gwait(uint64_t *bar, uint32_t par, int *status, 
     return true;
 }
 
+// 16-lane form, 16 columns: thread i gets lane (base + i % 16), columns [col + 32 (i / 16), + 16)
+__device__ __forceinline__ void tmem_ld_16x32bx2_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16], 32;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kGThreads, 1)
@@ -106,6 +117,8 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
     __shared__ uint32_t tmem_slot;
     __shared__ int bad_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // warps w and w + 4 reach the same quarter of the tensor-memory lanes; they split columns
+    const int quarter = warp & 3, wg = warp >> 2;
     const int H = p.H;
     const int unit = blockIdx.x;
     const int64_t n = unit / H;
@@ -138,18 +151,19 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
     const uint32_t tmem = tmem_slot;
     volatile int *bad = &bad_flag;
     const uint32_t sb = tc::smem_u32(sm);
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     float *bsm = reinterpret_cast<float *>(sm + kGB);
     float *betasm = bsm + 64;
     float *Af = reinterpret_cast<float *>(sm + kGAf);
     float *Tf = reinterpret_cast<float *>(sm + kGTf);
     float *Yf = reinterpret_cast<float *>(sm + kGY);
 
-    // the state entering the sequence: row k (= TMEM lane = thread) of h0, or zeros
+    // the state entering the sequence: row k (= TMEM lane) of h0, or zeros; columns 64 wg ..
     {
-        const float *src = p.h0 ? p.h0 + (static_cast<size_t>(n) * H + h) * kD * kD + tid * kD : nullptr;
+        const int k = quarter * 32 + lane;
+        const float *src = p.h0 ? p.h0 + (static_cast<size_t>(n) * H + h) * kD * kD + k * kD + 64 * wg : nullptr;
 #pragma unroll 1
-        for (int c4 = 0; c4 < 4; ++c4) {
+        for (int c4 = 0; c4 < 2; ++c4) {
             uint32_t r[32];
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
@@ -160,7 +174,7 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
                 r[i + 2] = __float_as_uint(x.z);
                 r[i + 3] = __float_as_uint(x.w);
             }
-            tc::tmem_st_32x32b_x32(tmem + lane_base + kGtS + 32 * c4, r);
+            tc::tmem_st_32x32b_x32(tmem + lane_base + kGtS + 64 * wg + 32 * c4, r);
         }
         tc::tmem_st_wait();
     }
@@ -184,6 +198,12 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
     tc::tc_fence_before();
     __syncthreads();
 
+    // g and beta of the next chunk, loaded a chunk ahead (threads 0-63: row tid)
+    float g_nx = 0.f, be_nx = 0.f;
+    if (tid < 64 && nch > 0 && tid < t1 - t0) {
+        g_nx = p.g[(t0 + tid) * H + h];
+        be_nx = p.beta[(t0 + tid) * H + h];
+    }
     uint32_t fpar = 0;      // bit b: next phase of full[b]
     uint32_t pending = 0;   // bit b: a load into buffer b is issued and not yet waited for
     if (nch > 0) pending = 1;
@@ -201,9 +221,14 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         }
         // log-decays and write strengths of the chunk (zero past nv), prefix sums b
         if (tid < 64) {
-            const bool live = tid < nv;
-            const float gv = live ? p.g[(c0 + tid) * H + h] : 0.f;
-            betasm[tid] = live ? p.beta[(c0 + tid) * H + h] : 0.f;
+            const float gv = g_nx;
+            betasm[tid] = be_nx;
+            const int64_t cn = c0 + kChunk;
+            g_nx = be_nx = 0.f;
+            if (c + 1 < nch && cn + tid < t1) {
+                g_nx = p.g[(cn + tid) * H + h];
+                be_nx = p.beta[(cn + tid) * H + h];
+            }
             float run = gv;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -234,18 +259,19 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         // meanwhile: K * beta e^b, V * beta, K * e^(bC - b) from the tiles (row r, 64 columns
         // per thread; rows >= nv zero)
         {
-            const int r = tid & 63, half = tid >> 6;
+            const int r = tid & 63, q4 = tid >> 6;   // row r, columns 32 q4 .. + 31
             const bool live = r < nv;
             const float br = bsm[r], be = betasm[r];
             const float fkb = live ? be * tc::ex2(br * kLog2eG) : 0.f;
             const float fkt = live ? tc::ex2((bC - br) * kLog2eG) : 0.f;
             const float fv = live ? be : 0.f;
+            const int half = q4 >> 1;
             const uint8_t *ksrc = sm + kGK + buf * kTile + half * kRegion;
             const uint8_t *vsrc = sm + kGV + buf * kTile + half * kRegion;
             uint8_t *dkb = sm + kGKbe + half * kRegion, *dkt = sm + kGKt + half * kRegion;
             uint8_t *dvb = sm + kGVb + half * kRegion;
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
+            for (int c8 = 4 * (q4 & 1); c8 < 4 * (q4 & 1) + 4; ++c8) {
                 const uint32_t off = sw(r, c8);
                 const uint4 kx = *reinterpret_cast<const uint4 *>(ksrc + off);
                 const uint4 vx = *reinterpret_cast<const uint4 *>(vsrc + off);
@@ -268,14 +294,15 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         // t = 16 warp + (lane & 15) in lanes 0-15 of the quarter; lanes 0-15 get columns 0-31
         // of those rows, lanes 16-31 columns 32-63)
         {
-            uint32_t x[32];
-            tc::tmem_ld_16x32bx2_x32(tmem + lane_base + kGtX, x);
+            // (the 16-column form: warps w and w + 4 take columns 16 wg .. + 15 of each half)
+            uint32_t x[16];
+            tmem_ld_16x32bx2_x16(tmem + lane_base + kGtX + 16 * wg, x);
             tc::tmem_ld_wait();
-            const int t = warp * 16 + (lane & 15), s0 = 32 * (lane >> 4);
+            const int t = quarter * 16 + (lane & 15), s0 = 32 * (lane >> 4) + 16 * wg;
             const float bt = bsm[t] * kLog2eG, be = betasm[t];
             float *arow = Af + t * kAS + s0;
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
+            for (int i = 0; i < 16; i += 4) {
                 float4 w;
                 w.x = (s0 + i < t) ? be * tc::ex2(bt - bsm[s0 + i] * kLog2eG) * __uint_as_float(x[i]) : 0.f;
                 w.y = (s0 + i + 1 < t) ? be * tc::ex2(bt - bsm[s0 + i + 1] * kLog2eG) * __uint_as_float(x[i + 1]) : 0.f;
@@ -305,54 +332,52 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
             for (int i = 0; i < 32; ++i) Tf[(o + i) * kAS + o + j] = col[i];
         }
         __syncthreads();
-        // Y = A21 T1 (rows 32-63, columns 0-31 of A times T1): thread: row i, columns 8 q8 .. + 7
+        // Y = A21 T1 (rows 32-63, columns 0-31 of A times T1) and then T21 = -T2 Y: thread:
+        // row i, columns j0 .. j0 + 3 (one scalar and one 16-byte load per m)
         {
-            const int i = tid >> 2, j0 = 8 * (tid & 3);
+            const int i = tid >> 3, j0 = 4 * (tid & 7);
+            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
             const float *ar = Af + (32 + i) * kAS;
-            float acc[8] = {};
-#pragma unroll 4
+#pragma unroll 8
             for (int m = 0; m < 32; ++m) {
-                const float am = ar[m];
-                const float *tr = Tf + m * kAS + j0;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = fmaf(am, tr[e], acc[e]);
+                const float4 tm = *reinterpret_cast<const float4 *>(Tf + m * kAS + j0);
+                const float u = ar[m];
+                y.x = fmaf(u, tm.x, y.x); y.y = fmaf(u, tm.y, y.y);
+                y.z = fmaf(u, tm.z, y.z); y.w = fmaf(u, tm.w, y.w);
             }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) Yf[i * 33 + j0 + e] = acc[e];
+            *reinterpret_cast<float4 *>(Yf + i * 36 + j0) = y;
         }
         __syncthreads();
-        // T21 = -T2 Y
         {
-            const int i = tid >> 2, j0 = 8 * (tid & 3);
+            const int i = tid >> 3, j0 = 4 * (tid & 7);
+            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
             const float *tr = Tf + (32 + i) * kAS + 32;
-            float acc[8] = {};
-#pragma unroll 4
+#pragma unroll 8
             for (int m = 0; m < 32; ++m) {
-                const float tm = tr[m];
-                const float *yr = Yf + m * 33 + j0;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = fmaf(tm, yr[e], acc[e]);
+                const float4 ym = *reinterpret_cast<const float4 *>(Yf + m * 36 + j0);
+                const float u = tr[m];
+                y.x = fmaf(u, ym.x, y.x); y.y = fmaf(u, ym.y, y.y);
+                y.z = fmaf(u, ym.z, y.z); y.w = fmaf(u, ym.w, y.w);
             }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) Tf[(32 + i) * kAS + j0 + e] = -acc[e];
+            *reinterpret_cast<float4 *>(Tf + (32 + i) * kAS + j0) = make_float4(-y.x, -y.y, -y.z, -y.w);
             // the upper off-diagonal block is zero
-#pragma unroll
-            for (int e = 0; e < 8; ++e) Tf[i * kAS + 32 + j0 + e] = 0.f;
+            *reinterpret_cast<float4 *>(Tf + i * kAS + 32 + j0) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         __syncthreads();
         // T to bf16, K-major [t][s] (one 64-column region): thread: row t, 32 columns
         {
-            const int t = tid & 63, half = tid >> 6;
-            const float *tr = Tf + t * kAS + 32 * half;
+            const int t = tid & 63, q4 = tid >> 6;   // row t, columns 16 q4 .. + 15
+            const float *tr = Tf + t * kAS + 16 * q4;
             uint8_t *dst = sm + kGT;
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
+            for (int c2 = 0; c2 < 2; ++c2) {
+                const int c4 = c2;
                 uint4 w;
                 w.x = float2_to_bf16x2(tr[8 * c4], tr[8 * c4 + 1]);
                 w.y = float2_to_bf16x2(tr[8 * c4 + 2], tr[8 * c4 + 3]);
                 w.z = float2_to_bf16x2(tr[8 * c4 + 4], tr[8 * c4 + 5]);
                 w.w = float2_to_bf16x2(tr[8 * c4 + 6], tr[8 * c4 + 7]);
-                *reinterpret_cast<uint4 *>(dst + sw(t, 4 * half + c4)) = w;
+                *reinterpret_cast<uint4 *>(dst + sw(t, 2 * q4 + c2)) = w;
             }
         }
         tc::fence_proxy_async_smem();
@@ -373,8 +398,9 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         {
             const float eC = tc::ex2(bC * kLog2eG);
             uint8_t *dst = sm + kGS;
+            const int krow = quarter * 32 + lane;
 #pragma unroll 1
-            for (int c4 = 0; c4 < 4; ++c4) {
+            for (int c4 = 2 * wg; c4 < 2 * wg + 2; ++c4) {
                 uint32_t r[32];
                 tc::tmem_ld_32x32b_x32(tmem + lane_base + kGtS + 32 * c4, r);
                 tc::tmem_ld_wait();
@@ -387,7 +413,7 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
                     w.y = float2_to_bf16x2(__uint_as_float(r[8 * q4 + 2]), __uint_as_float(r[8 * q4 + 3]));
                     w.z = float2_to_bf16x2(__uint_as_float(r[8 * q4 + 4]), __uint_as_float(r[8 * q4 + 5]));
                     w.w = float2_to_bf16x2(__uint_as_float(r[8 * q4 + 6]), __uint_as_float(r[8 * q4 + 7]));
-                    *reinterpret_cast<uint4 *>(reg + sw(tid, 4 * (c4 & 1) + q4)) = w;
+                    *reinterpret_cast<uint4 *>(reg + sw(krow, 4 * (c4 & 1) + q4)) = w;
                 }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * eC);
@@ -401,9 +427,9 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         // -W to bf16 [t][k] (K-major A of W S): thread: row t, columns 32 (lane >> 4) .. of each
         // 64-column half
         {
-            const int t = warp * 16 + (lane & 15), sh = lane >> 4;
-#pragma unroll 1
-            for (int hf = 0; hf < 2; ++hf) {
+            const int t = quarter * 16 + (lane & 15), sh = lane >> 4;
+            {
+                const int hf = wg;
                 uint32_t x[32];
                 tc::tmem_ld_16x32bx2_x32(tmem + lane_base + kGtW + 64 * hf, x);
                 tc::tmem_ld_wait();
@@ -436,11 +462,11 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         tc::tc_fence_after();
         // new_v to bf16: the MN-major B of the state update [s][v], and out to global memory
         {
-            const int t = warp * 16 + (lane & 15), sh = lane >> 4;
+            const int t = quarter * 16 + (lane & 15), sh = lane >> 4;
             const bool live = t < nv;
             uint16_t *grow = p.nv + ((c0 + t) * H + h) * kD;
-#pragma unroll 1
-            for (int hf = 0; hf < 2; ++hf) {
+            {
+                const int hf = wg;
                 uint32_t x[32];
                 tc::tmem_ld_16x32bx2_x32(tmem + lane_base + kGtU + 64 * hf, x);
                 tc::tmem_ld_wait();

@@ -197,7 +197,8 @@ def summarise_clocks(rows):
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of
 # each kernel as it stands, on the workload the bench times; retaken whenever a kernel changes
 # (None: not measured since the last change).
-MEASURED_TRAFFIC = {"prefill_fused": 251_610_112, "recurrent_step": 1_019_700_000,
+MEASURED_TRAFFIC = {"prefill_fused": None, "prefill_fused_varlen": 2_605_000_000,
+                    "prefill_fused_long": 5_130_000_000, "recurrent_step": 1_019_700_000,
                     "recurrent_step_indexed": 483_300_000, "output_norm_gate": 167_600_000,
                     "qk_prologue": 204_400_000, "gdn_step": 1_019_300_000,
                     "gdn_fwd": 775_600_000}
@@ -460,6 +461,7 @@ def run_ours(args, dist):
         launches_decode += prologue.pop("_launches")
         gdn_prefill = run_gdn_prefill(args, dist, dev, peaks, sala_gla, inputs)
         launches_decode += gdn_prefill.pop("_launches")
+        launches_decode += gdn_prefill["chunked"].pop("_launches")
 
     # the other prefill workloads: varlen (8 packed sequences, 66,560 tokens, h0), long
     # (131,072 tokens, h0) and tiny (256 tokens, 4 heads)
@@ -739,11 +741,13 @@ def run_decode_pool(args, dist, peaks, sala_gla, inputs, wd, q, k, v, g, o, scal
 
 
 def run_gdn_prefill(args, dist, dev, peaks, sala_gla, inputs):
-    """sala_gla_gdn_fwd, the gated delta rule's recurrent form over a batch of short sequences
-    (64 x 256 tokens, 32 heads; the form the GDN/KDA page uses for short prefills). It is bound
-    by fp32 FMA throughput, not by memory: the recurrence's 4 d^2 = 65,536 multiply-adds per
-    token and head (the kernel executes 3 d^2, keeping the decay as a scalar), against the
-    CUDA cores' 152 SMs x 128 FMA per cycle at the 2.07 GHz clock."""
+    """The gated delta rule over a batch of short sequences (64 x 256 tokens, 32 heads), in its
+    recurrent form (sala_gla_gdn_fwd, the form the GDN/KDA page uses for short prefills) and in
+    its chunked form (sala_gla_gdn_chunk_fwd, sub-object "chunked"). The recurrent kernel is
+    bound by fp32 FMA throughput, not by memory: the recurrence's 4 d^2 = 65,536 multiply-adds
+    per token and head (the kernel executes 3 d^2, keeping the decay as a scalar), against the
+    CUDA cores' 152 SMs x 128 FMA per cycle at the 2.07 GHz clock. The chunked call is
+    reported against the HBM roofline of its algorithmic bytes."""
     import torch
     lens = (256,) * 64
     H = 32
@@ -781,7 +785,46 @@ def run_gdn_prefill(args, dist, dev, peaks, sala_gla, inputs):
     flops = 2.0 * 4 * D * D * T * H
     peak_tflops = 152 * 128 * 2 * 2.07e9 / 1e12
     k_ach = flops / (kern[0] / kern[1] / 1e3) / 1e12
+    # the chunked form (sala_gla_gdn_chunk_fwd): the new_v pass on the tensor cores, then the
+    # chunked Simple GLA prefill; HBM-bound by its algorithmic bytes (q, k, v, g, beta read
+    # once, o written once, h0 read and hT written once per (sequence, head))
+    def call_chunked():
+        sala_gla.gdn_fwd(q, k, v, g, b, x["scale"], h0=h0, cu_seqlens=cu, o=o, hT=hT, chunked=True)
+
+    for _ in range(max(3, args.warmup)):
+        call_chunked()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(steps):
+        call_chunked()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms_c = dist.max(ev0.elapsed_time(ev1))
+    sala_gla.timing_enable(True)
+    for _ in range(steps):
+        call_chunked()
+    torch.cuda.synchronize()
+    sala_gla.timing_enable(False)
+    kc = sala_gla.timing_read()
+    assert sala_gla.get_device_status() == 0
+    nseq = len(lens)
+    gdn_bytes = T * H * (4 * D * 2 + 2 * 4) + 2 * nseq * H * D * D * 4
+    c_kernels = {n: {"us_per_launch": 1e3 * v[0] / v[1], "launches": v[1]} for n, v in kc.items() if v[1]}
+    c_launch_us = sum(1e3 * v[0] / v[1] for v in kc.values() if v[1])
+    c_ach = gdn_bytes / (ms_c / steps / 1e3) / 1e9
+    chunked = {
+        "metric": "gated-delta-rule chunked prefill tokens/s", "value": T * steps / (ms_c / 1e3) * dist.world,
+        "unit": "tokens/s", "ms_per_call": ms_c / steps, "kernels": c_kernels,
+        "speedup_vs_recurrent": (ms / steps) / (ms_c / steps),
+        "roofline": {"kernel": "gdn_newv + seg_table + prefill_fused (whole call)", "bound": "hbm",
+                     "achieved": c_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": c_ach / peaks["hbm_gbs"], "traffic": None,
+                     "bytes_per_call": gdn_bytes, "peak_source": peaks["source"],
+                     "mean_call_us_from_kernels": c_launch_us},
+        "_launches": sum(v[1] for v in kc.values()),
+    }
     return {
+        "chunked": chunked,
         "metric": "gated-delta-rule recurrent prefill tokens/s", "value": T * steps / (ms / 1e3) * dist.world,
         "unit": "tokens/s", "ms_per_call": ms / steps,
         "config": {"workload": "gdn_prefill", "seqlens": "64 x 256", "T": T, "H": H, "d": D,

@@ -11,7 +11,7 @@
 // the pass is: load o (thread t holds 8 consecutive features of each 1024-feature block, so
 // each warp instruction moves 512 contiguous bytes), sum of squares reduced over the CTA,
 // then z and the weight, and the product is stored. (H = 8, 16, 32, 64 take a variant with
-// everything loaded up front; other widths the general kernel below.) HBM-bound: 3 x 2 bytes per feature
+// o and z loaded up front; other widths the general kernel below.) HBM-bound: 3 x 2 bytes per feature
 // (o, z read, out written) plus the weight, which stays in L2.
 #include "launch.h"
 
@@ -90,34 +90,36 @@ output_norm_gate_kernel(const uint16_t *__restrict__ o, const uint16_t *__restri
     }
 }
 
-// The common widths (H = 8, 16, 32, 64: F = 8 kIt kThr features): o, z and the weight of the
-// token are all loaded up front (kIt 16-byte pieces each per thread of kThr), so each CTA has
-// its whole token in flight at once, with up to 1536 threads resident per SM (the register
-// budget of 40 per thread that leaves holds a token without spilling more than a word).
+// The common widths (H = 8, 16, 32, 64: F = 8 kIt kThr features): o and z of the token are
+// loaded up front (kIt 16-byte pieces each per thread of kThr), so each CTA has its whole
+// token in flight at once, with up to 1536 threads resident per SM; the weight (an L2 hit) is
+// read after the reduction, which keeps the registers within that budget. The arithmetic
+// runs on packed fp32 pairs (fma.rn.f32x2 / mul.rn.f32x2, rounding like the scalar forms):
+// at this rate the SM's instruction issue is close to a limit as well.
 template <int kIt, int kThr>
 __global__ void __launch_bounds__(kThr, 1536 / kThr)
 output_norm_gate_fixed_kernel(const uint16_t *__restrict__ o, const uint16_t *__restrict__ z,
                               const uint16_t *__restrict__ w, float eps, uint16_t *out) {
     constexpr int F = kIt * 8 * kThr;
     const size_t tok = static_cast<size_t>(blockIdx.x) * F;
-    uint4 ov[kIt], zv[kIt], wv[kIt];
+    uint4 ov[kIt], zv[kIt];
 #pragma unroll
     for (int m = 0; m < kIt; ++m) {
         const int e = 8 * (threadIdx.x + kThr * m);
         ov[m] = __ldcs(reinterpret_cast<const uint4 *>(o + tok + e));
         zv[m] = __ldcs(reinterpret_cast<const uint4 *>(z + tok + e));
-        wv[m] = __ldg(reinterpret_cast<const uint4 *>(w + e));
     }
-    float ss = 0.f;
+    float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int m = 0; m < kIt; ++m) {
         const uint32_t xs[4] = {ov[m].x, ov[m].y, ov[m].z, ov[m].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const float2 f = bf16x2_to_float2(xs[i]);
-            ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+            s2 = __ffma2_rn(f, f, s2);
         }
     }
+    float ss = s2.x + s2.y;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     __shared__ float part[kThr / 32];
@@ -127,19 +129,23 @@ output_norm_gate_fixed_kernel(const uint16_t *__restrict__ o, const uint16_t *__
 #pragma unroll
     for (int i = 0; i < kThr / 32; ++i) tot += part[i];
     const float rinv = 1.f / sqrtf(tot / static_cast<float>(F) + eps);
+    const float2 r2 = make_float2(rinv, rinv);
 #pragma unroll
     for (int m = 0; m < kIt; ++m) {
         const int e = 8 * (threadIdx.x + kThr * m);
+        const uint4 wv = __ldg(reinterpret_cast<const uint4 *>(w + e));
         const uint32_t xs[4] = {ov[m].x, ov[m].y, ov[m].z, ov[m].w},
                        zs[4] = {zv[m].x, zv[m].y, zv[m].z, zv[m].w},
-                       ws[4] = {wv[m].x, wv[m].y, wv[m].z, wv[m].w};
+                       ws[4] = {wv.x, wv.y, wv.z, wv.w};
         uint32_t r[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const float2 xf = bf16x2_to_float2(xs[i]), zf = bf16x2_to_float2(zs[i]),
                          wf = bf16x2_to_float2(ws[i]);
-            const float g0 = __fdividef(1.f, 1.f + __expf(-zf.x)), g1 = __fdividef(1.f, 1.f + __expf(-zf.y));
-            r[i] = float2_to_bf16x2(xf.x * rinv * wf.x * g0, xf.y * rinv * wf.y * g1);
+            const float2 g = make_float2(__fdividef(1.f, 1.f + __expf(-zf.x)),
+                                         __fdividef(1.f, 1.f + __expf(-zf.y)));
+            const float2 t = __fmul2_rn(__fmul2_rn(__fmul2_rn(xf, r2), wf), g);
+            r[i] = float2_to_bf16x2(t.x, t.y);
         }
         __stcs(reinterpret_cast<uint4 *>(out + tok + e), make_uint4(r[0], r[1], r[2], r[3]));
     }

@@ -7,11 +7,13 @@
 // pos * theta^(-i/64).
 //
 // One CTA per token, one warp per head at a time: lane l holds elements 4l .. 4l + 3 of q and
-// of k (8-byte accesses, a whole 256-byte head vector per warp instruction), the sum of
-// squares is a warp reduction, and the RoPE partner of lane l's elements sits in lane l ^ 16.
-// The angles depend only on the token's position (its index in its sequence plus the
-// sequence's start position), so their cos/sin are computed once per token. HBM-bound:
-// 2 x 256 B read and written per (token, head).
+// of k (8-byte accesses, a whole 256-byte head vector per warp instruction), and the RoPE
+// partner of lane l's elements sits in lane l ^ 16. The angles depend only on the token's
+// position (its index in its sequence plus the sequence's start position), so their cos/sin
+// are computed once per token. HBM-bound: 2 x 256 B read and written per (token, head); at
+// that rate the SM's instruction issue is close to a limit too, so the arithmetic is kept
+// lean: packed fp32 pairs (fma.rn.f32x2, rounding like the scalar forms), the sums of squares
+// of a warp's four heads reduced together, one reciprocal square root per lane.
 #include "launch.h"
 
 #include <cmath>
@@ -20,33 +22,63 @@ namespace sala {
 
 constexpr int kProThreads = 256;
 constexpr int kProWarps = kProThreads / 32;
-constexpr int kProHeadsInFlight = 4;   // heads per warp whose loads are issued together
+constexpr int kProHeadsInFlight = 4;   // heads per warp whose loads are issued together (warp_rms4)
 
-// One head vector (4 elements per lane), first stage: RMSNorm with weight w, the results
-// rounded to bf16 two to a word.
-__device__ __forceinline__ uint2 prologue_norm(uint2 xw, const float (&wv)[4], float eps) {
-    const float2 a01 = bf16x2_to_float2(xw.x), a23 = bf16x2_to_float2(xw.y);
-    float ss = a01.x * a01.x;
-    ss = fmaf(a01.y, a01.y, ss);
-    ss = fmaf(a23.x, a23.x, ss);
-    ss = fmaf(a23.y, a23.y, ss);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float r = rsqrtf(ss * (1.f / kD) + eps);
-    return make_uint2(float2_to_bf16x2(a01.x * r * wv[0], a01.y * r * wv[1]),
-                      float2_to_bf16x2(a23.x * r * wv[2], a23.y * r * wv[3]));
+// 1 / sqrt(x) for x >= eps > 0 (a mean of squares plus eps, always a normal number, so
+// flushing subnormals changes nothing).
+__device__ __forceinline__ float rms_rsqrt(float x) {
+    float r;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
 }
 
-// Second stage: RoPE with the lane's (cos, sin), bf16. The partners (lane l ^ 16) are
-// exchanged in the packed form; ssn is -sin for the first half of the vector (lanes 0-15) and
-// +sin for the second.
-__device__ __forceinline__ uint2 prologue_rope(uint2 y, const float (&cs)[4], const float (&ssn)[4]) {
+// Four sums of squares per lane (heads j = 0..3 of q, or of k) summed over the warp together:
+// the xor-16 step keeps two of them (sending the other two to the partner lane) and the xor-8
+// step one, so a lane then holds the partial of head 2 b4 + b3 (b4, b3: its lane bits 4 and
+// 3), which xor 4, 2 and 1 complete. Each lane turns its total into 1 / rms, and the four
+// factors are broadcast back from lanes 0, 8, 16 and 24.
+__device__ __forceinline__ void warp_rms4(const float (&v)[4], float eps, float (&rn)[4]) {
+    const int lane = threadIdx.x & 31;
+    const bool b4 = lane & 16, b3 = lane & 8;
+    float w[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = b4 ? v[i] : v[i + 2], keep = b4 ? v[i + 2] : v[i];
+        w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+    float t = (b3 ? w[1] : w[0]) + __shfl_xor_sync(0xffffffffu, b3 ? w[0] : w[1], 8);
+    t += __shfl_xor_sync(0xffffffffu, t, 4);
+    t += __shfl_xor_sync(0xffffffffu, t, 2);
+    t += __shfl_xor_sync(0xffffffffu, t, 1);
+    const float r = rms_rsqrt(fmaf(t, 1.f / kD, eps));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) rn[j] = __shfl_sync(0xffffffffu, r, 16 * (j >> 1) + 8 * (j & 1));
+}
+
+// This lane's part of a head vector's sum of squares (its 4 elements).
+__device__ __forceinline__ float sumsq4(uint2 xw) {
+    const float2 a01 = bf16x2_to_float2(xw.x), a23 = bf16x2_to_float2(xw.y);
+    const float2 s2 = __ffma2_rn(a23, a23, __fmul2_rn(a01, a01));
+    return s2.x + s2.y;
+}
+
+// RMSNorm's output for the lane's 4 elements: x / rms * w, rounded to bf16 two to a word.
+__device__ __forceinline__ uint2 scale4(uint2 xw, float r, const float2 (&wv)[2]) {
+    const float2 r2 = make_float2(r, r);
+    const float2 t0 = __fmul2_rn(__fmul2_rn(bf16x2_to_float2(xw.x), r2), wv[0]);
+    const float2 t1 = __fmul2_rn(__fmul2_rn(bf16x2_to_float2(xw.y), r2), wv[1]);
+    return make_uint2(float2_to_bf16x2(t0.x, t0.y), float2_to_bf16x2(t1.x, t1.y));
+}
+
+// RoPE with the lane's (cos, sin) pairs, bf16. The partners (lane l ^ 16) are exchanged in
+// the packed form; ssn is -sin for the first half of the vector (lanes 0-15) and +sin for the
+// second.
+__device__ __forceinline__ uint2 prologue_rope(uint2 y, const float2 (&cs)[2], const float2 (&ssn)[2]) {
     const uint32_t p01 = __shfl_xor_sync(0xffffffffu, y.x, 16);
     const uint32_t p23 = __shfl_xor_sync(0xffffffffu, y.y, 16);
-    const float2 y0 = bf16x2_to_float2(y.x), y1 = bf16x2_to_float2(y.y);
-    const float2 q0 = bf16x2_to_float2(p01), q1 = bf16x2_to_float2(p23);
-    return make_uint2(float2_to_bf16x2(fmaf(q0.x, ssn[0], y0.x * cs[0]), fmaf(q0.y, ssn[1], y0.y * cs[1])),
-                      float2_to_bf16x2(fmaf(q1.x, ssn[2], y1.x * cs[2]), fmaf(q1.y, ssn[3], y1.y * cs[3])));
+    const float2 u0 = __ffma2_rn(bf16x2_to_float2(p01), ssn[0], __fmul2_rn(bf16x2_to_float2(y.x), cs[0]));
+    const float2 u1 = __ffma2_rn(bf16x2_to_float2(p23), ssn[1], __fmul2_rn(bf16x2_to_float2(y.y), cs[1]));
+    return make_uint2(float2_to_bf16x2(u0.x, u0.y), float2_to_bf16x2(u1.x, u1.y));
 }
 
 // One CTA per token: the cos / sin of the 64 rotation angles are found once (into shared
@@ -95,29 +127,37 @@ qk_prologue_kernel(uint16_t *q, uint16_t *k, QkPrologue pro, SegTable t, const i
         const float pos = static_cast<float>(tok - seq_begin(t, n) + (start_pos ? start_pos[n] : 0));
         sincosf(pos * pro.inv_freq[threadIdx.x], &sn_s[threadIdx.x], &cs_s[threadIdx.x]);
     }
-    float wq[4], wk[4];
+    float2 wq[2], wk[2];
     {
         const uint2 a = *reinterpret_cast<const uint2 *>(pro.qw + 4 * lane);
         const uint2 b = *reinterpret_cast<const uint2 *>(pro.kw + 4 * lane);
-        const float2 a0 = bf16x2_to_float2(a.x), a1 = bf16x2_to_float2(a.y);
-        const float2 b0 = bf16x2_to_float2(b.x), b1 = bf16x2_to_float2(b.y);
-        wq[0] = a0.x; wq[1] = a0.y; wq[2] = a1.x; wq[3] = a1.y;
-        wk[0] = b0.x; wk[1] = b0.y; wk[2] = b1.x; wk[3] = b1.y;
+        wq[0] = bf16x2_to_float2(a.x); wq[1] = bf16x2_to_float2(a.y);
+        wk[0] = bf16x2_to_float2(b.x); wk[1] = bf16x2_to_float2(b.y);
     }
+    static_assert(kProHeadsInFlight == 4, "warp_rms4 reduces four heads at a time");
+    // (heads past H: zero or stale values, normalised but never stored)
     auto norm_group = [&]() {
 #pragma unroll
-        for (int j = 0; j < kProHeadsInFlight; ++j) {
-            xq[j] = prologue_norm(xq[j], wq, pro.eps);   // (heads past H: unused lanes' values)
-            xk[j] = prologue_norm(xk[j], wk, pro.eps);
+        for (int side = 0; side < 2; ++side) {
+            uint2 (&xs)[kProHeadsInFlight] = side ? xk : xq;
+            float v[4], rn[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = sumsq4(xs[j]);
+            warp_rms4(v, pro.eps, rn);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) xs[j] = scale4(xs[j], rn[j], side ? wk : wq);
         }
     };
     norm_group();
     __syncthreads();
-    float cs[4], ssn[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        cs[e] = cs_s[(4 * lane + e) & 63];
-        ssn[e] = lane < 16 ? -sn_s[(4 * lane + e) & 63] : sn_s[(4 * lane + e) & 63];
+    float2 cs[2], ssn[2];
+    {
+        const int a = (4 * lane) & 63;
+        const float sg = lane < 16 ? -1.f : 1.f;
+        cs[0] = make_float2(cs_s[a], cs_s[a + 1]);
+        cs[1] = make_float2(cs_s[a + 2], cs_s[a + 3]);
+        ssn[0] = make_float2(sg * sn_s[a], sg * sn_s[a + 1]);
+        ssn[1] = make_float2(sg * sn_s[a + 2], sg * sn_s[a + 3]);
     }
     for (int h0 = warp; h0 < H; h0 += kProWarps * kProHeadsInFlight) {
         if (h0 != warp) {

@@ -58,6 +58,28 @@ def test_prologue_prefill_packed(sg, lens, start):
     assert np.mean(qd.cpu().double().numpy() == q_ref) > 0.95
 
 
+@pytest.mark.parametrize("H", [32, 40])
+def test_prologue_prefill_wide(sg, H):
+    # 32 heads: four per warp in one group; 40: a second group per warp, partly past H
+    lens = [37, 200]
+    T = sum(lens)
+    q, k = _raw_tokens(T, H, seed=H)
+    qw, kw = _weights(3)
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int64)
+    qd, kd = q.cuda(), k.cuda()
+    sg.qk_prologue(qd, kd, qw.cuda(), kw.cuda(), 1e-6, 10000.0, cu_seqlens=cu.cuda())
+    torch.cuda.synchronize()
+    pos = np.concatenate([np.arange(L) for L in lens])
+    q_ref = oracle.qk_prologue(q, qw, pos[:, None])
+    k_ref = oracle.qk_prologue(k, kw, pos[:, None])
+    assert oracle.rel_fro(qd.cpu().float(), q_ref) <= 5e-3
+    assert oracle.rel_fro(kd.cpu().float(), k_ref) <= 5e-3
+    assert np.mean(kd.cpu().double().numpy() == k_ref) > 0.95
+    # every head of every token, separately
+    err = oracle.rel_fro_slices(kd.cpu().float(), k_ref, [(t, t + 1) for t in range(T)])
+    assert err.max() <= 2e-2, f"worst (token, head) error {err.max():.3e}"
+
+
 def test_prologue_prefill_rows(sg):
     # B = 2 rows of 100 tokens without cu_seqlens: positions restart per row
     q, k = _raw_tokens(200, 3, seed=5)

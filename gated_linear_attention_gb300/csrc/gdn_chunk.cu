@@ -13,18 +13,22 @@
 // Simple GLA prefill on (q, k, new_v, g), which returns o and the final states.
 //
 // One CTA of 256 threads per (sequence, head) walks the chunks in order, the state in tensor
-// memory in fp32 (lane = key row, column = value index). Contractions (tcgen05.mma kind::f16,
-// bf16 operands, fp32 accumulators in tensor memory):
+// memory in fp32 (lane = key row, column = value index); two CTAs share an SM (108 KB of
+// shared memory and 256 tensor-memory columns each), so one's serial phases overlap the
+// other's. Contractions (tcgen05.mma kind::f16, bf16 operands, fp32 accumulators in tensor
+// memory, all but the state in one 128-column region used in turn):
 //   X     = K K^T            M=64  N=64  K=128  (scores of the UT transform)
 //   W     = T (K_beta e^b)   M=64  N=128 K=64
-//   U     = T V_beta         M=64  N=128 K=64
+//   U     = T V_beta         M=64  N=128 K=64   (after W has been read out as -W in bf16)
 //   U    += (-W) S           M=64  N=128 K=128  (U becomes new_v)
-//   S    += K~^T new_v       M=128 N=128 K=64   (after S *= exp(b_C) in tensor memory)
+//   S    += K^T (e^(b_C - b) new_v)   M=128 N=128 K=64   (after S *= exp(b_C) in tensor memory;
+//                                     the decay sits on new_v's rows, so K's tile serves as is)
 // T itself is inverted on the CUDA cores in fp32 (two diagonal 32 x 32 blocks by forward
 // substitution, then the off-diagonal block T21 = -T2 A21 T1). Every factor is at most 1
-// (b is non-increasing), so no range handling is needed. K and V tiles arrive by TMA, double
-// buffered (the next chunk's tiles load while this one is processed). Every wait is bounded
-// (2 s); a timeout records SALA_ERR_TIMEOUT and the CTA stops after draining its MMAs.
+// (b is non-increasing), so no range handling is needed. K tiles arrive by TMA, double
+// buffered (the next chunk's tile loads while this one is processed); the V tile loads once
+// the previous chunk's U has read it. Every wait is bounded (2 s); a timeout records
+// SALA_ERR_TIMEOUT and the CTA stops after draining its MMAs and copies.
 #include "chunk_tc.cuh"
 
 namespace sala {
@@ -36,26 +40,35 @@ constexpr int kGThreads = 256;
 constexpr float kLog2eG = 1.4426950408889634f;
 constexpr int kAS = 68;   // row stride (floats) of the fp32 A and T matrices in shared memory
 
-// dynamic shared memory (offsets from a 1024-aligned base)
-constexpr uint32_t kGK = 0;                        // K tiles [2] (TMA)
-constexpr uint32_t kGV = kGK + 2 * kTile;          // V tiles [2] (TMA)
-constexpr uint32_t kGKbe = kGV + 2 * kTile;        // K * beta e^b (MN-major B of W)
-constexpr uint32_t kGVb = kGKbe + kTile;           // V * beta (MN-major B of U)
-constexpr uint32_t kGKt = kGVb + kTile;            // K * e^(bC - b) (MN-major A of the S update)
-constexpr uint32_t kGNv = kGKt + kTile;            // new_v bf16 (MN-major B of the S update)
-constexpr uint32_t kGW = kGNv + kTile;             // -W bf16 [t][k] (K-major A)
-constexpr uint32_t kGS = kGW + kTile;              // S bf16 [k][v] (MN-major B), 2 x 16 KB
-constexpr uint32_t kGT = kGS + 2 * kSRegion;       // T bf16 [t][s] (K-major A), one region
-constexpr uint32_t kGAf = kGT + kRegion;           // A fp32 [64][kAS]
-constexpr uint32_t kGTf = kGAf + 64 * kAS * 4;     // T fp32 [64][kAS]
-constexpr uint32_t kGY = kGTf + 64 * kAS * 4;      // Y = A21 T1 fp32 [32][36]
-constexpr uint32_t kGB = kGY + 32 * 36 * 4;        // b [64], beta [64]
+// dynamic shared memory (offsets from a 1024-aligned base); two CTAs share an SM, so regions
+// are reused across the phases of a chunk:
+//   K [2]  TMA tiles, double buffered; a tile is read by X = K K^T, made into K beta e^b, and
+//          is the A operand of the state update at the end of its chunk
+//   V      TMA tile, scaled in place to V beta (the next chunk's tile loads once U has read it)
+//   R      K beta e^b (B of W), then -W bf16 (A of W S), then new_v scaled per row (B of the
+//          state update)
+//   S      the state entering the chunk in bf16 [k][v] (B of W S), 2 x 16 KB
+//   T      T bf16 [t][s] (A of W and U), one 64-column region
+// During the inverse the fp32 A, T and Y = A21 T1 live in the S and T regions (free then;
+// T bf16 is written from the fp32 T, which sits in the S region, after A and Y are dead).
+constexpr uint32_t kGK = 0;
+constexpr uint32_t kGV = kGK + 2 * kTile;
+constexpr uint32_t kGR = kGV + kTile;
+constexpr uint32_t kGS = kGR + kTile;
+constexpr uint32_t kGT = kGS + 2 * kSRegion;
+constexpr uint32_t kGTf = kGS;                     // T fp32 [64][kAS]
+constexpr uint32_t kGAf = kGTf + 64 * kAS * 4;     // A fp32 [64][kAS]
+constexpr uint32_t kGY = kGAf + 64 * kAS * 4;      // Y fp32 [32][36]
+constexpr uint32_t kGB = kGT + kRegion;            // b [64], beta [64]
 constexpr uint32_t kGBytes = kGB + 2 * 64 * 4;
 constexpr uint32_t kGSmem = kGBytes + 1024;
-static_assert(kGSmem <= 227 * 1024, "shared memory budget");
+static_assert(kGY + 32 * 36 * 4 <= kGB, "inverse scratch fits the S and T regions");
+static_assert(kGTf + 64 * kAS * 4 <= kGT, "fp32 T does not overlap the bf16 T it is copied to");
+static_assert(2 * (kGSmem + 1024) <= 228 * 1024, "two CTAs per SM");
 
-// TMEM columns
-constexpr uint32_t kGtS = 0, kGtX = 128, kGtW = 192, kGtU = 320, kGtCols = 512;
+// TMEM columns: the fp32 state, and one accumulator region used in turn by X (64 columns), W,
+// and U / new_v (128 columns each)
+constexpr uint32_t kGtS = 0, kGtAcc = 128, kGtCols = 256;
 constexpr uint32_t kIdX = tc::idesc_bf16_f32(64, 64, 0, 0);
 constexpr uint32_t kIdWU = tc::idesc_bf16_f32(64, 128, 0, 1);
 constexpr uint32_t kIdS = tc::idesc_bf16_f32(128, 128, 1, 1);
@@ -108,12 +121,12 @@ __device__ __forceinline__ void tmem_ld_16x32bx2_x16(uint32_t taddr, uint32_t (&
 
 }  // namespace
 
-__global__ void __launch_bounds__(kGThreads, 1)
+__global__ void __launch_bounds__(kGThreads, 2)
 gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-    __shared__ uint64_t full[2], bar_x, bar_wu, bar_nv, bar_s, drain;
+    __shared__ uint64_t full_k[2], full_v, bar_x, bar_w, bar_nv, bar_s, drain;
     __shared__ uint32_t tmem_slot;
     __shared__ int bad_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -131,10 +144,11 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
     const int nch = static_cast<int>((t1 - t0 + kChunk - 1) / kChunk);
 
     if (tid == 0) {
-        tc::mbar_init(&full[0], 1);
-        tc::mbar_init(&full[1], 1);
+        tc::mbar_init(&full_k[0], 1);
+        tc::mbar_init(&full_k[1], 1);
+        tc::mbar_init(&full_v, 1);
         tc::mbar_init(&bar_x, 1);
-        tc::mbar_init(&bar_wu, 1);
+        tc::mbar_init(&bar_w, 1);
         tc::mbar_init(&bar_nv, 1);
         tc::mbar_init(&bar_s, 1);
         tc::mbar_init(&drain, 1);
@@ -179,21 +193,25 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         tc::tmem_st_wait();
     }
 
-    auto load_chunk = [&](int c) {   // thread 0: TMA of chunk c's K and V tiles
-        const int buf = c & 1;
+    auto load_k = [&](int c) {   // thread 0: TMA of chunk c's K tile into buffer c & 1
         const int32_t x0 = static_cast<int32_t>(t0 + int64_t(c) * kChunk);
-        uint64_t *bar = &full[buf];
-        tc::mbar_arrive_expect_tx(bar, 2 * kTile);
-        uint8_t *kd = sm + kGK + buf * kTile, *vd = sm + kGV + buf * kTile;
+        uint64_t *bar = &full_k[c & 1];
+        tc::mbar_arrive_expect_tx(bar, kTile);
+        uint8_t *kd = sm + kGK + (c & 1) * kTile;
         tc::tma_load_3d(kd, &maps.k, 0, h, x0, bar);
         tc::tma_load_3d(kd + kRegion, &maps.k, 64, h, x0, bar);
-        tc::tma_load_3d(vd, &maps.v, 0, h, x0, bar);
-        tc::tma_load_3d(vd + kRegion, &maps.v, 64, h, x0, bar);
+    };
+    auto load_v = [&](int c) {   // thread 0: TMA of chunk c's V tile
+        const int32_t x0 = static_cast<int32_t>(t0 + int64_t(c) * kChunk);
+        tc::mbar_arrive_expect_tx(&full_v, kTile);
+        tc::tma_load_3d(sm + kGV, &maps.v, 0, h, x0, &full_v);
+        tc::tma_load_3d(sm + kGV + kRegion, &maps.v, 64, h, x0, &full_v);
     };
     if (tid == 0 && nch > 0) {
         tc::tma_prefetch_desc(&maps.k);
         tc::tma_prefetch_desc(&maps.v);
-        load_chunk(0);
+        load_k(0);
+        load_v(0);
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -204,18 +222,20 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         g_nx = p.g[(t0 + tid) * H + h];
         be_nx = p.beta[(t0 + tid) * H + h];
     }
-    uint32_t fpar = 0;      // bit b: next phase of full[b]
-    uint32_t pending = 0;   // bit b: a load into buffer b is issued and not yet waited for
-    if (nch > 0) pending = 1;
+    uint32_t kpar = 0;      // bit b: next phase of full_k[b]
+    int vidx = 0;           // the chunk of the last V load issued
+    uint32_t pending = 0;   // bits 0, 1: a K load into that buffer, bit 2: a V load, issued and
+                            // not yet waited for
+    if (nch > 0) pending = 1u | 4u;
 #pragma unroll 1
     for (int c = 0; c < nch; ++c) {
         const int buf = c & 1;
         const int64_t c0 = t0 + int64_t(c) * kChunk;
         const int nv = static_cast<int>(min(int64_t(kChunk), t1 - c0));
-        if (c + 1 < nch) {   // its buffer was last read in chunk c - 1
+        if (c + 1 < nch) {   // its buffer was last read by chunk c - 1's state update
             if (tid == 0) {
                 tc::fence_proxy_async_smem();
-                load_chunk(c + 1);
+                load_k(c + 1);
             }
             pending |= 1u << ((c + 1) & 1);
         }
@@ -239,9 +259,13 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         }
         __syncthreads();
         if (tid >= 32 && tid < 64) bsm[tid] += bsm[31];
-        const bool ok_full = gwait(&full[buf], (fpar >> buf) & 1, status, bad);
-        fpar ^= 1u << buf;
-        pending &= ~(1u << buf);
+        bool ok_full = gwait(&full_k[buf], (kpar >> buf) & 1, status, bad);
+        if (ok_full) {
+            kpar ^= 1u << buf;
+            pending &= ~(1u << buf);
+        }
+        ok_full = ok_full && gwait(&full_v, c, status, bad);
+        if (ok_full) pending &= ~4u;
         if (__syncthreads_or(!ok_full)) break;
         const float bC = bsm[nv - 1];
         const uint32_t kt = sb + kGK + buf * kTile;
@@ -252,39 +276,34 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t o4 = ((ks >> 2) * kRegion + (ks & 3) * 32) >> 4;
-                tc::umma_bf16(tmem + kGtX, gdesc_k(kt) + o4, gdesc_k(kt) + o4, kIdX, ks > 0);
+                tc::umma_bf16(tmem + kGtAcc, gdesc_k(kt) + o4, gdesc_k(kt) + o4, kIdX, ks > 0);
             }
             tc::umma_commit(&bar_x);
         }
-        // meanwhile: K * beta e^b, V * beta, K * e^(bC - b) from the tiles (row r, 64 columns
-        // per thread; rows >= nv zero)
+        // meanwhile: K * beta e^b into R and V * beta in place, from the tiles (row r, 32
+        // columns per thread; rows >= nv zero)
         {
             const int r = tid & 63, q4 = tid >> 6;   // row r, columns 32 q4 .. + 31
             const bool live = r < nv;
             const float br = bsm[r], be = betasm[r];
             const float fkb = live ? be * tc::ex2(br * kLog2eG) : 0.f;
-            const float fkt = live ? tc::ex2((bC - br) * kLog2eG) : 0.f;
             const float fv = live ? be : 0.f;
             const int half = q4 >> 1;
             const uint8_t *ksrc = sm + kGK + buf * kTile + half * kRegion;
-            const uint8_t *vsrc = sm + kGV + buf * kTile + half * kRegion;
-            uint8_t *dkb = sm + kGKbe + half * kRegion, *dkt = sm + kGKt + half * kRegion;
-            uint8_t *dvb = sm + kGVb + half * kRegion;
+            uint8_t *vb = sm + kGV + half * kRegion;
+            uint8_t *dkb = sm + kGR + half * kRegion;
 #pragma unroll
             for (int c8 = 4 * (q4 & 1); c8 < 4 * (q4 & 1) + 4; ++c8) {
                 const uint32_t off = sw(r, c8);
                 const uint4 kx = *reinterpret_cast<const uint4 *>(ksrc + off);
-                const uint4 vx = *reinterpret_cast<const uint4 *>(vsrc + off);
+                const uint4 vx = *reinterpret_cast<const uint4 *>(vb + off);
                 uint4 y;
                 y.x = mul_bf16x2(kx.x, fkb); y.y = mul_bf16x2(kx.y, fkb);
                 y.z = mul_bf16x2(kx.z, fkb); y.w = mul_bf16x2(kx.w, fkb);
                 *reinterpret_cast<uint4 *>(dkb + off) = y;
-                y.x = mul_bf16x2(kx.x, fkt); y.y = mul_bf16x2(kx.y, fkt);
-                y.z = mul_bf16x2(kx.z, fkt); y.w = mul_bf16x2(kx.w, fkt);
-                *reinterpret_cast<uint4 *>(dkt + off) = y;
                 y.x = mul_bf16x2(vx.x, fv); y.y = mul_bf16x2(vx.y, fv);
                 y.z = mul_bf16x2(vx.z, fv); y.w = mul_bf16x2(vx.w, fv);
-                *reinterpret_cast<uint4 *>(dvb + off) = y;
+                *reinterpret_cast<uint4 *>(vb + off) = y;
             }
         }
         tc::fence_proxy_async_smem();
@@ -296,7 +315,7 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         {
             // (the 16-column form: warps w and w + 4 take columns 16 wg .. + 15 of each half)
             uint32_t x[16];
-            tmem_ld_16x32bx2_x16(tmem + lane_base + kGtX + 16 * wg, x);
+            tmem_ld_16x32bx2_x16(tmem + lane_base + kGtAcc + 16 * wg, x);
             tc::tmem_ld_wait();
             const int t = quarter * 16 + (lane & 15), s0 = 32 * (lane >> 4) + 16 * wg;
             const float bt = bsm[t] * kLog2eG, be = betasm[t];
@@ -311,6 +330,7 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
                 *reinterpret_cast<float4 *>(arow + i) = w;
             }
         }
+        tc::tc_fence_before();   // X is read: W may overwrite its columns
         __syncthreads();
         // T = (I + A)^-1. Diagonal blocks T1, T2 (32 x 32): thread (blk, j) solves column j by
         // forward substitution, T[i][j] = -sum_{m < i} A[i][m] T[m][j] with T[j][j] = 1 (the
@@ -382,16 +402,14 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         }
         tc::fence_proxy_async_smem();
         __syncthreads();
-        // W = T (K beta e^b), U = T (V beta)
+        // W = T (K beta e^b)
         if (tid == 0) {
             tc::tc_fence_after();
             const uint64_t dt = gdesc_k(sb + kGT);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                tc::umma_bf16(tmem + kGtW, dt + ((ks * 32) >> 4), gdesc_mn64(sb + kGKbe) + ks * (2048 >> 4), kIdWU, ks > 0);
-                tc::umma_bf16(tmem + kGtU, dt + ((ks * 32) >> 4), gdesc_mn64(sb + kGVb) + ks * (2048 >> 4), kIdWU, ks > 0);
-            }
-            tc::umma_commit(&bar_wu);
+            for (int ks = 0; ks < 4; ++ks)
+                tc::umma_bf16(tmem + kGtAcc, dt + ((ks * 32) >> 4), gdesc_mn64(sb + kGR) + ks * (2048 >> 4), kIdWU, ks > 0);
+            tc::umma_commit(&bar_w);
         }
         // meanwhile: the state entering the chunk to bf16 [k][v] (MN-major B of W S), and S
         // taken on by exp(bC) for the update at the end of the chunk (thread = key row k)
@@ -422,78 +440,90 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
             tc::tmem_st_wait();
         }
         tc::fence_proxy_async_smem();
-        if (__syncthreads_or(!gwait(&bar_wu, c, status, bad))) break;
+        if (__syncthreads_or(!gwait(&bar_w, c, status, bad))) break;
         tc::tc_fence_after();
-        // -W to bf16 [t][k] (K-major A of W S): thread: row t, columns 32 (lane >> 4) .. of each
-        // 64-column half
+        // -W to bf16 [t][k] in R (K-major A of W S; W has read K beta e^b): thread: row t,
+        // columns 32 (lane >> 4) .. of the 64-column half wg
         {
             const int t = quarter * 16 + (lane & 15), sh = lane >> 4;
-            {
-                const int hf = wg;
-                uint32_t x[32];
-                tc::tmem_ld_16x32bx2_x32(tmem + lane_base + kGtW + 64 * hf, x);
-                tc::tmem_ld_wait();
-                uint8_t *dst = sm + kGW + hf * kRegion;
+            uint32_t x[32];
+            tc::tmem_ld_16x32bx2_x32(tmem + lane_base + kGtAcc + 64 * wg, x);
+            tc::tmem_ld_wait();
+            uint8_t *dst = sm + kGR + wg * kRegion;
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    uint4 w;
-                    w.x = float2_to_bf16x2(-__uint_as_float(x[8 * c4]), -__uint_as_float(x[8 * c4 + 1]));
-                    w.y = float2_to_bf16x2(-__uint_as_float(x[8 * c4 + 2]), -__uint_as_float(x[8 * c4 + 3]));
-                    w.z = float2_to_bf16x2(-__uint_as_float(x[8 * c4 + 4]), -__uint_as_float(x[8 * c4 + 5]));
-                    w.w = float2_to_bf16x2(-__uint_as_float(x[8 * c4 + 6]), -__uint_as_float(x[8 * c4 + 7]));
-                    *reinterpret_cast<uint4 *>(dst + sw(t, 4 * sh + c4)) = w;
-                }
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint4 w;
+                w.x = float2_to_bf16x2(-__uint_as_float(x[8 * c4]), -__uint_as_float(x[8 * c4 + 1]));
+                w.y = float2_to_bf16x2(-__uint_as_float(x[8 * c4 + 2]), -__uint_as_float(x[8 * c4 + 3]));
+                w.z = float2_to_bf16x2(-__uint_as_float(x[8 * c4 + 4]), -__uint_as_float(x[8 * c4 + 5]));
+                w.w = float2_to_bf16x2(-__uint_as_float(x[8 * c4 + 6]), -__uint_as_float(x[8 * c4 + 7]));
+                *reinterpret_cast<uint4 *>(dst + sw(t, 4 * sh + c4)) = w;
             }
         }
         tc::fence_proxy_async_smem();
-        tc::tc_fence_before();
+        tc::tc_fence_before();   // W is read: U may overwrite its columns
         __syncthreads();
-        // new_v = U + (-W) S
+        // U = T (V beta), then new_v = U + (-W) S
         if (tid == 0) {
             tc::tc_fence_after();
+            const uint64_t dt = gdesc_k(sb + kGT);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                tc::umma_bf16(tmem + kGtAcc, dt + ((ks * 32) >> 4), gdesc_mn64(sb + kGV) + ks * (2048 >> 4), kIdWU, ks > 0);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t oa = ((ks >> 2) * kRegion + (ks & 3) * 32) >> 4;
-                tc::umma_bf16(tmem + kGtU, gdesc_k(sb + kGW) + oa, gdesc_mn128(sb + kGS) + ks * (2048 >> 4), kIdWU, 1u);
+                tc::umma_bf16(tmem + kGtAcc, gdesc_k(sb + kGR) + oa, gdesc_mn128(sb + kGS) + ks * (2048 >> 4), kIdWU, 1u);
             }
             tc::umma_commit(&bar_nv);
         }
         if (__syncthreads_or(!gwait(&bar_nv, c, status, bad))) break;
         tc::tc_fence_after();
-        // new_v to bf16: the MN-major B of the state update [s][v], and out to global memory
+        if (c + 1 < nch && tid == 0) {   // the V tile is read: the next chunk's may load
+            tc::fence_proxy_async_smem();
+            load_v(c + 1);
+            vidx = c + 1;
+            pending |= 4u;
+        }
+        // new_v out to global memory, and into R scaled by exp(bC - b_t) per row t (zero past
+        // nv): the MN-major B of the state update S += K^T (exp(bC - b) new_v)
         {
             const int t = quarter * 16 + (lane & 15), sh = lane >> 4;
             const bool live = t < nv;
+            const float ft = live ? tc::ex2((bC - bsm[t]) * kLog2eG) : 0.f;
             uint16_t *grow = p.nv + ((c0 + t) * H + h) * kD;
-            {
-                const int hf = wg;
-                uint32_t x[32];
-                tc::tmem_ld_16x32bx2_x32(tmem + lane_base + kGtU + 64 * hf, x);
-                tc::tmem_ld_wait();
-                uint8_t *dst = sm + kGNv + hf * kRegion;
+            uint32_t x[32];
+            tc::tmem_ld_16x32bx2_x32(tmem + lane_base + kGtAcc + 64 * wg, x);
+            tc::tmem_ld_wait();
+            uint8_t *dst = sm + kGR + wg * kRegion;
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    uint4 w;
-                    w.x = float2_to_bf16x2(__uint_as_float(x[8 * c4]), __uint_as_float(x[8 * c4 + 1]));
-                    w.y = float2_to_bf16x2(__uint_as_float(x[8 * c4 + 2]), __uint_as_float(x[8 * c4 + 3]));
-                    w.z = float2_to_bf16x2(__uint_as_float(x[8 * c4 + 4]), __uint_as_float(x[8 * c4 + 5]));
-                    w.w = float2_to_bf16x2(__uint_as_float(x[8 * c4 + 6]), __uint_as_float(x[8 * c4 + 7]));
-                    *reinterpret_cast<uint4 *>(dst + sw(t, 4 * sh + c4)) = w;
-                    if (live)
-                        *reinterpret_cast<uint4 *>(grow + 64 * hf + 32 * sh + 8 * c4) = w;
-                }
+            for (int c4 = 0; c4 < 4; ++c4) {
+                float f[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(x[8 * c4 + i]);
+                uint4 w;
+                w.x = float2_to_bf16x2(f[0], f[1]);
+                w.y = float2_to_bf16x2(f[2], f[3]);
+                w.z = float2_to_bf16x2(f[4], f[5]);
+                w.w = float2_to_bf16x2(f[6], f[7]);
+                if (live) *reinterpret_cast<uint4 *>(grow + 64 * wg + 32 * sh + 8 * c4) = w;
+                w.x = float2_to_bf16x2(f[0] * ft, f[1] * ft);
+                w.y = float2_to_bf16x2(f[2] * ft, f[3] * ft);
+                w.z = float2_to_bf16x2(f[4] * ft, f[5] * ft);
+                w.w = float2_to_bf16x2(f[6] * ft, f[7] * ft);
+                *reinterpret_cast<uint4 *>(dst + sw(t, 4 * sh + c4)) = w;
             }
         }
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
         __syncthreads();
-        // S += (K e^(bC - b))^T new_v
+        // S += K^T (exp(bC - b) new_v)
         if (tid == 0) {
             tc::tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                tc::umma_bf16(tmem + kGtS, gdesc_mn64(sb + kGKt) + ks * (2048 >> 4),
-                              gdesc_mn64(sb + kGNv) + ks * (2048 >> 4), kIdS, 1u);
+                tc::umma_bf16(tmem + kGtS, gdesc_mn64(kt) + ks * (2048 >> 4),
+                              gdesc_mn64(sb + kGR) + ks * (2048 >> 4), kIdS, 1u);
             tc::umma_commit(&bar_s);
         }
         if (__syncthreads_or(!gwait(&bar_s, c, status, bad))) break;
@@ -508,7 +538,8 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         if (!tc::mbar_wait(&drain, 0, kWaitNs)) record_status(status, SALA_ERR_TIMEOUT);
         // tiles still landing if the loop stopped early: every load issued, but not waited for
         for (int b = 0; b < 2; ++b)
-            if ((pending >> b) & 1) (void)tc::mbar_wait(&full[b], (fpar >> b) & 1, kWaitNs);
+            if ((pending >> b) & 1) (void)tc::mbar_wait(&full_k[b], (kpar >> b) & 1, kWaitNs);
+        if (pending & 4u) (void)tc::mbar_wait(&full_v, vidx & 1, kWaitNs);
     }
     __syncthreads();
     if (warp == 0) {

@@ -23,8 +23,8 @@
 //   U    += (-W) S           M=64  N=128 K=128  (U becomes new_v)
 //   S    += K^T (e^(b_C - b) new_v)   M=128 N=128 K=64   (after S *= exp(b_C) in tensor memory;
 //                                     the decay sits on new_v's rows, so K's tile serves as is)
-// T itself is inverted on the CUDA cores in fp32 (two diagonal 32 x 32 blocks by forward
-// substitution, then the off-diagonal block T21 = -T2 A21 T1). Every factor is at most 1
+// T itself is inverted on the CUDA cores in fp32 (four diagonal 16 x 16 blocks by forward
+// substitution, then the blocks below the diagonal by distance, T_ij = -T_ii sum_k A_ik T_kj). Every factor is at most 1
 // (b is non-increasing), so no range handling is needed. K tiles arrive by TMA, double
 // buffered (the next chunk's tile loads while this one is processed); the V tile loads once
 // the previous chunk's U has read it. Every wait is bounded (2 s); a timeout records
@@ -49,8 +49,8 @@ constexpr int kAS = 68;   // row stride (floats) of the fp32 A and T matrices in
 //          state update)
 //   S      the state entering the chunk in bf16 [k][v] (B of W S), 2 x 16 KB
 //   T      T bf16 [t][s] (A of W and U), one 64-column region
-// During the inverse the fp32 A, T and Y = A21 T1 live in the S and T regions (free then;
-// T bf16 is written from the fp32 T, which sits in the S region, after A and Y are dead).
+// During the inverse the fp32 A, T and the block sums P live in the S and T regions (free
+// then; T bf16 is written from the fp32 T, which sits in the S region, after A and P are dead).
 constexpr uint32_t kGK = 0;
 constexpr uint32_t kGV = kGK + 2 * kTile;
 constexpr uint32_t kGR = kGV + kTile;
@@ -58,11 +58,11 @@ constexpr uint32_t kGS = kGR + kTile;
 constexpr uint32_t kGT = kGS + 2 * kSRegion;
 constexpr uint32_t kGTf = kGS;                     // T fp32 [64][kAS]
 constexpr uint32_t kGAf = kGTf + 64 * kAS * 4;     // A fp32 [64][kAS]
-constexpr uint32_t kGY = kGAf + 64 * kAS * 4;      // Y fp32 [32][36]
+constexpr uint32_t kGY = kGAf + 64 * kAS * 4;      // P fp32 [48][20] (block sums of the inverse)
 constexpr uint32_t kGB = kGT + kRegion;            // b [64], beta [64]
 constexpr uint32_t kGBytes = kGB + 2 * 64 * 4;
 constexpr uint32_t kGSmem = kGBytes + 1024;
-static_assert(kGY + 32 * 36 * 4 <= kGB, "inverse scratch fits the S and T regions");
+static_assert(kGY + 48 * 20 * 4 <= kGB, "inverse scratch fits the S and T regions");
 static_assert(kGTf + 64 * kAS * 4 <= kGT, "fp32 T does not overlap the bf16 T it is copied to");
 static_assert(2 * (kGSmem + 1024) <= 228 * 1024, "two CTAs per SM");
 
@@ -170,7 +170,7 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
     float *betasm = bsm + 64;
     float *Af = reinterpret_cast<float *>(sm + kGAf);
     float *Tf = reinterpret_cast<float *>(sm + kGTf);
-    float *Yf = reinterpret_cast<float *>(sm + kGY);
+    float *Pf = reinterpret_cast<float *>(sm + kGY);   // block sums P of the inverse
 
     // the state entering the sequence: row k (= TMEM lane) of h0, or zeros; columns 64 wg ..
     {
@@ -332,16 +332,16 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         }
         tc::tc_fence_before();   // X is read: W may overwrite its columns
         __syncthreads();
-        // T = (I + A)^-1. Diagonal blocks T1, T2 (32 x 32): thread (blk, j) solves column j by
-        // forward substitution, T[i][j] = -sum_{m < i} A[i][m] T[m][j] with T[j][j] = 1 (the
-        // column is zero above j, so the sum may run over every m < i)
+        // T = (I + A)^-1 by 16 x 16 blocks. Diagonal blocks: thread (blk, j) of the first 64
+        // solves column j of block blk by forward substitution, T[i][j] = -sum_{m < i} A[i][m]
+        // T[m][j] with T[j][j] = 1 (the column is zero above j)
         if (tid < 64) {
-            const int blk = tid >> 5, j = tid & 31, o = 32 * blk;
-            float col[32];
+            const int blk = tid >> 4, j = tid & 15, o = 16 * blk;
+            float col[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) col[i] = (i == j) ? 1.f : 0.f;
+            for (int i = 0; i < 16; ++i) col[i] = (i == j) ? 1.f : 0.f;
 #pragma unroll
-            for (int i = 1; i < 32; ++i) {
+            for (int i = 1; i < 16; ++i) {
                 const float *ar = Af + (o + i) * kAS + o;
                 float acc = 0.f;
 #pragma unroll
@@ -349,54 +349,61 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
                 if (i > j) col[i] = -acc;
             }
 #pragma unroll
-            for (int i = 0; i < 32; ++i) Tf[(o + i) * kAS + o + j] = col[i];
+            for (int i = 0; i < 16; ++i) Tf[(o + i) * kAS + o + j] = col[i];
         }
         __syncthreads();
-        // Y = A21 T1 (rows 32-63, columns 0-31 of A times T1) and then T21 = -T2 Y: thread:
-        // row i, columns j0 .. j0 + 3 (one scalar and one 16-byte load per m)
-        {
-            const int i = tid >> 3, j0 = 4 * (tid & 7);
-            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float *ar = Af + (32 + i) * kAS;
-#pragma unroll 8
-            for (int m = 0; m < 32; ++m) {
-                const float4 tm = *reinterpret_cast<const float4 *>(Tf + m * kAS + j0);
-                const float u = ar[m];
-                y.x = fmaf(u, tm.x, y.x); y.y = fmaf(u, tm.y, y.y);
-                y.z = fmaf(u, tm.z, y.z); y.w = fmaf(u, tm.w, y.w);
+        // blocks below the diagonal, by distance d: T_ij = -T_ii sum_{k = j .. i-1} A_ik T_kj
+        // (i = j + d; every T_kj on the right is nearer the diagonal). Thread: block b of the
+        // level, row r, columns c0 .. c0 + 3; the sums go through P in the Y scratch.
+#pragma unroll 1
+        for (int d = 1; d < 4; ++d) {
+            const int nb = 4 - d, bi = tid >> 6, r = (tid >> 2) & 15, c0 = 4 * (tid & 3);
+            const int i = bi + d, j = bi;
+            if (bi < nb) {
+                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+                const float *ar = Af + (16 * i + r) * kAS;
+                for (int k = j; k < i; ++k) {
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) {
+                        const float u = ar[16 * k + m];
+                        const float4 tm = *reinterpret_cast<const float4 *>(Tf + (16 * k + m) * kAS + 16 * j + c0);
+                        y.x = fmaf(u, tm.x, y.x); y.y = fmaf(u, tm.y, y.y);
+                        y.z = fmaf(u, tm.z, y.z); y.w = fmaf(u, tm.w, y.w);
+                    }
+                }
+                *reinterpret_cast<float4 *>(Pf + (16 * bi + r) * 20 + c0) = y;
             }
-            *reinterpret_cast<float4 *>(Yf + i * 36 + j0) = y;
-        }
-        __syncthreads();
-        {
-            const int i = tid >> 3, j0 = 4 * (tid & 7);
-            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float *tr = Tf + (32 + i) * kAS + 32;
-#pragma unroll 8
-            for (int m = 0; m < 32; ++m) {
-                const float4 ym = *reinterpret_cast<const float4 *>(Yf + m * 36 + j0);
-                const float u = tr[m];
-                y.x = fmaf(u, ym.x, y.x); y.y = fmaf(u, ym.y, y.y);
-                y.z = fmaf(u, ym.z, y.z); y.w = fmaf(u, ym.w, y.w);
+            __syncthreads();
+            if (bi < nb) {
+                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+                const float *tr = Tf + (16 * i + r) * kAS + 16 * i;
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const float u = tr[m];
+                    const float4 pm = *reinterpret_cast<const float4 *>(Pf + (16 * bi + m) * 20 + c0);
+                    y.x = fmaf(u, pm.x, y.x); y.y = fmaf(u, pm.y, y.y);
+                    y.z = fmaf(u, pm.z, y.z); y.w = fmaf(u, pm.w, y.w);
+                }
+                *reinterpret_cast<float4 *>(Tf + (16 * i + r) * kAS + 16 * j + c0) = make_float4(-y.x, -y.y, -y.z, -y.w);
             }
-            *reinterpret_cast<float4 *>(Tf + (32 + i) * kAS + j0) = make_float4(-y.x, -y.y, -y.z, -y.w);
-            // the upper off-diagonal block is zero
-            *reinterpret_cast<float4 *>(Tf + i * kAS + 32 + j0) = make_float4(0.f, 0.f, 0.f, 0.f);
+            __syncthreads();
         }
-        __syncthreads();
-        // T to bf16, K-major [t][s] (one 64-column region): thread: row t, 32 columns
+        // T to bf16, K-major [t][s] (one 64-column region): thread: row t, columns 16 q4 .. + 15
+        // (block q4; blocks above the diagonal are zero)
         {
-            const int t = tid & 63, q4 = tid >> 6;   // row t, columns 16 q4 .. + 15
+            const int t = tid & 63, q4 = tid >> 6;
+            const bool upper = q4 > (t >> 4);
             const float *tr = Tf + t * kAS + 16 * q4;
             uint8_t *dst = sm + kGT;
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
-                const int c4 = c2;
-                uint4 w;
-                w.x = float2_to_bf16x2(tr[8 * c4], tr[8 * c4 + 1]);
-                w.y = float2_to_bf16x2(tr[8 * c4 + 2], tr[8 * c4 + 3]);
-                w.z = float2_to_bf16x2(tr[8 * c4 + 4], tr[8 * c4 + 5]);
-                w.w = float2_to_bf16x2(tr[8 * c4 + 6], tr[8 * c4 + 7]);
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (!upper) {
+                    w.x = float2_to_bf16x2(tr[8 * c2], tr[8 * c2 + 1]);
+                    w.y = float2_to_bf16x2(tr[8 * c2 + 2], tr[8 * c2 + 3]);
+                    w.z = float2_to_bf16x2(tr[8 * c2 + 4], tr[8 * c2 + 5]);
+                    w.w = float2_to_bf16x2(tr[8 * c2 + 6], tr[8 * c2 + 7]);
+                }
                 *reinterpret_cast<uint4 *>(dst + sw(t, 2 * q4 + c2)) = w;
             }
         }

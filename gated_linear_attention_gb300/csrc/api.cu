@@ -225,6 +225,7 @@ const char *sala_gla_status_string(int status) {
     case SALA_ERR_TOO_LARGE:
         return "problem needs more scratch than the no-allocation entry point's fixed buffer";
     case SALA_ERR_BAD_INDEX: return "a state index is at or past the pool size";
+    case SALA_ERR_DEBUG_CHECK: return "debug build: a device-side index check failed (access skipped)";
     default: return "unknown status";
     }
 }
@@ -337,13 +338,14 @@ int sala_gla_qk_prologue(void *q, void *k, const sala_qk_prologue *prologue,
         overlaps(k, vec, prologue->q_weight, wb) || overlaps(k, vec, prologue->k_weight, wb))
         return SALA_ERR_INVALID_ARG;
     int err = SALA_OK;
-    if (!device_state(&err)) return err;
+    DeviceState *d = device_state(&err);
+    if (!d) return err;
     SegTable tab{};
     tab.cu = cu_seqlens;
     tab.T_row = T;
     tab.nseq = nseq;
     if (launch_qk_prologue(q, k, make_qk_prologue(prologue, nullptr), tab, start_pos, T_total, H,
-                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
+                           d->status, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SALA_ERR_CUDA;
     return SALA_OK;
 }

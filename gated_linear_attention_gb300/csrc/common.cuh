@@ -17,6 +17,18 @@ __device__ __forceinline__ void record_status(int *status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
 
+// Index checks of the debug build (compiled with SALA_GLA_DEBUG): a failed check records
+// SALA_ERR_DEBUG_CHECK in the status word and returns false, and the caller skips the access
+// it guards. In the release build the check is the constant true and costs nothing.
+#ifdef SALA_GLA_DEBUG
+__device__ __forceinline__ bool dcheck(bool ok, int *status) {
+    if (!ok) record_status(status, SALA_ERR_DEBUG_CHECK);
+    return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool dcheck(bool, int *) { return true; }
+#endif
+
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }

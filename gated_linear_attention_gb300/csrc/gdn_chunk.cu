@@ -496,7 +496,7 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         // nv): the MN-major B of the state update S += K^T (exp(bC - b) new_v)
         {
             const int t = quarter * 16 + (lane & 15), sh = lane >> 4;
-            const bool live = t < nv;
+            const bool live = t < nv && dcheck(c0 + t < t1 && t1 <= p.T_total, status);
             const float ft = live ? tc::ex2((bC - bsm[t]) * kLog2eG) : 0.f;
             uint16_t *grow = p.nv + ((c0 + t) * H + h) * kD;
             uint32_t x[32];

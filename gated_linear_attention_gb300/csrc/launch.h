@@ -64,7 +64,7 @@ cudaError_t launch_recurrent_step_indexed(const void *q, const void *k, const vo
 // The q/k prologue in place on a prefill's q and k ([T_total, H, 128] rows; positions from
 // the segment table's sequence bounds plus start_pos).
 cudaError_t launch_qk_prologue(void *q, void *k, const QkPrologue &pro, const SegTable &t,
-                               const int64_t *start_pos, int64_t T_total, int H,
+                               const int64_t *start_pos, int64_t T_total, int H, int *status,
                                cudaStream_t stream);
 
 // Segment table from cu_seqlens (or B equal rows); also zeroes the work ticket and the

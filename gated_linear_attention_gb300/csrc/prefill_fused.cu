@@ -479,7 +479,11 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             if (static_cast<int64_t>(u) < total_units) {
                 info.sigma = u / H;
                 info.h = static_cast<int>(u % H);
-                if (locate_segment(t, info.sigma, info.n, info.t0, info.t1)) {
+                // (debug build: the segment lies inside its sequence and the tokens)
+                if (locate_segment(t, info.sigma, info.n, info.t0, info.t1) &&
+                    dcheck(info.n >= 0 && info.n < t.nseq && seq_begin(t, info.n) <= info.t0 &&
+                           info.t0 < info.t1 && info.t1 <= seq_begin(t, info.n + 1) &&
+                           info.t1 <= seq_begin(t, t.nseq), status)) {
                     info.valid = 1;
                     info.nch = static_cast<int>((info.t1 - info.t0 + kChunk - 1) / kChunk);
                     info.first = info.t0 == seq_begin(t, info.n);
@@ -1284,7 +1288,7 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                         tc::tma_store_3d(&maps.o, 32 * quarter, h, static_cast<int32_t>(c0), stg);
                         tc::tma_store_commit();
                     }
-                } else {
+                } else if (dcheck(nv > 0 && c0 + nv <= info.t1, status)) {
                     // ragged chunk: only its nv rows go out (the rows past it belong to another
                     // sequence), 64 bytes per row
                     __syncwarp();

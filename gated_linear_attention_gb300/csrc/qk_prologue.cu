@@ -87,7 +87,7 @@ __device__ __forceinline__ uint2 prologue_rope(uint2 y, const float2 (&cs)[2], c
 // group's normalisation runs while the angles are computed; one barrier separates the two.
 __global__ void __launch_bounds__(kProThreads, 5)
 qk_prologue_kernel(uint16_t *q, uint16_t *k, QkPrologue pro, SegTable t, const int64_t *start_pos,
-                   int64_t T_total, int H) {
+                   int64_t T_total, int H, int *status) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tok = blockIdx.x;
     const size_t row = static_cast<size_t>(tok) * H;
@@ -112,6 +112,7 @@ qk_prologue_kernel(uint16_t *q, uint16_t *k, QkPrologue pro, SegTable t, const i
     // angle i and finds the position itself (the sequence: largest n with begin(n) <= tok), so
     // the angles need no barrier of their own and overlap the first group's normalisation
     __shared__ float cs_s[64], sn_s[64];
+    __shared__ bool skip_s;
     if (threadIdx.x < 64) {
         int64_t n = 0;
         if (t.cu) {
@@ -126,6 +127,9 @@ qk_prologue_kernel(uint16_t *q, uint16_t *k, QkPrologue pro, SegTable t, const i
         }
         const float pos = static_cast<float>(tok - seq_begin(t, n) + (start_pos ? start_pos[n] : 0));
         sincosf(pos * pro.inv_freq[threadIdx.x], &sn_s[threadIdx.x], &cs_s[threadIdx.x]);
+        // debug build: the token lies in the sequence found (cu_seqlens is not validated here)
+        if (threadIdx.x == 0)
+            skip_s = !dcheck(seq_begin(t, n) <= tok && tok < seq_begin(t, n + 1), status);
     }
     float2 wq[2], wk[2];
     {
@@ -150,6 +154,7 @@ qk_prologue_kernel(uint16_t *q, uint16_t *k, QkPrologue pro, SegTable t, const i
     };
     norm_group();
     __syncthreads();
+    if (skip_s) return;   // (only ever set in the debug build)
     float2 cs[2], ssn[2];
     {
         const int a = (4 * lane) & 63;
@@ -189,12 +194,13 @@ QkPrologue make_qk_prologue(const sala_qk_prologue *p, const int64_t *positions)
 }
 
 cudaError_t launch_qk_prologue(void *q, void *k, const QkPrologue &pro, const SegTable &t,
-                               const int64_t *start_pos, int64_t T_total, int H,
+                               const int64_t *start_pos, int64_t T_total, int H, int *status,
                                cudaStream_t stream) {
     if (T_total == 0) return cudaSuccess;
     LaunchTimer timer(kKQkPrologue, stream);
     qk_prologue_kernel<<<static_cast<unsigned>(T_total), kProThreads, 0, stream>>>(
-        static_cast<uint16_t *>(q), static_cast<uint16_t *>(k), pro, t, start_pos, T_total, H);
+        static_cast<uint16_t *>(q), static_cast<uint16_t *>(k), pro, t, start_pos, T_total, H,
+        status);
     return cudaGetLastError();
 }
 

@@ -21,6 +21,7 @@ STATUS_NAMES = {
     0: "SALA_OK", 1: "SALA_ERR_INVALID_ARG", 2: "SALA_ERR_MISALIGNED",
     3: "SALA_ERR_UNSUPPORTED", 4: "SALA_ERR_CUDA", 5: "SALA_ERR_TIMEOUT",
     6: "SALA_ERR_BAD_SEQLENS", 7: "SALA_ERR_TOO_LARGE", 8: "SALA_ERR_BAD_INDEX",
+    9: "SALA_ERR_DEBUG_CHECK",
 }
 SALA_STATE_F32, SALA_STATE_BF16 = 0, 1
 
@@ -68,16 +69,20 @@ class SalaError(RuntimeError):
 
 
 def library_path() -> str:
-    return _build.LIB
+    """The library the binding loads: the debug build when SALA_GLA_DEBUG=1, else the release
+    build."""
+    return _build.LIB_DEBUG if os.environ.get("SALA_GLA_DEBUG") == "1" else _build.LIB
 
 
 def load(path: str | None = None):
-    """Load the compiled library (raises OSError if it is missing)."""
+    """Load the compiled library (raises OSError if it is missing); ``path`` loads another
+    build without making it the binding's library."""
     global _lib
     if _lib is None or path is not None:
-        p = path or _build.LIB
+        p = path or library_path()
         if not os.path.exists(p):
-            raise OSError(f"{p} not found: build it with gated_linear_attention_gb300.build.build()")
+            raise OSError(f"{p} not found: build it with gated_linear_attention_gb300.build.build()"
+                          f"{'(debug=True)' if p == _build.LIB_DEBUG else ''}")
         lib = ctypes.CDLL(p)
         for name, (argtypes, restype) in SIGNATURES.items():
             fn = getattr(lib, name)

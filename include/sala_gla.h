@@ -50,7 +50,9 @@ typedef enum {
     SALA_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up */
     SALA_ERR_BAD_SEQLENS = 6, /* device-detected: cu_seqlens not monotone or last != T */
     SALA_ERR_TOO_LARGE = 7,   /* sala_gla_chunk_fwd_noalloc: problem exceeds its fixed scratch */
-    SALA_ERR_BAD_INDEX = 8    /* device-detected: a state index at or past the pool size */
+    SALA_ERR_BAD_INDEX = 8,   /* device-detected: a state index at or past the pool size */
+    SALA_ERR_DEBUG_CHECK = 9  /* debug build only (SALA_GLA_DEBUG): a device-side index check
+                                 failed; the access it guards was skipped */
 } sala_status;
 
 /*

@@ -45,6 +45,26 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_debug_build_exports_every_declared_symbol():
+    # the SALA_GLA_DEBUG build: same ABI, device-side index checks compiled in
+    path = B.build(debug=True)
+    assert path == B.LIB_DEBUG and path != B.LIB
+    from gated_linear_attention_gb300 import sala_gla
+    dlib = sala_gla.load(path)
+    for name in declared_functions():
+        assert hasattr(dlib, name), name
+    assert dlib.sala_gla_status_string(9).decode().startswith("debug build")
+    assert sala_gla.STATUS_NAMES[9] == "SALA_ERR_DEBUG_CHECK"
+
+
+def test_debug_library_is_selected_by_environment(monkeypatch):
+    from gated_linear_attention_gb300 import sala_gla
+    monkeypatch.setenv("SALA_GLA_DEBUG", "1")
+    assert sala_gla.library_path() == B.LIB_DEBUG
+    monkeypatch.delenv("SALA_GLA_DEBUG")
+    assert sala_gla.library_path() == B.LIB
+
+
 def test_binding_covers_every_declared_symbol():
     from gated_linear_attention_gb300 import sala_gla
     assert sorted(sala_gla.SIGNATURES) == declared_functions()

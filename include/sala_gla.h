@@ -177,11 +177,14 @@ int sala_gla_recurrent_step_indexed(const void *q, const void *k, const void *v,
 /*
  * The q/k prologue (see sala_qk_prologue) in place on the q and k of a prefill, before
  * sala_gla_chunk_fwd. A separate pass: the chunked prefill loads its q and k tiles straight
- * into shared memory by TMA, so the prologue is not applied on that load.
+ * into shared memory by TMA, and the per-element work of the prologue on its critical path
+ * costs more than this pass's read and write of q and k.
  *
  *   q, k         bf16 [B, T, H, 128] (packed [T, H, 128] with cu_seqlens), rewritten in place.
  *   cu_seqlens   int64 [num_seqs + 1] DEVICE array as for sala_gla_chunk_fwd, or NULL (B rows
- *                of T tokens).
+ *                of T tokens). It must be valid (non-decreasing, from 0 to T); this call does
+ *                not check it on the device (the debug build does: SALA_ERR_DEBUG_CHECK, and
+ *                tokens it cannot place in a sequence are left as they are).
  *   start_pos    int64 [Nseq] DEVICE array, the position of each sequence's first token here
  *                (a continued sequence), or NULL for 0. A token's position is start_pos[n]
  *                plus its index in sequence n.

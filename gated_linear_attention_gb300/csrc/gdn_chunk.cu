@@ -270,8 +270,10 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         const float bC = bsm[nv - 1];
         const uint32_t kt = sb + kGK + buf * kTile;
 
-        // X = K K^T
+        // X = K K^T (and the previous chunk's new_v stores have read the S region, which the
+        // inverse below reuses)
         if (tid == 0) {
+            tc::tma_store_wait_read<0>();
             tc::tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
@@ -499,6 +501,9 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
             const bool live = t < nv && dcheck(c0 + t < t1 && t1 <= p.T_total, status);
             const float ft = live ? tc::ex2((bC - bsm[t]) * kLog2eG) : 0.f;
             uint16_t *grow = p.nv + ((c0 + t) * H + h) * kD;
+            // a whole chunk leaves by TMA stores of four [64 t][32 v] boxes staged in the S region
+            // (free until the next chunk's inverse); a ragged one row by row
+            uint8_t *stg = sm + kGS + (2 * wg + sh) * 4096 + t * 64;
             uint32_t x[32];
             tc::tmem_ld_16x32bx2_x32(tmem + lane_base + kGtAcc + 64 * wg, x);
             tc::tmem_ld_wait();
@@ -513,7 +518,8 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
                 w.y = float2_to_bf16x2(f[2], f[3]);
                 w.z = float2_to_bf16x2(f[4], f[5]);
                 w.w = float2_to_bf16x2(f[6], f[7]);
-                if (live) *reinterpret_cast<uint4 *>(grow + 64 * wg + 32 * sh + 8 * c4) = w;
+                if (nv == kChunk) *reinterpret_cast<uint4 *>(stg + 16 * c4) = w;
+                else if (live) *reinterpret_cast<uint4 *>(grow + 64 * wg + 32 * sh + 8 * c4) = w;
                 w.x = float2_to_bf16x2(f[0] * ft, f[1] * ft);
                 w.y = float2_to_bf16x2(f[2] * ft, f[3] * ft);
                 w.z = float2_to_bf16x2(f[4] * ft, f[5] * ft);
@@ -524,7 +530,7 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
         __syncthreads();
-        // S += K^T (exp(bC - b) new_v)
+        // S += K^T (exp(bC - b) new_v); new_v of a whole chunk out
         if (tid == 0) {
             tc::tc_fence_after();
 #pragma unroll
@@ -532,6 +538,12 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
                 tc::umma_bf16(tmem + kGtS, gdesc_mn64(kt) + ks * (2048 >> 4),
                               gdesc_mn64(sb + kGR) + ks * (2048 >> 4), kIdS, 1u);
             tc::umma_commit(&bar_s);
+            if (nv == kChunk) {
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    tc::tma_store_3d(&maps.o, 32 * b, h, static_cast<int32_t>(c0), sm + kGS + b * 4096);
+                tc::tma_store_commit();
+            }
         }
         if (__syncthreads_or(!gwait(&bar_s, c, status, bad))) break;
         tc::tc_fence_after();
@@ -541,6 +553,7 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
     tc::tc_fence_before();
     __syncthreads();
     if (tid == 0) {
+        tc::tma_store_wait_all<0>();
         tc::umma_commit(&drain);
         if (!tc::mbar_wait(&drain, 0, kWaitNs)) record_status(status, SALA_ERR_TIMEOUT);
         // tiles still landing if the loop stopped early: every load issued, but not waited for
@@ -565,7 +578,7 @@ cudaError_t launch_gdn_newv(const void *k, const void *v, const float *g, const 
                             int *status, cudaStream_t st) {
     if (t.nseq == 0 || T_total == 0) return cudaSuccess;
     tck::TcMaps maps;
-    // the q and o maps are not used here: k and v stand in for them
+    // the q map is not used here (k stands in for it); the o map stores new_v
     cudaError_t e = tck::make_maps(&maps, k, k, v, nv, T_total, H);
     if (e != cudaSuccess) return e;
     GdnChunkArgs p;

@@ -172,6 +172,34 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
     float *Tf = reinterpret_cast<float *>(sm + kGTf);
     float *Pf = reinterpret_cast<float *>(sm + kGY);   // block sums P of the inverse
 
+    auto load_k = [&](int c) {   // thread 0: TMA of chunk c's K tile into buffer c & 1
+        const int32_t x0 = static_cast<int32_t>(t0 + int64_t(c) * kChunk);
+        uint64_t *bar = &full_k[c & 1];
+        tc::mbar_arrive_expect_tx(bar, kTile);
+        uint8_t *kd = sm + kGK + (c & 1) * kTile;
+        tc::tma_load_3d(kd, &maps.k, 0, h, x0, bar);
+        tc::tma_load_3d(kd + kRegion, &maps.k, 64, h, x0, bar);
+    };
+    auto load_v = [&](int c) {   // thread 0: TMA of chunk c's V tile
+        const int32_t x0 = static_cast<int32_t>(t0 + int64_t(c) * kChunk);
+        tc::mbar_arrive_expect_tx(&full_v, kTile);
+        tc::tma_load_3d(sm + kGV, &maps.v, 0, h, x0, &full_v);
+        tc::tma_load_3d(sm + kGV + kRegion, &maps.v, 64, h, x0, &full_v);
+    };
+    // the first chunk's tiles and gates are requested before the state is read in, so that
+    // their latencies overlap
+    if (tid == 0 && nch > 0) {
+        tc::tma_prefetch_desc(&maps.k);
+        tc::tma_prefetch_desc(&maps.v);
+        load_k(0);
+        load_v(0);
+    }
+    // g and beta of the next chunk, loaded a chunk ahead (threads 0-63: row tid)
+    float g_nx = 0.f, be_nx = 0.f;
+    if (tid < 64 && nch > 0 && tid < t1 - t0) {
+        g_nx = p.g[(t0 + tid) * H + h];
+        be_nx = p.beta[(t0 + tid) * H + h];
+    }
     // the state entering the sequence: row k (= TMEM lane) of h0, or zeros; columns 64 wg ..
     {
         const int k = quarter * 32 + lane;
@@ -193,35 +221,8 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         tc::tmem_st_wait();
     }
 
-    auto load_k = [&](int c) {   // thread 0: TMA of chunk c's K tile into buffer c & 1
-        const int32_t x0 = static_cast<int32_t>(t0 + int64_t(c) * kChunk);
-        uint64_t *bar = &full_k[c & 1];
-        tc::mbar_arrive_expect_tx(bar, kTile);
-        uint8_t *kd = sm + kGK + (c & 1) * kTile;
-        tc::tma_load_3d(kd, &maps.k, 0, h, x0, bar);
-        tc::tma_load_3d(kd + kRegion, &maps.k, 64, h, x0, bar);
-    };
-    auto load_v = [&](int c) {   // thread 0: TMA of chunk c's V tile
-        const int32_t x0 = static_cast<int32_t>(t0 + int64_t(c) * kChunk);
-        tc::mbar_arrive_expect_tx(&full_v, kTile);
-        tc::tma_load_3d(sm + kGV, &maps.v, 0, h, x0, &full_v);
-        tc::tma_load_3d(sm + kGV + kRegion, &maps.v, 64, h, x0, &full_v);
-    };
-    if (tid == 0 && nch > 0) {
-        tc::tma_prefetch_desc(&maps.k);
-        tc::tma_prefetch_desc(&maps.v);
-        load_k(0);
-        load_v(0);
-    }
     tc::tc_fence_before();
     __syncthreads();
-
-    // g and beta of the next chunk, loaded a chunk ahead (threads 0-63: row tid)
-    float g_nx = 0.f, be_nx = 0.f;
-    if (tid < 64 && nch > 0 && tid < t1 - t0) {
-        g_nx = p.g[(t0 + tid) * H + h];
-        be_nx = p.beta[(t0 + tid) * H + h];
-    }
     uint32_t kpar = 0;      // bit b: next phase of full_k[b]
     int vidx = 0;           // the chunk of the last V load issued
     uint32_t pending = 0;   // bits 0, 1: a K load into that buffer, bit 2: a V load, issued and

@@ -98,12 +98,12 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t w, __nv_bfloat162 f2) {
 
 struct TcMaps {
     CUtensorMap q, k, v;   // loads: box 64 x 1 x 64, 128-byte swizzle
-    CUtensorMap o;         // stores: box 32 x 1 x 64, no swizzle
+    CUtensorMap o;         // stores: box 32 x 1 x 64, no swizzle or (o_sw64) 64-byte swizzle
 };
 
 // host: 3-D tensor maps over q, k, v and o viewed as [T_total, H, 128] bf16
 cudaError_t make_maps(TcMaps *m, const void *q, const void *k, const void *v, const void *o,
-                      int64_t T_total, int H);
+                      int64_t T_total, int H, bool o_sw64 = false);
 
 }  // namespace tck
 }  // namespace sala

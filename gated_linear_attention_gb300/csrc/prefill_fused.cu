@@ -1214,13 +1214,22 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
         }
     } else if (warp >= 12) {
         // =============================== output warps ===============================
-        // Warp quarter q writes value columns j = 32 q + lane of every token: o_t = factor_t
-        // O^T[j][t], staged as a [64 t x 32 j] bf16 tile and written by one TMA store per warp
-        // (direct stores when the chunk is ragged: the rows past it belong to another sequence).
+        // Warp quarter q writes value columns j = 32 q .. + 31 of every token: o_t = factor_t
+        // O^T[j][t], staged as a [64 t x 32 j] bf16 tile (64-byte swizzle) and written by one
+        // TMA store per warp (direct stores when the chunk is ragged: the rows past it belong
+        // to another sequence). O^T is read in the 16-lane fragment order, in which each lane
+        // holds two neighbouring tokens of one value column, so transposing 8 x 8 matrix
+        // stores put the tile in place without any exchange between lanes.
         const int wtid = threadIdx.x - 384;
         const int quarter = warp & 3;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         uint8_t *stg = sm + kOst + quarter * kOstWarp;
+        // this lane's row address for each stmatrix: matrix k = lane / 8 (value columns
+        // 8 k .. + 7 of the warp's 32), row p = lane % 8 (token 8 m + p), 16-byte chunk k
+        // swizzled by token bits 2..1
+        const int p8 = lane & 7, k8 = lane >> 3;
+        const uint32_t st_addr = tc::smem_u32(stg) + p8 * 64 + 16 * (k8 ^ ((p8 >> 1) & 3));
+        const int tl = 2 * (lane & 3);   // this lane's tokens: 8 m + tl, 8 m + tl + 1
         const GateRec *recC = reinterpret_cast<const GateRec *>(sm + kGate) + kRecA;
         uint32_t us = 0, cc = 0, jc = 0;
         for (;;) {
@@ -1234,52 +1243,42 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             for (int c = 0; c < nch; ++c) {
                 const int64_t c0 = info.t0 + int64_t(c) * kChunk;
                 const int nv = static_cast<int>(min(int64_t(kChunk), info.t1 - c0));
-                // lane l's factors for tokens l and 32 + l (broadcast below), from the chunk's
-                // gate record
+                // the factors of this lane's 16 tokens, from the chunk's gate record
                 wait_nv(&gc_full[jc % kRecC], jc / kRecC, true, abort_v, status);
                 const GateRec *R = recC + jc % kRecC;
                 const bool fast = R->fast != 0;
-                const float b_lo = R->b[lane], b_hi = R->b[32 + lane], base = R->base;
+                const float base = R->base;
+                float2 ft[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) ft[m] = *reinterpret_cast<const float2 *>(&R->b[8 * m + tl]);
                 warp_arrive(&gc_empty[jc % kRecC]);
                 ++jc;
-                const float f_lo = fast ? a.scale * tc::ex2((base + b_lo) * kLog2e) : a.scale;
-                const float f_hi = fast ? a.scale * tc::ex2((base + b_hi) * kLog2e) : a.scale;
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    ft[m] = fast ? make_float2(a.scale * tc::ex2((base + ft[m].x) * kLog2e),
+                                               a.scale * tc::ex2((base + ft[m].y) * kLog2e))
+                                 : make_float2(a.scale, a.scale);
                 const uint32_t ob = cc & 1;
                 wait_nv(&o_full[ob], cc >> 1, true, abort_v, status);
                 if (wtid == 0) TRACE(4, 9, c);
                 tc::tc_fence_after();
+                // o0: value columns 0-15 of the warp's 32, o1: 16-31
                 uint32_t o0[32], o1[32];
-                tc::tmem_ld_32x32b_x32(tmem + lane_base + kTO + 64 * ob, o0);
-                tc::tmem_ld_32x32b_x32(tmem + lane_base + kTO + 64 * ob + 32, o1);
+                tc::tmem_ld_16x256b_x8(tmem + lane_base + kTO + 64 * ob, o0);
+                tc::tmem_ld_16x256b_x8(tmem + lane_base + (16u << 16) + kTO + 64 * ob, o1);
                 tc::tmem_ld_wait();
                 tc::tc_fence_before();
                 warp_arrive(&o_free[ob]);
-                // Stage [64 t][32 j] bf16: neighbouring lanes swap one value per token pair, so
-                // that each lane holds two adjacent columns of one token (even lane: token t,
-                // odd lane: token t + 1), scales them and writes one 32-bit word.
                 if (lane == 0) tc::tma_store_wait_read<0>();   // staging tile free again
                 __syncwarp();
-                const bool odd = lane & 1;
-                uint8_t *col = stg + 4 * (lane >> 1);
 #pragma unroll
-                for (int tp = 0; tp < 32; tp += 2) {
-                    const int tk = tp + (lane & 1);
-                    const float ft = __shfl_sync(0xffffffffu, f_lo, tk);
-                    const float mine = __uint_as_float(odd ? o0[tp + 1] : o0[tp]);
-                    const float give = __uint_as_float(odd ? o0[tp] : o0[tp + 1]);
-                    const float got = __shfl_xor_sync(0xffffffffu, give, 1);
-                    *reinterpret_cast<uint32_t *>(col + tk * 64) =
-                        odd ? float2_to_bf16x2(got * ft, mine * ft) : float2_to_bf16x2(mine * ft, got * ft);
-                }
-#pragma unroll
-                for (int tp = 0; tp < 32; tp += 2) {
-                    const int tk = tp + (lane & 1);
-                    const float ft = __shfl_sync(0xffffffffu, f_hi, tk);
-                    const float mine = __uint_as_float(odd ? o1[tp + 1] : o1[tp]);
-                    const float give = __uint_as_float(odd ? o1[tp] : o1[tp + 1]);
-                    const float got = __shfl_xor_sync(0xffffffffu, give, 1);
-                    *reinterpret_cast<uint32_t *>(col + (32 + tk) * 64) =
-                        odd ? float2_to_bf16x2(got * ft, mine * ft) : float2_to_bf16x2(mine * ft, got * ft);
+                for (int m = 0; m < 8; ++m) {
+                    const float fa = ft[m].x, fb = ft[m].y;
+                    tc::stmatrix_x4_trans(st_addr + 512 * m,
+                                          float2_to_bf16x2(__uint_as_float(o0[4 * m]) * fa, __uint_as_float(o0[4 * m + 1]) * fb),
+                                          float2_to_bf16x2(__uint_as_float(o0[4 * m + 2]) * fa, __uint_as_float(o0[4 * m + 3]) * fb),
+                                          float2_to_bf16x2(__uint_as_float(o1[4 * m]) * fa, __uint_as_float(o1[4 * m + 1]) * fb),
+                                          float2_to_bf16x2(__uint_as_float(o1[4 * m + 2]) * fa, __uint_as_float(o1[4 * m + 3]) * fb));
                 }
                 if (nv == kChunk) {
                     tc::fence_proxy_async_smem();
@@ -1295,8 +1294,8 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
                     uint16_t *orow = a.o + (c0 * H + h) * kD + 32 * quarter + lane;
 #pragma unroll 1
                     for (int tt = 0; tt < nv; ++tt)
-                        orow[static_cast<size_t>(tt) * H * kD] =
-                            *reinterpret_cast<const uint16_t *>(stg + tt * 64 + 2 * lane);
+                        orow[static_cast<size_t>(tt) * H * kD] = *reinterpret_cast<const uint16_t *>(
+                            stg + tt * 64 + 16 * ((lane >> 3) ^ ((tt >> 1) & 3)) + 2 * (lane & 7));
                 }
                 if (wtid == 0) TRACE(4, 10, c);
                 ++cc;
@@ -1324,7 +1323,8 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 cudaError_t g_encode_err = cudaSuccess;
 std::once_flag g_encode_once;
 
-cudaError_t encode_map(CUtensorMap *map, const void *base, int64_t T_total, int H, bool store) {
+cudaError_t encode_map(CUtensorMap *map, const void *base, int64_t T_total, int H, bool store,
+                       bool sw64 = false) {
     std::call_once(g_encode_once, []() {
         cudaDriverEntryPointQueryResult q;
         g_encode_err = cudaGetDriverEntryPointByVersion(
@@ -1342,18 +1342,19 @@ cudaError_t encode_map(CUtensorMap *map, const void *base, int64_t T_total, int 
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                           strides, store ? box_store : box_load, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          store ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                          store ? (sw64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE)
+                                : CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 }  // namespace
 
 cudaError_t make_maps(TcMaps *m, const void *q, const void *k, const void *v, const void *o,
-                      int64_t T_total, int H) {
+                      int64_t T_total, int H, bool o_sw64) {
     cudaError_t e = encode_map(&m->q, q, T_total, H, false);
     if (e == cudaSuccess) e = encode_map(&m->k, k, T_total, H, false);
     if (e == cudaSuccess) e = encode_map(&m->v, v, T_total, H, false);
-    if (e == cudaSuccess) e = encode_map(&m->o, o, T_total, H, true);
+    if (e == cudaSuccess) e = encode_map(&m->o, o, T_total, H, true, o_sw64);
     return e;
 }
 
@@ -1370,7 +1371,7 @@ cudaError_t launch_prefill_fused(const ChunkArgs &a, const SegTable &t, int64_t 
                                  int *status, cudaStream_t st) {
     if (T_total > 0 && max_units > 0) {
         tck::TcMaps maps;
-        cudaError_t e = tck::make_maps(&maps, a.q, a.k, a.v, a.o, T_total, a.H);
+        cudaError_t e = tck::make_maps(&maps, a.q, a.k, a.v, a.o, T_total, a.H, true);
         if (e != cudaSuccess) return e;
         FusedArgs f;
         f.c = a;

@@ -44,4 +44,30 @@ __device__ __forceinline__ uint32_t float2_to_bf16x2(float x, float y) {
     return *reinterpret_cast<uint32_t *>(&p);
 }
 
+// Start of a kernel launched by launch_dependent: the next kernel on the stream may be
+// scheduled once every CTA of this one has passed here, and nothing below runs before the
+// previous kernel on the stream has completed and its writes are visible.
+__device__ __forceinline__ void dependent_start() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launch as a programmatic dependent of the work before it on the stream: only the launch
+// latency overlaps the previous grid's last wave (the kernel begins with dependent_start).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, unsigned block, cudaStream_t st,
+                             Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 }  // namespace sala

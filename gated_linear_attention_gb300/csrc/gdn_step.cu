@@ -24,6 +24,7 @@ gdn_step_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
                 const uint16_t *__restrict__ v, const float *__restrict__ g,
                 const float *__restrict__ beta, float scale, float *__restrict__ S,
                 uint16_t *__restrict__ o) {
+    dependent_start();   // (launched by launch_dependent: one decode step after another)
     const int unit = blockIdx.x;  // n * H + h
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float *Su = S + static_cast<size_t>(unit) * kD * kD;
@@ -110,10 +111,10 @@ cudaError_t launch_gdn_step(const void *q, const void *k, const void *v, const f
                             cudaStream_t stream) {
     if (units == 0) return cudaSuccess;
     LaunchTimer timer(kKGdnStep, stream);
-    gdn_step_kernel<<<static_cast<unsigned>(units), kGdnThreads, 0, stream>>>(
-        static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k),
-        static_cast<const uint16_t *>(v), g, beta, scale, S, static_cast<uint16_t *>(o));
-    return cudaGetLastError();
+    return launch_dependent(gdn_step_kernel, static_cast<unsigned>(units), kGdnThreads, stream,
+                            static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k),
+                            static_cast<const uint16_t *>(v), g, beta, scale, S,
+                            static_cast<uint16_t *>(o));
 }
 
 }  // namespace sala

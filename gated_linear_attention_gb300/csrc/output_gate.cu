@@ -102,9 +102,7 @@ output_norm_gate_fixed_kernel(const uint16_t *__restrict__ o, const uint16_t *__
                               const uint16_t *__restrict__ w, float eps, uint16_t *out) {
     constexpr int F = kIt * 8 * kThr;
     const size_t tok = static_cast<size_t>(blockIdx.x) * F;
-    // launched as a programmatic dependent (see launch_output_norm_gate)
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    dependent_start();   // (launched by launch_dependent)
     uint4 ov[kIt], zv[kIt];
 #pragma unroll
     for (int m = 0; m < kIt; ++m) {
@@ -162,28 +160,12 @@ cudaError_t launch_output_norm_gate(const void *o, const void *z, const void *w,
                *wb = static_cast<const uint16_t *>(w);
     auto *outb = static_cast<uint16_t *>(out);
     const unsigned grid = static_cast<unsigned>(T);
-    // the fixed-width kernels go out as programmatic dependents of the work before them on the
-    // stream: the next kernel may be scheduled once every CTA of this one has started, and each
-    // CTA reads nothing before the previous kernel has completed (griddepcontrol.wait), so only
-    // the launch latency overlaps
-    auto pdl = [&](auto kern, unsigned threads) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(threads);
-        cfg.dynamicSmemBytes = 0;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kern, ob, zb, wb, eps, outb);
-    };
+    // the fixed-width kernels go out as programmatic dependents of the work before them
     switch (H) {
-    case 8: return pdl(output_norm_gate_fixed_kernel<1, 128>, 128);
-    case 16: return pdl(output_norm_gate_fixed_kernel<1, 256>, 256);
-    case 32: return pdl(output_norm_gate_fixed_kernel<2, 256>, 256);
-    case 64: return pdl(output_norm_gate_fixed_kernel<2, 512>, 512);
+    case 8: return launch_dependent(output_norm_gate_fixed_kernel<1, 128>, grid, 128, stream, ob, zb, wb, eps, outb);
+    case 16: return launch_dependent(output_norm_gate_fixed_kernel<1, 256>, grid, 256, stream, ob, zb, wb, eps, outb);
+    case 32: return launch_dependent(output_norm_gate_fixed_kernel<2, 256>, grid, 256, stream, ob, zb, wb, eps, outb);
+    case 64: return launch_dependent(output_norm_gate_fixed_kernel<2, 512>, grid, 512, stream, ob, zb, wb, eps, outb);
     default:
         output_norm_gate_kernel<<<grid, kGateThreads, 0, stream>>>(ob, zb, wb, eps, outb, H * kD);
     }

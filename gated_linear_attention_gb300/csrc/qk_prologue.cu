@@ -91,11 +91,7 @@ qk_prologue_kernel(uint16_t *q, uint16_t *k, QkPrologue pro, SegTable t, const i
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tok = blockIdx.x;
     const size_t row = static_cast<size_t>(tok) * H;
-    // launched as a programmatic dependent (see launch_qk_prologue): the next kernel may be
-    // scheduled as soon as every CTA of this one has started; nothing is read before the
-    // previous kernel on the stream has completed
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    dependent_start();   // (launched by launch_dependent)
     // the first group of heads is loaded before anything else (its latency overlaps the
     // position lookup and the angles)
     uint2 xq[kProHeadsInFlight], xk[kProHeadsInFlight];
@@ -203,20 +199,9 @@ cudaError_t launch_qk_prologue(void *q, void *k, const QkPrologue &pro, const Se
                                cudaStream_t stream) {
     if (T_total == 0) return cudaSuccess;
     LaunchTimer timer(kKQkPrologue, stream);
-    // a programmatic dependent of the work before it on the stream: only the launch latency
-    // overlaps (every CTA waits for the previous kernel before reading anything)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(T_total));
-    cfg.blockDim = dim3(kProThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, qk_prologue_kernel, static_cast<uint16_t *>(q), static_cast<uint16_t *>(k),
-                              pro, t, start_pos, T_total, H, status);
+    return launch_dependent(qk_prologue_kernel, static_cast<unsigned>(T_total), kProThreads, stream,
+                            static_cast<uint16_t *>(q), static_cast<uint16_t *>(k), pro, t, start_pos,
+                            T_total, H, status);
 }
 
 }  // namespace sala

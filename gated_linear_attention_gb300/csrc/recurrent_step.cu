@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
 recurrent_step_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
                       const uint16_t *__restrict__ v, const float *__restrict__ g, float scale,
                       StateRef ref, uint16_t *__restrict__ o, int *status, QkPrologue pro) {
+    dependent_start();   // (launched by launch_dependent: one decode step after another)
     const int unit = blockIdx.x;  // n * H + h
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t vec = static_cast<size_t>(unit) * kD;
@@ -224,11 +225,10 @@ cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, c
                                   cudaStream_t stream) {
     if (units == 0) return cudaSuccess;
     LaunchTimer timer(kKRecurrentStep, stream);
-    recurrent_step_kernel<false><<<static_cast<unsigned>(units), kDecodeThreads, 0, stream>>>(
-        static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k),
-        static_cast<const uint16_t *>(v), g, scale, StateRef{S, nullptr, 0, 1},
-        static_cast<uint16_t *>(o), nullptr, QkPrologue{});
-    return cudaGetLastError();
+    return launch_dependent(recurrent_step_kernel<false>, static_cast<unsigned>(units), kDecodeThreads,
+                            stream, static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k),
+                            static_cast<const uint16_t *>(v), g, scale, StateRef{S, nullptr, 0, 1},
+                            static_cast<uint16_t *>(o), nullptr, QkPrologue{});
 }
 
 cudaError_t launch_recurrent_step_indexed(const void *q, const void *k, const void *v,
@@ -244,10 +244,10 @@ cudaError_t launch_recurrent_step_indexed(const void *q, const void *k, const vo
                *vb = static_cast<const uint16_t *>(v);
     auto *ob = static_cast<uint16_t *>(o);
     if (bf16)
-        recurrent_step_kernel<true><<<blocks, kDecodeThreads, 0, stream>>>(qb, kb, vb, g, scale, ref, ob, status, pro);
-    else
-        recurrent_step_kernel<false><<<blocks, kDecodeThreads, 0, stream>>>(qb, kb, vb, g, scale, ref, ob, status, pro);
-    return cudaGetLastError();
+        return launch_dependent(recurrent_step_kernel<true>, blocks, kDecodeThreads, stream, qb, kb, vb, g,
+                                scale, ref, ob, status, pro);
+    return launch_dependent(recurrent_step_kernel<false>, blocks, kDecodeThreads, stream, qb, kb, vb, g,
+                            scale, ref, ob, status, pro);
 }
 
 }  // namespace sala

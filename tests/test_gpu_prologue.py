@@ -91,6 +91,34 @@ def test_prologue_prefill_rows(sg):
     assert oracle.rel_fro(qd.cpu().reshape(200, 3, 128).float(), oracle.qk_prologue(q, qw, pos[:, None])) <= 5e-3
 
 
+def test_dependent_launches_read_what_the_previous_one_wrote(sg):
+    # the prologue and the output gate go out as programmatic dependents of the kernel before
+    # them: back-to-back calls on the same tensors (each reading the previous one's output),
+    # with no synchronisation in between, must give the oracle applied in sequence
+    T, H = 4096, 8
+    q, k = _raw_tokens(T, H, seed=21)
+    qw, kw = _weights(4)
+    qd, kd = q.cuda(), k.cuda()
+    cu = torch.tensor([0, T], dtype=torch.int64)
+    for _ in range(3):
+        sg.qk_prologue(qd, kd, qw.cuda(), kw.cuda(), 1e-6, 10000.0, cu_seqlens=cu.cuda())
+    gen = torch.Generator().manual_seed(22)
+    z = torch.randn((T, H * 128), generator=gen).to(torch.bfloat16)
+    w = (1 + 0.1 * torch.randn(H * 128, generator=gen)).to(torch.bfloat16)
+    out = torch.empty((T, H * 128), dtype=torch.bfloat16, device="cuda")
+    sg.output_norm_gate(qd.reshape(T, H * 128), z.cuda(), w.cuda(), 1e-6, out=out)
+    torch.cuda.synchronize()
+    pos = np.arange(T)[:, None]
+    q_ref, k_ref = q, k
+    for _ in range(3):
+        q_ref = torch.from_numpy(oracle.qk_prologue(q_ref, qw, pos)).to(torch.bfloat16)
+        k_ref = torch.from_numpy(oracle.qk_prologue(k_ref, kw, pos)).to(torch.bfloat16)
+    assert oracle.rel_fro(qd.cpu().float(), q_ref.float()) <= 1e-2
+    assert oracle.rel_fro(kd.cpu().float(), k_ref.float()) <= 1e-2
+    g_ref = oracle.output_norm_gate(qd.cpu().reshape(T, H * 128), z, w)
+    assert oracle.rel_fro(out.cpu().float(), g_ref) <= 1e-2
+
+
 def test_prologue_then_prefill_matches_oracle(sg):
     # the layer's path: prologue in place, then the chunked prefill
     x = inputs.make_prefill("varlen", seqlens=(700, 300), H=4, seed=17)

@@ -58,11 +58,11 @@ constexpr uint32_t kGS = kGR + kTile;
 constexpr uint32_t kGT = kGS + 2 * kSRegion;
 constexpr uint32_t kGTf = kGS;                     // T fp32 [64][kAS]
 constexpr uint32_t kGAf = kGTf + 64 * kAS * 4;     // A fp32 [64][kAS]
-constexpr uint32_t kGY = kGAf + 64 * kAS * 4;      // P fp32 [48][20] (block sums of the inverse)
+constexpr uint32_t kGY = kGAf + 64 * kAS * 4;      // P fp32 [32][20], then X fp32 [32][36] (inverse)
 constexpr uint32_t kGB = kGT + kRegion;            // b [64], beta [64]
 constexpr uint32_t kGBytes = kGB + 2 * 64 * 4;
 constexpr uint32_t kGSmem = kGBytes + 1024;
-static_assert(kGY + 48 * 20 * 4 <= kGB, "inverse scratch fits the S and T regions");
+static_assert(kGY + 32 * 36 * 4 <= kGB, "inverse scratch fits the S and T regions");
 static_assert(kGTf + 64 * kAS * 4 <= kGT, "fp32 T does not overlap the bf16 T it is copied to");
 static_assert(2 * (kGSmem + 1024) <= 228 * 1024, "two CTAs per SM");
 
@@ -170,7 +170,8 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
     float *betasm = bsm + 64;
     float *Af = reinterpret_cast<float *>(sm + kGAf);
     float *Tf = reinterpret_cast<float *>(sm + kGTf);
-    float *Pf = reinterpret_cast<float *>(sm + kGY);   // block sums P of the inverse
+    float *Pf = reinterpret_cast<float *>(sm + kGY);   // block products of the inverse
+    float *Xf = Pf;                                    // [32][36] (after P is dead)
 
     auto load_k = [&](int c) {   // thread 0: TMA of chunk c's K tile into buffer c & 1
         const int32_t x0 = static_cast<int32_t>(t0 + int64_t(c) * kChunk);
@@ -355,39 +356,71 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
             for (int i = 0; i < 16; ++i) Tf[(o + i) * kAS + o + j] = col[i];
         }
         __syncthreads();
-        // blocks below the diagonal, by distance d: T_ij = -T_ii sum_{k = j .. i-1} A_ik T_kj
-        // (i = j + d; every T_kj on the right is nearer the diagonal). Thread: block b of the
-        // level, row r, columns c0 .. c0 + 3; the sums go through P in the Y scratch.
-#pragma unroll 1
-        for (int d = 1; d < 4; ++d) {
-            const int nb = 4 - d, bi = tid >> 6, r = (tid >> 2) & 15, c0 = 4 * (tid & 3);
-            const int i = bi + d, j = bi;
-            if (bi < nb) {
+        // blocks below the diagonal, by the blocked inverse of a lower-triangular matrix
+        // [[T_a, 0], [X, T_b]]^-1 = [[T_a^-1, 0], [-T_b^-1 X T_a^-1, T_b^-1]]: first the lower
+        // 16 x 16 block of each diagonal 32 x 32 half (T_10 = -T_11 A_10 T_00 and T_32 =
+        // -T_33 A_32 T_22), then the lower-left 32 x 32 block, -T_hi (A_[32:64][0:32] T_lo) with
+        // T_lo, T_hi the inverses of the two halves. The upper triangles of the blocks on the
+        // diagonal are zero (the solve above wrote them) and those above it are never read.
+        {
+            // Y = A_{i,i-1} T_{i-1,i-1} for i = 1, 3 (into P): thread: half hb, row r, columns
+            // c0 .. c0 + 3
+            const int hb = tid >> 6, r = (tid >> 2) & 15, c0 = 4 * (tid & 3);
+            const int i = 2 * hb + 1, j = 2 * hb;
+            if (hb < 2) {
                 float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-                const float *ar = Af + (16 * i + r) * kAS;
-                for (int k = j; k < i; ++k) {
+                const float *ar = Af + (16 * i + r) * kAS + 16 * j;
 #pragma unroll
-                    for (int m = 0; m < 16; ++m) {
-                        const float u = ar[16 * k + m];
-                        const float4 tm = *reinterpret_cast<const float4 *>(Tf + (16 * k + m) * kAS + 16 * j + c0);
-                        y.x = fmaf(u, tm.x, y.x); y.y = fmaf(u, tm.y, y.y);
-                        y.z = fmaf(u, tm.z, y.z); y.w = fmaf(u, tm.w, y.w);
-                    }
+                for (int m = 0; m < 16; ++m) {
+                    const float u = ar[m];
+                    const float4 tm = *reinterpret_cast<const float4 *>(Tf + (16 * j + m) * kAS + 16 * j + c0);
+                    y.x = fmaf(u, tm.x, y.x); y.y = fmaf(u, tm.y, y.y);
+                    y.z = fmaf(u, tm.z, y.z); y.w = fmaf(u, tm.w, y.w);
                 }
-                *reinterpret_cast<float4 *>(Pf + (16 * bi + r) * 20 + c0) = y;
+                *reinterpret_cast<float4 *>(Pf + (16 * hb + r) * 20 + c0) = y;
             }
             __syncthreads();
-            if (bi < nb) {
+            if (hb < 2) {   // T_{i,i-1} = -T_ii Y
                 float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
                 const float *tr = Tf + (16 * i + r) * kAS + 16 * i;
 #pragma unroll
                 for (int m = 0; m < 16; ++m) {
                     const float u = tr[m];
-                    const float4 pm = *reinterpret_cast<const float4 *>(Pf + (16 * bi + m) * 20 + c0);
+                    const float4 pm = *reinterpret_cast<const float4 *>(Pf + (16 * hb + m) * 20 + c0);
                     y.x = fmaf(u, pm.x, y.x); y.y = fmaf(u, pm.y, y.y);
                     y.z = fmaf(u, pm.z, y.z); y.w = fmaf(u, pm.w, y.w);
                 }
-                *reinterpret_cast<float4 *>(Tf + (16 * i + r) * kAS + 16 * j + c0) = make_float4(-y.x, -y.y, -y.z, -y.w);
+                *reinterpret_cast<float4 *>(Tf + (16 * i + r) * kAS + 16 * j + c0) =
+                    make_float4(-y.x, -y.y, -y.z, -y.w);
+            }
+            __syncthreads();
+            // Z = A_[32:64][0:32] T_lo (into the scratch X): thread: row rr, columns cc .. cc + 3;
+            // T_lo[m][n] = 0 for n > m, so the sum starts at m = cc
+            const int rr = tid >> 3, cc = 4 * (tid & 7);
+            {
+                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+                const float *ar = Af + (32 + rr) * kAS;
+#pragma unroll 4
+                for (int m = cc; m < 32; ++m) {
+                    const float u = ar[m];
+                    const float4 tm = *reinterpret_cast<const float4 *>(Tf + m * kAS + cc);
+                    y.x = fmaf(u, tm.x, y.x); y.y = fmaf(u, tm.y, y.y);
+                    y.z = fmaf(u, tm.z, y.z); y.w = fmaf(u, tm.w, y.w);
+                }
+                *reinterpret_cast<float4 *>(Xf + rr * 36 + cc) = y;
+            }
+            __syncthreads();
+            {   // T_[32:64][0:32] = -T_hi Z; T_hi[rr][m] = 0 for m > rr
+                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+                const float *tr = Tf + (32 + rr) * kAS + 32;
+#pragma unroll 4
+                for (int m = 0; m <= rr; ++m) {
+                    const float u = tr[m];
+                    const float4 xm = *reinterpret_cast<const float4 *>(Xf + m * 36 + cc);
+                    y.x = fmaf(u, xm.x, y.x); y.y = fmaf(u, xm.y, y.y);
+                    y.z = fmaf(u, xm.z, y.z); y.w = fmaf(u, xm.w, y.w);
+                }
+                *reinterpret_cast<float4 *>(Tf + (32 + rr) * kAS + cc) = make_float4(-y.x, -y.y, -y.z, -y.w);
             }
             __syncthreads();
         }

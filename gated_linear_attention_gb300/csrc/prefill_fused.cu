@@ -1041,6 +1041,12 @@ prefill_fused_kernel(const __grid_constant__ TcMaps maps, FusedArgs f, SegTable 
             if (!info.valid) break;
             const int h = info.h, nch = info.nch;
             if (lane == 0) TRACE(quarter == 0 ? 3 : 4 + quarter, 1, us);
+            // a first segment's incoming state is the caller's h0, known from the start: bring
+            // its 64 KB into L2 during the state pass (the hand-off reads it 32 rows at a time)
+            if (info.first && f.h0) {
+                const char *hb = reinterpret_cast<const char *>(f.h0 + (info.n * H + h) * kD * kD);
+                for (int i = wtid; i < kD * kD * 4 / 128; i += 128) tc::prefetch_l2_keep(hb + 128 * i);
+            }
 
             // ---------------- state pass: columns 64-127 of every K' tile ----------------
             // (the scaling warps take columns 0-63); and the segment's total log-decay

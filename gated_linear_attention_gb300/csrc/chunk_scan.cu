@@ -55,14 +55,25 @@ seg_table_kernel(SegTable t, int64_t T_total, uint32_t *ticket, uint32_t *flags,
         if (bad) record_status(status, SALA_ERR_BAD_SEQLENS);
     }
     if (bad || !hT) return;
-    // hT of empty sequences (the block-wide flag `bad` is final after the barrier above)
+    // hT of empty sequences (the block-wide flag `bad` is final after the barrier above): a
+    // block of kPrepThreads sequences at a time, each thread testing one, then the block copies
+    // the state of every empty one
     constexpr int kVec = kD * kD / 4;   // float4 per (sequence, head)
-    for (int64_t n = 0; n < t.nseq; ++n) {
-        if (seq_begin(t, n + 1) != seq_begin(t, n)) continue;
-        float4 *dst = reinterpret_cast<float4 *>(hT + n * H * kD * kD);
-        const float4 *src = h0 ? reinterpret_cast<const float4 *>(h0 + n * H * kD * kD) : nullptr;
-        for (int64_t i = threadIdx.x; i < static_cast<int64_t>(H) * kVec; i += kPrepThreads)
-            dst[i] = src ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    __shared__ bool empty[kPrepThreads];
+    for (int64_t n0b = 0; n0b < t.nseq; n0b += kPrepThreads) {
+        const int64_t nt = n0b + threadIdx.x;
+        empty[threadIdx.x] = nt < t.nseq && seq_begin(t, nt + 1) == seq_begin(t, nt);
+        __syncthreads();
+        const int64_t nb = ::min(static_cast<int64_t>(kPrepThreads), t.nseq - n0b);
+        for (int64_t m = 0; m < nb; ++m) {
+            if (!empty[m]) continue;
+            const int64_t n = n0b + m;
+            float4 *dst = reinterpret_cast<float4 *>(hT + n * H * kD * kD);
+            const float4 *src = h0 ? reinterpret_cast<const float4 *>(h0 + n * H * kD * kD) : nullptr;
+            for (int64_t i = threadIdx.x; i < static_cast<int64_t>(H) * kVec; i += kPrepThreads)
+                dst[i] = src ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncthreads();   // (the flags are rewritten for the next block of sequences)
     }
 }
 

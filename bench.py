@@ -355,6 +355,7 @@ def run_ours(args, dist):
     torch.cuda.synchronize()
     sala_gla.timing_enable(False)
     kern = sala_gla.timing_read()
+    step_pct = call_percentiles(stream, step, args.steps)
     ms_max = dist.max(ms)
     tokens_all = dist.sum(T_total * args.steps)
     value = tokens_all / (ms_max / 1e3)
@@ -492,6 +493,7 @@ def run_ours(args, dist):
             "step_roofline": {"bytes_per_step": step_bytes,
                               "roofline_tokens_per_s": step_roof_rate,
                               "frac": (value / dist.world) / step_roof_rate},
+            "step_us_percentiles": step_pct,
             "kernels": kernels,
             "gpu_launches": launches,
             "e2e": e2e,
@@ -548,6 +550,7 @@ def run_prefill_config(args, dist, dev, peaks, sala_gla, inputs, name):
     torch.cuda.synchronize()
     sala_gla.timing_enable(False)
     kern = sala_gla.timing_read()
+    step_pct = call_percentiles(stream, lambda i: step(), args.steps)
     assert sala_gla.get_device_status() == 0
     has_h0 = x["h0"] is not None
     nbytes = prefill_bytes(T_total, w.H, nseq, has_h0, True)
@@ -570,6 +573,7 @@ def run_prefill_config(args, dist, dev, peaks, sala_gla, inputs, name):
                      "peak_source": peaks["source"], "mean_launch_us": 1e3 * k_ms / k_n},
         "step_roofline": {"bytes_per_step": nbytes, "roofline_tokens_per_s": step_rate,
                           "frac": (value / dist.world) / step_rate},
+        "step_us_percentiles": step_pct,
         "kernels": {k: {"ms_total": v[0], "launches": v[1],
                         "us_per_launch": (1e3 * v[0] / v[1]) if v[1] else None}
                     for k, v in kern.items() if v[1]},
@@ -838,6 +842,23 @@ def run_gdn_prefill(args, dist, dev, peaks, sala_gla, inputs):
 
 
 SIDE_LAUNCHES = 40
+
+
+def call_percentiles(stream, call, n):
+    """p10 / p50 / p90 of n single calls, CUDA events around each on the launching stream (a
+    pass of its own: the events add host work between launches)."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(evs):
+        a.record(stream)
+        call(i)
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = sorted(1e3 * a.elapsed_time(b) for a, b in evs)
+    at = lambda q: us[int(round(q * (len(us) - 1)))]
+    return {"calls": n, "p10_us": at(0.1), "p50_us": at(0.5), "p90_us": at(0.9)}
 
 
 def side_loop_us(stream, call):

@@ -277,8 +277,9 @@ __device__ __forceinline__ void store_row_scaled(uint8_t *dst, int row, const ui
 }
 
 // Exact route, scores: columns 32 half .. + 31 of row t of P' (already masked and rounded to
-// bf16 in the SW128 tile at pp) times exp(b_t - b_s) for every causal column s <= t (rare).
-__device__ __forceinline__ void exact_pp_weights(uint8_t *pp, const float *b, int t, int half) {
+// bf16 in the SW128 tile at pp) times exp(b_t - b_s) for every causal column s <= t (rare; kept
+// out of line, like exact_q_scale, so that the scaling warps' hot loop stays short).
+__device__ __noinline__ void exact_pp_weights(uint8_t *pp, const float *b, int t, int half) {
     const float bt = b[t] * kLog2e;
 #pragma unroll 1
     for (int c8 = 4 * half; c8 < 4 * half + 4; ++c8) {
@@ -297,7 +298,7 @@ __device__ __forceinline__ void exact_pp_weights(uint8_t *pp, const float *b, in
 
 // Exact route, queries: row `row` (columns 64 half .. + 63) of the Q tile at qt becomes
 // exp(b_row) q_row, read from global memory (the tile has been consumed by M1).
-__device__ __forceinline__ void exact_q_scale(uint8_t *qt, const uint16_t *q, int64_t c0, int row, int half,
+__device__ __noinline__ void exact_q_scale(uint8_t *qt, const uint16_t *q, int64_t c0, int row, int half,
                                            int nv, int H, int h, float b_row) {
     uint4 x[8];
     if (row < nv) {

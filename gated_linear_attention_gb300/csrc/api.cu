@@ -3,6 +3,7 @@
 #include <atomic>
 #include <cstdlib>
 #include <mutex>
+#include <string>
 #include <vector>
 
 #include "launch.h"
@@ -54,6 +55,8 @@ DeviceState *device_state(int *err) {
         if (d.init_error != cudaSuccess) return;
         d.init_error = setup_fused_kernel();
         if (d.init_error != cudaSuccess) return;
+        d.init_error = setup_pair_kernel();
+        if (d.init_error != cudaSuccess) return;
         d.init_error = setup_gdn_chunk_kernel();
     });
     if (d.init_error != cudaSuccess) {
@@ -82,7 +85,7 @@ std::atomic<uint32_t> g_epoch{0};
 const char *const kKernelNames[kKernelCount] = {"seg_table", "prefill_fused", "recurrent_step",
                                                 "recurrent_step_indexed", "output_norm_gate",
                                                 "qk_prologue", "gdn_step", "gdn_fwd",
-                                                "gdn_newv"};
+                                                "gdn_newv", "prefill_pair"};
 struct TimingRecord {
     int id;
     cudaEvent_t start, stop;
@@ -161,6 +164,20 @@ std::atomic<uint64_t> g_fault_wait_ns{0};
 std::atomic<int64_t> g_fault_withhold{-1};
 }  // namespace
 
+// Prefill kernel choice: -1 until first read from SALA_GLA_PREFILL, then 0 (per call), 1, 2.
+std::atomic<int> g_prefill_kernel{-1};
+
+int prefill_kernel_choice() {
+    int k = g_prefill_kernel.load();
+    if (k < 0) {
+        const char *e = getenv("SALA_GLA_PREFILL");
+        const int v = !e ? 0 : std::string(e) == "pair" ? 2 : std::string(e) == "fused" ? 1 : 0;
+        g_prefill_kernel.compare_exchange_strong(k, v);
+        k = g_prefill_kernel.load();
+    }
+    return k;
+}
+
 void prefill_fault_knobs(uint64_t *wait_ns, int64_t *withhold) {
     *wait_ns = g_fault_wait_ns.load();
     *withhold = g_fault_withhold.load();
@@ -171,6 +188,12 @@ void prefill_fault_knobs(uint64_t *wait_ns, int64_t *withhold) {
 using namespace sala;
 
 extern "C" {
+
+int sala_gla_set_prefill_kernel(int kernel) {
+    if (kernel < 0 || kernel > 2) return SALA_ERR_INVALID_ARG;
+    g_prefill_kernel.store(kernel);
+    return SALA_OK;
+}
 
 int sala_gla_debug_prefill_knobs(uint64_t flag_wait_ns, int64_t withhold_unit) {
     if (withhold_unit < -1) return SALA_ERR_INVALID_ARG;
@@ -540,9 +563,16 @@ int sala_gla_chunk_fwd(const void *q, const void *k, const void *v, const float 
     float *incl = reinterpret_cast<float *>(ws + off_bytes + tick_bytes + flag_bytes);
 
     int rc = SALA_OK;
+    // many waves of units per SM: two CTAs per SM overlap each other's serial chains; a few
+    // waves: one unit per SM (twice as many units in flight would lengthen the chains of
+    // hand-offs within a wave)
+    const int which = prefill_kernel_choice();
+    const bool pair = which == 2 || (which == 0 && T_total * H > int64_t(8192) * d->sm_count);
     if (launch_seg_table(tab, T_total, ticket, flags, max_units, H, h0, hT, d->status, st) != cudaSuccess ||
-        launch_prefill_fused(a, tab, T_total, max_units, h0, hT, incl, flags, ticket,
-                             next_prefill_epoch(), d->sm_count, d->status, st) != cudaSuccess)
+        (pair ? launch_prefill_pair(a, tab, T_total, max_units, h0, hT, incl, flags, ticket,
+                                    next_prefill_epoch(), 2 * d->sm_count, d->status, st)
+              : launch_prefill_fused(a, tab, T_total, max_units, h0, hT, incl, flags, ticket,
+                                     next_prefill_epoch(), d->sm_count, d->status, st)) != cudaSuccess)
         rc = SALA_ERR_CUDA;
     if (cudaFreeAsync(ws, st) != cudaSuccess) rc = SALA_ERR_CUDA;
     return rc;

@@ -18,6 +18,7 @@ enum KernelId {
     kKGdnStep,
     kKGdnFwd,
     kKGdnNewv,
+    kKPrefillPair,
     kKernelCount
 };
 
@@ -78,6 +79,14 @@ cudaError_t launch_seg_table(const SegTable &t, int64_t T_total, uint32_t *ticke
 // states, `flags` [max_units] words, `ticket` one word; `epoch` is nonzero and differs from
 // the previous call's. `status` receives SALA_ERR_TIMEOUT if a bounded wait gives up.
 cudaError_t setup_fused_kernel();
+
+// The same prefill at two CTAs per SM (prefill_pair.cu): one unit in flight per CTA, half of
+// an SM's shared and tensor memory each; `grid` up to twice the SM count. Same arguments.
+cudaError_t launch_prefill_pair(const ChunkArgs &a, const SegTable &t, int64_t T_total,
+                                int64_t max_units, const float *h0, float *hT, float *incl,
+                                uint32_t *flags, uint32_t *ticket, uint32_t epoch, int grid,
+                                int *status, cudaStream_t st);
+cudaError_t setup_pair_kernel();
 cudaError_t launch_prefill_fused(const ChunkArgs &a, const SegTable &t, int64_t T_total,
                                  int64_t max_units, const float *h0, float *hT, float *incl,
                                  uint32_t *flags, uint32_t *ticket, uint32_t epoch, int grid,

@@ -59,6 +59,7 @@ SIGNATURES = {
     "sala_gla_kernel_count": ([], ctypes.c_int),
     "sala_gla_kernel_name": ([ctypes.c_int], ctypes.c_char_p),
     "sala_gla_debug_prefill_knobs": ([ctypes.c_uint64, _i64], ctypes.c_int),
+    "sala_gla_set_prefill_kernel": ([_i32], ctypes.c_int),
 }
 
 
@@ -383,6 +384,12 @@ def timing_read() -> dict:
                "sala_gla_timing_read")
         out[lib.sala_gla_kernel_name(i).decode()] = (ms.value, n.value)
     return out
+
+
+def set_prefill_kernel(kernel: int) -> None:
+    """Which chunked-prefill kernel ``chunk_fwd`` runs (``sala_gla_set_prefill_kernel``): 0 chosen
+    per call, 1 one unit per SM, 2 two CTAs per SM."""
+    _check(load().sala_gla_set_prefill_kernel(int(kernel)), "sala_gla_set_prefill_kernel")
 
 
 def debug_prefill_knobs(flag_wait_ns: int = 0, withhold_unit: int = -1) -> None:

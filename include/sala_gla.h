@@ -327,6 +327,21 @@ int sala_gla_chunk_fwd_noalloc(const void *q, const void *k, const void *v, cons
  */
 int sala_gla_debug_prefill_knobs(uint64_t flag_wait_ns, int64_t withhold_unit);
 
+/*
+ * Which kernel sala_gla_chunk_fwd runs for the chunked prefill; both compute the same result
+ * (the recurrence of "MiniCPM-SALA — Complete Blueprint", "Simple GLA Recurrence", in the
+ * chunked form of "Formulas and Code for Adapting Inference to GDN/KDA Linear Modules",
+ * section 1.2) and differ in how a GB300 runs it:
+ *   0  chosen per call (the default): kernel 2 when the call holds more than 8192 token-heads
+ *      per SM (many waves of units), else kernel 1;
+ *   1  one unit (segment, head) per SM at a time, its steps split over fifteen warps;
+ *   2  two CTAs per SM, one unit each, in half of the SM's shared and tensor memory.
+ * The environment variable SALA_GLA_PREFILL ("fused" for 1, "pair" for 2) sets the initial
+ * choice. Process-wide; affects every later sala_gla_chunk_fwd call (sala_gla_chunk_fwd_noalloc
+ * always runs kernel 1). Errors: SALA_ERR_INVALID_ARG (any other value).
+ */
+int sala_gla_set_prefill_kernel(int kernel);
+
 /* Static English description of a sala_status value (never NULL). */
 const char *sala_gla_status_string(int status);
 

@@ -272,3 +272,11 @@ def test_binding_refuses_cpu_tensors(lib):
     with pytest.raises(ValueError):
         sala_gla.recurrent_step(q[0], q[0], q[0], g[0], 0.1,
                                 torch.zeros((4, 1, 128, 128)))
+
+
+def test_prefill_kernel_choice(lib):
+    # host-side setting, no CUDA involved: 0 per call, 1 one unit per SM, 2 two CTAs per SM
+    assert lib.sala_gla_set_prefill_kernel(3) == 1     # SALA_ERR_INVALID_ARG
+    assert lib.sala_gla_set_prefill_kernel(-1) == 1
+    for k in (1, 2, 0):
+        assert lib.sala_gla_set_prefill_kernel(k) == 0

@@ -198,7 +198,8 @@ def summarise_clocks(rows):
 # one launch of each kernel as it stands (-k <kernel> -c 1), on the workload the bench times;
 # retaken whenever a kernel changes (None: not measured since the last change).
 MEASURED_TRAFFIC = {"prefill_fused": 251_700_000, "prefill_fused_varlen": 2_615_000_000,
-                    "prefill_fused_long": 5_140_000_000, "recurrent_step": 1_021_800_000,
+                    "prefill_fused_long": 5_140_000_000, "prefill_pair_long": 6_122_000_000,
+                    "prefill_pair_varlen": 3_113_000_000, "recurrent_step": 1_021_800_000,
                     "recurrent_step_indexed": 486_100_000, "output_norm_gate": 160_700_000,
                     "qk_prologue": 211_300_000, "gdn_step": 1_022_200_000,
                     "gdn_fwd": 775_600_000}

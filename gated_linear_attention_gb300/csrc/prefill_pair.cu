@@ -28,7 +28,7 @@
 // state and the output epilogue. Every wait is bounded (2 s of %globaltimer); a timeout
 // records SALA_ERR_TIMEOUT, stops the CTA's work, drains its copies and products, frees its
 // tensor memory and returns.
-#include "chunk_tc.cuh"
+#include "prefill_common.cuh"
 
 namespace sala {
 namespace {
@@ -36,8 +36,6 @@ namespace {
 using namespace tck;
 
 constexpr int kPThreads = 256;
-constexpr float kLog2eP = 1.4426950408889634f;
-constexpr float kFastRangeP = 60.f;   // max |log-factor| (natural log) of the factored route
 
 // dynamic shared memory (offsets from a 1024-aligned base)
 constexpr uint32_t kPSlot = 2 * kTile;             // state pass: K | V of one chunk
@@ -88,107 +86,9 @@ __device__ unsigned int g_ptrace_n[4];
     } while (0)
 #endif
 
-struct PairArgs {
-    ChunkArgs c;            // q, k, v, g, scale, o, H
-    const float *h0;        // [nseq, H, 128, 128] or null
-    float *hT;              // [nseq, H, 128, 128] or null
-    float *incl;            // [units, 128, 128]: S_out of each (segment, head)
-    uint32_t *flags;        // [units]: == epoch once incl of that unit is published
-    uint32_t *ticket;       // work counter, zeroed by the table kernel
-    uint32_t epoch;
-    uint64_t flag_wait_ns;  // limit of the wait for the predecessor's published state
-    const uint32_t *withheld;   // failure-path test: this unit's flag is never released (or null)
-};
 
-struct PUnit {
-    int valid, h, nch, first, last;
-    int64_t sigma, n, t0, t1;
-};
 
-__device__ __forceinline__ uint64_t pdesc_k(uint32_t addr) {          // K-major, SW128
-    return tc::smem_desc_sw128(0, 16, 1024) | ((addr >> 4) & 0x3FFFu);
-}
-__device__ __forceinline__ uint64_t pdesc_mn8(uint32_t addr) {        // MN-major, 8 KB atoms
-    return tc::smem_desc_sw128(0, kRegion, 1024) | ((addr >> 4) & 0x3FFFu);
-}
 
-// Log-decays of one chunk as one warp sees them: lane l holds the inclusive prefix sums b[2l],
-// b[2l+1] of g over the chunk's nv valid tokens (constant past nv).
-struct PGate {
-    float b0, b1, bC, mx;
-};
-
-__device__ __forceinline__ float2 pload_gate(const float *__restrict__ g, int64_t c0, int nv, int H, int h) {
-    const int l = threadIdx.x & 31;
-    return make_float2(2 * l < nv ? __ldg(g + (c0 + 2 * l) * H + h) : 0.f,
-                       2 * l + 1 < nv ? __ldg(g + (c0 + 2 * l + 1) * H + h) : 0.f);
-}
-
-__device__ __forceinline__ PGate pscan_gate(float2 a, int nv) {
-    const int l = threadIdx.x & 31;
-    const float pair = a.x + a.y;
-    float run = pair;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, run, off);
-        if (l >= off) run += y;
-    }
-    PGate G;
-    G.b0 = run - pair + a.x;
-    G.b1 = run;
-    float mx = fmaxf(fabsf(G.b0), fabsf(G.b1));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    G.bC = __shfl_sync(0xffffffffu, ((nv - 1) & 1) ? G.b1 : G.b0, (nv - 1) >> 1);
-    G.mx = mx;
-    return G;
-}
-
-// How one output chunk is weighted, from its gate and `run`, the log-decay from the reference
-// point to the chunk start (updated to the next chunk's): the factored route while every factor
-// stays within [e^-60, e^60] (moving the reference to the chunk start when it would not), the
-// exact route when the chunk's own range is wider.
-struct PPlan {
-    float base, pre;
-    bool fast, moved;
-};
-
-__device__ __forceinline__ PPlan pplan_chunk(const PGate &G, float &run) {
-    PPlan p;
-    if (fabsf(run) + G.mx <= kFastRangeP) {
-        p.fast = true;
-        p.moved = false;
-        p.pre = 0.f;
-        p.base = run;
-        run = run + G.bC;
-    } else if (G.mx <= kFastRangeP) {
-        p.fast = true;
-        p.moved = true;
-        p.pre = run;
-        p.base = 0.f;
-        run = G.bC;
-    } else {
-        p.fast = false;
-        p.moved = true;
-        p.pre = run;
-        p.base = 0.f;
-        run = 0.f;
-    }
-    return p;
-}
-
-// One chunk's record: prefix sums b; state pass: the chunk's total bC and the total D of the
-// later chunks of the segment; output pass: the plan.
-struct alignas(16) PRec {
-    float b[64];
-    float bC;
-    float D;
-    float base;
-    float e1;       // exp(pre) if the reference moves before the chunk, else 1
-    float eC;       // exact route: exp(bC), else 1
-    uint32_t fast, moved, pad;
-};
-static_assert(sizeof(PRec) == 288, "record size");
 
 __device__ __forceinline__ void pwait(uint64_t *bar, uint32_t par, volatile int *abort_v, int *status) {
     (void)wait_or_abort(bar, par & 1, abort_v, status);
@@ -220,28 +120,7 @@ __device__ __forceinline__ bool pwg_wait(uint64_t *bar, uint32_t par, volatile i
     return !named_any(kBarW, 128, bad);
 }
 
-__device__ __forceinline__ void pwarp_arrive(uint64_t *bar) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) tc::mbar_arrive(bar);
-}
 
-// Exact route, scores: columns 32 half .. + 31 of row t of P' (masked and rounded already)
-// times exp(b_t - b_s) for every causal column s <= t.
-__device__ __noinline__ void pexact_pp(uint8_t *pp, const float *b, int t, int half) {
-    const float bt = b[t] * kLog2eP;
-#pragma unroll 1
-    for (int c8 = 4 * half; c8 < 4 * half + 4; ++c8) {
-        uint4 x = *reinterpret_cast<const uint4 *>(pp + sw(t, c8));
-        uint32_t *w = reinterpret_cast<uint32_t *>(&x);
-        for (int e = 0; e < 4; ++e) {
-            const int s = 8 * c8 + 2 * e;
-            const float2 f = bf16x2_to_float2(w[e]);
-            w[e] = float2_to_bf16x2(s <= t ? f.x * tc::ex2(bt - b[s] * kLog2eP) : 0.f,
-                                    s + 1 <= t ? f.y * tc::ex2(bt - b[s + 1] * kLog2eP) : 0.f);
-        }
-        *reinterpret_cast<uint4 *>(pp + sw(t, c8)) = x;
-    }
-}
 
 // Exact route: row `row` (columns 64 half .. + 63) of the tile at dst becomes exp(f_row) x_row
 // for the bf16 rows of global memory at src (zero past nv). Used for q_t <- exp(b_t) q_t (M1 has
@@ -255,7 +134,7 @@ __device__ __noinline__ void pexact_rows(uint8_t *dst, const uint16_t *src, int6
     } else {
         for (int c8 = 0; c8 < 8; ++c8) x[c8] = make_uint4(0u, 0u, 0u, 0u);
     }
-    const __nv_bfloat162 f2 = __float2bfloat162_rn(row < nv ? tc::ex2(f_row * kLog2eP) : 0.f);
+    const __nv_bfloat162 f2 = __float2bfloat162_rn(row < nv ? tc::ex2(f_row * kLog2e) : 0.f);
     uint8_t *base = dst + half * kRegion;
     for (int c8 = 0; c8 < 8; ++c8) {
         uint4 y;
@@ -270,7 +149,7 @@ __device__ __noinline__ void pexact_rows(uint8_t *dst, const uint16_t *src, int6
 }  // namespace
 
 __global__ void __launch_bounds__(kPThreads, 2)
-prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t, int *status) {
+prefill_pair_kernel(const __grid_constant__ TcMaps maps, PrefillArgs f, SegTable t, int *status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -280,7 +159,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
     __shared__ uint64_t kp_ready, kp_free, p_full, pp_ready, zb_ready, zb_free, z_full, o_full, po_free;
     __shared__ uint64_t ga_full[kPRecA], ga_empty[kPRecA], gc_full[kPRecC], gc_empty[kPRecC];
     __shared__ uint64_t pub_ready, pub_free, drain;
-    __shared__ PUnit units[2];
+    __shared__ UnitInfo units[2];
     __shared__ int kfast;
     __shared__ uint32_t *pub_flag;
     __shared__ int pub_cmd;          // 0: nothing this unit, 1: release pub_flag, 2: stop
@@ -347,8 +226,8 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const bool table_ok = t.seg_off[t.nseq + 1] == 1;
     const int64_t total_units = table_ok ? t.seg_off[t.nseq] * H : 0;
-    PRec *recA = reinterpret_cast<PRec *>(sm + kPGate);
-    PRec *recC = recA + kPRecA;
+    GateRec *recA = reinterpret_cast<GateRec *>(sm + kPGate);
+    GateRec *recC = recA + kPRecA;
 
     if (warp == 0) {
         // =============================== producer ===============================
@@ -372,7 +251,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
             uint32_t u = 0;
             if (lane == 0) u = atomicAdd(f.ticket, 1u);
             u = __shfl_sync(0xffffffffu, u, 0);
-            PUnit info{};
+            UnitInfo info{};
             info.valid = 0;
             if (static_cast<int64_t>(u) < total_units) {
                 info.sigma = u / H;
@@ -468,7 +347,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
         for (;;) {
             const uint32_t slot = us & 1;
             if (!W(&unit_full[slot], us >> 1)) break;
-            const PUnit info = units[slot];
+            const UnitInfo info = units[slot];
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&unit_empty[slot]);
             if (!info.valid) break;
@@ -480,7 +359,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
                 if (lane == 0) PTRACE(1, 4, r);
                 tc::tc_fence_after();
                 const uint32_t k_s = sb + s * kPSlot, v_s = k_s + kTile;
-                const uint64_t da = pdesc_mn8(v_s), db = pdesc_mn8(k_s);
+                const uint64_t da = desc_mn8(v_s), db = desc_mn8(k_s);
                 if (tc::elect_one()) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
@@ -498,13 +377,13 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
             for (int c = 0; c < nch && ok; ++c) {
                 const uint32_t b = oc & 1;
                 const uint32_t q_s = sb + kPQ + b * kTile, v_s = sb + kPV + b * kTile;
-                const uint64_t dq = pdesc_k(q_s), dv = pdesc_mn8(v_s);
+                const uint64_t dq = desc_k(q_s), dv = desc_mn8(v_s);
                 // M1: P = Q K~^T (raw K on the exact route)
                 if (!(ok = W(&kp_ready, oc) && W(&q_full[b], oc >> 1) && (oc == 0 || W(&po_free, oc - 1)))) break;
                 if (lane == 0) PTRACE(1, 1, c);
                 tc::tc_fence_after();
                 const bool fast = kfast != 0;
-                const uint64_t dk = pdesc_k(sb + kPK);
+                const uint64_t dk = desc_k(sb + kPK);
                 if (tc::elect_one()) {
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
@@ -515,7 +394,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
                 }
                 __syncwarp();
                 const bool m4 = c + 1 < nch;
-                const uint64_t dk4 = pdesc_mn8(sb + kPK);
+                const uint64_t dk4 = desc_mn8(sb + kPK);
                 // the state has been copied (M4 may update it) and V has landed
                 if (!(ok = W(&zb_ready, zbc) && W(&v_full[b], oc >> 1))) break;
                 if (lane == 0) PTRACE(1, 2, c);
@@ -536,7 +415,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
                 if (!(ok = W(&pp_ready, oc))) break;
                 if (lane == 0) PTRACE(1, 3, c);
                 tc::tc_fence_after();
-                const uint64_t dp = pdesc_k(sb + kPP);
+                const uint64_t dp = desc_k(sb + kPP);
                 if (tc::elect_one()) {
                     if (m4 && !fast) {
 #pragma unroll
@@ -581,7 +460,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
             const uint32_t slot = us & 1;
             const bool bad = !wait_or_abort(&unit_full[slot], (us >> 1) & 1, abort_v, status);
             if (__any_sync(0xffffffffu, bad)) break;
-            const PUnit info = units[slot];
+            const UnitInfo info = units[slot];
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&unit_empty[slot]);
             if (!info.valid) break;
@@ -595,21 +474,21 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
             };
             auto chunk_of = [&](int j) { return j < nch ? nch - 1 - j : j - nch; };
             bool ok = true;
-            float2 g0 = pload_gate(a.g, c0_of(chunk_of(0)), nv_of(chunk_of(0)), H, h);
-            float2 g1 = pload_gate(a.g, c0_of(chunk_of(1)), nv_of(chunk_of(1)), H, h);
+            float2 g0 = load_gate(a.g, c0_of(chunk_of(0)), nv_of(chunk_of(0)), H, h);
+            float2 g1 = load_gate(a.g, c0_of(chunk_of(1)), nv_of(chunk_of(1)), H, h);
             float D = 0.f, run = 0.f;
 #pragma unroll 1
             for (int j = 0; j < 2 * nch; ++j) {
                 const int c = chunk_of(j);
-                const PGate G = pscan_gate(g0, nv_of(c));
+                const Gate G = scan_gate(g0, nv_of(c));
                 g0 = g1;
-                if (j + 2 < 2 * nch) g1 = pload_gate(a.g, c0_of(chunk_of(j + 2)), nv_of(chunk_of(j + 2)), H, h);
+                if (j + 2 < 2 * nch) g1 = load_gate(a.g, c0_of(chunk_of(j + 2)), nv_of(chunk_of(j + 2)), H, h);
                 const bool state = j < nch;
                 uint64_t *empty_b = state ? ga_empty : gc_empty;
                 const uint32_t n = state ? ja : jc;
                 const int R = state ? kPRecA : kPRecC;
                 if (!(ok = claim(empty_b, n, R))) break;
-                PRec *rec = (state ? recA : recC) + n % R;
+                GateRec *rec = (state ? recA : recC) + n % R;
                 *reinterpret_cast<float2 *>(&rec->b[2 * lane]) = make_float2(G.b0, G.b1);
                 if (state) {
                     if (lane == 0) {
@@ -618,12 +497,12 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
                     }
                     D += G.bC;
                 } else {
-                    const PPlan P = pplan_chunk(G, run);
+                    const Plan P = plan_chunk(G, run);
                     if (lane == 0) {
                         rec->bC = G.bC;
                         rec->base = P.base;
-                        rec->e1 = P.moved ? tc::ex2(P.pre * kLog2eP) : 1.f;
-                        rec->eC = P.fast ? 1.f : tc::ex2(G.bC * kLog2eP);
+                        rec->e1 = P.moved ? tc::ex2(P.pre * kLog2e) : 1.f;
+                        rec->eC = P.fast ? 1.f : tc::ex2(G.bC * kLog2e);
                         rec->fast = P.fast;
                         rec->moved = P.moved;
                     }
@@ -673,7 +552,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
         for (;;) {
             const uint32_t slot = us & 1;
             if (!pwg_wait(&unit_full[slot], us >> 1, abort_v, status)) break;
-            const PUnit info = units[slot];
+            const UnitInfo info = units[slot];
             named_sync(kBarW, 128);
             if (wtid == 0) tc::mbar_arrive(&unit_empty[slot]);
             if (!info.valid) break;
@@ -693,12 +572,12 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
                 const int64_t c0 = c0_of(nch - 1 - r);
                 const uint32_t s = (jobA + r) % kPSlots;
                 pwait(&ga_full[ja % kPRecA], ja / kPRecA, abort_v, status);
-                const PRec *R = recA + ja % kPRecA;
+                const GateRec *R = recA + ja % kPRecA;
                 const float e = R->bC + R->D - R->b[srow];
                 D += R->bC;
-                pwarp_arrive(&ga_empty[ja % kPRecA]);
+                warp_arrive(&ga_empty[ja % kPRecA]);
                 ++ja;
-                const float fac = c0 + srow < info.t1 ? tc::ex2(e * kLog2eP) : 0.f;
+                const float fac = c0 + srow < info.t1 ? tc::ex2(e * kLog2e) : 0.f;
                 pwait(&ka_full[s], (jobA + r) / kPSlots, abort_v, status);
                 uint8_t *base = sm + s * kPSlot + shalf * kRegion;
                 uint4 x[8];
@@ -714,7 +593,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
                     *reinterpret_cast<uint4 *>(base + sw(srow, c8)) = y;
                 }
                 tc::fence_proxy_async_smem();
-                pwarp_arrive(&ka_ready[s]);
+                warp_arrive(&ka_ready[s]);
             }
             jobA += nch;
 
@@ -742,7 +621,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
                 // to the chunk end
                 pwait(&gc_full[jc % kPRecC], jc / kPRecC, abort_v, status);
                 const float zfac = recC[jc % kPRecC].eC;
-                const float eB = tc::ex2(D * kLog2eP);
+                const float eB = tc::ex2(D * kLog2e);
                 float *dst = info.last ? (f.hT ? f.hT + (info.n * H + h) * kD * kD : nullptr)
                                        : f.incl + (static_cast<size_t>(info.sigma) * H + h) * kD * kD;
                 const float *src = info.first
@@ -779,7 +658,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
                 }
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
-                pwarp_arrive(&zb_ready);
+                warp_arrive(&zb_ready);
                 ++zbc;
                 // the publisher releases the flag once all four warps have stored S_out
                 if (npub >= 1) pwait(&pub_free, npub - 1, abort_v, status);
@@ -787,7 +666,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
                     pub_cmd = info.last ? 0 : 1;
                     pub_flag = f.flags + info.sigma * H + h;
                 }
-                pwarp_arrive(&pub_ready);
+                warp_arrive(&pub_ready);
                 ++npub;
                 if (wtid == 0) PTRACE(3, 4, us);
             }
@@ -808,12 +687,12 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
                     kx[i] = krow + 8 * i < nv ? tc::ldg_nc_hint(src + i * kstep, drop) : make_uint4(0u, 0u, 0u, 0u);
             };
             // K~ of chunk c from the rows in kx: k exp(-(base + b_s)), or the raw keys (exact route)
-            auto make_k = [&](int c, const PRec *R) {
+            auto make_k = [&](int c, const GateRec *R) {
                 const int nv = nv_of(c);
                 const bool fast = R->fast != 0;
                 if (oc + c >= 1) pwait(&kp_free, oc + c - 1, abort_v, status);
                 const int lr = 2 * quarter + (lane & 1) + 8 * ((lane & 15) >> 1);
-                const float myfac = lr < nv ? (fast ? tc::ex2((-R->base - R->b[lr]) * kLog2eP) : 1.f) : 0.f;
+                const float myfac = lr < nv ? (fast ? tc::ex2((-R->base - R->b[lr]) * kLog2e) : 1.f) : 0.f;
                 uint8_t *kd = sm + kPK + (kc16 >> 3) * kRegion;
                 const int par = lane >> 4;
 #pragma unroll
@@ -829,7 +708,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
                 }
                 if (wtid == 0) kfast = fast;
                 tc::fence_proxy_async_smem();
-                pwarp_arrive(&kp_ready);
+                warp_arrive(&kp_ready);
             };
             load_rows(0);
             make_k(0, recC + jc % kPRecC);
@@ -842,7 +721,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
                 const int64_t c0 = c0_of(c);
                 const int nv = nv_of(c);
                 const uint32_t b = (oc + c) & 1;
-                const PRec *R = recC + (jc + c) % kPRecC;   // (waited for already)
+                const GateRec *R = recC + (jc + c) % kPRecC;   // (waited for already)
                 const bool fast = R->fast != 0;
                 // P': the scores, masked (s <= t < nv) and rounded to bf16 (K-major rows t)
                 pwait(&p_full, oc + c, abort_v, status);
@@ -873,7 +752,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
                     if (!fast) {
                         // exact route: P'[t, s] *= exp(b_t - b_s); q_t <- exp(b_t) q_t (M1 has
                         // read Q); the weighted keys k_s exp(b_C - b_s) for M4 (M1 has read the raw)
-                        if (tr < nv) pexact_pp(pp, R->b, tr, sh);
+                        if (tr < nv) exact_pp_weights(pp, R->b, tr, sh);
                         pexact_rows(sm + kPQ + b * kTile, reinterpret_cast<const uint16_t *>(a.q), c0, srow,
                                     shalf, nv, H, h, R->b[srow]);
                         if (c + 1 < nch)
@@ -881,13 +760,13 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
                                         H, h, R->bC - R->b[srow]);
                     }
                     tc::fence_proxy_async_smem();
-                    pwarp_arrive(&pp_ready);
+                    warp_arrive(&pp_ready);
                     if (wtid == 0) PTRACE(2, 2, c);
                 }
                 if (c + 1 < nch) {
                     // K~ of the next chunk (once M1 and M4 of this one have read this chunk's)
                     pwait(&gc_full[(jc + c + 1) % kPRecC], (jc + c + 1) / kPRecC, abort_v, status);
-                    const PRec *Rn = recC + (jc + c + 1) % kPRecC;
+                    const GateRec *Rn = recC + (jc + c + 1) % kPRecC;
                     load_rows(c + 1);
                     if (wtid == 0) PTRACE(2, 3, c);
                     make_k(c + 1, Rn);
@@ -933,7 +812,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
                     }
                     tc::tmem_st_wait();
                     tc::tc_fence_before();
-                    pwarp_arrive(&zb_ready);
+                    warp_arrive(&zb_ready);
                     if (wtid == 0) PTRACE(2, 7, c);
                     ++zbc;
                 }
@@ -950,14 +829,14 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
                     tc::tmem_ld_16x256b_x8(tmem + lane_base + (16u << 16) + kPtPO, o1);
                     tc::tmem_ld_wait();
                     tc::tc_fence_before();
-                    pwarp_arrive(&po_free);   // the columns may take the next scores
+                    warp_arrive(&po_free);   // the columns may take the next scores
                     if (lane == 0) tc::tma_store_wait_read<0>();   // staging tile free again
                     __syncwarp();
 #pragma unroll
                     for (int m = 0; m < 8; ++m) {
                         const float2 bb = *reinterpret_cast<const float2 *>(&R->b[8 * m + tl]);
-                        const float fa = fast ? a.scale * tc::ex2((base + bb.x) * kLog2eP) : a.scale;
-                        const float fb = fast ? a.scale * tc::ex2((base + bb.y) * kLog2eP) : a.scale;
+                        const float fa = fast ? a.scale * tc::ex2((base + bb.x) * kLog2e) : a.scale;
+                        const float fb = fast ? a.scale * tc::ex2((base + bb.y) * kLog2e) : a.scale;
                         pstmatrix_x2_trans(st_a + 512 * m,
                                            float2_to_bf16x2(__uint_as_float(o0[4 * m]) * fa, __uint_as_float(o0[4 * m + 1]) * fb),
                                            float2_to_bf16x2(__uint_as_float(o0[4 * m + 2]) * fa, __uint_as_float(o0[4 * m + 3]) * fb));
@@ -965,7 +844,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
                                            float2_to_bf16x2(__uint_as_float(o1[4 * m]) * fa, __uint_as_float(o1[4 * m + 1]) * fb),
                                            float2_to_bf16x2(__uint_as_float(o1[4 * m + 2]) * fa, __uint_as_float(o1[4 * m + 3]) * fb));
                     }
-                    pwarp_arrive(&gc_empty[(jc + c) % kPRecC]);   // done with this chunk's record
+                    warp_arrive(&gc_empty[(jc + c) % kPRecC]);   // done with this chunk's record
                     if (nv == kChunk) {
                         tc::fence_proxy_async_smem();
                         __syncwarp();
@@ -988,7 +867,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
             jc += nch;
             // the region may take the next unit's tiles once this unit's stores have read it
             if (lane == 0) tc::tma_store_wait_read<0>();
-            pwarp_arrive(&unit_free);
+            warp_arrive(&unit_free);
             if (named_any(kBarW, 128, *abort_v != 0)) break;
             ++us;
         }
@@ -997,7 +876,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PairArgs f, SegTable t,
         if (!named_any(kBarW, 128, *abort_v != 0)) {
             if (npub >= 1) pwait(&pub_free, npub - 1, abort_v, status);
             if (wtid == 0) pub_cmd = 2;
-            pwarp_arrive(&pub_ready);
+            warp_arrive(&pub_ready);
         }
     }
 
@@ -1022,7 +901,7 @@ cudaError_t launch_prefill_pair(const ChunkArgs &a, const SegTable &t, int64_t T
         tck::TcMaps maps;
         cudaError_t e = tck::make_maps(&maps, a.q, a.k, a.v, a.o, T_total, a.H, true);
         if (e != cudaSuccess) return e;
-        PairArgs f;
+        PrefillArgs f;
         f.c = a;
         f.h0 = h0;
         f.hT = hT;

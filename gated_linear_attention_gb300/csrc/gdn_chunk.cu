@@ -108,17 +108,6 @@ __device__ __forceinline__ bool gwait(uint64_t *bar, uint32_t par, int *status, 
     return true;
 }
 
-// 16-lane form, 16 columns: thread i gets lane (base + i % 16), columns [col + 32 (i / 16), + 16)
-__device__ __forceinline__ void tmem_ld_16x32bx2_x16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16], 32;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-
 }  // namespace
 
 __global__ void __launch_bounds__(kGThreads, 2)
@@ -319,7 +308,7 @@ gdn_newv_kernel(const __grid_constant__ TcMaps maps, GdnChunkArgs p, int *status
         {
             // (the 16-column form: warps w and w + 4 take columns 16 wg .. + 15 of each half)
             uint32_t x[16];
-            tmem_ld_16x32bx2_x16(tmem + lane_base + kGtAcc + 16 * wg, x);
+            tc::tmem_ld_16x32bx2_x16(tmem + lane_base + kGtAcc + 16 * wg, x);
             tc::tmem_ld_wait();
             const int t = quarter * 16 + (lane & 15), s0 = 32 * (lane >> 4) + 16 * wg;
             const float bt = bsm[t] * kLog2eG, be = betasm[t];

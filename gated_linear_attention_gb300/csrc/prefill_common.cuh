@@ -144,6 +144,20 @@ __device__ __noinline__ void exact_pp_weights(uint8_t *pp, const float *b, int t
     }
 }
 
+// Bounded wait (if `need`) whose failure only sets the abort flag (see the epilogue loops).
+__device__ __forceinline__ void wait_nv(uint64_t *bar, uint32_t par, bool need,
+                                        volatile int *abort_v, int *status) {
+    if (need) (void)wait_or_abort(bar, par & 1, abort_v, status);
+}
+
+// Bounded wait on an mbarrier phase by every thread of a group of n threads (if `need`),
+// then an OR-vote so that all of them take the same branch. Returns false if any failed.
+__device__ __forceinline__ bool wg_wait(uint64_t *bar, uint32_t par, bool need, int bar_id,
+                                        volatile int *abort_v, int *status, int n = 128) {
+    const bool bad = need ? !wait_or_abort(bar, par & 1, abort_v, status) : false;
+    return !named_any(bar_id, n, bad);
+}
+
 // Per-warp arrival: the warp's lanes have finished their part; lane 0 arrives for the warp.
 __device__ __forceinline__ void warp_arrive(uint64_t *bar) {
     __syncwarp();

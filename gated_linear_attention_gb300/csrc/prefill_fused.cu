@@ -131,20 +131,6 @@ __device__ unsigned long long g_wait_acc[32];
 
 
 
-// Bounded wait (if `need`) whose failure only sets the abort flag (see the epilogue loops).
-__device__ __forceinline__ void wait_nv(uint64_t *bar, uint32_t par, bool need,
-                                        volatile int *abort_v, int *status) {
-    if (need) (void)wait_or_abort(bar, par & 1, abort_v, status);
-}
-
-// Bounded wait on an mbarrier phase by every thread of a group of n threads (if `need`),
-// then an OR-vote so that all of them take the same branch. Returns false if any failed.
-__device__ __forceinline__ bool wg_wait(uint64_t *bar, uint32_t par, bool need, int bar_id,
-                                        volatile int *abort_v, int *status, int n = 128) {
-    const bool bad = need ? !wait_or_abort(bar, par & 1, abort_v, status) : false;
-    return !named_any(bar_id, n, bad);
-}
-
 // 64 bf16 of one row, scaled by f, to a [64 x 128 B] SW128 region row. kExact: product in
 // fp32, rounded once; otherwise f is rounded to bf16 and each pair takes one packed multiply
 // (about 5x fewer instructions, one more rounding of the factor: used for the output pass,

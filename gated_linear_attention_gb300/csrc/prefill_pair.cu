@@ -90,37 +90,12 @@ __device__ unsigned int g_ptrace_n[4];
 
 
 
-__device__ __forceinline__ void pwait(uint64_t *bar, uint32_t par, volatile int *abort_v, int *status) {
-    (void)wait_or_abort(bar, par & 1, abort_v, status);
-}
-
-// The 16-lane tensor-memory load, 16 columns: thread i gets lane (base + i % 16), columns
-// [col + 32 (i / 16), + 16).
-__device__ __forceinline__ void tmem_ld_16x32bx2_x16_p(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16], 32;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-
 // Two 8 x 8 bf16 matrices stored transposed (lanes 0-15 give the row addresses).
 __device__ __forceinline__ void pstmatrix_x2_trans(uint32_t saddr, uint32_t r0, uint32_t r1) {
     asm volatile("stmatrix.sync.aligned.m8n8.x2.trans.shared.b16 [%0], {%1, %2};" ::"r"(saddr), "r"(r0),
                  "r"(r1)
                  : "memory");
 }
-
-// Bounded wait of every worker thread, then an OR-vote so that all of them take the same
-// branch. Returns false if any gave up.
-__device__ __forceinline__ bool pwg_wait(uint64_t *bar, uint32_t par, volatile int *abort_v, int *status) {
-    const bool bad = !wait_or_abort(bar, par & 1, abort_v, status);
-    return !named_any(kBarW, 128, bad);
-}
-
-
 
 // Exact route: row `row` (columns 64 half .. + 63) of the tile at dst becomes exp(f_row) x_row
 // for the bf16 rows of global memory at src (zero past nv). Used for q_t <- exp(b_t) q_t (M1 has
@@ -551,7 +526,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PrefillArgs f, SegTable
         const int tl = 2 * (lane & 3);
         for (;;) {
             const uint32_t slot = us & 1;
-            if (!pwg_wait(&unit_full[slot], us >> 1, abort_v, status)) break;
+            if (!wg_wait(&unit_full[slot], us >> 1, true, kBarW, abort_v, status)) break;
             const UnitInfo info = units[slot];
             named_sync(kBarW, 128);
             if (wtid == 0) tc::mbar_arrive(&unit_empty[slot]);
@@ -571,14 +546,14 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PrefillArgs f, SegTable
             for (int r = 0; r < nch; ++r) {
                 const int64_t c0 = c0_of(nch - 1 - r);
                 const uint32_t s = (jobA + r) % kPSlots;
-                pwait(&ga_full[ja % kPRecA], ja / kPRecA, abort_v, status);
+                wait_nv(&ga_full[ja % kPRecA], ja / kPRecA, true, abort_v, status);
                 const GateRec *R = recA + ja % kPRecA;
                 const float e = R->bC + R->D - R->b[srow];
                 D += R->bC;
                 warp_arrive(&ga_empty[ja % kPRecA]);
                 ++ja;
                 const float fac = c0 + srow < info.t1 ? tc::ex2(e * kLog2e) : 0.f;
-                pwait(&ka_full[s], (jobA + r) / kPSlots, abort_v, status);
+                wait_nv(&ka_full[s], (jobA + r) / kPSlots, true, abort_v, status);
                 uint8_t *base = sm + s * kPSlot + shalf * kRegion;
                 uint4 x[8];
 #pragma unroll
@@ -619,7 +594,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PrefillArgs f, SegTable
                 tc::tc_fence_after();
                 // chunk 0 starts at the reference point; the exact route keeps the state scaled
                 // to the chunk end
-                pwait(&gc_full[jc % kPRecC], jc / kPRecC, abort_v, status);
+                wait_nv(&gc_full[jc % kPRecC], jc / kPRecC, true, abort_v, status);
                 const float zfac = recC[jc % kPRecC].eC;
                 const float eB = tc::ex2(D * kLog2e);
                 float *dst = info.last ? (f.hT ? f.hT + (info.n * H + h) * kD * kD : nullptr)
@@ -628,7 +603,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PrefillArgs f, SegTable
                     ? (f.h0 ? f.h0 + (info.n * H + h) * kD * kD : nullptr)
                     : f.incl + (static_cast<size_t>(info.sigma - 1) * H + h) * kD * kD;
                 // (the bf16 copy of the previous unit's last chunk has been read: ds_full)
-                if (zbc >= 1) pwait(&zb_free, zbc - 1, abort_v, status);
+                if (zbc >= 1) wait_nv(&zb_free, zbc - 1, true, abort_v, status);
 #pragma unroll 1
                 for (int k4 = 0; k4 < 4; ++k4) {
                     float sv[32];
@@ -661,7 +636,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PrefillArgs f, SegTable
                 warp_arrive(&zb_ready);
                 ++zbc;
                 // the publisher releases the flag once all four warps have stored S_out
-                if (npub >= 1) pwait(&pub_free, npub - 1, abort_v, status);
+                if (npub >= 1) wait_nv(&pub_free, npub - 1, true, abort_v, status);
                 if (wtid == 0) {
                     pub_cmd = info.last ? 0 : 1;
                     pub_flag = f.flags + info.sigma * H + h;
@@ -690,7 +665,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PrefillArgs f, SegTable
             auto make_k = [&](int c, const GateRec *R) {
                 const int nv = nv_of(c);
                 const bool fast = R->fast != 0;
-                if (oc + c >= 1) pwait(&kp_free, oc + c - 1, abort_v, status);
+                if (oc + c >= 1) wait_nv(&kp_free, oc + c - 1, true, abort_v, status);
                 const int lr = 2 * quarter + (lane & 1) + 8 * ((lane & 15) >> 1);
                 const float myfac = lr < nv ? (fast ? tc::ex2((-R->base - R->b[lr]) * kLog2e) : 1.f) : 0.f;
                 uint8_t *kd = sm + kPK + (kc16 >> 3) * kRegion;
@@ -724,7 +699,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PrefillArgs f, SegTable
                 const GateRec *R = recC + (jc + c) % kPRecC;   // (waited for already)
                 const bool fast = R->fast != 0;
                 // P': the scores, masked (s <= t < nv) and rounded to bf16 (K-major rows t)
-                pwait(&p_full, oc + c, abort_v, status);
+                wait_nv(&p_full, oc + c, true, abort_v, status);
                 if (wtid == 0) PTRACE(2, 1, c);
                 tc::tc_fence_after();
                 {
@@ -733,7 +708,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PrefillArgs f, SegTable
 #pragma unroll 1
                     for (int hp = 0; hp < 2; ++hp) {
                         uint32_t p[16];
-                        tmem_ld_16x32bx2_x16_p(tmem + lane_base + kPtPO + 16 * hp, p);
+                        tc::tmem_ld_16x32bx2_x16(tmem + lane_base + kPtPO + 16 * hp, p);
                         tc::tmem_ld_wait();
 #pragma unroll
                         for (int c4 = 0; c4 < 2; ++c4) {
@@ -765,7 +740,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PrefillArgs f, SegTable
                 }
                 if (c + 1 < nch) {
                     // K~ of the next chunk (once M1 and M4 of this one have read this chunk's)
-                    pwait(&gc_full[(jc + c + 1) % kPRecC], (jc + c + 1) / kPRecC, abort_v, status);
+                    wait_nv(&gc_full[(jc + c + 1) % kPRecC], (jc + c + 1) / kPRecC, true, abort_v, status);
                     const GateRec *Rn = recC + (jc + c + 1) % kPRecC;
                     load_rows(c + 1);
                     if (wtid == 0) PTRACE(2, 3, c);
@@ -776,10 +751,10 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PrefillArgs f, SegTable
                     // exact route), once M4 of this chunk has updated Z and M2 has read the old copy
                     const float e1 = Rn->e1, eC = Rn->eC;
                     const bool moved = Rn->moved != 0;
-                    pwait(&z_full, zfc, abort_v, status);
+                    wait_nv(&z_full, zfc, true, abort_v, status);
                     ++zfc;
                     if (wtid == 0) PTRACE(2, 5, c);
-                    pwait(&zb_free, zbc - 1, abort_v, status);
+                    wait_nv(&zb_free, zbc - 1, true, abort_v, status);
                     if (wtid == 0) PTRACE(2, 6, c);
                     tc::tc_fence_after();
                     const uint32_t zb_base = tmem + lane_base + kPtZb;
@@ -821,7 +796,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PrefillArgs f, SegTable
                 // one TMA store per warp (direct stores when the chunk is ragged)
                 {
                     const float base = R->base;
-                    pwait(&o_full, oc + c, abort_v, status);
+                    wait_nv(&o_full, oc + c, true, abort_v, status);
                     if (wtid == 0) PTRACE(2, 8, c);
                     tc::tc_fence_after();
                     uint32_t o0[32], o1[32];
@@ -874,7 +849,7 @@ prefill_pair_kernel(const __grid_constant__ TcMaps maps, PrefillArgs f, SegTable
         if (lane == 0) tc::tma_store_wait_all<0>();
         // stop the publisher (after an abort it stops by itself)
         if (!named_any(kBarW, 128, *abort_v != 0)) {
-            if (npub >= 1) pwait(&pub_free, npub - 1, abort_v, status);
+            if (npub >= 1) wait_nv(&pub_free, npub - 1, true, abort_v, status);
             if (wtid == 0) pub_cmd = 2;
             warp_arrive(&pub_ready);
         }

@@ -314,6 +314,18 @@ __device__ __forceinline__ void tmem_ld_16x32bx2_x32(uint32_t taddr, uint32_t (&
         : "r"(taddr));
 }
 
+// The same 16-lane form, 16 columns: thread i gets lane (base + i % 16), columns
+// [col + 32 (i / 16), + 16).
+__device__ __forceinline__ void tmem_ld_16x32bx2_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16], 32;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
 // 16 lanes x 64 columns in the mma-fragment order: for repetition m (columns 8 m .. + 7),
 // thread i gets r[4 m] = (lane base + i / 4, column 8 m + 2 (i % 4)), r[4 m + 1] the next
 // column of that lane, and r[4 m + 2], r[4 m + 3] the same two columns of lane base + 8 + i / 4.
